@@ -1,0 +1,1197 @@
+// C ABI of liblora_mlp.so: argument validation, workspace planning, TMA descriptor set-up
+// and the kernel sequence of each entry point.  See include/lora_mlp.h for the contract.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <initializer_list>
+
+#include "lm_internal.h"
+#include "lora_mlp.h"
+
+using namespace lm;
+
+namespace {
+
+thread_local char g_err[768] = "";
+
+lm_status fail(lm_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+#define LM_TRY(expr)                      \
+    do {                                  \
+        const lm_status _s = (expr);      \
+        if (_s != LM_OK) return _s;       \
+    } while (0)
+
+lm_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(LM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define LM_CUDA(expr, what)                                \
+    do {                                                   \
+        const cudaError_t _e = (expr);                     \
+        if (_e != cudaSuccess) return cuda_fail(_e, what); \
+    } while (0)
+
+// ------------------------------------------------------------------ device / driver entry
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+lm_status get_encode() {
+    if (g_encode) return LM_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return fail(LM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return LM_OK;
+}
+
+lm_status device_sms(int* sms) {
+    static int cached[64] = {0};  // 0 unknown, > 0 SM count, -1 unsupported
+    int dev = 0;
+    LM_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(LM_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    if (cached[dev] == 0) {
+        int major = 0, minor = 0, n = 0;
+        LM_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "cudaDeviceGetAttribute");
+        LM_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "cudaDeviceGetAttribute");
+        LM_CUDA(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute");
+        cached[dev] = (major == 10 && minor == 3) ? n : -1;
+    }
+    if (cached[dev] < 0)
+        return fail(LM_ERR_UNSUPPORTED, "device %d is not compute capability 10.3; the kernels are built for sm_103a", dev);
+    *sms = cached[dev];
+    return LM_OK;
+}
+
+lm_status ready(int* sms) {
+    LM_TRY(device_sms(sms));
+    return get_encode();
+}
+
+// ------------------------------------------------------------------ validation
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+lm_status need_ptr(const void* p, const char* name) {
+    if (!p) return fail(LM_ERR_NULL, "%s is NULL", name);
+    if (!aligned16(p)) return fail(LM_ERR_ALIGN, "%s is not 16-byte aligned", name);
+    return LM_OK;
+}
+
+lm_status check_dim(int64_t v, const char* name) {
+    if (v <= 0 || v % 32 != 0 || v > (int64_t(1) << 20))
+        return fail(LM_ERR_SHAPE, "%s = %lld must be a positive multiple of 32 (at most 2^20)", name, (long long)v);
+    return LM_OK;
+}
+
+lm_status check_T(int64_t T) {
+    if (T < 0 || T > (int64_t(1) << 30)) return fail(LM_ERR_SHAPE, "T = %lld out of range", (long long)T);
+    return LM_OK;
+}
+
+lm_status check_r(int32_t r) {
+    if (r < 8 || r > 64 || r % 8 != 0) return fail(LM_ERR_SHAPE, "r = %d must be a multiple of 8 in [8, 64]", r);
+    return LM_OK;
+}
+
+lm_status check_lora(const lm_lora* L, const char* name, int64_t in, int64_t out, int32_t r) {
+    if (!L) return fail(LM_ERR_NULL, "%s is NULL", name);
+    if (L->r != r) return fail(LM_ERR_SHAPE, "%s.r = %d differs from r = %d", name, L->r, r);
+    if (L->W.rows != out || L->W.cols != in)
+        return fail(LM_ERR_SHAPE, "%s.W is %lld x %lld, expected %lld x %lld (out x in)", name, (long long)L->W.rows,
+                    (long long)L->W.cols, (long long)out, (long long)in);
+    if (!std::isfinite(L->s)) return fail(LM_ERR_SHAPE, "%s.s is not finite", name);
+    char buf[64];
+    if (L->W.kind == LM_WEIGHT_BF16) {
+        snprintf(buf, sizeof buf, "%s.W.w", name);
+        LM_TRY(need_ptr(L->W.w, buf));
+    } else if (L->W.kind == LM_WEIGHT_NF4) {
+        return fail(LM_ERR_UNSUPPORTED, "%s: NF4 base weights are not available in this build of the GEMMs", name);
+    } else {
+        return fail(LM_ERR_DTYPE, "%s.W.kind = %d is not a known weight kind", name, L->W.kind);
+    }
+    snprintf(buf, sizeof buf, "%s.A", name);
+    LM_TRY(need_ptr(L->A, buf));
+    snprintf(buf, sizeof buf, "%s.B", name);
+    LM_TRY(need_ptr(L->B, buf));
+    return LM_OK;
+}
+
+struct Span {
+    const void* p;
+    size_t bytes;
+    const char* name;
+};
+
+bool overlap(const Span& a, const Span& b) {
+    if (!a.p || !b.p || !a.bytes || !b.bytes) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// every output against every input and every other output
+lm_status check_alias(std::initializer_list<Span> outs, std::initializer_list<Span> ins) {
+    const Span* o = outs.begin();
+    for (size_t i = 0; i < outs.size(); ++i) {
+        for (const Span& in : ins)
+            if (overlap(o[i], in)) return fail(LM_ERR_ALIAS, "%s overlaps %s", o[i].name, in.name);
+        for (size_t j = i + 1; j < outs.size(); ++j)
+            if (overlap(o[i], o[j])) return fail(LM_ERR_ALIAS, "%s overlaps %s", o[i].name, o[j].name);
+    }
+    return LM_OK;
+}
+
+Span wspan(const lm_lora* L, const char* name) {
+    return Span{L->W.w, (size_t)(L->W.rows * L->W.cols * 2), name};
+}
+
+// ------------------------------------------------------------------ workspace planning
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+struct Bump {
+    size_t off = 0;
+    size_t take(size_t bytes) {
+        off = (off + 255) & ~size_t(255);
+        const size_t o = off;
+        off += bytes;
+        return o;
+    }
+};
+
+constexpr int kMaxSplits = 8;
+
+struct Dims {
+    int64_t T, ldT;
+    int32_t r, rp;
+};
+
+Dims make_dims(int64_t T, int32_t r) {
+    Dims D;
+    D.T = T;
+    D.ldT = round_up(std::max<int64_t>(T, 1), 64);
+    D.r = r;
+    D.rp = (int32_t)round_up(r, 16);
+    return D;
+}
+
+// rank-r product buffer: (T x cols) bf16 and its transpose (cols x ldT)
+struct RankBuf {
+    size_t rows_off, t_off;
+};
+
+RankBuf take_rank(Bump& b, const Dims& D, int cols) {
+    RankBuf r;
+    r.rows_off = b.take((size_t)D.T * cols * 2);
+    r.t_off = b.take((size_t)cols * D.ldT * 2);
+    return r;
+}
+
+struct MlpPlan {
+    Dims D;
+    RankBuf xa, ha;         // saved: s*[X Ag^T | X Au^T] (T x 2rp), s*h Ad^T (T x rp)
+    size_t saved_total;
+    size_t part;            // workspace
+    RankBuf gd, gg, gu;     // s*dY Bd, s*de Bg, s*du Bu
+    size_t de, du;
+    size_t ws_total;
+};
+
+MlpPlan plan_mlp(int64_t T, int64_t d, int64_t n, int32_t r) {
+    MlpPlan P;
+    P.D = make_dims(T, r);
+    const int64_t rp = P.D.rp;
+    Bump s;
+    P.xa = take_rank(s, P.D, 2 * rp);
+    P.ha = take_rank(s, P.D, rp);
+    P.saved_total = s.off;
+    Bump w;
+    w.take(256);  // error word
+    const int64_t part_elems = std::max<int64_t>(T * 2 * rp, 3 * (n + d) * rp);
+    P.part = w.take((size_t)kMaxSplits * part_elems * 4);
+    P.gd = take_rank(w, P.D, rp);
+    P.gg = take_rank(w, P.D, rp);
+    P.gu = take_rank(w, P.D, rp);
+    P.de = w.take((size_t)T * n * 2);
+    P.du = w.take((size_t)T * n * 2);
+    P.ws_total = w.off;
+    return P;
+}
+
+struct QkvPlan {
+    Dims D;
+    RankBuf xa;             // saved: s*[X Aq^T | X Ak^T | X Av^T] (T x 3rp)
+    size_t saved_total;
+    size_t part;
+    RankBuf g[3];
+    size_t ws_total;
+};
+
+QkvPlan plan_qkv(int64_t T, int64_t d, int64_t nq, int64_t nk, int64_t nv, int32_t r) {
+    QkvPlan P;
+    P.D = make_dims(T, r);
+    const int64_t rp = P.D.rp;
+    Bump s;
+    P.xa = take_rank(s, P.D, 3 * rp);
+    P.saved_total = s.off;
+    Bump w;
+    w.take(256);
+    const int64_t part_elems = std::max<int64_t>(T * 3 * rp, (3 * d + nq + nk + nv) * rp);
+    P.part = w.take((size_t)kMaxSplits * part_elems * 4);
+    for (int i = 0; i < 3; ++i) P.g[i] = take_rank(w, P.D, rp);
+    P.ws_total = w.off;
+    return P;
+}
+
+struct OPlan {
+    Dims D;
+    RankBuf xa;
+    size_t saved_total;
+    size_t part;
+    RankBuf g;
+    size_t ws_total;
+};
+
+OPlan plan_o(int64_t T, int64_t d_in, int64_t d_out, int32_t r) {
+    OPlan P;
+    P.D = make_dims(T, r);
+    const int64_t rp = P.D.rp;
+    Bump s;
+    P.xa = take_rank(s, P.D, rp);
+    P.saved_total = s.off;
+    Bump w;
+    w.take(256);
+    const int64_t part_elems = std::max<int64_t>(T * rp, (d_in + d_out) * rp);
+    P.part = w.take((size_t)kMaxSplits * part_elems * 4);
+    P.g = take_rank(w, P.D, rp);
+    P.ws_total = w.off;
+    return P;
+}
+
+// ------------------------------------------------------------------ GEMM launch builder
+struct Builder {
+    Params p;
+    int nmaps = 0;
+    lm_status st = LM_OK;
+    GemmKind kind;
+
+    explicit Builder(GemmKind k) : kind(k) { memset(&p, 0, sizeof p); }
+
+    // 2D bf16 tensor (rows x cols, row stride ld elements), box = 64 columns x box_rows rows
+    int map(const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+        if (st != LM_OK) return 0;
+        if (nmaps >= kMaxMaps) {
+            st = fail(LM_ERR_UNSUPPORTED, "too many tensor maps in one launch");
+            return 0;
+        }
+        cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+        cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+        cuuint32_t es[2] = {1u, 1u};
+        const CUresult r = g_encode(&p.maps[nmaps], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            st = fail(LM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %lld x %lld tensor, box rows %d", (int)r,
+                      (long long)rows, (long long)cols, box_rows);
+            return 0;
+        }
+        p.map_bytes[nmaps] = 128u * (uint32_t)box_rows;
+        p.map_w[nmaps] = (int32_t)cols;
+        return nmaps++;
+    }
+
+    Prob& prob() {
+        Prob& P = p.prob[p.nprob++];
+        memset(&P, 0, sizeof P);
+        P.splits = 1;
+        for (int s = 0; s < kMaxSegs; ++s)
+            for (int i = 0; i < 3; ++i) P.seg[s].b_map[i] = -1;
+        return P;
+    }
+
+    // tiles, split-K and work-unit numbering; returns the grid size
+    int finish(int sms, int32_t* err) {
+        p.err = err;
+        const bool partial = (kind == G_PART_KK || kind == G_PART_KMN || kind == G_PART_MNK);
+        int64_t tiles = 0;
+        for (int i = 0; i < p.nprob; ++i) {
+            Prob& P = p.prob[i];
+            P.tiles_m = (int32_t)((P.M + kBM - 1) / kBM);
+            tiles += (int64_t)P.tiles_m * P.tiles_n;
+        }
+        int S = 1;
+        if (partial) S = (int)std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, (2 * sms + tiles - 1) / tiles));
+        int64_t units = 0;
+        for (int i = 0; i < p.nprob; ++i) {
+            Prob& P = p.prob[i];
+            if (partial) {
+                const int nkb = (P.seg[0].kext + kBK - 1) / kBK;
+                P.kb_per_split = (nkb + S - 1) / S;
+                P.splits = (nkb + P.kb_per_split - 1) / P.kb_per_split;
+            } else {
+                P.splits = 1;
+                P.kb_per_split = 0;
+            }
+            P.unit_begin = (int32_t)units;
+            units += (int64_t)P.tiles_m * P.tiles_n * P.splits;
+        }
+        p.total_units = (int32_t)units;
+        return (int)std::min<int64_t>(units, sms);
+    }
+
+    lm_status launch(int sms, int32_t* err, cudaStream_t st_) {
+        if (st != LM_OK) return st;
+        const int grid = finish(sms, err);
+        if (grid == 0) return LM_OK;
+        const cudaError_t e = launch_gemm(kind, p, grid, st_);
+        if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
+        return LM_OK;
+    }
+};
+
+Seg& seg(Prob& P, int i) {
+    P.nseg = std::max(P.nseg, i + 1);
+    return P.seg[i];
+}
+
+// rank-r input projection, K-major B made of stacked A matrices:
+//   part[ks][t][i*rp + j] = sum_k Z[t][k] * A_i[j][k]
+void add_rowproj_in(Builder& b, const uint16_t* Z, int64_t T, int64_t K, std::initializer_list<const uint16_t*> As,
+                    const Dims& D, float* part) {
+    Prob& P = b.prob();
+    const int cnt = (int)As.size();
+    P.M = (int32_t)T;
+    P.N = cnt * D.rp;
+    P.bn = cnt * D.rp;
+    P.tiles_n = 1;
+    Seg& S = seg(P, 0);
+    S.a_map = b.map(Z, T, K, K, 128);
+    int i = 0;
+    for (const uint16_t* A : As) S.b_map[i++] = b.map(A, D.r, K, K, D.rp);
+    S.b_rows = D.rp;
+    S.kext = (int32_t)K;
+    P.out0 = part;
+    P.ld_out = P.bn;
+    P.split_stride = T * P.bn;
+}
+
+// rank-r output-gradient projection, MN-major B:  part[ks][t][j] = sum_c dO[t][c] * Bm[c][j]
+void add_rowproj_out(Builder& b, const uint16_t* dO, int64_t T, int64_t C, const uint16_t* Bm, const Dims& D,
+                     float* part) {
+    Prob& P = b.prob();
+    P.M = (int32_t)T;
+    P.N = D.rp;
+    P.bn = D.rp;
+    P.tiles_n = 1;
+    Seg& S = seg(P, 0);
+    S.a_map = b.map(dO, T, C, C, 128);
+    S.b_map[0] = b.map(Bm, C, D.r, D.r, 64);
+    S.kext = (int32_t)C;
+    P.out0 = part;
+    P.ld_out = P.bn;
+    P.split_stride = T * P.bn;
+}
+
+// column reduction over tokens: part[ks][c][j] = sum_t Z[t][c] * PT[j][t]
+void add_colreduce(Builder& b, const uint16_t* Z, int64_t T, int64_t C, const uint16_t* PT, const Dims& D,
+                   float* part) {
+    Prob& P = b.prob();
+    P.M = (int32_t)C;
+    P.N = D.rp;
+    P.bn = D.rp;
+    P.tiles_n = 1;
+    Seg& S = seg(P, 0);
+    S.a_map = b.map(Z, T, C, C, 64);
+    S.b_map[0] = b.map(PT, D.rp, T, D.ldT, D.rp);
+    S.kext = (int32_t)T;
+    P.out0 = part;
+    P.ld_out = P.bn;
+    P.split_stride = C * P.bn;
+}
+
+lm_status fin_rows(const Builder& b, std::initializer_list<FinRowJob> jobs, int64_t T, cudaStream_t st) {
+    FinRowJob js[3];
+    int n = 0;
+    for (const FinRowJob& j : jobs) {
+        js[n] = j;
+        js[n].splits = b.p.prob[n].splits;
+        ++n;
+    }
+    const cudaError_t e = launch_fin_rowproj(js, n, T, st);
+    if (e != cudaSuccess) return cuda_fail(e, "rank-r finalisation launch");
+    return LM_OK;
+}
+
+lm_status fin_cols(const Builder& b, FinColJob* js, int n, cudaStream_t st) {
+    for (int i = 0; i < n; ++i) js[i].splits = b.p.prob[i].splits;
+    const cudaError_t e = launch_fin_colreduce(js, n, st);
+    if (e != cudaSuccess) return cuda_fail(e, "gradient finalisation launch");
+    return LM_OK;
+}
+
+template <typename T_>
+T_* at(void* base, size_t off) {
+    return reinterpret_cast<T_*>(static_cast<char*>(base) + off);
+}
+template <typename T_>
+const T_* at(const void* base, size_t off) {
+    return reinterpret_cast<const T_*>(static_cast<const char*>(base) + off);
+}
+
+}  // namespace
+
+// ====================================================================== utilities
+extern "C" const char* lm_last_error(void) { return g_err; }
+
+extern "C" lm_status lm_nf4_codebook(float* out) {
+    if (!out) return fail(LM_ERR_NULL, "out is NULL");
+    nf4_codebook_host(out);
+    return LM_OK;
+}
+
+extern "C" lm_status lm_workspace_reset(void* ws, lm_stream stream) {
+    LM_TRY(need_ptr(ws, "ws"));
+    LM_CUDA(cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream), "cudaMemsetAsync");
+    return LM_OK;
+}
+
+extern "C" lm_status lm_workspace_check(void* ws, lm_stream stream) {
+    LM_TRY(need_ptr(ws, "ws"));
+    int32_t h[4] = {0, 0, 0, 0};
+    LM_CUDA(cudaMemcpyAsync(h, ws, sizeof h, cudaMemcpyDeviceToHost, (cudaStream_t)stream), "cudaMemcpyAsync");
+    LM_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "cudaStreamSynchronize");
+    if (h[0] != 0) {
+        LM_CUDA(cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream), "cudaMemsetAsync");
+        LM_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "cudaStreamSynchronize");
+        return fail((lm_status)h[0], "a kernel gave up on a bounded wait (role %d, block %d)", h[1], h[2]);
+    }
+    return LM_OK;
+}
+
+// ====================================================================== LoRA MLP
+extern "C" lm_status lora_mlp_saved_size(int64_t T, int32_t r, size_t* bytes) {
+    if (!bytes) return fail(LM_ERR_NULL, "bytes is NULL");
+    LM_TRY(check_T(T));
+    LM_TRY(check_r(r));
+    *bytes = plan_mlp(T, 32, 32, r).saved_total;
+    return LM_OK;
+}
+
+extern "C" lm_status lora_mlp_workspace_size(int64_t T, int64_t d, int64_t n, int32_t r, size_t* bytes) {
+    if (!bytes) return fail(LM_ERR_NULL, "bytes is NULL");
+    LM_TRY(check_T(T));
+    LM_TRY(check_dim(d, "d"));
+    LM_TRY(check_dim(n, "n"));
+    LM_TRY(check_r(r));
+    *bytes = plan_mlp(T, d, n, r).ws_total;
+    return LM_OK;
+}
+
+static lm_status check_mlp_common(int64_t T, int64_t d, int64_t n, int32_t act, const lm_lora* gate,
+                                  const lm_lora* up, const lm_lora* down) {
+    LM_TRY(check_T(T));
+    LM_TRY(check_dim(d, "d"));
+    LM_TRY(check_dim(n, "n"));
+    if (act != LM_ACT_SWIGLU && act != LM_ACT_GEGLU_ERF) return fail(LM_ERR_DTYPE, "act = %d is not known", act);
+    if (!gate) return fail(LM_ERR_NULL, "gate is NULL");
+    LM_TRY(check_r(gate->r));
+    LM_TRY(check_lora(gate, "gate", d, n, gate->r));
+    LM_TRY(check_lora(up, "up", d, n, gate->r));
+    LM_TRY(check_lora(down, "down", n, d, gate->r));
+    return LM_OK;
+}
+
+extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, const uint16_t* X,
+                                  const lm_lora* gate, const lm_lora* up, const lm_lora* down, uint16_t* y,
+                                  uint16_t* e_save, uint16_t* u_save, uint16_t* h_save, void* saved,
+                                  size_t saved_bytes, void* ws, size_t ws_bytes, lm_stream stream) {
+    LM_TRY(check_mlp_common(T, d, n, act, gate, up, down));
+    LM_TRY(need_ptr(X, "X"));
+    LM_TRY(need_ptr(y, "y"));
+    LM_TRY(need_ptr(e_save, "e_save"));
+    LM_TRY(need_ptr(u_save, "u_save"));
+    LM_TRY(need_ptr(h_save, "h_save"));
+    LM_TRY(need_ptr(saved, "saved"));
+    LM_TRY(need_ptr(ws, "ws"));
+    const int32_t r = gate->r;
+    const MlpPlan PL = plan_mlp(T, d, n, r);
+    if (saved_bytes < PL.saved_total)
+        return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
+    if (ws_bytes < PL.ws_total) return fail(LM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, PL.ws_total);
+    const size_t td = (size_t)T * d * 2, tn = (size_t)T * n * 2;
+    LM_TRY(check_alias({{y, td, "y"}, {e_save, tn, "e_save"}, {u_save, tn, "u_save"}, {h_save, tn, "h_save"},
+                        {saved, PL.saved_total, "saved"}, {ws, PL.ws_total, "ws"}},
+                       {{X, td, "X"}, wspan(gate, "gate.W"), wspan(up, "up.W"), wspan(down, "down.W"),
+                        {gate->A, (size_t)r * d * 2, "gate.A"}, {gate->B, (size_t)n * r * 2, "gate.B"},
+                        {up->A, (size_t)r * d * 2, "up.A"}, {up->B, (size_t)n * r * 2, "up.B"},
+                        {down->A, (size_t)r * n * 2, "down.A"}, {down->B, (size_t)d * r * 2, "down.B"}}));
+    if (T == 0) return LM_OK;
+    int sms = 0;
+    LM_TRY(ready(&sms));
+    cudaStream_t st = (cudaStream_t)stream;
+    const Dims& D = PL.D;
+    const int rp = D.rp;
+    int32_t* err = static_cast<int32_t*>(ws);
+    float* part = at<float>(ws, PL.part);
+    uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
+    uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
+    uint16_t* ha = at<uint16_t>(saved, PL.ha.rows_off);
+    uint16_t* haT = at<uint16_t>(saved, PL.ha.t_off);
+
+    {  // s*[X Ag^T | X Au^T]
+        Builder b(G_PART_KK);
+        add_rowproj_in(b, X, T, d, {gate->A, up->A}, D, part);
+        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(fin_rows(b, {FinRowJob{part, T * 2 * rp, 0, 2 * rp, rp, {gate->s, up->s, 0.f}, xa, xaT, D.ldT}}, T, st));
+    }
+    {  // e, u and h = act(e) * u; the rank-r terms enter the same accumulator
+        Builder b(G_GLU_FWD);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)n;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((n + 127) / 128);
+        P.n_step = 128;
+        P.out_col_step = 128;
+        P.act = act;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(X, T, d, d, 128);
+        S0.b_map[0] = b.map(gate->W.w, n, d, d, 128);
+        S0.b_map[1] = b.map(up->W.w, n, d, d, 128);
+        S0.b_rows = 128;
+        S0.kext = (int32_t)d;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(xa, T, 2 * rp, 2 * rp, 128);
+        S1.b_map[0] = b.map(gate->B, n, r, r, 128);
+        S1.b_map[1] = b.map(up->B, n, r, r, 128);
+        S1.b_xoff[1] = -rp;
+        S1.b_rows = 128;
+        S1.kext = 2 * rp;
+        S1.dual_split = rp;
+        P.out0 = e_save;
+        P.out1 = u_save;
+        P.out2 = h_save;
+        P.ld_out = n;
+        LM_TRY(b.launch(sms, err, st));
+    }
+    {  // s_d * h Ad^T
+        Builder b(G_PART_KK);
+        add_rowproj_in(b, h_save, T, n, {down->A}, D, part);
+        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(fin_rows(b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, ha, haT, D.ldT}}, T, st));
+    }
+    {  // y = h Wd^T + (s_d h Ad^T) Bd^T
+        Builder b(G_STORE_KK);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)d;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((d + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(h_save, T, n, n, 128);
+        S0.b_map[0] = b.map(down->W.w, d, n, n, 256);
+        S0.kext = (int32_t)n;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(ha, T, rp, rp, 128);
+        S1.b_map[0] = b.map(down->B, d, r, r, 256);
+        S1.kext = rp;
+        P.out0 = y;
+        P.ld_out = d;
+        LM_TRY(b.launch(sms, err, st));
+    }
+    return LM_OK;
+}
+
+extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, const uint16_t* X, const uint16_t* dY,
+                                  const uint16_t* e_save, const uint16_t* u_save, const uint16_t* h_save,
+                                  const void* saved, size_t saved_bytes, const lm_lora* gate, const lm_lora* up,
+                                  const lm_lora* down, uint16_t* dX, float* dA_gate, float* dB_gate, float* dA_up,
+                                  float* dB_up, float* dA_down, float* dB_down, void* ws, size_t ws_bytes,
+                                  lm_stream stream) {
+    LM_TRY(check_mlp_common(T, d, n, act, gate, up, down));
+    LM_TRY(need_ptr(X, "X"));
+    LM_TRY(need_ptr(dY, "dY"));
+    LM_TRY(need_ptr(e_save, "e_save"));
+    LM_TRY(need_ptr(u_save, "u_save"));
+    LM_TRY(need_ptr(h_save, "h_save"));
+    LM_TRY(need_ptr(saved, "saved"));
+    LM_TRY(need_ptr(dX, "dX"));
+    LM_TRY(need_ptr(dA_gate, "dA_gate"));
+    LM_TRY(need_ptr(dB_gate, "dB_gate"));
+    LM_TRY(need_ptr(dA_up, "dA_up"));
+    LM_TRY(need_ptr(dB_up, "dB_up"));
+    LM_TRY(need_ptr(dA_down, "dA_down"));
+    LM_TRY(need_ptr(dB_down, "dB_down"));
+    LM_TRY(need_ptr(ws, "ws"));
+    const int32_t r = gate->r;
+    const MlpPlan PL = plan_mlp(T, d, n, r);
+    if (saved_bytes < PL.saved_total)
+        return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
+    if (ws_bytes < PL.ws_total) return fail(LM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, PL.ws_total);
+    const size_t td = (size_t)T * d * 2, tn = (size_t)T * n * 2;
+    const size_t ad = (size_t)r * d * 4, an = (size_t)r * n * 4;
+    LM_TRY(check_alias({{dX, td, "dX"}, {dA_gate, ad, "dA_gate"}, {dB_gate, an, "dB_gate"}, {dA_up, ad, "dA_up"},
+                        {dB_up, an, "dB_up"}, {dA_down, an, "dA_down"}, {dB_down, ad, "dB_down"},
+                        {ws, PL.ws_total, "ws"}},
+                       {{X, td, "X"}, {dY, td, "dY"}, {e_save, tn, "e_save"}, {u_save, tn, "u_save"},
+                        {h_save, tn, "h_save"}, {saved, PL.saved_total, "saved"}, wspan(gate, "gate.W"),
+                        wspan(up, "up.W"), wspan(down, "down.W")}));
+    if (T == 0) {
+        // no tokens: every LoRA gradient is an empty sum
+        cudaStream_t st = (cudaStream_t)stream;
+        LM_CUDA(cudaMemsetAsync(dA_gate, 0, ad, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dA_up, 0, ad, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dB_down, 0, ad, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dB_gate, 0, an, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dB_up, 0, an, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dA_down, 0, an, st), "cudaMemsetAsync");
+        return LM_OK;
+    }
+    int sms = 0;
+    LM_TRY(ready(&sms));
+    cudaStream_t st = (cudaStream_t)stream;
+    const Dims& D = PL.D;
+    const int rp = D.rp;
+    int32_t* err = static_cast<int32_t*>(ws);
+    float* part = at<float>(ws, PL.part);
+    const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
+    const uint16_t* haT = at<uint16_t>(saved, PL.ha.t_off);
+    uint16_t* gd = at<uint16_t>(ws, PL.gd.rows_off);
+    uint16_t* gdT = at<uint16_t>(ws, PL.gd.t_off);
+    uint16_t* gg = at<uint16_t>(ws, PL.gg.rows_off);
+    uint16_t* ggT = at<uint16_t>(ws, PL.gg.t_off);
+    uint16_t* gu = at<uint16_t>(ws, PL.gu.rows_off);
+    uint16_t* guT = at<uint16_t>(ws, PL.gu.t_off);
+    uint16_t* de = at<uint16_t>(ws, PL.de);
+    uint16_t* du = at<uint16_t>(ws, PL.du);
+
+    {  // Gd = s_d dY Bd, formed once (feeds dh and dA_down)
+        Builder b(G_PART_KMN);
+        add_rowproj_out(b, dY, T, d, down->B, D, part);
+        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(fin_rows(b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st));
+    }
+    {  // dh = dY Wd + Gd Ad with the activation backward in the epilogue: de, du
+        Builder b(G_GLU_BWD);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)n;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((n + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
+        P.act = act;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(dY, T, d, d, 128);
+        S0.b_map[0] = b.map(down->W.w, d, n, n, 64);
+        S0.kext = (int32_t)d;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(gd, T, rp, rp, 128);
+        S1.b_map[0] = b.map(down->A, r, n, n, 64);
+        S1.kext = rp;
+        P.in0 = e_save;
+        P.in1 = u_save;
+        P.ld_in = n;
+        P.out0 = de;
+        P.out1 = du;
+        P.ld_out = n;
+        LM_TRY(b.launch(sms, err, st));
+    }
+    {  // Gg = s_g de Bg, Gu = s_u du Bu, formed once (feed dA and dX)
+        Builder b(G_PART_KMN);
+        float* part_u = part + (size_t)kMaxSplits * T * rp;
+        add_rowproj_out(b, de, T, n, gate->B, D, part);
+        add_rowproj_out(b, du, T, n, up->B, D, part_u);
+        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(fin_rows(b,
+                        {FinRowJob{part, T * rp, 0, rp, rp, {gate->s, 0.f, 0.f}, gg, ggT, D.ldT},
+                         FinRowJob{part_u, T * rp, 0, rp, rp, {up->s, 0.f, 0.f}, gu, guT, D.ldT}},
+                        T, st));
+    }
+    {  // the six LoRA gradients as column reductions over the tokens
+        Builder b(G_PART_MNK);
+        float* p0 = part;
+        float* p1 = p0 + (size_t)kMaxSplits * n * rp;   // dA_down  (C = n)
+        float* p2 = p1 + (size_t)kMaxSplits * d * rp;   // dB_down  (C = d)
+        float* p3 = p2 + (size_t)kMaxSplits * d * rp;   // dA_gate  (C = d)
+        float* p4 = p3 + (size_t)kMaxSplits * n * rp;   // dB_gate  (C = n)
+        float* p5 = p4 + (size_t)kMaxSplits * d * rp;   // dA_up    (C = d)
+        add_colreduce(b, h_save, T, n, gdT, D, p0);          // dA_down^T = h^T Gd
+        add_colreduce(b, dY, T, d, haT, D, p1);              // dB_down   = dY^T (s h Ad^T)
+        add_colreduce(b, X, T, d, ggT, D, p2);               // dA_gate^T = X^T Gg
+        add_colreduce(b, de, T, n, xaT, D, p3);              // dB_gate   = de^T (s X Ag^T)
+        add_colreduce(b, X, T, d, guT, D, p4);               // dA_up^T   = X^T Gu
+        add_colreduce(b, du, T, n, xaT + (size_t)rp * D.ldT, D, p5);  // dB_up = du^T (s X Au^T)
+        LM_TRY(b.launch(sms, err, st));
+        FinColJob js[6] = {
+            {p0, n * rp, n, 0, rp, r, 1, dA_down}, {p1, d * rp, d, 0, rp, r, 0, dB_down},
+            {p2, d * rp, d, 0, rp, r, 1, dA_gate}, {p3, n * rp, n, 0, rp, r, 0, dB_gate},
+            {p4, d * rp, d, 0, rp, r, 1, dA_up},   {p5, n * rp, n, 0, rp, r, 0, dB_up},
+        };
+        LM_TRY(fin_cols(b, js, 6, st));
+    }
+    {  // dX = de Wg + du Wu + Gg Ag + Gu Au
+        Builder b(G_STORE_KMN);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)d;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((d + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(de, T, n, n, 128);
+        S0.b_map[0] = b.map(gate->W.w, n, d, d, 64);
+        S0.kext = (int32_t)n;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(du, T, n, n, 128);
+        S1.b_map[0] = b.map(up->W.w, n, d, d, 64);
+        S1.kext = (int32_t)n;
+        Seg& S2 = seg(P, 2);
+        S2.a_map = b.map(gg, T, rp, rp, 128);
+        S2.b_map[0] = b.map(gate->A, r, d, d, 64);
+        S2.kext = rp;
+        Seg& S3 = seg(P, 3);
+        S3.a_map = b.map(gu, T, rp, rp, 128);
+        S3.b_map[0] = b.map(up->A, r, d, d, 64);
+        S3.kext = rp;
+        P.out0 = dX;
+        P.ld_out = d;
+        LM_TRY(b.launch(sms, err, st));
+    }
+    return LM_OK;
+}
+
+// ====================================================================== LoRA QKV
+extern "C" lm_status lora_qkv_saved_size(int64_t T, int32_t r, size_t* bytes) {
+    if (!bytes) return fail(LM_ERR_NULL, "bytes is NULL");
+    LM_TRY(check_T(T));
+    LM_TRY(check_r(r));
+    *bytes = plan_qkv(T, 32, 32, 32, 32, r).saved_total;
+    return LM_OK;
+}
+
+extern "C" lm_status lora_qkv_workspace_size(int64_t T, int64_t d, int64_t nq, int64_t nk, int64_t nv, int32_t r,
+                                             size_t* bytes) {
+    if (!bytes) return fail(LM_ERR_NULL, "bytes is NULL");
+    LM_TRY(check_T(T));
+    LM_TRY(check_dim(d, "d"));
+    LM_TRY(check_dim(nq, "nq"));
+    LM_TRY(check_dim(nk, "nk"));
+    LM_TRY(check_dim(nv, "nv"));
+    LM_TRY(check_r(r));
+    *bytes = plan_qkv(T, d, nq, nk, nv, r).ws_total;
+    return LM_OK;
+}
+
+static lm_status check_qkv_common(int64_t T, int64_t d, int64_t nq, int64_t nk, int64_t nv, const lm_lora* q,
+                                  const lm_lora* k, const lm_lora* v) {
+    LM_TRY(check_T(T));
+    LM_TRY(check_dim(d, "d"));
+    LM_TRY(check_dim(nq, "nq"));
+    LM_TRY(check_dim(nk, "nk"));
+    LM_TRY(check_dim(nv, "nv"));
+    if (!q) return fail(LM_ERR_NULL, "q is NULL");
+    LM_TRY(check_r(q->r));
+    LM_TRY(check_lora(q, "q", d, nq, q->r));
+    LM_TRY(check_lora(k, "k", d, nk, q->r));
+    LM_TRY(check_lora(v, "v", d, nv, q->r));
+    return LM_OK;
+}
+
+extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, int64_t nv, const uint16_t* X,
+                                  const lm_lora* q, const lm_lora* k, const lm_lora* v, uint16_t* Q, uint16_t* K,
+                                  uint16_t* V, void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                                  lm_stream stream) {
+    LM_TRY(check_qkv_common(T, d, nq, nk, nv, q, k, v));
+    LM_TRY(need_ptr(X, "X"));
+    LM_TRY(need_ptr(Q, "Q"));
+    LM_TRY(need_ptr(K, "K"));
+    LM_TRY(need_ptr(V, "V"));
+    LM_TRY(need_ptr(saved, "saved"));
+    LM_TRY(need_ptr(ws, "ws"));
+    const int32_t r = q->r;
+    const QkvPlan PL = plan_qkv(T, d, nq, nk, nv, r);
+    if (saved_bytes < PL.saved_total)
+        return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
+    if (ws_bytes < PL.ws_total) return fail(LM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, PL.ws_total);
+    LM_TRY(check_alias({{Q, (size_t)T * nq * 2, "Q"}, {K, (size_t)T * nk * 2, "K"}, {V, (size_t)T * nv * 2, "V"},
+                        {saved, PL.saved_total, "saved"}, {ws, PL.ws_total, "ws"}},
+                       {{X, (size_t)T * d * 2, "X"}, wspan(q, "q.W"), wspan(k, "k.W"), wspan(v, "v.W")}));
+    if (T == 0) return LM_OK;
+    int sms = 0;
+    LM_TRY(ready(&sms));
+    cudaStream_t st = (cudaStream_t)stream;
+    const Dims& D = PL.D;
+    const int rp = D.rp;
+    int32_t* err = static_cast<int32_t*>(ws);
+    float* part = at<float>(ws, PL.part);
+    uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
+    uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
+    {
+        Builder b(G_PART_KK);
+        add_rowproj_in(b, X, T, d, {q->A, k->A, v->A}, D, part);
+        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(fin_rows(b, {FinRowJob{part, T * 3 * rp, 0, 3 * rp, rp, {q->s, k->s, v->s}, xa, xaT, D.ldT}}, T, st));
+    }
+    {
+        Builder b(G_STORE_KK);
+        const int xmap = b.map(X, T, d, d, 128);
+        const int amap = b.map(xa, T, 3 * rp, 3 * rp, 128);
+        const lm_lora* Ls[3] = {q, k, v};
+        uint16_t* outs[3] = {Q, K, V};
+        const int64_t ns[3] = {nq, nk, nv};
+        for (int i = 0; i < 3; ++i) {
+            Prob& P = b.prob();
+            P.M = (int32_t)T;
+            P.N = (int32_t)ns[i];
+            P.bn = 256;
+            P.tiles_n = (int32_t)((ns[i] + 255) / 256);
+            P.n_step = 256;
+            P.out_col_step = 256;
+            Seg& S0 = seg(P, 0);
+            S0.a_map = xmap;
+            S0.b_map[0] = b.map(Ls[i]->W.w, ns[i], d, d, 256);
+            S0.kext = (int32_t)d;
+            Seg& S1 = seg(P, 1);
+            S1.a_map = amap;
+            S1.a_xoff = i * rp;
+            S1.b_map[0] = b.map(Ls[i]->B, ns[i], r, r, 256);
+            S1.kext = rp;
+            P.out0 = outs[i];
+            P.ld_out = ns[i];
+        }
+        LM_TRY(b.launch(sms, err, st));
+    }
+    return LM_OK;
+}
+
+extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, int64_t nv, const uint16_t* X,
+                                  const uint16_t* dQ, const uint16_t* dK, const uint16_t* dV, const void* saved,
+                                  size_t saved_bytes, const lm_lora* q, const lm_lora* k, const lm_lora* v,
+                                  uint16_t* dX, float* dA_q, float* dB_q, float* dA_k, float* dB_k, float* dA_v,
+                                  float* dB_v, void* ws, size_t ws_bytes, lm_stream stream) {
+    LM_TRY(check_qkv_common(T, d, nq, nk, nv, q, k, v));
+    LM_TRY(need_ptr(X, "X"));
+    LM_TRY(need_ptr(dQ, "dQ"));
+    LM_TRY(need_ptr(dK, "dK"));
+    LM_TRY(need_ptr(dV, "dV"));
+    LM_TRY(need_ptr(saved, "saved"));
+    LM_TRY(need_ptr(dX, "dX"));
+    LM_TRY(need_ptr(dA_q, "dA_q"));
+    LM_TRY(need_ptr(dB_q, "dB_q"));
+    LM_TRY(need_ptr(dA_k, "dA_k"));
+    LM_TRY(need_ptr(dB_k, "dB_k"));
+    LM_TRY(need_ptr(dA_v, "dA_v"));
+    LM_TRY(need_ptr(dB_v, "dB_v"));
+    LM_TRY(need_ptr(ws, "ws"));
+    const int32_t r = q->r;
+    const QkvPlan PL = plan_qkv(T, d, nq, nk, nv, r);
+    if (saved_bytes < PL.saved_total)
+        return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
+    if (ws_bytes < PL.ws_total) return fail(LM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, PL.ws_total);
+    const size_t ad = (size_t)r * d * 4;
+    LM_TRY(check_alias({{dX, (size_t)T * d * 2, "dX"}, {dA_q, ad, "dA_q"}, {dA_k, ad, "dA_k"}, {dA_v, ad, "dA_v"},
+                        {dB_q, (size_t)nq * r * 4, "dB_q"}, {dB_k, (size_t)nk * r * 4, "dB_k"},
+                        {dB_v, (size_t)nv * r * 4, "dB_v"}, {ws, PL.ws_total, "ws"}},
+                       {{X, (size_t)T * d * 2, "X"}, {dQ, (size_t)T * nq * 2, "dQ"}, {dK, (size_t)T * nk * 2, "dK"},
+                        {dV, (size_t)T * nv * 2, "dV"}, {saved, PL.saved_total, "saved"}, wspan(q, "q.W"),
+                        wspan(k, "k.W"), wspan(v, "v.W")}));
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T == 0) {
+        LM_CUDA(cudaMemsetAsync(dA_q, 0, ad, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dA_k, 0, ad, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dA_v, 0, ad, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dB_q, 0, (size_t)nq * r * 4, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dB_k, 0, (size_t)nk * r * 4, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dB_v, 0, (size_t)nv * r * 4, st), "cudaMemsetAsync");
+        return LM_OK;
+    }
+    int sms = 0;
+    LM_TRY(ready(&sms));
+    const Dims& D = PL.D;
+    const int rp = D.rp;
+    int32_t* err = static_cast<int32_t*>(ws);
+    float* part = at<float>(ws, PL.part);
+    const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
+    const lm_lora* Ls[3] = {q, k, v};
+    const uint16_t* dOut[3] = {dQ, dK, dV};
+    const int64_t ns[3] = {nq, nk, nv};
+    uint16_t* g[3];
+    uint16_t* gT[3];
+    for (int i = 0; i < 3; ++i) {
+        g[i] = at<uint16_t>(ws, PL.g[i].rows_off);
+        gT[i] = at<uint16_t>(ws, PL.g[i].t_off);
+    }
+    {  // G_x = s_x dOut_x B_x, formed once per projection
+        Builder b(G_PART_KMN);
+        float* parts[3];
+        for (int i = 0; i < 3; ++i) {
+            parts[i] = part + (size_t)i * kMaxSplits * T * rp;
+            add_rowproj_out(b, dOut[i], T, ns[i], Ls[i]->B, D, parts[i]);
+        }
+        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(fin_rows(b,
+                        {FinRowJob{parts[0], T * rp, 0, rp, rp, {q->s, 0.f, 0.f}, g[0], gT[0], D.ldT},
+                         FinRowJob{parts[1], T * rp, 0, rp, rp, {k->s, 0.f, 0.f}, g[1], gT[1], D.ldT},
+                         FinRowJob{parts[2], T * rp, 0, rp, rp, {v->s, 0.f, 0.f}, g[2], gT[2], D.ldT}},
+                        T, st));
+    }
+    {  // dA_x^T = X^T G_x,  dB_x = dOut_x^T (s X A_x^T)
+        Builder b(G_PART_MNK);
+        FinColJob js[6];
+        float* p = part;
+        float* dAs[3] = {dA_q, dA_k, dA_v};
+        float* dBs[3] = {dB_q, dB_k, dB_v};
+        for (int i = 0; i < 3; ++i) {
+            add_colreduce(b, X, T, d, gT[i], D, p);
+            js[2 * i] = FinColJob{p, d * rp, d, 0, rp, r, 1, dAs[i]};
+            p += (size_t)kMaxSplits * d * rp;
+            add_colreduce(b, dOut[i], T, ns[i], xaT + (size_t)i * rp * D.ldT, D, p);
+            js[2 * i + 1] = FinColJob{p, ns[i] * rp, ns[i], 0, rp, r, 0, dBs[i]};
+            p += (size_t)kMaxSplits * ns[i] * rp;
+        }
+        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(fin_cols(b, js, 6, st));
+    }
+    {  // dX = sum_x dOut_x W_x + G_x A_x
+        Builder b(G_STORE_KMN);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)d;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((d + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
+        for (int i = 0; i < 3; ++i) {
+            Seg& S = seg(P, i);
+            S.a_map = b.map(dOut[i], T, ns[i], ns[i], 128);
+            S.b_map[0] = b.map(Ls[i]->W.w, ns[i], d, d, 64);
+            S.kext = (int32_t)ns[i];
+        }
+        for (int i = 0; i < 3; ++i) {
+            Seg& S = seg(P, 3 + i);
+            S.a_map = b.map(g[i], T, rp, rp, 128);
+            S.b_map[0] = b.map(Ls[i]->A, r, d, d, 64);
+            S.kext = rp;
+        }
+        P.out0 = dX;
+        P.ld_out = d;
+        LM_TRY(b.launch(sms, err, st));
+    }
+    return LM_OK;
+}
+
+// ====================================================================== LoRA O
+extern "C" lm_status lora_o_saved_size(int64_t T, int32_t r, size_t* bytes) {
+    if (!bytes) return fail(LM_ERR_NULL, "bytes is NULL");
+    LM_TRY(check_T(T));
+    LM_TRY(check_r(r));
+    *bytes = plan_o(T, 32, 32, r).saved_total;
+    return LM_OK;
+}
+
+extern "C" lm_status lora_o_workspace_size(int64_t T, int64_t d_in, int64_t d_out, int32_t r, size_t* bytes) {
+    if (!bytes) return fail(LM_ERR_NULL, "bytes is NULL");
+    LM_TRY(check_T(T));
+    LM_TRY(check_dim(d_in, "d_in"));
+    LM_TRY(check_dim(d_out, "d_out"));
+    LM_TRY(check_r(r));
+    *bytes = plan_o(T, d_in, d_out, r).ws_total;
+    return LM_OK;
+}
+
+static lm_status check_o_common(int64_t T, int64_t d_in, int64_t d_out, const lm_lora* o) {
+    LM_TRY(check_T(T));
+    LM_TRY(check_dim(d_in, "d_in"));
+    LM_TRY(check_dim(d_out, "d_out"));
+    if (!o) return fail(LM_ERR_NULL, "o is NULL");
+    LM_TRY(check_r(o->r));
+    LM_TRY(check_lora(o, "o", d_in, d_out, o->r));
+    return LM_OK;
+}
+
+extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const uint16_t* X, const lm_lora* o,
+                                uint16_t* Y, void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                                lm_stream stream) {
+    LM_TRY(check_o_common(T, d_in, d_out, o));
+    LM_TRY(need_ptr(X, "X"));
+    LM_TRY(need_ptr(Y, "Y"));
+    LM_TRY(need_ptr(saved, "saved"));
+    LM_TRY(need_ptr(ws, "ws"));
+    const int32_t r = o->r;
+    const OPlan PL = plan_o(T, d_in, d_out, r);
+    if (saved_bytes < PL.saved_total)
+        return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
+    if (ws_bytes < PL.ws_total) return fail(LM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, PL.ws_total);
+    LM_TRY(check_alias({{Y, (size_t)T * d_out * 2, "Y"}, {saved, PL.saved_total, "saved"}, {ws, PL.ws_total, "ws"}},
+                       {{X, (size_t)T * d_in * 2, "X"}, wspan(o, "o.W")}));
+    if (T == 0) return LM_OK;
+    int sms = 0;
+    LM_TRY(ready(&sms));
+    cudaStream_t st = (cudaStream_t)stream;
+    const Dims& D = PL.D;
+    const int rp = D.rp;
+    int32_t* err = static_cast<int32_t*>(ws);
+    float* part = at<float>(ws, PL.part);
+    uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
+    uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
+    {
+        Builder b(G_PART_KK);
+        add_rowproj_in(b, X, T, d_in, {o->A}, D, part);
+        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(fin_rows(b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st));
+    }
+    {
+        Builder b(G_STORE_KK);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)d_out;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((d_out + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(X, T, d_in, d_in, 128);
+        S0.b_map[0] = b.map(o->W.w, d_out, d_in, d_in, 256);
+        S0.kext = (int32_t)d_in;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(xa, T, rp, rp, 128);
+        S1.b_map[0] = b.map(o->B, d_out, r, r, 256);
+        S1.kext = rp;
+        P.out0 = Y;
+        P.ld_out = d_out;
+        LM_TRY(b.launch(sms, err, st));
+    }
+    return LM_OK;
+}
+
+extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const uint16_t* X, const uint16_t* dY,
+                                const void* saved, size_t saved_bytes, const lm_lora* o, uint16_t* dX, float* dA,
+                                float* dB, void* ws, size_t ws_bytes, lm_stream stream) {
+    LM_TRY(check_o_common(T, d_in, d_out, o));
+    LM_TRY(need_ptr(X, "X"));
+    LM_TRY(need_ptr(dY, "dY"));
+    LM_TRY(need_ptr(saved, "saved"));
+    LM_TRY(need_ptr(dX, "dX"));
+    LM_TRY(need_ptr(dA, "dA"));
+    LM_TRY(need_ptr(dB, "dB"));
+    LM_TRY(need_ptr(ws, "ws"));
+    const int32_t r = o->r;
+    const OPlan PL = plan_o(T, d_in, d_out, r);
+    if (saved_bytes < PL.saved_total)
+        return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
+    if (ws_bytes < PL.ws_total) return fail(LM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, PL.ws_total);
+    LM_TRY(check_alias({{dX, (size_t)T * d_in * 2, "dX"}, {dA, (size_t)r * d_in * 4, "dA"},
+                        {dB, (size_t)d_out * r * 4, "dB"}, {ws, PL.ws_total, "ws"}},
+                       {{X, (size_t)T * d_in * 2, "X"}, {dY, (size_t)T * d_out * 2, "dY"},
+                        {saved, PL.saved_total, "saved"}, wspan(o, "o.W")}));
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T == 0) {
+        LM_CUDA(cudaMemsetAsync(dA, 0, (size_t)r * d_in * 4, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dB, 0, (size_t)d_out * r * 4, st), "cudaMemsetAsync");
+        return LM_OK;
+    }
+    int sms = 0;
+    LM_TRY(ready(&sms));
+    const Dims& D = PL.D;
+    const int rp = D.rp;
+    int32_t* err = static_cast<int32_t*>(ws);
+    float* part = at<float>(ws, PL.part);
+    const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
+    uint16_t* g = at<uint16_t>(ws, PL.g.rows_off);
+    uint16_t* gT = at<uint16_t>(ws, PL.g.t_off);
+    {  // G = s dY B, formed once (feeds dA and dX)
+        Builder b(G_PART_KMN);
+        add_rowproj_out(b, dY, T, d_out, o->B, D, part);
+        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(fin_rows(b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, g, gT, D.ldT}}, T, st));
+    }
+    {  // dA^T = X^T G, dB = dY^T (s X A^T)
+        Builder b(G_PART_MNK);
+        float* p0 = part;
+        float* p1 = p0 + (size_t)kMaxSplits * d_in * rp;
+        add_colreduce(b, X, T, d_in, gT, D, p0);
+        add_colreduce(b, dY, T, d_out, xaT, D, p1);
+        LM_TRY(b.launch(sms, err, st));
+        FinColJob js[2] = {{p0, d_in * rp, d_in, 0, rp, r, 1, dA}, {p1, d_out * rp, d_out, 0, rp, r, 0, dB}};
+        LM_TRY(fin_cols(b, js, 2, st));
+    }
+    {  // dX = dY W + G A
+        Builder b(G_STORE_KMN);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)d_in;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((d_in + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(dY, T, d_out, d_out, 128);
+        S0.b_map[0] = b.map(o->W.w, d_out, d_in, d_in, 64);
+        S0.kext = (int32_t)d_out;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(g, T, rp, rp, 128);
+        S1.b_map[0] = b.map(o->A, r, d_in, d_in, 64);
+        S1.kext = rp;
+        P.out0 = dX;
+        P.ld_out = d_in;
+        LM_TRY(b.launch(sms, err, st));
+    }
+    return LM_OK;
+}
+
+// ====================================================================== NF4
+extern "C" lm_status nf4_pack(const uint16_t* W, int64_t numel, uint8_t* codes, int8_t* absmax_q, float* group_scale,
+                              lm_stream stream) {
+    if (numel < 0 || numel % 16384 != 0)
+        return fail(LM_ERR_SHAPE, "numel = %lld must be a non-negative multiple of 64*256", (long long)numel);
+    LM_TRY(need_ptr(W, "W"));
+    LM_TRY(need_ptr(codes, "codes"));
+    LM_TRY(need_ptr(absmax_q, "absmax_q"));
+    LM_TRY(need_ptr(group_scale, "group_scale"));
+    LM_TRY(check_alias({{codes, (size_t)numel / 2, "codes"}, {absmax_q, (size_t)numel / 64, "absmax_q"},
+                        {group_scale, (size_t)numel / 16384 * 4, "group_scale"}},
+                       {{W, (size_t)numel * 2, "W"}}));
+    if (numel == 0) return LM_OK;
+    int sms = 0;
+    LM_TRY(device_sms(&sms));
+    const cudaError_t e = launch_nf4_pack(W, numel, codes, absmax_q, group_scale, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "nf4_pack launch");
+    return LM_OK;
+}
+
+extern "C" lm_status nf4_dequant(const uint8_t* codes, const int8_t* absmax_q, const float* group_scale, int64_t numel,
+                                 int32_t out_dtype, void* out, lm_stream stream) {
+    if (numel < 0 || numel % 16384 != 0)
+        return fail(LM_ERR_SHAPE, "numel = %lld must be a non-negative multiple of 64*256", (long long)numel);
+    if (out_dtype != LM_OUT_F32 && out_dtype != LM_OUT_BF16)
+        return fail(LM_ERR_DTYPE, "out_dtype = %d is not known", out_dtype);
+    LM_TRY(need_ptr(codes, "codes"));
+    LM_TRY(need_ptr(absmax_q, "absmax_q"));
+    LM_TRY(need_ptr(group_scale, "group_scale"));
+    LM_TRY(need_ptr(out, "out"));
+    const size_t ob = (size_t)numel * (out_dtype == LM_OUT_F32 ? 4 : 2);
+    LM_TRY(check_alias({{out, ob, "out"}}, {{codes, (size_t)numel / 2, "codes"},
+                                            {absmax_q, (size_t)numel / 64, "absmax_q"},
+                                            {group_scale, (size_t)numel / 16384 * 4, "group_scale"}}));
+    if (numel == 0) return LM_OK;
+    int sms = 0;
+    LM_TRY(device_sms(&sms));
+    const cudaError_t e =
+        launch_nf4_dequant(codes, absmax_q, group_scale, numel, out_dtype == LM_OUT_BF16, out, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "nf4_dequant launch");
+    return LM_OK;
+}

@@ -1,0 +1,249 @@
+// Memory-bound helper kernels: finalisation of split-K partials of the rank-r products, and
+// NF4 pack / dequantise ("loralei" README, QLoRA section: NF4 with 64-element blocks and
+// block scales double-quantised per 256 blocks).
+#include <cmath>
+
+#include "lm_internal.h"
+
+namespace lm {
+
+// ------------------------------------------------------------------ split-K finalisation
+struct FinRowJobs {
+    FinRowJob j[3];
+};
+
+__global__ void __launch_bounds__(256) fin_rowproj_kernel(FinRowJobs jobs, int64_t T) {
+    const FinRowJob& J = jobs.j[blockIdx.y];
+    const int64_t total = (int64_t)J.ncols * T;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int col = (int)(idx / T);
+        const int64_t t = idx - (int64_t)col * T;
+        const float* src = J.part + t * J.ncols + col;
+        float acc = 0.0f;
+        for (int ks = 0; ks < J.splits; ++ks) acc += src[(int64_t)ks * J.split_stride];
+        const float v = acc * J.s[col / J.group];
+        const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        const uint16_t bits = *reinterpret_cast<const uint16_t*>(&b);
+        J.out[t * J.ncols + col] = bits;
+        J.outT[(int64_t)col * J.ldT + t] = bits;
+    }
+}
+
+cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cudaStream_t st) {
+    FinRowJobs js{};
+    int64_t most = 0;
+    for (int i = 0; i < njobs; ++i) {
+        js.j[i] = jobs[i];
+        most = std::max<int64_t>(most, (int64_t)jobs[i].ncols * T);
+    }
+    const int threads = 256;
+    const int64_t blocks = std::min<int64_t>((most + threads - 1) / threads, 4096);
+    fin_rowproj_kernel<<<dim3((unsigned)std::max<int64_t>(blocks, 1), njobs), threads, 0, st>>>(js, T);
+    return cudaGetLastError();
+}
+
+struct FinColJobs {
+    FinColJob j[6];
+};
+
+__global__ void __launch_bounds__(256) fin_colreduce_kernel(FinColJobs jobs) {
+    const FinColJob& J = jobs.j[blockIdx.y];
+    const int64_t total = J.C * J.r;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        int64_t c;
+        int j;
+        if (J.transposed) {  // out[j][c], consecutive threads -> consecutive c
+            j = (int)(idx / J.C);
+            c = idx - (int64_t)j * J.C;
+        } else {             // out[c][j]
+            c = idx / J.r;
+            j = (int)(idx - c * J.r);
+        }
+        const float* src = J.part + c * J.rp + j;
+        float acc = 0.0f;
+        for (int ks = 0; ks < J.splits; ++ks) acc += src[(int64_t)ks * J.split_stride];
+        J.out[idx] = acc;
+    }
+}
+
+cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t st) {
+    FinColJobs js{};
+    int64_t most = 0;
+    for (int i = 0; i < njobs; ++i) {
+        js.j[i] = jobs[i];
+        most = std::max<int64_t>(most, jobs[i].C * jobs[i].r);
+    }
+    const int threads = 256;
+    const int64_t blocks = std::min<int64_t>((most + threads - 1) / threads, 4096);
+    fin_colreduce_kernel<<<dim3((unsigned)std::max<int64_t>(blocks, 1), njobs), threads, 0, st>>>(js);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ NF4
+// The 16 NormalFloat-4 values as printed in the QLoRA paper (Dettmers et al. 2023, appendix
+// "NormalFloat 4-bit data type"); every literal is an exact fp32 value.
+static const float kNf4Code[16] = {
+    -1.0f,
+    -0.6961928009986877f,
+    -0.5250730514526367f,
+    -0.39491748809814453f,
+    -0.28444138169288635f,
+    -0.18477343022823334f,
+    -0.09105003625154495f,
+    0.0f,
+    0.07958029955625534f,
+    0.16093020141124725f,
+    0.24611230194568634f,
+    0.33791524171829224f,
+    0.44070982933044434f,
+    0.5626170039176941f,
+    0.7229568362236023f,
+    1.0f,
+};
+
+void nf4_codebook_host(float* out16) {
+    for (int i = 0; i < 16; ++i) out16[i] = kNf4Code[i];
+}
+
+struct Nf4Tables {
+    float code[16];
+    // thr[i] = the smallest fp32 strictly above the exact midpoint of code[i] and code[i+1]:
+    // for an fp32 v, (v >= thr[i]) <=> (v is strictly closer to code[i+1] than to code[i]),
+    // so an exact tie stays with the lower index.
+    float thr[15];
+};
+
+static Nf4Tables make_tables() {
+    Nf4Tables t;
+    for (int i = 0; i < 16; ++i) t.code[i] = kNf4Code[i];
+    for (int i = 0; i < 15; ++i) {
+        const double mid = 0.5 * ((double)kNf4Code[i] + (double)kNf4Code[i + 1]);  // exact
+        float f = (float)mid;
+        if ((double)f <= mid) f = std::nextafter(f, INFINITY);
+        t.thr[i] = f;
+    }
+    return t;
+}
+
+// One CTA per group of 256 blocks (16384 elements); thread t quantises block t.
+__global__ void __launch_bounds__(256) nf4_pack_kernel(const uint16_t* __restrict__ W,
+                                                       uint8_t* __restrict__ codes,
+                                                       int8_t* __restrict__ absmax_q,
+                                                       float* __restrict__ scale, Nf4Tables tb) {
+    __shared__ float wmax[8];
+    const int64_t g = blockIdx.x;
+    const int t = threadIdx.x;
+    const int64_t b = g * 256 + t;
+    const uint4* src = reinterpret_cast<const uint4*>(W + b * 64);
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 v = __ldg(src + i);
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(w[i])), fabsf(bf16hi(w[i]))));
+    float m = amax;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((t & 31) == 0) wmax[t >> 5] = m;
+    __syncthreads();
+    float gmax = wmax[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) gmax = fmaxf(gmax, wmax[i]);
+    const float c = __fdiv_rn(gmax, 127.0f);
+    if (t == 0) scale[g] = c;
+    int q = 0;
+    if (c > 0.0f) {
+        q = (int)rintf(__fdiv_rn(amax, c));
+        q = min(max(q, 0), 127);
+    }
+    absmax_q[b] = (int8_t)q;
+
+    uint32_t packed[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) packed[i] = 0;
+#pragma unroll
+    for (int e = 0; e < 64; ++e) {
+        const uint32_t word = w[e >> 1];
+        const float x = (e & 1) ? bf16hi(word) : bf16lo(word);
+        const float v = amax > 0.0f ? __fdiv_rn(x, amax) : 0.0f;
+        uint32_t idx = 0;
+#pragma unroll
+        for (int k = 0; k < 15; ++k) idx += (v >= tb.thr[k]) ? 1u : 0u;
+        // element 2i -> high nibble of byte i; byte i sits at bits 8*(i%4) of word i/4
+        const int byte = e >> 1;
+        const uint32_t nib = (e & 1) ? idx : (idx << 4);
+        packed[byte >> 2] |= nib << (8 * (byte & 3));
+    }
+    uint4* dst = reinterpret_cast<uint4*>(codes + b * 32);
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+}
+
+cudaError_t launch_nf4_pack(const uint16_t* W, int64_t numel, uint8_t* codes, int8_t* absmax_q,
+                            float* scale, cudaStream_t st) {
+    static const Nf4Tables tb = make_tables();
+    const int64_t groups = numel / 16384;
+    if (groups == 0) return cudaSuccess;
+    nf4_pack_kernel<<<(unsigned)groups, 256, 0, st>>>(W, codes, absmax_q, scale, tb);
+    return cudaGetLastError();
+}
+
+// Each thread decodes 8 elements (4 code bytes).
+__global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint32_t* __restrict__ codes,
+                                                          const int8_t* __restrict__ absmax_q,
+                                                          const float* __restrict__ scale,
+                                                          int64_t n8, int bf16_out, void* out,
+                                                          Nf4Tables tb) {
+    __shared__ float cb[16];
+    if (threadIdx.x < 16) cb[threadIdx.x] = tb.code[threadIdx.x];
+    __syncthreads();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t c4 = __ldg(codes + i);
+        const int64_t blk = i >> 3;  // 8 elements per thread, 64 per block
+        const float amax = __fmul_rn((float)__ldg(absmax_q + blk), __ldg(scale + (blk >> 8)));
+        float w[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t byte = (c4 >> (8 * k)) & 0xFFu;
+            w[2 * k] = __fmul_rn(cb[byte >> 4], amax);
+            w[2 * k + 1] = __fmul_rn(cb[byte & 15u], amax);
+        }
+        if (bf16_out) {
+            uint4 v;
+            v.x = pack_bf16x2(w[0], w[1]);
+            v.y = pack_bf16x2(w[2], w[3]);
+            v.z = pack_bf16x2(w[4], w[5]);
+            v.w = pack_bf16x2(w[6], w[7]);
+            reinterpret_cast<uint4*>(out)[i] = v;
+        } else {
+            float4* o = reinterpret_cast<float4*>(out) + 2 * i;
+            o[0] = make_float4(w[0], w[1], w[2], w[3]);
+            o[1] = make_float4(w[4], w[5], w[6], w[7]);
+        }
+    }
+}
+
+cudaError_t launch_nf4_dequant(const uint8_t* codes, const int8_t* absmax_q, const float* scale,
+                               int64_t numel, bool bf16_out, void* out, cudaStream_t st) {
+    static const Nf4Tables tb = make_tables();
+    const int64_t n8 = numel / 8;
+    if (n8 == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, (int64_t)sms * 8);
+    nf4_dequant_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(codes), absmax_q,
+                                                          scale, n8, bf16_out ? 1 : 0, out, tb);
+    return cudaGetLastError();
+}
+
+}  // namespace lm

@@ -1,0 +1,502 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a with segmented K.
+//
+// One work unit computes a 128 x bn fp32 accumulator tile in TMEM:
+//     D[m, j] = sum over segments  sum_k  A_seg[m, k] * B_seg[j, k]
+// where each segment has its own TMA tensor maps.  The rank-r LoRA term of a projection is
+// one more segment of the same accumulator (A = s * X A^T, B = LoRA B), so the low-rank
+// product is added by extra K steps of the MMA instead of a separate matmul.
+//
+// Roles (320 threads):
+//   warp 0 lane 0  TMA producer: fills a ring of shared-memory stages (A tile 128 x 64,
+//                  B tile bn x 64, both 128-byte swizzled, K-major or MN-major).
+//   warp 1 lane 0  MMA issuer: tcgen05.mma kind::f16 (bf16 in, fp32 accumulate), commits
+//                  each stage back to the producer and each finished tile to the epilogue.
+//   warps 2..9     epilogue: TMEM -> registers (tcgen05.ld) -> fused epilogue -> global.
+// Two TMEM accumulators alternate so the epilogue of one tile overlaps the mainloop of the
+// next.  Every wait is bounded: on timeout the kernel records an error and returns.
+#pragma once
+
+#include "lm_ptx.cuh"
+
+namespace lm {
+
+enum : int { EPI_STORE = 0, EPI_GLU_FWD = 1, EPI_GLU_BWD = 2, EPI_PARTIAL = 3 };
+enum : int { ACT_SWIGLU = 0, ACT_GEGLU = 1 };
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kMaxMaps = 24;
+constexpr int kMaxProbs = 6;
+constexpr int kMaxSegs = 6;
+constexpr int kNumEpiWarps = 8;
+constexpr int kNumThreads = 64 + 32 * kNumEpiWarps;
+constexpr int kErrTimeout = 8;  // == LM_ERR_TIMEOUT
+
+// One K segment of a problem.
+struct Seg {
+    int32_t a_map;        // tensor map of A (K-major: box 64 x 128; MN-major: box 64 x 64)
+    int32_t b_map[3];     // B tensor maps; -1 = unused.  MN-major B uses b_map[0] only.
+    int32_t b_xoff[3];    // K-major B: added to the K coordinate of b_map[i]
+    int32_t b_rows;       // K-major B: block i lands at smem row i * b_rows
+    int32_t kext;         // K extent of the segment (elements)
+    int32_t dual_split;   // > 0: K steps with k < dual_split use B block 0 and the first bn/2
+                          // accumulator columns, the others B block 1 and the second half
+    int32_t a_xoff;       // added to the K coordinate of A
+};
+
+struct Prob {
+    int32_t M, N;               // output rows; output columns (per half for GLU_FWD)
+    int32_t tiles_m, tiles_n;
+    int32_t splits, kb_per_split;  // split-K (single-segment problems only)
+    int32_t unit_begin;
+    int32_t nseg;
+    int32_t bn;                 // accumulator columns per tile (multiple of 16, <= BN_MAX)
+    int32_t n_step;             // B rows (K-major) / B columns (MN-major) per N tile
+    int32_t out_col_step;       // output columns per N tile
+    int32_t act;
+    Seg seg[kMaxSegs];
+    void* out0;
+    void* out1;
+    void* out2;
+    const void* in0;
+    const void* in1;
+    int64_t ld_out, ld_in;      // elements
+    int64_t split_stride;       // PARTIAL: elements between split slices
+};
+
+struct Params {  // CUtensorMap members carry their own 128-byte alignment
+    CUtensorMap maps[kMaxMaps];
+    uint32_t map_bytes[kMaxMaps];   // bytes one box of the map delivers
+    int32_t map_w[kMaxMaps];        // inner (K or MN) extent of the map, elements
+    Prob prob[kMaxProbs];
+    int32_t nprob;
+    int32_t total_units;
+    int32_t* err;
+};
+
+template <int BN_MAX, bool A_MN, bool B_MN>
+struct GemmCfg {
+    static constexpr int A_BYTES = kBM * kBK * 2;
+    static constexpr int B_BYTES = (BN_MAX < 64 ? 64 : BN_MAX) * kBK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
+    static constexpr int TMEM_COLS = 2 * BN_MAX < 32 ? 32 : 2 * BN_MAX;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+    static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns must be a power of two");
+    static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
+};
+
+struct Unit {
+    int pi, mb, nb, ks;
+};
+
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+    Unit r;
+    int pi = 0;
+    while (pi + 1 < p.nprob && u >= p.prob[pi + 1].unit_begin) ++pi;
+    const Prob& P = p.prob[pi];
+    int local = u - P.unit_begin;
+    r.pi = pi;
+    r.ks = local % P.splits;
+    local /= P.splits;
+    // rasterise in groups of 16 M tiles so concurrently running tiles share B panels
+    const int GM = 16;
+    const int per_group = GM * P.tiles_n;
+    const int g = local / per_group, w = local % per_group;
+    const int gm = min(GM, P.tiles_m - g * GM);
+    r.mb = g * GM + w % gm;
+    r.nb = w / gm;
+    return r;
+}
+
+__device__ __forceinline__ void record_error(const Params& p, int code, int where) {
+    if (p.err) {
+        atomicExch(p.err, code);
+        p.err[1] = where;
+        p.err[2] = blockIdx.x;
+    }
+}
+
+// ---------------------------------------------------------------- activations
+__device__ __forceinline__ float act_fwd(int act, float x) {
+    if (act == ACT_SWIGLU) return x / (1.0f + __expf(-x));
+    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+// returns act(x) and act'(x)
+__device__ __forceinline__ void act_fwd_bwd(int act, float x, float& f, float& df) {
+    if (act == ACT_SWIGLU) {
+        const float sg = 1.0f / (1.0f + __expf(-x));
+        f = x * sg;
+        df = sg * (1.0f + x * (1.0f - sg));
+    } else {
+        const float cdf = 0.5f * (1.0f + erff(x * 0.70710678118654752f));
+        const float pdf = 0.39894228040143268f * __expf(-0.5f * x * x);
+        f = x * cdf;
+        df = cdf + x * pdf;
+    }
+}
+
+// ---------------------------------------------------------------- epilogues
+template <int BN_MAX, int EPI>
+__device__ __forceinline__ void epilogue_tile(const Prob& P, const Unit& U, uint32_t tacc, int hh,
+                                              int64_t m, bool mvalid) {
+    if constexpr (EPI == EPI_STORE) {
+        const int half = P.bn >> 1;
+#pragma unroll 1
+        for (int c = 0; c < half; c += 32) {
+            const int col = hh * half + c;
+            uint32_t a[16], b[16];
+            tmem_ld_x16(tacc + col, a);
+            tmem_ld_x16(tacc + col + 16, b);
+            tmem_ld_wait32(a, b);
+            const int64_t gcol = (int64_t)U.nb * P.out_col_step + col;
+            if (mvalid && gcol < P.N) {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out0) + m * P.ld_out + gcol);
+                uint4 v0, v1, v2, v3;
+                v0.x = pack_bf16x2(__uint_as_float(a[0]), __uint_as_float(a[1]));
+                v0.y = pack_bf16x2(__uint_as_float(a[2]), __uint_as_float(a[3]));
+                v0.z = pack_bf16x2(__uint_as_float(a[4]), __uint_as_float(a[5]));
+                v0.w = pack_bf16x2(__uint_as_float(a[6]), __uint_as_float(a[7]));
+                v1.x = pack_bf16x2(__uint_as_float(a[8]), __uint_as_float(a[9]));
+                v1.y = pack_bf16x2(__uint_as_float(a[10]), __uint_as_float(a[11]));
+                v1.z = pack_bf16x2(__uint_as_float(a[12]), __uint_as_float(a[13]));
+                v1.w = pack_bf16x2(__uint_as_float(a[14]), __uint_as_float(a[15]));
+                v2.x = pack_bf16x2(__uint_as_float(b[0]), __uint_as_float(b[1]));
+                v2.y = pack_bf16x2(__uint_as_float(b[2]), __uint_as_float(b[3]));
+                v2.z = pack_bf16x2(__uint_as_float(b[4]), __uint_as_float(b[5]));
+                v2.w = pack_bf16x2(__uint_as_float(b[6]), __uint_as_float(b[7]));
+                v3.x = pack_bf16x2(__uint_as_float(b[8]), __uint_as_float(b[9]));
+                v3.y = pack_bf16x2(__uint_as_float(b[10]), __uint_as_float(b[11]));
+                v3.z = pack_bf16x2(__uint_as_float(b[12]), __uint_as_float(b[13]));
+                v3.w = pack_bf16x2(__uint_as_float(b[14]), __uint_as_float(b[15]));
+                dst[0] = v0;
+                dst[1] = v1;
+                dst[2] = v2;
+                dst[3] = v3;
+            }
+        }
+    } else if constexpr (EPI == EPI_GLU_FWD) {
+        // accumulator columns [0, bn/2) hold e (gate), [bn/2, bn) hold u (up) for the same
+        // output columns; write e, u and h = act(e) * u, with h taken from the bf16 e and u.
+        const int half = P.bn >> 1;      // 128
+        const int per = half >> 1;       // columns per epilogue half
+#pragma unroll 1
+        for (int c = 0; c < per; c += 16) {
+            const int col = hh * per + c;
+            uint32_t g[16], u[16];
+            tmem_ld_x16(tacc + col, g);
+            tmem_ld_x16(tacc + half + col, u);
+            tmem_ld_wait32(g, u);
+            const int64_t gcol = (int64_t)U.nb * P.out_col_step + col;
+            if (mvalid && gcol < P.N) {
+                uint32_t eo[8], uo[8], ho[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    eo[i] = pack_bf16x2(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+                    uo[i] = pack_bf16x2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+                    const float e0 = bf16lo(eo[i]), e1 = bf16hi(eo[i]);
+                    const float u0 = bf16lo(uo[i]), u1 = bf16hi(uo[i]);
+                    ho[i] = pack_bf16x2(act_fwd(P.act, e0) * u0, act_fwd(P.act, e1) * u1);
+                }
+                const int64_t off = m * P.ld_out + gcol;
+                uint4* de = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out0) + off);
+                uint4* du = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out1) + off);
+                uint4* dh = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out2) + off);
+                de[0] = make_uint4(eo[0], eo[1], eo[2], eo[3]);
+                de[1] = make_uint4(eo[4], eo[5], eo[6], eo[7]);
+                du[0] = make_uint4(uo[0], uo[1], uo[2], uo[3]);
+                du[1] = make_uint4(uo[4], uo[5], uo[6], uo[7]);
+                dh[0] = make_uint4(ho[0], ho[1], ho[2], ho[3]);
+                dh[1] = make_uint4(ho[4], ho[5], ho[6], ho[7]);
+            }
+        }
+    } else if constexpr (EPI == EPI_GLU_BWD) {
+        // accumulator = dh; with the saved e, u:  de = dh * u * act'(e),  du = dh * act(e)
+        const int half = P.bn >> 1;
+#pragma unroll 1
+        for (int c = 0; c < half; c += 16) {
+            const int col = hh * half + c;
+            const int64_t gcol = (int64_t)U.nb * P.out_col_step + col;
+            const bool ok = mvalid && gcol < P.N;
+            uint4 e4[2], u4[2];
+            if (ok) {
+                const uint4* pe = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(P.in0) + m * P.ld_in + gcol);
+                const uint4* pu = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(P.in1) + m * P.ld_in + gcol);
+                e4[0] = __ldg(pe);
+                e4[1] = __ldg(pe + 1);
+                u4[0] = __ldg(pu);
+                u4[1] = __ldg(pu + 1);
+            }
+            uint32_t a[16];
+            tmem_ld_x16(tacc + col, a);
+            tmem_ld_wait16(a);
+            if (ok) {
+                const uint32_t ev[8] = {e4[0].x, e4[0].y, e4[0].z, e4[0].w, e4[1].x, e4[1].y, e4[1].z, e4[1].w};
+                const uint32_t uv[8] = {u4[0].x, u4[0].y, u4[0].z, u4[0].w, u4[1].x, u4[1].y, u4[1].z, u4[1].w};
+                uint32_t deo[8], duo[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float f0, df0, f1, df1;
+                    const float e0 = bf16lo(ev[i]), e1 = bf16hi(ev[i]);
+                    const float u0 = bf16lo(uv[i]), u1 = bf16hi(uv[i]);
+                    act_fwd_bwd(P.act, e0, f0, df0);
+                    act_fwd_bwd(P.act, e1, f1, df1);
+                    const float h0 = __uint_as_float(a[2 * i]), h1 = __uint_as_float(a[2 * i + 1]);
+                    deo[i] = pack_bf16x2(h0 * u0 * df0, h1 * u1 * df1);
+                    duo[i] = pack_bf16x2(h0 * f0, h1 * f1);
+                }
+                const int64_t off = m * P.ld_out + gcol;
+                uint4* pde = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out0) + off);
+                uint4* pdu = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out1) + off);
+                pde[0] = make_uint4(deo[0], deo[1], deo[2], deo[3]);
+                pde[1] = make_uint4(deo[4], deo[5], deo[6], deo[7]);
+                pdu[0] = make_uint4(duo[0], duo[1], duo[2], duo[3]);
+                pdu[1] = make_uint4(duo[4], duo[5], duo[6], duo[7]);
+            }
+        }
+    } else {  // EPI_PARTIAL: raw fp32 accumulator to out0[ks][m][0..bn)
+#pragma unroll 1
+        for (int c = hh * 16; c < P.bn; c += 32) {
+            uint32_t a[16];
+            tmem_ld_x16(tacc + c, a);
+            tmem_ld_wait16(a);
+            if (mvalid) {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(P.out0) + (int64_t)U.ks * P.split_stride +
+                                                        m * P.ld_out + c);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
+                                         __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+template <int BN_MAX, bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_constant__ Params p) {
+    using C = GemmCfg<BN_MAX, A_MN, B_MN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* tfull = empty + C::STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&tfull[a]), 1);
+            mbar_init(smem_u32(&tempty[a]), kNumEpiWarps);
+        }
+        mbar_init(smem_u32(drain), 1);
+        *s_abort = 0;
+        fence_mbar_init();
+        for (int i = 0; i < kMaxMaps; ++i)
+            if (p.map_bytes[i]) tma_prefetch_map(&p.maps[i]);
+    }
+    __syncwarp();
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+                const Unit U = decode_unit(p, u);
+                const Prob& P = p.prob[U.pi];
+                for (int si = 0; ok && si < P.nseg; ++si) {
+                    const Seg& S = P.seg[si];
+                    const int nkb = (S.kext + kBK - 1) / kBK;
+                    int kb0 = 0, kb1 = nkb;
+                    if (P.splits > 1) {
+                        kb0 = U.ks * P.kb_per_split;
+                        kb1 = min(nkb, kb0 + P.kb_per_split);
+                    }
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t sA = smem_u32(smem + stage * C::STAGE_BYTES);
+                        const uint32_t sB = sA + C::A_BYTES;
+                        const uint32_t fb = smem_u32(&full[stage]);
+                        const int kx = kb * kBK;
+                        // which B loads are issued (a box entirely outside the tensor is skipped;
+                        // no MMA reads the stage region it would have filled)
+                        uint32_t bytes = C::A_BYTES;
+                        bool use_b[3] = {false, false, false};
+                        int nch = 0;
+                        if constexpr (B_MN) {
+                            nch = (P.bn + 63) >> 6;
+                            bytes += nch * 8192u;
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 3; ++i) {
+                                const int mi = S.b_map[i];
+                                if (mi >= 0) {
+                                    const int x = kx + S.b_xoff[i];
+                                    use_b[i] = (x + kBK > 0) && (x < p.map_w[mi]);
+                                    if (use_b[i]) bytes += p.map_bytes[mi];
+                                }
+                            }
+                        }
+                        mbar_expect_tx(fb, bytes);
+                        if constexpr (A_MN) {
+                            tma_load_2d(sA, &p.maps[S.a_map], fb, U.mb * kBM, kx);
+                            tma_load_2d(sA + 8192, &p.maps[S.a_map], fb, U.mb * kBM + 64, kx);
+                        } else {
+                            tma_load_2d(sA, &p.maps[S.a_map], fb, kx + S.a_xoff, U.mb * kBM);
+                        }
+                        if constexpr (B_MN) {
+                            for (int c = 0; c < nch; ++c)
+                                tma_load_2d(sB + c * 8192, &p.maps[S.b_map[0]], fb, U.nb * P.n_step + c * 64, kx);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 3; ++i)
+                                if (use_b[i])
+                                    tma_load_2d(sB + i * S.b_rows * 128, &p.maps[S.b_map[i]], fb, kx + S.b_xoff[i],
+                                                U.nb * P.n_step);
+                        }
+                        if (++stage == C::STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                record_error(p, kErrTimeout, 1);
+                *s_abort = 1;
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------- MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t aphase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+                const Unit U = decode_unit(p, u);
+                const Prob& P = p.prob[U.pi];
+                if (!mbar_wait(smem_u32(&tempty[acc]), aphase ^ 1u, s_abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + acc * BN_MAX;
+                const uint32_t idesc = make_idesc_bf16(kBM, P.bn, A_MN, B_MN);
+                const uint32_t idesc_h = make_idesc_bf16(kBM, P.bn >> 1, A_MN, B_MN);
+                uint32_t accum = 0;
+                for (int si = 0; ok && si < P.nseg; ++si) {
+                    const Seg& S = P.seg[si];
+                    const int nkb = (S.kext + kBK - 1) / kBK;
+                    int kb0 = 0, kb1 = nkb;
+                    if (P.splits > 1) {
+                        kb0 = U.ks * P.kb_per_split;
+                        kb1 = min(nkb, kb0 + P.kb_per_split);
+                    }
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(smem_u32(&full[stage]), phase, s_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sA = smem_u32(smem + stage * C::STAGE_BYTES);
+                        const uint32_t sB = sA + C::A_BYTES;
+                        const int rem = S.kext - kb * kBK;
+                        const int nsteps = rem >= kBK ? 4 : (rem + 15) >> 4;
+                        for (int ks = 0; ks < nsteps; ++ks) {
+                            const uint64_t ad = A_MN ? make_sdesc_sw128(sA + ks * 2048, 8192, 1024)
+                                                     : make_sdesc_sw128(sA + ks * 32, 16, 1024);
+                            if (!B_MN && S.dual_split > 0) {
+                                const int hf = (kb * kBK + ks * 16) >= S.dual_split ? 1 : 0;
+                                const uint32_t bo = sB + hf * (P.bn >> 1) * 128 + ks * 32;
+                                umma_bf16(d0 + hf * (P.bn >> 1), ad, make_sdesc_sw128(bo, 16, 1024), idesc_h, accum);
+                            } else {
+                                const uint64_t bd = B_MN ? make_sdesc_sw128(sB + ks * 2048, 8192, 1024)
+                                                         : make_sdesc_sw128(sB + ks * 32, 16, 1024);
+                                umma_bf16(d0, ad, bd, idesc, accum);
+                            }
+                            accum = 1;
+                        }
+                        umma_commit(smem_u32(&empty[stage]));
+                        if (++stage == C::STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&tfull[acc]));
+                acc ^= 1;
+                if (acc == 0) aphase ^= 1u;
+            }
+            if (!ok) {
+                record_error(p, kErrTimeout, 2);
+                *s_abort = 1;
+            }
+            // wait until every MMA this thread issued has finished before TMEM is released
+            umma_commit(smem_u32(drain));
+            volatile int never = 0;
+            mbar_wait(smem_u32(drain), 0, &never);
+        }
+    } else {  // ---------------- epilogue warps
+        const int ew = warp - 2;
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int hh = ew >> 2;  // which half of the tile's columns
+        int acc = 0;
+        uint32_t aphase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+            const Unit U = decode_unit(p, u);
+            const Prob& P = p.prob[U.pi];
+            if (!mbar_wait(smem_u32(&tfull[acc]), aphase, s_abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN_MAX;
+            const int row = q * 32 + lane;
+            const int64_t m = (int64_t)U.mb * kBM + row;
+            epilogue_tile<BN_MAX, EPI>(P, U, tacc, hh, m, m < P.M);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+            acc ^= 1;
+            if (acc == 0) aphase ^= 1u;
+        }
+        if (!ok && lane == 0) {
+            record_error(p, kErrTimeout, 3);
+            *s_abort = 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace lm

@@ -1,0 +1,39 @@
+// Instantiations of the backward-pass GEMM variants and the variant dispatcher.
+#include "lm_internal.h"
+
+namespace lm {
+
+cudaError_t launch_gemm_fwd(GemmKind k, const Params& p, int grid, cudaStream_t st);
+
+template <int BN_MAX, bool A_MN, bool B_MN, int EPI>
+static cudaError_t launch_variant(const Params& p, int grid, cudaStream_t st) {
+    constexpr int smem = GemmCfg<BN_MAX, A_MN, B_MN>::SMEM_BYTES;
+    auto k = gemm_kernel<BN_MAX, A_MN, B_MN, EPI>;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = 1;
+    }
+    k<<<grid, kNumThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+int gemm_bn_max(GemmKind k) { return (k == G_PART_KMN || k == G_PART_MNK) ? 64 : 256; }
+bool gemm_a_mn(GemmKind k) { return k == G_PART_MNK; }
+bool gemm_b_mn(GemmKind k) { return k == G_GLU_BWD || k == G_STORE_KMN || k == G_PART_KMN; }
+
+cudaError_t launch_gemm(GemmKind k, const Params& p, int grid, cudaStream_t st) {
+    switch (k) {
+        case G_GLU_BWD: return launch_variant<256, false, true, EPI_GLU_BWD>(p, grid, st);
+        case G_STORE_KMN: return launch_variant<256, false, true, EPI_STORE>(p, grid, st);
+        case G_PART_KMN: return launch_variant<64, false, true, EPI_PARTIAL>(p, grid, st);
+        case G_PART_MNK: return launch_variant<64, true, false, EPI_PARTIAL>(p, grid, st);
+        default: return launch_gemm_fwd(k, p, grid, st);
+    }
+}
+
+}  // namespace lm

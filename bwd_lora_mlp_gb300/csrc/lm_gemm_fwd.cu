@@ -1,0 +1,32 @@
+// Instantiations of the forward-pass GEMM variants.
+#include "lm_internal.h"
+
+namespace lm {
+
+template <int BN_MAX, bool A_MN, bool B_MN, int EPI>
+static cudaError_t launch_variant(const Params& p, int grid, cudaStream_t st) {
+    constexpr int smem = GemmCfg<BN_MAX, A_MN, B_MN>::SMEM_BYTES;
+    auto k = gemm_kernel<BN_MAX, A_MN, B_MN, EPI>;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = 1;
+    }
+    k<<<grid, kNumThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_fwd(GemmKind k, const Params& p, int grid, cudaStream_t st) {
+    switch (k) {
+        case G_GLU_FWD: return launch_variant<256, false, false, EPI_GLU_FWD>(p, grid, st);
+        case G_STORE_KK: return launch_variant<256, false, false, EPI_STORE>(p, grid, st);
+        case G_PART_KK: return launch_variant<256, false, false, EPI_PARTIAL>(p, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace lm

@@ -1,0 +1,65 @@
+// Host-side declarations shared by the translation units of liblora_mlp.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lm_gemm.cuh"
+
+namespace lm {
+
+// The GEMM variants built (BN_MAX, A major, B major, epilogue).
+enum GemmKind : int {
+    G_GLU_FWD = 0,   // 256, K, K, GLU_FWD    gate/up forward with fused SwiGLU / GeGLU
+    G_STORE_KK = 1,  // 256, K, K, STORE      down / O / QKV forward
+    G_GLU_BWD = 2,   // 256, K, MN, GLU_BWD   dh = dY Wd (+ rank-r) with fused activation backward
+    G_STORE_KMN = 3, // 256, K, MN, STORE     dX = sum dOut W (+ rank-r)
+    G_PART_KK = 4,   // 256, K, K, PARTIAL    X A^T (rank-r input projection), split-K partials
+    G_PART_KMN = 5,  //  64, K, MN, PARTIAL   dOut B (rank-r output-gradient projection)
+    G_PART_MNK = 6,  //  64, MN, K, PARTIAL   column reductions over T for dA / dB
+    G_NUM_KINDS = 7
+};
+
+int gemm_bn_max(GemmKind k);
+bool gemm_a_mn(GemmKind k);
+bool gemm_b_mn(GemmKind k);
+cudaError_t launch_gemm(GemmKind k, const Params& p, int grid, cudaStream_t st);
+
+// Finalisation of split-K partials of rank-r projections:
+//   out[t][c] = bf16(s[c / group] * sum_ks part[ks][t][c]), also written transposed to
+//   outT[c][t] (row stride ldT).
+struct FinRowJob {
+    const float* part;
+    int64_t split_stride;
+    int32_t splits;
+    int32_t ncols;
+    int32_t group;
+    float s[3];
+    uint16_t* out;
+    uint16_t* outT;
+    int64_t ldT;
+};
+cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cudaStream_t st);
+
+// Finalisation of split-K partials of the dA / dB column reductions:
+//   dB layout (transposed == 0): out[c][j] = sum_ks part[ks][c][j], j < r
+//   dA layout (transposed == 1): out[j][c] = sum_ks part[ks][c][j]
+struct FinColJob {
+    const float* part;
+    int64_t split_stride;
+    int64_t C;
+    int32_t splits;
+    int32_t rp;
+    int32_t r;
+    int32_t transposed;
+    float* out;
+};
+cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t st);
+
+cudaError_t launch_nf4_pack(const uint16_t* W, int64_t numel, uint8_t* codes, int8_t* absmax_q,
+                            float* scale, cudaStream_t st);
+cudaError_t launch_nf4_dequant(const uint8_t* codes, const int8_t* absmax_q, const float* scale,
+                               int64_t numel, bool bf16_out, void* out, cudaStream_t st);
+void nf4_codebook_host(float* out16);
+
+}  // namespace lm

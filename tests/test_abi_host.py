@@ -1,0 +1,144 @@
+"""Host-side tests of the C ABI (no GPU needed): the library builds and loads, exports every
+entry point of include/lora_mlp.h, its NF4 table equals the oracle's bit for bit, and argument
+errors are reported before anything reaches the device."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from bwd_lora_mlp_gb300 import build as B
+from bwd_lora_mlp_gb300 import lib as L
+from oracle import nf4 as onf4
+
+
+@pytest.fixture(scope="module")
+def so():
+    B.build()
+    return L.load()
+
+
+def test_exports_every_header_symbol(so):
+    names = L.header_symbols()
+    assert len(names) == 18
+    for n in names:
+        assert hasattr(so, n), n
+    assert set(names) == set(L._SIGS)
+
+
+def test_codebook_matches_oracle_bitwise(so):
+    cb = np.array(L.lm_nf4_codebook(), dtype=np.float32)
+    assert np.array_equal(cb.view(np.uint32), onf4.codebook().view(np.uint32))
+
+
+def _size(fn, *args):
+    out = ctypes.c_size_t(0)
+    st = L.call_status(fn, *args, ctypes.byref(out))
+    return st, out.value
+
+
+def test_size_queries():
+    st, s1 = _size("lora_mlp_workspace_size", 512, 256, 704, 8)
+    assert st == L.LM_OK and s1 > 2 * 512 * 704 * 2
+    st, s2 = _size("lora_mlp_workspace_size", 1024, 256, 704, 8)
+    assert st == L.LM_OK and s2 > s1
+    assert _size("lora_mlp_workspace_size", 512, 250, 704, 8)[0] == L.LM_ERR_SHAPE
+    assert _size("lora_mlp_workspace_size", 512, 256, 704, 12)[0] == L.LM_ERR_SHAPE
+    assert _size("lora_mlp_workspace_size", 512, 256, 704, 72)[0] == L.LM_ERR_SHAPE
+    assert _size("lora_mlp_workspace_size", -1, 256, 704, 8)[0] == L.LM_ERR_SHAPE
+    assert L.call_status("lora_mlp_saved_size", 512, 8, None) == L.LM_ERR_NULL
+    for fn, args in (("lora_mlp_saved_size", (0, 16)), ("lora_qkv_saved_size", (100, 16)),
+                     ("lora_o_saved_size", (100, 64)), ("lora_qkv_workspace_size", (100, 256, 256, 64, 64, 16)),
+                     ("lora_o_workspace_size", (100, 256, 128, 16))):
+        st, v = _size(fn, *args)
+        assert st == L.LM_OK and v > 0, fn
+
+
+# ---------------------------------------------------------------------------- fake device pointers
+# Validation runs on the host before any CUDA call, so distinct aligned integers stand in for
+# device buffers; none is ever dereferenced.
+
+class Fake:
+    def __init__(self):
+        self.next = 1 << 32
+
+    def __call__(self, nbytes):
+        p = self.next
+        self.next += (int(nbytes) + 4095) // 4096 * 4096 + 4096
+        return p
+
+
+def _lora(fake, din, dout, r, s=2.0):
+    w = L.lm_weight()
+    w.kind, w.rows, w.cols = L.LM_WEIGHT_BF16, dout, din
+    w.w = fake(din * dout * 2)
+    x = L.lm_lora()
+    x.W, x.A, x.B, x.r, x.s = w, fake(r * din * 2), fake(dout * r * 2), r, s
+    return x
+
+
+def _mlp_args(T=512, d=256, n=704, r=8, **over):
+    f = Fake()
+    a = dict(T=T, d=d, n=n, act=L.LM_ACT_SWIGLU, X=f(T * d * 2), gate=_lora(f, d, n, r), up=_lora(f, d, n, r),
+             down=_lora(f, n, d, r), y=f(T * d * 2), e=f(T * n * 2), u=f(T * n * 2), h=f(T * n * 2))
+    a["saved_bytes"] = _size("lora_mlp_saved_size", T, r)[1]
+    a["saved"] = f(a["saved_bytes"])
+    a["ws_bytes"] = _size("lora_mlp_workspace_size", T, d, n, r)[1]
+    a["ws"] = f(a["ws_bytes"])
+    a.update(over)
+    return a
+
+
+def _fwd(a):
+    return L.call_status("lora_mlp_fwd", a["T"], a["d"], a["n"], a["act"], a["X"], ctypes.byref(a["gate"]),
+                         ctypes.byref(a["up"]), ctypes.byref(a["down"]), a["y"], a["e"], a["u"], a["h"],
+                         a["saved"], a["saved_bytes"], a["ws"], a["ws_bytes"], None)
+
+
+def test_mlp_fwd_argument_errors(so):
+    assert _fwd(_mlp_args(X=None)) == L.LM_ERR_NULL
+    a = _mlp_args()
+    assert _fwd(dict(a, X=a["X"] + 2)) == L.LM_ERR_ALIGN
+    assert _fwd(dict(a, y=a["X"])) == L.LM_ERR_ALIAS                       # in-place not offered
+    assert _fwd(dict(a, h=a["e"] + 64)) == L.LM_ERR_ALIAS                  # two outputs overlap
+    assert _fwd(dict(a, ws_bytes=a["ws_bytes"] - 1)) == L.LM_ERR_WORKSPACE
+    assert _fwd(dict(a, saved_bytes=16)) == L.LM_ERR_WORKSPACE
+    assert _fwd(dict(a, act=7)) == L.LM_ERR_DTYPE
+    assert _fwd(dict(a, d=250)) == L.LM_ERR_SHAPE
+    b = _mlp_args()
+    b["up"].r = 16
+    assert _fwd(b) == L.LM_ERR_SHAPE                                       # ranks differ
+    c = _mlp_args()
+    c["down"].W.rows = 128
+    assert _fwd(c) == L.LM_ERR_SHAPE                                       # W shape mismatch
+    k = _mlp_args()
+    k["gate"].W.kind = 5
+    assert _fwd(k) == L.LM_ERR_DTYPE
+    z = _mlp_args()
+    z["gate"].s = float("nan")
+    assert _fwd(z) == L.LM_ERR_SHAPE
+    assert "gate.s" in L.last_error()
+
+
+def test_empty_token_count_is_a_no_op(so):
+    a = _mlp_args(T=0)
+    assert _fwd(a) == L.LM_OK
+
+
+def test_without_device_reports_cuda_error(so):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    st = _fwd(_mlp_args())
+    assert st in (L.LM_ERR_CUDA, L.LM_ERR_UNSUPPORTED)
+    assert L.last_error()
+
+
+def test_nf4_argument_errors(so):
+    f = Fake()
+    W, c, q, s = f(16384 * 2), f(8192), f(256), f(64)
+    assert L.call_status("nf4_pack", W, 16384 + 64, c, q, s, None) == L.LM_ERR_SHAPE
+    assert L.call_status("nf4_pack", W, 16384, None, q, s, None) == L.LM_ERR_NULL
+    assert L.call_status("nf4_pack", W, 16384, W + 16, q, s, None) == L.LM_ERR_ALIAS
+    assert L.call_status("nf4_pack", W, 0, c, q, s, None) == L.LM_OK
+    assert L.call_status("nf4_dequant", c, q, s, 16384, 9, f(65536), None) == L.LM_ERR_DTYPE
+    assert L.call_status("nf4_dequant", c, q, s, 16384, L.LM_OUT_F32, c, None) == L.LM_ERR_ALIAS
