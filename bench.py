@@ -1,0 +1,409 @@
+"""Benchmark of the LoRA MLP forward + backward on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one lora_mlp_fwd + lora_mlp_bwd of the Llama-3-8B-shaped LoRA SwiGLU MLP
+(T = 4 x 2048 tokens, d = 4096, n = 14336, r = 16, alpha = 32, bf16 base) on seeded synthetic
+inputs already resident in HBM.  The working set (weights 336 MiB, activations > 1 GiB) is
+larger than the 129 MB L2, so no flush is needed between steps.  Multi-GPU runs are replicas
+(the path has no exchange step): every rank runs the same step on its own GPU and the value is
+the tokens all ranks processed divided by the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle on the host cores (rank 0 only), each step a
+bounded token sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "LoRA-MLP fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def mlp_flops(T, d, n, r):
+    """Algorithmic flops of one fwd+bwd: six base GEMMs (3 forward, dh, 2 in dX) and the rank-r
+    products of the three projections (forward X A^T, (XA) B^T; backward G = dOut B, dA, dB, G A)."""
+    return 12 * T * d * n + 18 * T * r * (d + n)
+
+
+def kernel_flops(tag, T, d, n, r):
+    """Algorithmic flops of one launch of the tagged GEMM kernel (rank-r terms at rank r)."""
+    return {
+        "mlp.gateup": 2 * T * d * 2 * n + 2 * 2 * T * r * n,
+        "mlp.down": 2 * T * n * d + 2 * T * r * d,
+        "mlp.dh": 2 * T * d * n + 2 * T * r * n,
+        "mlp.dX": 2 * T * 2 * n * d + 2 * 2 * T * r * d,
+    }.get(tag)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def src_digest():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "bwd_lora_mlp_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(tag, workload):
+    """DRAM bytes per launch of `tag` from the committed ncu summary, if it was taken on the
+    current kernel sources; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rows = json.load(f)
+    except Exception:
+        return None
+    dig = src_digest()
+    for r in rows:
+        if r.get("tag") == tag and r.get("workload") == workload and r.get("src_digest") == dig:
+            return r.get("bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_id)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) == len(self.FIELDS):
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for nm, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------------
+# the oracle on host cores (reference arm and cpu_baseline)
+
+def oracle_step(w, inp64, Ts):
+    from oracle import lora as O
+    p = inp64["p"]
+    X = inp64["X"][:Ts]
+    dY = inp64["dY"][:Ts]
+    O.mlp_backward(X, dY, p, w.act)
+
+
+def oracle_inputs(w, inp):
+    from oracle import lora as O
+    p = {}
+    for t, k in (("gate", "g"), ("up", "u"), ("down", "d")):
+        p["W" + k] = O.from_bf16(inp["W_" + t])
+        p["A" + k] = O.from_bf16(inp["A_" + t])
+        p["B" + k] = O.from_bf16(inp["B_" + t])
+        p["s" + k] = w.s
+    return {"p": p, "X": O.from_bf16(inp["X"]), "dY": O.from_bf16(inp["dY"])}
+
+
+def pick_sample(w, inp64, budget_s):
+    Ts = 64
+    t0 = time.perf_counter()
+    oracle_step(w, inp64, Ts)
+    dt = time.perf_counter() - t0
+    Ts = int(min(w.T, max(64, Ts * budget_s / max(dt, 1e-3))) // 64 * 64)
+    return max(Ts, 64)
+
+
+def cpu_baseline(w, inp, budget_s=12.0):
+    inp64 = oracle_inputs(w, inp)
+    Ts = pick_sample(w, inp64, budget_s)
+    t0 = time.perf_counter()
+    oracle_step(w, inp64, Ts)
+    dt = time.perf_counter() - t0
+    return {"value": Ts / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "fp64 numpy oracle fwd+bwd of %d of the %d tokens, full d=%d, n=%d, r=%d; %.1f s"
+                      % (Ts, w.T, w.projs[0].d_in, w.projs[0].d_out, w.r, dt)}
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return 0
+    from bwd_lora_mlp_gb300 import synth
+    inp = synth.make_inputs(w)
+    inp64 = oracle_inputs(w, inp)
+    Ts = pick_sample(w, inp64, 2.0)
+    for _ in range(args.warmup):
+        oracle_step(w, inp64, Ts)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, inp64, Ts)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = Ts / dt
+    d, n = w.projs[0].d_in, w.projs[0].d_out
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "d": d, "n": n, "r": w.r, "alpha": w.alpha, "act": w.act,
+                       "tokens_per_step": Ts},
+            "tflops": mlp_flops(Ts, d, n, w.r) / dt / 1e12,
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": "%d tokens of %d per step" % (Ts, w.T)},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama3_8b_mlp_bf16")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="run the workload's shapes with this many tokens (small cases for profiling)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from bwd_lora_mlp_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    assert w.kind == "mlp", "bench.py times the LoRA MLP workloads"
+    if args.tokens:
+        w = synth.scaled_workload(w, T=args.tokens)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        rc = run_reference(args, w, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return rc
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from bwd_lora_mlp_gb300 import lib as L
+
+    T, d, n, r = w.T, w.projs[0].d_in, w.projs[0].d_out, w.r
+    inp = synth.make_inputs(w)
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+    def host_pinned(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    mk = lambda t: L.Lora(dev(inp["W_" + t]), dev(inp["A_" + t]), dev(inp["B_" + t]), w.s)
+    gate, up, down = mk("gate"), mk("up"), mk("down")
+    X, dY = dev(inp["X"]), dev(inp["dY"])
+    fw = L.lora_mlp_fwd(X, gate, up, down, act=w.act)
+    bw = L.lora_mlp_bwd(X, dY, fw, gate, up, down, act=w.act)
+    stream = torch.cuda.current_stream()
+
+    def step(Xs, dYs):
+        L.lora_mlp_fwd(Xs, gate, up, down, act=w.act, y=fw["y"], e=fw["e"], u=fw["u"], h=fw["h"],
+                       saved=fw["saved"], ws=fw["ws"])
+        L.lora_mlp_bwd(Xs, dYs, fw, gate, up, down, act=w.act, dX=bw["dX"],
+                       grads={k: v for k, v in bw.items() if k != "dX"})
+
+    for _ in range(args.warmup):
+        step(X, dY)
+    torch.cuda.synchronize()
+    L.lm_workspace_check(fw["ws"])
+
+    # ---- timed region: inputs resident in HBM
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    sampler = ClockSampler("GPU-" + str(props.uuid) if getattr(props, "uuid", None) else local)
+    L.lm_profile_reset()
+    L.lm_profile_enable(True)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(X, dY)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    L.lm_profile_enable(False)
+    prof = L.lm_profile_summary()
+    L.lm_workspace_check(fw["ws"])
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(ms, world)
+
+    peaks, peak_src = load_peaks()
+    flops = mlp_flops(T, d, n, r)
+    value = world * T / (ms / 1e3)
+    tflops = world * flops / (ms / 1e3) / 1e12
+    launches = sum(c for c, _ in prof.values())
+    # dominant kernel: the tag with the largest share of the timed region
+    dom = max(prof.items(), key=lambda kv: kv[1][1])
+    dom_tag, (dom_n, dom_ms) = dom
+    per_launch_ms = dom_ms / dom_n
+    kf = kernel_flops(dom_tag, T, d, n, r)
+    roofline = None
+    if kf is not None:
+        ach = kf / (per_launch_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roofline = {"bound": "tensor", "kernel": dom_tag, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                    "frac": ach / peak, "traffic": committed_traffic(dom_tag, w.name),
+                    "peak_source": peak_src + " sustained bf16", "flops_per_launch": kf,
+                    "ms_per_launch": per_launch_ms}
+
+    # ---- end to end through the C ABI from pinned host buffers
+    hX, hdY = host_pinned(inp["X"]), host_pinned(inp["dY"])
+    host_out = {"y": torch.empty_like(fw["y"], device="cpu").pin_memory(),
+                "dX": torch.empty_like(bw["dX"], device="cpu").pin_memory()}
+    host_g = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in bw.items() if k != "dX"}
+    Xd, dYd = torch.empty_like(X), torch.empty_like(dY)
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        Xd.copy_(hX, non_blocking=True)
+        dYd.copy_(hdY, non_blocking=True)
+        step(Xd, dYd)
+        host_out["y"].copy_(fw["y"], non_blocking=True)
+        host_out["dX"].copy_(bw["dX"], non_blocking=True)
+        for k, v in host_g.items():
+            v.copy_(bw[k], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = (hX.numel() + hdY.numel()) * 2
+    d2h = (host_out["y"].numel() + host_out["dX"].numel()) * 2 + sum(v.numel() * 4 for v in host_g.values())
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded W~N(0,0.02), A~U(+-1/sqrt(in)), B~N(0,0.02), X~N(0,1), dY~N(0,0.01), bf16",
+        "config": {"workload": w.name, "T": T, "d": d, "n": n, "r": r, "alpha": w.alpha, "act": w.act,
+                   "base": "bf16", "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "no flush: the working set (weights 336 MiB, X/dY/y/dX 256 MiB, e/u/h/de/du 1.1 GiB) "
+                         "exceeds the 129 MB L2"},
+        "tflops": tflops,
+        "roofline_step": {"bound": "tensor", "achieved": tflops / world, "peak": peaks["bf16_tflops_sustained"],
+                          "unit": "TFLOP/s", "frac": tflops / world / peaks["bf16_tflops_sustained"],
+                          "peak_source": peak_src + " sustained bf16"},
+        "roofline": roofline,
+        "gpu_launches": launches,
+        "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
+        "clocks": clocks,
+        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -8,6 +8,9 @@
 #include <cstdio>
 #include <cstring>
 #include <initializer_list>
+#include <mutex>
+#include <string>
+#include <vector>
 
 #include "lm_internal.h"
 #include "lora_mlp.h"
@@ -41,6 +44,48 @@ lm_status cuda_fail(cudaError_t e, const char* what) {
         const cudaError_t _e = (expr);                     \
         if (_e != cudaSuccess) return cuda_fail(_e, what); \
     } while (0)
+
+// ------------------------------------------------------------------ tracing
+struct ProfRec {
+    const char* tag;
+    cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t prof_event() {
+    if (!g_prof_pool.empty()) {
+        cudaEvent_t e = g_prof_pool.back();
+        g_prof_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Records an event pair around the kernel launched inside its lifetime (when tracing is on).
+struct ProfScope {
+    ProfRec rec{};
+    bool on = false;
+    cudaStream_t st;
+    ProfScope(const char* tag, cudaStream_t s) : st(s) {
+        std::lock_guard<std::mutex> g(g_prof_mu);
+        if (!g_prof_on) return;
+        rec.tag = tag;
+        rec.a = prof_event();
+        rec.b = prof_event();
+        on = rec.a && rec.b && cudaEventRecord(rec.a, st) == cudaSuccess;
+    }
+    ~ProfScope() {
+        if (!on) return;
+        cudaEventRecord(rec.b, st);
+        std::lock_guard<std::mutex> g(g_prof_mu);
+        g_prof.push_back(rec);
+    }
+};
 
 // ------------------------------------------------------------------ device / driver entry
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -349,10 +394,11 @@ struct Builder {
         return (int)std::min<int64_t>(units, sms);
     }
 
-    lm_status launch(int sms, int32_t* err, cudaStream_t st_) {
+    lm_status launch(const char* tag, int sms, int32_t* err, cudaStream_t st_) {
         if (st != LM_OK) return st;
         const int grid = finish(sms, err);
         if (grid == 0) return LM_OK;
+        ProfScope prof(tag, st_);
         const cudaError_t e = launch_gemm(kind, p, grid, st_);
         if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
         return LM_OK;
@@ -419,7 +465,8 @@ void add_colreduce(Builder& b, const uint16_t* Z, int64_t T, int64_t C, const ui
     P.split_stride = C * P.bn;
 }
 
-lm_status fin_rows(const Builder& b, std::initializer_list<FinRowJob> jobs, int64_t T, cudaStream_t st) {
+lm_status fin_rows(const char* tag, const Builder& b, std::initializer_list<FinRowJob> jobs, int64_t T,
+                   cudaStream_t st) {
     FinRowJob js[3];
     int n = 0;
     for (const FinRowJob& j : jobs) {
@@ -427,13 +474,15 @@ lm_status fin_rows(const Builder& b, std::initializer_list<FinRowJob> jobs, int6
         js[n].splits = b.p.prob[n].splits;
         ++n;
     }
+    ProfScope prof(tag, st);
     const cudaError_t e = launch_fin_rowproj(js, n, T, st);
     if (e != cudaSuccess) return cuda_fail(e, "rank-r finalisation launch");
     return LM_OK;
 }
 
-lm_status fin_cols(const Builder& b, FinColJob* js, int n, cudaStream_t st) {
+lm_status fin_cols(const char* tag, const Builder& b, FinColJob* js, int n, cudaStream_t st) {
     for (int i = 0; i < n; ++i) js[i].splits = b.p.prob[i].splits;
+    ProfScope prof(tag, st);
     const cudaError_t e = launch_fin_colreduce(js, n, st);
     if (e != cudaSuccess) return cuda_fail(e, "gradient finalisation launch");
     return LM_OK;
@@ -475,6 +524,55 @@ extern "C" lm_status lm_workspace_check(void* ws, lm_stream stream) {
         LM_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "cudaStreamSynchronize");
         return fail((lm_status)h[0], "a kernel gave up on a bounded wait (role %d, block %d)", h[1], h[2]);
     }
+    return LM_OK;
+}
+
+// ====================================================================== tracing
+extern "C" lm_status lm_profile_enable(int32_t on) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    g_prof_on = on != 0;
+    return LM_OK;
+}
+
+extern "C" lm_status lm_profile_reset(void) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    for (const ProfRec& r : g_prof) {
+        cudaEventSynchronize(r.b);
+        g_prof_pool.push_back(r.a);
+        g_prof_pool.push_back(r.b);
+    }
+    g_prof.clear();
+    return LM_OK;
+}
+
+extern "C" lm_status lm_profile_summary(char* buf, size_t buf_len) {
+    if (!buf || buf_len == 0) return fail(LM_ERR_NULL, "buf is NULL or empty");
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    struct Agg {
+        std::string tag;
+        long long n;
+        double ms;
+    };
+    std::vector<Agg> agg;
+    for (const ProfRec& r : g_prof) {
+        LM_CUDA(cudaEventSynchronize(r.b), "cudaEventSynchronize");
+        float ms = 0.f;
+        LM_CUDA(cudaEventElapsedTime(&ms, r.a, r.b), "cudaEventElapsedTime");
+        size_t i = 0;
+        while (i < agg.size() && agg[i].tag != r.tag) ++i;
+        if (i == agg.size()) agg.push_back(Agg{r.tag, 0, 0.0});
+        agg[i].n += 1;
+        agg[i].ms += ms;
+    }
+    std::string out;
+    char line[160];
+    for (const Agg& a : agg) {
+        snprintf(line, sizeof line, "%s\t%lld\t%.6f\n", a.tag.c_str(), a.n, a.ms);
+        out += line;
+    }
+    const size_t n = std::min(out.size(), buf_len - 1);
+    memcpy(buf, out.data(), n);
+    buf[n] = 0;
     return LM_OK;
 }
 
@@ -551,8 +649,8 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     {  // s*[X Ag^T | X Au^T]
         Builder b(G_PART_KK);
         add_rowproj_in(b, X, T, d, {gate->A, up->A}, D, part);
-        LM_TRY(b.launch(sms, err, st));
-        LM_TRY(fin_rows(b, {FinRowJob{part, T * 2 * rp, 0, 2 * rp, rp, {gate->s, up->s, 0.f}, xa, xaT, D.ldT}}, T, st));
+        LM_TRY(b.launch("mlp.xa", sms, err, st));
+        LM_TRY(fin_rows("mlp.xa.fin", b, {FinRowJob{part, T * 2 * rp, 0, 2 * rp, rp, {gate->s, up->s, 0.f}, xa, xaT, D.ldT}}, T, st));
     }
     {  // e, u and h = act(e) * u; the rank-r terms enter the same accumulator
         Builder b(G_GLU_FWD);
@@ -582,13 +680,13 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         P.out1 = u_save;
         P.out2 = h_save;
         P.ld_out = n;
-        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(b.launch("mlp.gateup", sms, err, st));
     }
     {  // s_d * h Ad^T
         Builder b(G_PART_KK);
         add_rowproj_in(b, h_save, T, n, {down->A}, D, part);
-        LM_TRY(b.launch(sms, err, st));
-        LM_TRY(fin_rows(b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, ha, haT, D.ldT}}, T, st));
+        LM_TRY(b.launch("mlp.ha", sms, err, st));
+        LM_TRY(fin_rows("mlp.ha.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, ha, haT, D.ldT}}, T, st));
     }
     {  // y = h Wd^T + (s_d h Ad^T) Bd^T
         Builder b(G_STORE_KK);
@@ -609,7 +707,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         S1.kext = rp;
         P.out0 = y;
         P.ld_out = d;
-        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(b.launch("mlp.down", sms, err, st));
     }
     return LM_OK;
 }
@@ -680,8 +778,8 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     {  // Gd = s_d dY Bd, formed once (feeds dh and dA_down)
         Builder b(G_PART_KMN);
         add_rowproj_out(b, dY, T, d, down->B, D, part);
-        LM_TRY(b.launch(sms, err, st));
-        LM_TRY(fin_rows(b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st));
+        LM_TRY(b.launch("mlp.gd", sms, err, st));
+        LM_TRY(fin_rows("mlp.gd.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st));
     }
     {  // dh = dY Wd + Gd Ad with the activation backward in the epilogue: de, du
         Builder b(G_GLU_BWD);
@@ -707,15 +805,15 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         P.out0 = de;
         P.out1 = du;
         P.ld_out = n;
-        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(b.launch("mlp.dh", sms, err, st));
     }
     {  // Gg = s_g de Bg, Gu = s_u du Bu, formed once (feed dA and dX)
         Builder b(G_PART_KMN);
         float* part_u = part + (size_t)kMaxSplits * T * rp;
         add_rowproj_out(b, de, T, n, gate->B, D, part);
         add_rowproj_out(b, du, T, n, up->B, D, part_u);
-        LM_TRY(b.launch(sms, err, st));
-        LM_TRY(fin_rows(b,
+        LM_TRY(b.launch("mlp.gg_gu", sms, err, st));
+        LM_TRY(fin_rows("mlp.gg_gu.fin", b,
                         {FinRowJob{part, T * rp, 0, rp, rp, {gate->s, 0.f, 0.f}, gg, ggT, D.ldT},
                          FinRowJob{part_u, T * rp, 0, rp, rp, {up->s, 0.f, 0.f}, gu, guT, D.ldT}},
                         T, st));
@@ -734,13 +832,13 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         add_colreduce(b, de, T, n, xaT, D, p3);              // dB_gate   = de^T (s X Ag^T)
         add_colreduce(b, X, T, d, guT, D, p4);               // dA_up^T   = X^T Gu
         add_colreduce(b, du, T, n, xaT + (size_t)rp * D.ldT, D, p5);  // dB_up = du^T (s X Au^T)
-        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(b.launch("mlp.dAdB", sms, err, st));
         FinColJob js[6] = {
             {p0, n * rp, n, 0, rp, r, 1, dA_down}, {p1, d * rp, d, 0, rp, r, 0, dB_down},
             {p2, d * rp, d, 0, rp, r, 1, dA_gate}, {p3, n * rp, n, 0, rp, r, 0, dB_gate},
             {p4, d * rp, d, 0, rp, r, 1, dA_up},   {p5, n * rp, n, 0, rp, r, 0, dB_up},
         };
-        LM_TRY(fin_cols(b, js, 6, st));
+        LM_TRY(fin_cols("mlp.dAdB.fin", b, js, 6, st));
     }
     {  // dX = de Wg + du Wu + Gg Ag + Gu Au
         Builder b(G_STORE_KMN);
@@ -769,7 +867,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         S3.kext = rp;
         P.out0 = dX;
         P.ld_out = d;
-        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(b.launch("mlp.dX", sms, err, st));
     }
     return LM_OK;
 }
@@ -843,8 +941,8 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     {
         Builder b(G_PART_KK);
         add_rowproj_in(b, X, T, d, {q->A, k->A, v->A}, D, part);
-        LM_TRY(b.launch(sms, err, st));
-        LM_TRY(fin_rows(b, {FinRowJob{part, T * 3 * rp, 0, 3 * rp, rp, {q->s, k->s, v->s}, xa, xaT, D.ldT}}, T, st));
+        LM_TRY(b.launch("qkv.xa", sms, err, st));
+        LM_TRY(fin_rows("qkv.xa.fin", b, {FinRowJob{part, T * 3 * rp, 0, 3 * rp, rp, {q->s, k->s, v->s}, xa, xaT, D.ldT}}, T, st));
     }
     {
         Builder b(G_STORE_KK);
@@ -873,7 +971,7 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             P.out0 = outs[i];
             P.ld_out = ns[i];
         }
-        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(b.launch("qkv.fwd", sms, err, st));
     }
     return LM_OK;
 }
@@ -942,8 +1040,8 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             parts[i] = part + (size_t)i * kMaxSplits * T * rp;
             add_rowproj_out(b, dOut[i], T, ns[i], Ls[i]->B, D, parts[i]);
         }
-        LM_TRY(b.launch(sms, err, st));
-        LM_TRY(fin_rows(b,
+        LM_TRY(b.launch("qkv.g", sms, err, st));
+        LM_TRY(fin_rows("qkv.g.fin", b,
                         {FinRowJob{parts[0], T * rp, 0, rp, rp, {q->s, 0.f, 0.f}, g[0], gT[0], D.ldT},
                          FinRowJob{parts[1], T * rp, 0, rp, rp, {k->s, 0.f, 0.f}, g[1], gT[1], D.ldT},
                          FinRowJob{parts[2], T * rp, 0, rp, rp, {v->s, 0.f, 0.f}, g[2], gT[2], D.ldT}},
@@ -963,8 +1061,8 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             js[2 * i + 1] = FinColJob{p, ns[i] * rp, ns[i], 0, rp, r, 0, dBs[i]};
             p += (size_t)kMaxSplits * ns[i] * rp;
         }
-        LM_TRY(b.launch(sms, err, st));
-        LM_TRY(fin_cols(b, js, 6, st));
+        LM_TRY(b.launch("qkv.dAdB", sms, err, st));
+        LM_TRY(fin_cols("qkv.dAdB.fin", b, js, 6, st));
     }
     {  // dX = sum_x dOut_x W_x + G_x A_x
         Builder b(G_STORE_KMN);
@@ -989,7 +1087,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         }
         P.out0 = dX;
         P.ld_out = d;
-        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(b.launch("qkv.dX", sms, err, st));
     }
     return LM_OK;
 }
@@ -1051,8 +1149,8 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     {
         Builder b(G_PART_KK);
         add_rowproj_in(b, X, T, d_in, {o->A}, D, part);
-        LM_TRY(b.launch(sms, err, st));
-        LM_TRY(fin_rows(b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st));
+        LM_TRY(b.launch("o.xa", sms, err, st));
+        LM_TRY(fin_rows("o.xa.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st));
     }
     {
         Builder b(G_STORE_KK);
@@ -1073,7 +1171,7 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         S1.kext = rp;
         P.out0 = Y;
         P.ld_out = d_out;
-        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(b.launch("o.fwd", sms, err, st));
     }
     return LM_OK;
 }
@@ -1116,8 +1214,8 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     {  // G = s dY B, formed once (feeds dA and dX)
         Builder b(G_PART_KMN);
         add_rowproj_out(b, dY, T, d_out, o->B, D, part);
-        LM_TRY(b.launch(sms, err, st));
-        LM_TRY(fin_rows(b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, g, gT, D.ldT}}, T, st));
+        LM_TRY(b.launch("o.g", sms, err, st));
+        LM_TRY(fin_rows("o.g.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, g, gT, D.ldT}}, T, st));
     }
     {  // dA^T = X^T G, dB = dY^T (s X A^T)
         Builder b(G_PART_MNK);
@@ -1125,9 +1223,9 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         float* p1 = p0 + (size_t)kMaxSplits * d_in * rp;
         add_colreduce(b, X, T, d_in, gT, D, p0);
         add_colreduce(b, dY, T, d_out, xaT, D, p1);
-        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(b.launch("o.dAdB", sms, err, st));
         FinColJob js[2] = {{p0, d_in * rp, d_in, 0, rp, r, 1, dA}, {p1, d_out * rp, d_out, 0, rp, r, 0, dB}};
-        LM_TRY(fin_cols(b, js, 2, st));
+        LM_TRY(fin_cols("o.dAdB.fin", b, js, 2, st));
     }
     {  // dX = dY W + G A
         Builder b(G_STORE_KMN);
@@ -1148,7 +1246,7 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         S1.kext = rp;
         P.out0 = dX;
         P.ld_out = d_in;
-        LM_TRY(b.launch(sms, err, st));
+        LM_TRY(b.launch("o.dX", sms, err, st));
     }
     return LM_OK;
 }

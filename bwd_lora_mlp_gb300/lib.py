@@ -60,6 +60,9 @@ _SIGS = {
     "lm_nf4_codebook": ([ctypes.POINTER(ctypes.c_float)], _I32),
     "lm_workspace_reset": ([_P, _P], _I32),
     "lm_workspace_check": ([_P, _P], _I32),
+    "lm_profile_enable": ([_I32], _I32),
+    "lm_profile_reset": ([], _I32),
+    "lm_profile_summary": ([ctypes.c_char_p, _SZ], _I32),
     "lora_mlp_saved_size": ([_I64, _I32, _SZP], _I32),
     "lora_mlp_workspace_size": ([_I64, _I64, _I64, _I32, _SZP], _I32),
     "lora_mlp_fwd": ([_I64, _I64, _I64, _I32, _P, _LP, _LP, _LP, _P, _P, _P, _P, _P, _SZ, _P, _SZ, _P], _I32),
@@ -210,6 +213,25 @@ def lm_nf4_codebook() -> list:
 
 def lm_workspace_check(ws: torch.Tensor, stream=None) -> None:
     _call("lm_workspace_check", _ptr(ws, torch.uint8, "ws"), _stream(stream))
+
+
+def lm_profile_enable(on: bool = True) -> None:
+    _call("lm_profile_enable", 1 if on else 0)
+
+
+def lm_profile_reset() -> None:
+    _call("lm_profile_reset")
+
+
+def lm_profile_summary() -> dict:
+    """{tag: (launches, total_ms)} of the kernels launched while tracing was on."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    _call("lm_profile_summary", buf, len(buf))
+    out = {}
+    for line in buf.value.decode().splitlines():
+        tag, n, ms = line.split("\t")
+        out[tag] = (int(n), float(ms))
+    return out
 
 
 def lora_mlp_saved_size(T: int, r: int) -> int:

@@ -118,6 +118,16 @@ LM_API lm_status lm_workspace_reset(void* ws, lm_stream stream);
  * a kernel recorded a timeout since the last reset (LM_OK otherwise).  This call synchronises. */
 LM_API lm_status lm_workspace_check(void* ws, lm_stream stream);
 
+/* ---- tracing ---------------------------------------------------------------------------
+ * When enabled, the library records a CUDA event pair around every kernel it launches, on the
+ * launch stream, tagged with the call site (e.g. "mlp.dX").  lm_profile_summary synchronises on
+ * the recorded events and writes one line per tag, "tag<TAB>launches<TAB>total_ms\n", into the
+ * host buffer `buf` (truncated to buf_len - 1 characters, always NUL-terminated).  Host only;
+ * recording costs two cudaEventRecord calls per launch and nothing when disabled. */
+LM_API lm_status lm_profile_enable(int32_t on);
+LM_API lm_status lm_profile_reset(void);
+LM_API lm_status lm_profile_summary(char* buf, size_t buf_len);
+
 /* ---- LoRA MLP ([LO] LoRA MLP autograd function; [UN] LoRA_MLP) -------------------------
  *   e = X Wg^T + sg (X Ag^T) Bg^T,   u = X Wu^T + su (X Au^T) Bu^T,
  *   h = act(e) * u  (act = SiLU or exact-erf GELU),   y = h Wd^T + sd (h Ad^T) Bd^T.

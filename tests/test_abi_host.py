@@ -19,7 +19,7 @@ def so():
 
 def test_exports_every_header_symbol(so):
     names = L.header_symbols()
-    assert len(names) == 18
+    assert len(names) == 21
     for n in names:
         assert hasattr(so, n), n
     assert set(names) == set(L._SIGS)
@@ -142,3 +142,11 @@ def test_nf4_argument_errors(so):
     assert L.call_status("nf4_pack", W, 0, c, q, s, None) == L.LM_OK
     assert L.call_status("nf4_dequant", c, q, s, 16384, 9, f(65536), None) == L.LM_ERR_DTYPE
     assert L.call_status("nf4_dequant", c, q, s, 16384, L.LM_OUT_F32, c, None) == L.LM_ERR_ALIAS
+
+
+def test_profile_summary_empty_without_launches(so):
+    L.lm_profile_enable(True)
+    L.lm_profile_reset()
+    assert L.lm_profile_summary() == {}
+    L.lm_profile_enable(False)
+    assert L.call_status("lm_profile_summary", None, 0) == L.LM_ERR_NULL
