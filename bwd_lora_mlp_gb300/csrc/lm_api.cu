@@ -499,6 +499,17 @@ const T_* at(const void* base, size_t off) {
 
 }  // namespace
 
+// Sets the calling thread's last-error text from another translation unit of the library.
+namespace lm {
+lm_status report_error(lm_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+}  // namespace lm
+
 // ====================================================================== utilities
 extern "C" const char* lm_last_error(void) { return g_err; }
 

@@ -77,6 +77,7 @@ _SIGS = {
     "lora_o_workspace_size": ([_I64, _I64, _I64, _I32, _SZP], _I32),
     "lora_o_fwd": ([_I64, _I64, _I64, _P, _LP, _P, _P, _SZ, _P, _SZ, _P], _I32),
     "lora_o_bwd": ([_I64, _I64, _I64, _P, _P, _P, _SZ, _LP, _P, _P, _P, _P, _SZ, _P], _I32),
+    "lora_o_bwd_static": ([_I64, _I64, _I64, _P, _P, _P, _SZ, _LP, _P, _P, _P, _P], _I32),
     "nf4_pack": ([_P, _I64, _P, _P, _P, _P], _I32),
     "nf4_dequant": ([_P, _P, _P, _I64, _I32, _P, _P], _I32),
 }
@@ -378,6 +379,23 @@ def lora_o_bwd(X, dY, fwd: dict, o: Lora, dX=None, dA=None, dB=None, ws=None, st
     _call("lora_o_bwd", T, d_in, d_out, _ptr(X, bf, "X"), _ptr(dY, bf, "dY"), _ptr(saved, torch.uint8, "saved"),
           saved.numel(), ctypes.byref(L), _ptr(dX, bf, "dX"), _ptr(dA, f32, "dA"), _ptr(dB, f32, "dB"),
           _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+    return {"dX": dX, "dA": dA, "dB": dB}
+
+
+def lora_o_bwd_static(X, dY, fwd: dict, o: Lora, dX=None, dA=None, dB=None, stream=None) -> dict:
+    """lora_o_bwd with the library's static device scratch (no workspace argument)."""
+    T, d_in = X.shape
+    d_out = _rows(o)
+    r = o.r
+    dev, bf, f32 = X.device, torch.bfloat16, torch.float32
+    dX = torch.empty((T, d_in), dtype=bf, device=dev) if dX is None else dX
+    dA = torch.empty((r, d_in), dtype=f32, device=dev) if dA is None else dA
+    dB = torch.empty((d_out, r), dtype=f32, device=dev) if dB is None else dB
+    saved = fwd["saved"]
+    L = o.c_struct()
+    _call("lora_o_bwd_static", T, d_in, d_out, _ptr(X, bf, "X"), _ptr(dY, bf, "dY"),
+          _ptr(saved, torch.uint8, "saved"), saved.numel(), ctypes.byref(L), _ptr(dX, bf, "dX"),
+          _ptr(dA, f32, "dA"), _ptr(dB, f32, "dB"), _stream(stream))
     return {"dX": dX, "dA": dA, "dB": dB}
 
 

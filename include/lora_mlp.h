@@ -192,6 +192,23 @@ LM_API lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const uint16
                      const lm_lora* o, uint16_t* dX, float* dA, float* dB,
                      void* ws, size_t ws_bytes, lm_stream stream);
 
+/* lora_o_bwd_static: lora_o_bwd for callers that must not allocate device memory (for example a
+ * plugin whose host framework owns the device memory pool, a process under a hard device-memory
+ * cap, or a latency-critical loop that cannot afford cudaFree's device-wide wait).  The web pages
+ * have no counterpart: this is a deployment variant, not a step of the method.  The arguments and
+ * results are those of lora_o_bwd without ws / ws_bytes: the scratch is a 16 MiB __device__ array
+ * inside the library, held by every GPU that loads it until the process exits.  Shapes whose
+ * lora_o_workspace_size exceeds 16 MiB are rejected with LM_ERR_WORKSPACE before any device work.
+ * The call allocates nothing.  All calls share the one array and it keeps the last call's contents;
+ * each call clears the error word on its stream, so calls whose kernels overlap on the GPU race and
+ * must be ordered by the caller.  The first call on a device (that device current) looks up the
+ * array's address; make it before capturing any stream.  A bounded-wait timeout inside the kernels
+ * cannot be read back through lm_workspace_check here; it shows as wrong results only. */
+LM_API lm_status lora_o_bwd_static(int64_t T, int64_t d_in, int64_t d_out, const uint16_t* X,
+                                   const uint16_t* dY, const void* saved, size_t saved_bytes,
+                                   const lm_lora* o, uint16_t* dX, float* dA, float* dB,
+                                   lm_stream stream);
+
 /* ---- NF4 ([LL] QLoRA section) -----------------------------------------------------------
  * nf4_pack: quantise numel bf16 values W (flattened row-major) to NF4.  numel must be a
  * multiple of 16384.  Per 64-element block b: absmax_b = max |x|; per group g of 256 blocks:

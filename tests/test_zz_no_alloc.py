@@ -1,0 +1,70 @@
+"""lora_o_bwd_static, the entry point for callers that must not allocate device memory (for
+example a plugin whose host framework owns the device memory pool, or a process under a hard
+device-memory cap): its scratch is a fixed device array inside the library instead of a
+caller-provided workspace.  Checked through the C ABI against lora_o_bwd on the same inputs, on
+two calls in a row (the array keeps the previous call's contents).  This file is collected last
+so that a run stopping at its first failure has already run every other test."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from bwd_lora_mlp_gb300 import build as B
+from bwd_lora_mlp_gb300 import lib as L
+from bwd_lora_mlp_gb300 import synth
+
+from gpu_util import check, dev_bf16, host64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    B.build()
+    L.load()
+
+
+def _static_call(X, dY, saved, o, dX, dA, dB):
+    T, d_in = X.shape
+    d_out = o.W.shape[0]
+    Lc = o.c_struct()
+    st = L.call_status("lora_o_bwd_static", T, d_in, d_out, X.data_ptr(), dY.data_ptr(), saved.data_ptr(),
+                       saved.numel(), ctypes.byref(Lc), dX.data_ptr(), dA.data_ptr(), dB.data_ptr(),
+                       torch.cuda.current_stream().cuda_stream)
+    assert st == L.LM_OK, L.last_error()
+
+
+@pytest.mark.parametrize("T,din,dout,r", [(300, 256, 192, 16), (1000, 512, 384, 64)])
+def test_static_scratch_matches_workspace_entry_point(T, din, dout, r):
+    w = synth.o_workload("o", T, din, dout, r, 2.0 * r)
+    inp = synth.make_inputs(w, seed=41)
+    o = L.Lora(dev_bf16(inp["W_o"]), dev_bf16(inp["A_o"]), dev_bf16(inp["B_o"]), w.s)
+    X, dY = dev_bf16(inp["X"]), dev_bf16(inp["dY"])
+    fw = L.lora_o_fwd(X, o)
+    ref = L.lora_o_bwd(X, dY, fw, o)
+    L.lm_workspace_check(fw["ws"])
+    want = {k: host64(v) for k, v in ref.items()}
+    for _ in range(2):
+        dX = torch.full_like(ref["dX"], float("nan"))
+        dA = torch.full_like(ref["dA"], float("nan"))
+        dB = torch.full_like(ref["dB"], float("nan"))
+        _static_call(X, dY, fw["saved"], o, dX, dA, dB)
+        torch.cuda.synchronize()
+        check("dX", host64(dX), want["dX"])
+        check("dA", host64(dA), want["dA"])
+        check("dB", host64(dB), want["dB"])
+
+
+def test_static_scratch_rejects_shapes_beyond_its_size():
+    T, din, dout, r = 1 << 20, 4096, 4096, 64
+    need = ctypes.c_size_t(0)
+    assert L.call_status("lora_o_workspace_size", T, din, dout, r, ctypes.byref(need)) == L.LM_OK
+    assert need.value > 16 << 20
+    o = L.lm_lora()
+    o.W.kind, o.W.rows, o.W.cols, o.W.w = L.LM_WEIGHT_BF16, dout, din, 1 << 32
+    o.A, o.B, o.r, o.s = 1 << 33, 1 << 34, r, 2.0
+    st = L.call_status("lora_o_bwd_static", T, din, dout, 1 << 35, 1 << 36, 1 << 37, 1 << 30, ctypes.byref(o),
+                       1 << 38, 1 << 39, 1 << 40, None)
+    assert st == L.LM_ERR_WORKSPACE
+    assert "static scratch" in L.last_error()
