@@ -283,8 +283,14 @@ def main():
     def host_pinned(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()
 
-    mk = lambda t: L.Lora(dev(inp["W_" + t]), dev(inp["A_" + t]), dev(inp["B_" + t]), w.s)
+    def mk(t):
+        W = dev(inp["W_" + t])
+        if w.nf4:  # quantise the frozen base on the device; packing is not part of the step
+            W = L.nf4_pack(W)
+        return L.Lora(W, dev(inp["A_" + t]), dev(inp["B_" + t]), w.s)
+
     gate, up, down = mk("gate"), mk("up"), mk("down")
+    torch.cuda.synchronize()
     X, dY = dev(inp["X"]), dev(inp["dY"])
     fw = L.lora_mlp_fwd(X, gate, up, down, act=w.act)
     bw = L.lora_mlp_bwd(X, dY, fw, gate, up, down, act=w.act)
@@ -383,7 +389,7 @@ def main():
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded W~N(0,0.02), A~U(+-1/sqrt(in)), B~N(0,0.02), X~N(0,1), dY~N(0,0.01), bf16",
         "config": {"workload": w.name, "T": T, "d": d, "n": n, "r": r, "alpha": w.alpha, "act": w.act,
-                   "base": "bf16", "parallelism": "replicas" if world > 1 else "single",
+                   "base": "nf4" if w.nf4 else "bf16", "parallelism": "replicas" if world > 1 else "single",
                    "l2": "no flush: the working set (weights 336 MiB, X/dY/y/dX 256 MiB, e/u/h/de/du 1.1 GiB) "
                          "exceeds the 129 MB L2"},
         "tflops": tflops,

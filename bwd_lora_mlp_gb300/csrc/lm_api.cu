@@ -161,7 +161,14 @@ lm_status check_lora(const lm_lora* L, const char* name, int64_t in, int64_t out
         snprintf(buf, sizeof buf, "%s.W.w", name);
         LM_TRY(need_ptr(L->W.w, buf));
     } else if (L->W.kind == LM_WEIGHT_NF4) {
-        return fail(LM_ERR_UNSUPPORTED, "%s: NF4 base weights are not available in this build of the GEMMs", name);
+        if ((L->W.rows * L->W.cols) % 16384 != 0 || L->W.cols % 64 != 0)
+            return fail(LM_ERR_SHAPE, "%s: an NF4 weight needs rows*cols %% 16384 == 0 and cols %% 64 == 0", name);
+        snprintf(buf, sizeof buf, "%s.W.codes", name);
+        LM_TRY(need_ptr(L->W.codes, buf));
+        snprintf(buf, sizeof buf, "%s.W.absmax_q", name);
+        LM_TRY(need_ptr(L->W.absmax_q, buf));
+        snprintf(buf, sizeof buf, "%s.W.group_scale", name);
+        LM_TRY(need_ptr(L->W.group_scale, buf));
     } else {
         return fail(LM_ERR_DTYPE, "%s.W.kind = %d is not a known weight kind", name, L->W.kind);
     }
@@ -197,7 +204,18 @@ lm_status check_alias(std::initializer_list<Span> outs, std::initializer_list<Sp
 }
 
 Span wspan(const lm_lora* L, const char* name) {
+    if (L->W.kind == LM_WEIGHT_NF4) return Span{L->W.codes, (size_t)(L->W.rows * L->W.cols / 2), name};
     return Span{L->W.w, (size_t)(L->W.rows * L->W.cols * 2), name};
+}
+
+// every projection of one call must use the same kind of base weight
+lm_status same_kind(std::initializer_list<const lm_lora*> Ls, bool* nf4) {
+    const lm_lora* first = *Ls.begin();
+    for (const lm_lora* L : Ls)
+        if (L->W.kind != first->W.kind)
+            return fail(LM_ERR_UNSUPPORTED, "the projections of one call mix bf16 and NF4 base weights");
+    *nf4 = first->W.kind == LM_WEIGHT_NF4;
+    return LM_OK;
 }
 
 // ------------------------------------------------------------------ workspace planning
@@ -326,10 +344,57 @@ OPlan plan_o(int64_t T, int64_t d_in, int64_t d_out, int32_t r) {
 struct Builder {
     Params p;
     int nmaps = 0;
+    int nnf4 = 0;
+    int tile_m = kBM;
     lm_status st = LM_OK;
     GemmKind kind;
 
-    explicit Builder(GemmKind k) : kind(k) { memset(&p, 0, sizeof p); }
+    explicit Builder(GemmKind k) : kind(k) {
+        memset(&p, 0, sizeof p);
+        if (gemm_is_nf4(k)) {
+            tile_m = 256;
+            nf4_codebook_host(p.nf4_code);
+        }
+    }
+
+    // 2D uint8 tensor (NF4 codes: rows x cols bytes), box = box_w bytes x box_rows rows, no swizzle
+    int map_u8(const void* base, int64_t rows, int64_t cols, int64_t ld, int box_w, int box_rows) {
+        if (st != LM_OK) return 0;
+        if (nmaps >= kMaxMaps) {
+            st = fail(LM_ERR_UNSUPPORTED, "too many tensor maps in one launch");
+            return 0;
+        }
+        cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)ld};
+        cuuint32_t box[2] = {(cuuint32_t)box_w, (cuuint32_t)box_rows};
+        cuuint32_t es[2] = {1u, 1u};
+        const CUresult r = g_encode(&p.maps[nmaps], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            st = fail(LM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for NF4 codes %lld x %lld bytes", (int)r,
+                      (long long)rows, (long long)cols);
+            return 0;
+        }
+        p.map_bytes[nmaps] = (uint32_t)(box_w * box_rows);
+        p.map_w[nmaps] = (int32_t)cols;
+        return nmaps++;
+    }
+
+    // codes map of an NF4 weight read K-major (forward: box 32 bytes = 64 elements x rows)
+    int codes_k(const lm_weight& W, int box_rows) { return map_u8(W.codes, W.rows, W.cols / 2, W.cols / 2, 32, box_rows); }
+    // codes map of an NF4 weight read MN-major (input gradient: box 64 bytes = 128 elements x 64 rows)
+    int codes_mn(const lm_weight& W) { return map_u8(W.codes, W.rows, W.cols / 2, W.cols / 2, 64, 64); }
+
+    int nf4src(const lm_weight& W) {
+        if (st != LM_OK) return -1;
+        if (nnf4 >= 4) {
+            st = fail(LM_ERR_UNSUPPORTED, "too many NF4 weights in one launch");
+            return -1;
+        }
+        p.nf4[nnf4] = Nf4Src{W.absmax_q, W.group_scale, W.rows, W.cols};
+        return nnf4++;
+    }
 
     // 2D bf16 tensor (rows x cols, row stride ld elements), box = 64 columns x box_rows rows
     int map(const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
@@ -359,8 +424,10 @@ struct Builder {
         Prob& P = p.prob[p.nprob++];
         memset(&P, 0, sizeof P);
         P.splits = 1;
-        for (int s = 0; s < kMaxSegs; ++s)
+        for (int s = 0; s < kMaxSegs; ++s) {
             for (int i = 0; i < 3; ++i) P.seg[s].b_map[i] = -1;
+            P.seg[s].b_nf4[0] = P.seg[s].b_nf4[1] = -1;
+        }
         return P;
     }
 
@@ -371,7 +438,7 @@ struct Builder {
         int64_t tiles = 0;
         for (int i = 0; i < p.nprob; ++i) {
             Prob& P = p.prob[i];
-            P.tiles_m = (int32_t)((P.M + kBM - 1) / kBM);
+            P.tiles_m = (int32_t)((P.M + tile_m - 1) / tile_m);
             tiles += (int64_t)P.tiles_m * P.tiles_n;
         }
         int S = 1;
@@ -617,6 +684,8 @@ static lm_status check_mlp_common(int64_t T, int64_t d, int64_t n, int32_t act, 
     LM_TRY(check_lora(gate, "gate", d, n, gate->r));
     LM_TRY(check_lora(up, "up", d, n, gate->r));
     LM_TRY(check_lora(down, "down", n, d, gate->r));
+    bool nf4 = false;
+    LM_TRY(same_kind({gate, up, down}, &nf4));
     return LM_OK;
 }
 
@@ -633,6 +702,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     LM_TRY(need_ptr(saved, "saved"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = gate->r;
+    const bool nf4 = gate->W.kind == LM_WEIGHT_NF4;
     const MlpPlan PL = plan_mlp(T, d, n, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -663,7 +733,39 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(b.launch("mlp.xa", sms, err, st));
         LM_TRY(fin_rows("mlp.xa.fin", b, {FinRowJob{part, T * 2 * rp, 0, 2 * rp, rp, {gate->s, up->s, 0.f}, xa, xaT, D.ldT}}, T, st));
     }
-    {  // e, u and h = act(e) * u; the rank-r terms enter the same accumulator
+    if (nf4) {
+        // NF4 base: 256 x 128 tiles of 64 gate + 64 up columns, codes decoded in the mainloop
+        Builder b(G_NF4_GLU_FWD);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)n;
+        P.bn = 128;
+        P.tiles_n = (int32_t)((n + 63) / 64);
+        P.n_step = 64;
+        P.out_col_step = 64;
+        P.act = act;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(X, T, d, d, 128);
+        S0.b_map[0] = b.codes_k(gate->W, 64);
+        S0.b_map[1] = b.codes_k(up->W, 64);
+        S0.b_nf4[0] = b.nf4src(gate->W);
+        S0.b_nf4[1] = b.nf4src(up->W);
+        S0.b_rows = 64;
+        S0.kext = (int32_t)d;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(xa, T, 2 * rp, 2 * rp, 128);
+        S1.b_map[0] = b.map(gate->B, n, r, r, 64);
+        S1.b_map[1] = b.map(up->B, n, r, r, 64);
+        S1.b_xoff[1] = -rp;
+        S1.b_rows = 64;
+        S1.kext = 2 * rp;
+        S1.dual_split = rp;
+        P.out0 = e_save;
+        P.out1 = u_save;
+        P.out2 = h_save;
+        P.ld_out = n;
+        LM_TRY(b.launch("mlp.gateup", sms, err, st));
+    } else {  // e, u and h = act(e) * u; the rank-r terms enter the same accumulator
         Builder b(G_GLU_FWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;
@@ -699,7 +801,28 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(b.launch("mlp.ha", sms, err, st));
         LM_TRY(fin_rows("mlp.ha.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, ha, haT, D.ldT}}, T, st));
     }
-    {  // y = h Wd^T + (s_d h Ad^T) Bd^T
+    if (nf4) {
+        Builder b(G_NF4_STORE_K);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)d;
+        P.bn = 128;
+        P.tiles_n = (int32_t)((d + 127) / 128);
+        P.n_step = 128;
+        P.out_col_step = 128;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(h_save, T, n, n, 128);
+        S0.b_map[0] = b.codes_k(down->W, 128);
+        S0.b_nf4[0] = b.nf4src(down->W);
+        S0.kext = (int32_t)n;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(ha, T, rp, rp, 128);
+        S1.b_map[0] = b.map(down->B, d, r, r, 128);
+        S1.kext = rp;
+        P.out0 = y;
+        P.ld_out = d;
+        LM_TRY(b.launch("mlp.down", sms, err, st));
+    } else {  // y = h Wd^T + (s_d h Ad^T) Bd^T
         Builder b(G_STORE_KK);
         Prob& P = b.prob();
         P.M = (int32_t)T;
@@ -745,6 +868,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     LM_TRY(need_ptr(dB_down, "dB_down"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = gate->r;
+    const bool nf4 = gate->W.kind == LM_WEIGHT_NF4;
     const MlpPlan PL = plan_mlp(T, d, n, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -792,7 +916,33 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(b.launch("mlp.gd", sms, err, st));
         LM_TRY(fin_rows("mlp.gd.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st));
     }
-    {  // dh = dY Wd + Gd Ad with the activation backward in the epilogue: de, du
+    if (nf4) {
+        Builder b(G_NF4_GLU_BWD);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)n;
+        P.bn = 128;
+        P.tiles_n = (int32_t)((n + 127) / 128);
+        P.n_step = 128;
+        P.out_col_step = 128;
+        P.act = act;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(dY, T, d, d, 128);
+        S0.b_map[0] = b.codes_mn(down->W);
+        S0.b_nf4[0] = b.nf4src(down->W);
+        S0.kext = (int32_t)d;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(gd, T, rp, rp, 128);
+        S1.b_map[0] = b.map(down->A, r, n, n, 64);
+        S1.kext = rp;
+        P.in0 = e_save;
+        P.in1 = u_save;
+        P.ld_in = n;
+        P.out0 = de;
+        P.out1 = du;
+        P.ld_out = n;
+        LM_TRY(b.launch("mlp.dh", sms, err, st));
+    } else {  // dh = dY Wd + Gd Ad with the activation backward in the epilogue: de, du
         Builder b(G_GLU_BWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;
@@ -851,7 +1001,33 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         };
         LM_TRY(fin_cols("mlp.dAdB.fin", b, js, 6, st));
     }
-    {  // dX = de Wg + du Wu + Gg Ag + Gu Au
+    if (nf4) {
+        Builder b(G_NF4_STORE_MN);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)d;
+        P.bn = 128;
+        P.tiles_n = (int32_t)((d + 127) / 128);
+        P.n_step = 128;
+        P.out_col_step = 128;
+        const lm_lora* Ls[2] = {gate, up};
+        const uint16_t* dOut[2] = {de, du};
+        const uint16_t* G[2] = {gg, gu};
+        for (int i = 0; i < 2; ++i) {
+            Seg& S = seg(P, i);
+            S.a_map = b.map(dOut[i], T, n, n, 128);
+            S.b_map[0] = b.codes_mn(Ls[i]->W);
+            S.b_nf4[0] = b.nf4src(Ls[i]->W);
+            S.kext = (int32_t)n;
+            Seg& R = seg(P, 2 + i);
+            R.a_map = b.map(G[i], T, rp, rp, 128);
+            R.b_map[0] = b.map(Ls[i]->A, r, d, d, 64);
+            R.kext = rp;
+        }
+        P.out0 = dX;
+        P.ld_out = d;
+        LM_TRY(b.launch("mlp.dX", sms, err, st));
+    } else {  // dX = de Wg + du Wu + Gg Ag + Gu Au
         Builder b(G_STORE_KMN);
         Prob& P = b.prob();
         P.M = (int32_t)T;
@@ -917,6 +1093,8 @@ static lm_status check_qkv_common(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     LM_TRY(check_lora(q, "q", d, nq, q->r));
     LM_TRY(check_lora(k, "k", d, nk, q->r));
     LM_TRY(check_lora(v, "v", d, nv, q->r));
+    bool nf4 = false;
+    LM_TRY(same_kind({q, k, v}, &nf4));
     return LM_OK;
 }
 
@@ -932,6 +1110,7 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     LM_TRY(need_ptr(saved, "saved"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = q->r;
+    const bool nf4 = q->W.kind == LM_WEIGHT_NF4;
     const QkvPlan PL = plan_qkv(T, d, nq, nk, nv, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -955,7 +1134,36 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         LM_TRY(b.launch("qkv.xa", sms, err, st));
         LM_TRY(fin_rows("qkv.xa.fin", b, {FinRowJob{part, T * 3 * rp, 0, 3 * rp, rp, {q->s, k->s, v->s}, xa, xaT, D.ldT}}, T, st));
     }
-    {
+    if (nf4) {
+        Builder b(G_NF4_STORE_K);
+        const int xmap = b.map(X, T, d, d, 128);
+        const int amap = b.map(xa, T, 3 * rp, 3 * rp, 128);
+        const lm_lora* Ls[3] = {q, k, v};
+        uint16_t* outs[3] = {Q, K, V};
+        const int64_t ns[3] = {nq, nk, nv};
+        for (int i = 0; i < 3; ++i) {
+            Prob& P = b.prob();
+            P.M = (int32_t)T;
+            P.N = (int32_t)ns[i];
+            P.bn = 128;
+            P.tiles_n = (int32_t)((ns[i] + 127) / 128);
+            P.n_step = 128;
+            P.out_col_step = 128;
+            Seg& S0 = seg(P, 0);
+            S0.a_map = xmap;
+            S0.b_map[0] = b.codes_k(Ls[i]->W, 128);
+            S0.b_nf4[0] = b.nf4src(Ls[i]->W);
+            S0.kext = (int32_t)d;
+            Seg& S1 = seg(P, 1);
+            S1.a_map = amap;
+            S1.a_xoff = i * rp;
+            S1.b_map[0] = b.map(Ls[i]->B, ns[i], r, r, 128);
+            S1.kext = rp;
+            P.out0 = outs[i];
+            P.ld_out = ns[i];
+        }
+        LM_TRY(b.launch("qkv.fwd", sms, err, st));
+    } else {
         Builder b(G_STORE_KK);
         const int xmap = b.map(X, T, d, d, 128);
         const int amap = b.map(xa, T, 3 * rp, 3 * rp, 128);
@@ -1007,6 +1215,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     LM_TRY(need_ptr(dB_v, "dB_v"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = q->r;
+    const bool nf4 = q->W.kind == LM_WEIGHT_NF4;
     const QkvPlan PL = plan_qkv(T, d, nq, nk, nv, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1075,7 +1284,32 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         LM_TRY(b.launch("qkv.dAdB", sms, err, st));
         LM_TRY(fin_cols("qkv.dAdB.fin", b, js, 6, st));
     }
-    {  // dX = sum_x dOut_x W_x + G_x A_x
+    if (nf4) {  // dX = sum_x dOut_x W_x + G_x A_x
+        Builder b(G_NF4_STORE_MN);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)d;
+        P.bn = 128;
+        P.tiles_n = (int32_t)((d + 127) / 128);
+        P.n_step = 128;
+        P.out_col_step = 128;
+        for (int i = 0; i < 3; ++i) {
+            Seg& S = seg(P, i);
+            S.a_map = b.map(dOut[i], T, ns[i], ns[i], 128);
+            S.b_map[0] = b.codes_mn(Ls[i]->W);
+            S.b_nf4[0] = b.nf4src(Ls[i]->W);
+            S.kext = (int32_t)ns[i];
+        }
+        for (int i = 0; i < 3; ++i) {
+            Seg& S = seg(P, 3 + i);
+            S.a_map = b.map(g[i], T, rp, rp, 128);
+            S.b_map[0] = b.map(Ls[i]->A, r, d, d, 64);
+            S.kext = rp;
+        }
+        P.out0 = dX;
+        P.ld_out = d;
+        LM_TRY(b.launch("qkv.dX", sms, err, st));
+    } else {  // dX = sum_x dOut_x W_x + G_x A_x
         Builder b(G_STORE_KMN);
         Prob& P = b.prob();
         P.M = (int32_t)T;
@@ -1141,6 +1375,7 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(need_ptr(saved, "saved"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = o->r;
+    const bool nf4 = o->W.kind == LM_WEIGHT_NF4;
     const OPlan PL = plan_o(T, d_in, d_out, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1163,7 +1398,28 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         LM_TRY(b.launch("o.xa", sms, err, st));
         LM_TRY(fin_rows("o.xa.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st));
     }
-    {
+    if (nf4) {
+        Builder b(G_NF4_STORE_K);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)d_out;
+        P.bn = 128;
+        P.tiles_n = (int32_t)((d_out + 127) / 128);
+        P.n_step = 128;
+        P.out_col_step = 128;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(X, T, d_in, d_in, 128);
+        S0.b_map[0] = b.codes_k(o->W, 128);
+        S0.b_nf4[0] = b.nf4src(o->W);
+        S0.kext = (int32_t)d_in;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(xa, T, rp, rp, 128);
+        S1.b_map[0] = b.map(o->B, d_out, r, r, 128);
+        S1.kext = rp;
+        P.out0 = Y;
+        P.ld_out = d_out;
+        LM_TRY(b.launch("o.fwd", sms, err, st));
+    } else {
         Builder b(G_STORE_KK);
         Prob& P = b.prob();
         P.M = (int32_t)T;
@@ -1199,6 +1455,7 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(need_ptr(dB, "dB"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = o->r;
+    const bool nf4 = o->W.kind == LM_WEIGHT_NF4;
     const OPlan PL = plan_o(T, d_in, d_out, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1238,7 +1495,28 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         FinColJob js[2] = {{p0, d_in * rp, d_in, 0, rp, r, 1, dA}, {p1, d_out * rp, d_out, 0, rp, r, 0, dB}};
         LM_TRY(fin_cols("o.dAdB.fin", b, js, 2, st));
     }
-    {  // dX = dY W + G A
+    if (nf4) {  // dX = dY W + G A
+        Builder b(G_NF4_STORE_MN);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)d_in;
+        P.bn = 128;
+        P.tiles_n = (int32_t)((d_in + 127) / 128);
+        P.n_step = 128;
+        P.out_col_step = 128;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(dY, T, d_out, d_out, 128);
+        S0.b_map[0] = b.codes_mn(o->W);
+        S0.b_nf4[0] = b.nf4src(o->W);
+        S0.kext = (int32_t)d_out;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(g, T, rp, rp, 128);
+        S1.b_map[0] = b.map(o->A, r, d_in, d_in, 64);
+        S1.kext = rp;
+        P.out0 = dX;
+        P.ld_out = d_in;
+        LM_TRY(b.launch("o.dX", sms, err, st));
+    } else {  // dX = dY W + G A
         Builder b(G_STORE_KMN);
         Prob& P = b.prob();
         P.M = (int32_t)T;

@@ -42,6 +42,15 @@ struct Seg {
     int32_t dual_split;   // > 0: K steps with k < dual_split use B block 0 and the first bn/2
                           // accumulator columns, the others B block 1 and the second half
     int32_t a_xoff;       // added to the K coordinate of A
+    int32_t b_nf4[2];     // NF4 kernel: index into Params::nf4 of the weight whose codes b_map[i]
+                          // holds (-1: b_map[i] is a bf16 operand loaded as is)
+};
+
+// An NF4-packed base weight as the decode warps of the NF4 GEMM see it.
+struct Nf4Src {
+    const int8_t* absmax_q;   // rows * cols / 64 block scales
+    const float* scale;       // rows * cols / 16384 group scales
+    int64_t rows, cols;       // of the weight (out x in)
 };
 
 struct Prob {
@@ -69,6 +78,8 @@ struct Params {  // CUtensorMap members carry their own 128-byte alignment
     uint32_t map_bytes[kMaxMaps];   // bytes one box of the map delivers
     int32_t map_w[kMaxMaps];        // inner (K or MN) extent of the map, elements
     Prob prob[kMaxProbs];
+    Nf4Src nf4[4];
+    float nf4_code[16];             // the NF4 values (NF4 kernel only)
     int32_t nprob;
     int32_t total_units;
     int32_t* err;
@@ -137,14 +148,15 @@ __device__ __forceinline__ void act_fwd_bwd(int act, float x, float& f, float& d
 }
 
 // ---------------------------------------------------------------- epilogues
-template <int BN_MAX, int EPI>
-__device__ __forceinline__ void epilogue_tile(const Prob& P, const Unit& U, uint32_t tacc, int hh,
-                                              int64_t m, bool mvalid) {
+// Columns [c_lo, c_hi) of the accumulator row this thread holds (GLU_FWD: the gate columns of
+// that range and the matching up columns bn/2 further on).  PARTIAL takes every column with
+// stride `c_step` starting at c_lo.
+template <int EPI>
+__device__ __forceinline__ void epilogue_cols(const Prob& P, const Unit& U, uint32_t tacc, int c_lo, int c_hi,
+                                              int c_step, int64_t m, bool mvalid) {
     if constexpr (EPI == EPI_STORE) {
-        const int half = P.bn >> 1;
 #pragma unroll 1
-        for (int c = 0; c < half; c += 32) {
-            const int col = hh * half + c;
+        for (int col = c_lo; col < c_hi; col += 32) {
             uint32_t a[16], b[16];
             tmem_ld_x16(tacc + col, a);
             tmem_ld_x16(tacc + col + 16, b);
@@ -178,11 +190,9 @@ __device__ __forceinline__ void epilogue_tile(const Prob& P, const Unit& U, uint
     } else if constexpr (EPI == EPI_GLU_FWD) {
         // accumulator columns [0, bn/2) hold e (gate), [bn/2, bn) hold u (up) for the same
         // output columns; write e, u and h = act(e) * u, with h taken from the bf16 e and u.
-        const int half = P.bn >> 1;      // 128
-        const int per = half >> 1;       // columns per epilogue half
+        const int half = P.bn >> 1;
 #pragma unroll 1
-        for (int c = 0; c < per; c += 16) {
-            const int col = hh * per + c;
+        for (int col = c_lo; col < c_hi; col += 16) {
             uint32_t g[16], u[16];
             tmem_ld_x16(tacc + col, g);
             tmem_ld_x16(tacc + half + col, u);
@@ -212,10 +222,8 @@ __device__ __forceinline__ void epilogue_tile(const Prob& P, const Unit& U, uint
         }
     } else if constexpr (EPI == EPI_GLU_BWD) {
         // accumulator = dh; with the saved e, u:  de = dh * u * act'(e),  du = dh * act(e)
-        const int half = P.bn >> 1;
 #pragma unroll 1
-        for (int c = 0; c < half; c += 16) {
-            const int col = hh * half + c;
+        for (int col = c_lo; col < c_hi; col += 16) {
             const int64_t gcol = (int64_t)U.nb * P.out_col_step + col;
             const bool ok = mvalid && gcol < P.N;
             uint4 e4[2], u4[2];
@@ -256,7 +264,7 @@ __device__ __forceinline__ void epilogue_tile(const Prob& P, const Unit& U, uint
         }
     } else {  // EPI_PARTIAL: raw fp32 accumulator to out0[ks][m][0..bn)
 #pragma unroll 1
-        for (int c = hh * 16; c < P.bn; c += 32) {
+        for (int c = c_lo; c < c_hi; c += c_step) {
             uint32_t a[16];
             tmem_ld_x16(tacc + c, a);
             tmem_ld_wait16(a);
@@ -269,6 +277,21 @@ __device__ __forceinline__ void epilogue_tile(const Prob& P, const Unit& U, uint
                                          __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
             }
         }
+    }
+}
+
+// The one-CTA kernel's split of a tile's columns between its two epilogue warp groups.
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile(const Prob& P, const Unit& U, uint32_t tacc, int hh, int64_t m,
+                                              bool mvalid) {
+    const int half = P.bn >> 1;
+    if constexpr (EPI == EPI_GLU_FWD) {
+        const int per = half >> 1;
+        epilogue_cols<EPI>(P, U, tacc, hh * per, hh * per + per, 16, m, mvalid);
+    } else if constexpr (EPI == EPI_PARTIAL) {
+        epilogue_cols<EPI>(P, U, tacc, hh * 16, P.bn, 32, m, mvalid);
+    } else {
+        epilogue_cols<EPI>(P, U, tacc, hh * half, hh * half + half, 0, m, mvalid);
     }
 }
 
@@ -477,7 +500,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN_MAX;
             const int row = q * 32 + lane;
             const int64_t m = (int64_t)U.mb * kBM + row;
-            epilogue_tile<BN_MAX, EPI>(P, U, tacc, hh, m, m < P.M);
+            epilogue_tile<EPI>(P, U, tacc, hh, m, m < P.M);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));

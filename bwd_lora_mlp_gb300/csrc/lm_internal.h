@@ -17,8 +17,16 @@ enum GemmKind : int {
     G_PART_KK = 4,   // 256, K, K, PARTIAL    X A^T (rank-r input projection), split-K partials
     G_PART_KMN = 5,  //  64, K, MN, PARTIAL   dOut B (rank-r output-gradient projection)
     G_PART_MNK = 6,  //  64, MN, K, PARTIAL   column reductions over T for dA / dB
-    G_NUM_KINDS = 7
+    // NF4 base weight decoded in the mainloop; 256 x 128 tiles
+    G_NF4_GLU_FWD = 7,   // K-major NF4 B, GLU_FWD
+    G_NF4_STORE_K = 8,   // K-major NF4 B, STORE
+    G_NF4_GLU_BWD = 9,   // MN-major NF4 B, GLU_BWD
+    G_NF4_STORE_MN = 10, // MN-major NF4 B, STORE
+    G_NUM_KINDS = 11
 };
+
+inline bool gemm_is_nf4(GemmKind k) { return k >= G_NF4_GLU_FWD; }
+cudaError_t launch_gemm_nf4(GemmKind k, const Params& p, int grid, cudaStream_t st);
 
 int gemm_bn_max(GemmKind k);
 bool gemm_a_mn(GemmKind k);
