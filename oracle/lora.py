@@ -100,6 +100,12 @@ def lora_w_backward(X, dY, W, A, B, s):
     return {"dX": dX, "dA": dA, "dB": dB, "G": G}
 
 
+def lora_w_lora_grads(X, dY, A, B, s):
+    """dA and dB of lora_w_backward without its base-weight dX GEMM (O(T r (in + out)) work)."""
+    G = dY @ B
+    return {"dA": s * (G.T @ X), "dB": s * (dY.T @ (X @ A.T))}
+
+
 # ----------------------------------------------------------------------------------------------
 # LoRA MLP ("LoRA Optimizations": LoRA MLP autograd function; unsloth LoRA_MLP):
 #   e = X Wg^T + sg (X Ag^T) Bg^T,  u = X Wu^T + su (X Au^T) Bu^T,
@@ -147,6 +153,25 @@ def mlp_backward(X, dY, p, act="swiglu"):
     dX = de @ p["Wg"] + du @ p["Wu"] + p["sg"] * (Gg @ p["Ag"]) + p["su"] * (Gu @ p["Au"])
     return {"dX": dX, "dAg": dAg, "dBg": dBg, "dAu": dAu, "dBu": dBu, "dAd": dAd, "dBd": dBd,
             "de": de, "du": du, "dh": dh, "Gg": Gg, "Gu": Gu, "Gd": Gd, **fw}
+
+
+def mlp_backward_columns(X, dY, p, cols, act="swiglu"):
+    """dB_gate[cols], dB_up[cols] and dA_down[:, cols] of mlp_backward, for a subset of the n
+    intermediate features.  Column c of e, u, h, dh, de, du depends only on row c of W_g, W_u, B_g,
+    B_u and column c of W_d, A_d (plus the rank-r products X A^T and dY B_d), so these gradient
+    entries cost O(T * d) per column instead of the full O(T * d * n) backward."""
+    f, fprime = ACTS[act]
+    cols = np.asarray(cols)
+    XAg = X @ p["Ag"].T
+    XAu = X @ p["Au"].T
+    Gd = dY @ p["Bd"]
+    e = X @ p["Wg"][cols].T + p["sg"] * (XAg @ p["Bg"][cols].T)
+    u = X @ p["Wu"][cols].T + p["su"] * (XAu @ p["Bu"][cols].T)
+    h = f(e) * u
+    dh = dY @ p["Wd"][:, cols] + p["sd"] * (Gd @ p["Ad"][:, cols])
+    de = dh * u * fprime(e)
+    du = dh * f(e)
+    return {"dBg": p["sg"] * (de.T @ XAg), "dBu": p["su"] * (du.T @ XAu), "dAd": p["sd"] * (Gd.T @ h)}
 
 
 # ----------------------------------------------------------------------------------------------

@@ -94,18 +94,28 @@ def quantize(w32: np.ndarray):
     q[nz] = np.clip(np.rint(ratio), 0, 127).astype(np.int8)               # half-even
     absmax_q = q.reshape(-1)
 
-    cb = codebook().astype(np.float64)
     safe = np.where(absmax > 0, absmax, np.float32(1.0)).astype(np.float32)
     idx = np.empty(x.size, dtype=np.uint8)
-    chunk = 1 << 14                                                        # blocks per pass
+    chunk = 1 << 16                                                        # blocks per pass
     for b0 in range(0, nb, chunk):
         b1 = min(nb, b0 + chunk)
         v = (blocks[b0:b1] / safe[b0:b1, None]).astype(np.float32)       # fp32 RN division
         v = np.where(absmax[b0:b1, None] > 0, v, np.float32(0.0))
-        dist = np.abs(v.astype(np.float64)[..., None] - cb[None, None, :])  # exact in fp64
-        idx[b0 * BLOCK:b1 * BLOCK] = np.argmin(dist, axis=-1).reshape(-1)   # first = lower index
+        idx[b0 * BLOCK:b1 * BLOCK] = nearest_code(v.reshape(-1))
     codes = ((idx[0::2] << 4) | idx[1::2]).astype(np.uint8)
     return codes, absmax_q, scale
+
+
+def nearest_code(v32: np.ndarray) -> np.ndarray:
+    """Index of the nearest codebook value to each fp32 v, an exact tie going to the lower index.
+
+    The codebook is strictly increasing, so v is nearer to code[i+1] than to code[i] exactly
+    when v exceeds their midpoint; the midpoints of two fp32 values are exact in fp64, and so is
+    the comparison with an fp32 v.  The index is therefore the number of midpoints strictly
+    below v (a tie, v equal to a midpoint, is not counted and stays with the lower code)."""
+    cb = codebook().astype(np.float64)
+    mids = 0.5 * (cb[:-1] + cb[1:])
+    return np.searchsorted(mids, np.asarray(v32, dtype=np.float32).astype(np.float64), side="left").astype(np.uint8)
 
 
 def unpack_indices(codes: np.ndarray) -> np.ndarray:

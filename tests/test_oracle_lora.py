@@ -200,3 +200,22 @@ def test_adapter_param_count_matches_page():
     # two extra bytes per parameter for the weight and two for the gradient
     # "about 167 MiB": 43,646,976 * 4 B = 166.5 MiB
     assert abs(n * 4 / 2 ** 20 - gold["extra_mib_rounded"]) <= 0.5
+
+
+@pytest.mark.parametrize("act", ["swiglu", "geglu"])
+def test_column_sampled_gradients_equal_full_backward(act):
+    X, dY, p = _small_mlp(act=act)
+    full = O.mlp_backward(X, dY, p, act)
+    cols = [0, 3, 17, 79]
+    part = O.mlp_backward_columns(X, dY, p, cols, act)
+    np.testing.assert_allclose(part["dBg"], full["dBg"][cols], rtol=1e-12, atol=1e-16)
+    np.testing.assert_allclose(part["dBu"], full["dBu"][cols], rtol=1e-12, atol=1e-16)
+    np.testing.assert_allclose(part["dAd"], full["dAd"][:, cols], rtol=1e-12, atol=1e-16)
+
+
+def test_lora_grads_without_dX_equal_full_backward():
+    X, (dY, _, _), p = _small_qkv()
+    full = O.lora_w_backward(X, dY, p["Wq"], p["Aq"], p["Bq"], p["sq"])
+    part = O.lora_w_lora_grads(X, dY, p["Aq"], p["Bq"], p["sq"])
+    np.testing.assert_allclose(part["dA"], full["dA"], rtol=1e-13, atol=1e-16)
+    np.testing.assert_allclose(part["dB"], full["dB"], rtol=1e-13, atol=1e-16)

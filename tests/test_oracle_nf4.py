@@ -168,3 +168,17 @@ def test_bf16_rounding_of_dequantised_base():
     half_ulp = 2.0 ** (e - 8)          # bf16 keeps 8 significant bits
     assert np.all(np.abs(wb[nz].astype(np.float64) - w[nz]) <= half_ulp)
     assert np.all(wb[~nz] == 0)
+
+
+def test_nearest_code_equals_argmin_of_exact_distances():
+    """The midpoint count equals the plain argmin of |v - code| (first minimum = lower index),
+    on random values, every midpoint (ties), the codes themselves and their fp32 neighbours."""
+    cb = nf4.codebook()
+    rng = np.random.default_rng(21)
+    v = [rng.uniform(-1, 1, 20000).astype(np.float32)]
+    mids = [np.float32((float(a) + float(b)) / 2) for a, b in zip(cb[:-1], cb[1:])]
+    near = [np.nextafter(np.float32(m), np.float32(d)) for m in mids for d in (-2, 2)]
+    v.append(np.array(mids + near + list(cb) + [0.0, -0.0], dtype=np.float32))
+    v = np.concatenate(v)
+    dist = np.abs(v.astype(np.float64)[:, None] - cb.astype(np.float64)[None, :])
+    assert np.array_equal(nf4.nearest_code(v), np.argmin(dist, axis=1).astype(np.uint8))
