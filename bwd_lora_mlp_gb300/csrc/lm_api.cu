@@ -266,6 +266,7 @@ struct MlpPlan {
     size_t part;            // workspace
     RankBuf gd, gg, gu;     // s*dY Bd, s*de Bg, s*du Bu
     size_t de, du;
+    size_t bdiag;           // [Bg | 0 ; 0 | Bu] (2n x 2rp) for the CTA-pair gate/up GEMM
     size_t ws_total;
 };
 
@@ -286,6 +287,7 @@ MlpPlan plan_mlp(int64_t T, int64_t d, int64_t n, int32_t r) {
     P.gu = take_rank(w, P.D, rp);
     P.de = w.take((size_t)T * n * 2);
     P.du = w.take((size_t)T * n * 2);
+    P.bdiag = w.take((size_t)2 * n * 2 * rp * 2);
     P.ws_total = w.off;
     return P;
 }
@@ -355,6 +357,7 @@ struct Builder {
             tile_m = 256;
             nf4_codebook_host(p.nf4_code);
         }
+        if (gemm_is_pair(k)) tile_m = 256;
     }
 
     // 2D uint8 tensor (NF4 codes: rows x cols bytes), box = box_w bytes x box_rows rows, no swizzle
@@ -466,7 +469,8 @@ struct Builder {
         const int grid = finish(sms, err);
         if (grid == 0) return LM_OK;
         ProfScope prof(tag, st_);
-        const cudaError_t e = launch_gemm(kind, p, grid, st_);
+        const cudaError_t e = gemm_is_pair(kind) ? launch_gemm_pair(kind, p, p.total_units, st_)
+                                                 : launch_gemm(kind, p, grid, st_);
         if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
         return LM_OK;
     }
@@ -766,7 +770,12 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         P.ld_out = n;
         LM_TRY(b.launch("mlp.gateup", sms, err, st));
     } else {  // e, u and h = act(e) * u; the rank-r terms enter the same accumulator
-        Builder b(G_GLU_FWD);
+        // CTA pair: CTA 0 holds the 128 W_g rows of a tile, CTA 1 the matching 128 W_u rows;
+        // the rank-r segment multiplies [s XAg | s XAu] by the block-diagonal [Bg | 0 ; 0 | Bu]
+        uint16_t* bdiag = at<uint16_t>(ws, PL.bdiag);
+        const cudaError_t be = launch_blockdiag(gate->B, up->B, n, r, rp, bdiag, st);
+        if (be != cudaSuccess) return cuda_fail(be, "rank-r operand launch");
+        Builder b(G2_GLU_FWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)n;
@@ -779,16 +788,12 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         S0.a_map = b.map(X, T, d, d, 128);
         S0.b_map[0] = b.map(gate->W.w, n, d, d, 128);
         S0.b_map[1] = b.map(up->W.w, n, d, d, 128);
-        S0.b_rows = 128;
         S0.kext = (int32_t)d;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(xa, T, 2 * rp, 2 * rp, 128);
-        S1.b_map[0] = b.map(gate->B, n, r, r, 128);
-        S1.b_map[1] = b.map(up->B, n, r, r, 128);
-        S1.b_xoff[1] = -rp;
-        S1.b_rows = 128;
+        S1.b_map[0] = b.map(bdiag, n, 2 * rp, 2 * rp, 128);
+        S1.b_map[1] = b.map(bdiag + (size_t)n * 2 * rp, n, 2 * rp, 2 * rp, 128);
         S1.kext = 2 * rp;
-        S1.dual_split = rp;
         P.out0 = e_save;
         P.out1 = u_save;
         P.out2 = h_save;
@@ -823,7 +828,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         P.ld_out = d;
         LM_TRY(b.launch("mlp.down", sms, err, st));
     } else {  // y = h Wd^T + (s_d h Ad^T) Bd^T
-        Builder b(G_STORE_KK);
+        Builder b(G2_STORE_K);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
@@ -833,11 +838,13 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         P.out_col_step = 256;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(h_save, T, n, n, 128);
-        S0.b_map[0] = b.map(down->W.w, d, n, n, 256);
+        S0.b_map[0] = b.map(down->W.w, d, n, n, 128);
+        S0.b_rank_off = 128;
         S0.kext = (int32_t)n;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(ha, T, rp, rp, 128);
-        S1.b_map[0] = b.map(down->B, d, r, r, 256);
+        S1.b_map[0] = b.map(down->B, d, r, r, 128);
+        S1.b_rank_off = 128;
         S1.kext = rp;
         P.out0 = y;
         P.ld_out = d;
@@ -943,7 +950,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         P.ld_out = n;
         LM_TRY(b.launch("mlp.dh", sms, err, st));
     } else {  // dh = dY Wd + Gd Ad with the activation backward in the epilogue: de, du
-        Builder b(G_GLU_BWD);
+        Builder b(G2_GLU_BWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)n;
@@ -955,10 +962,12 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(dY, T, d, d, 128);
         S0.b_map[0] = b.map(down->W.w, d, n, n, 64);
+        S0.b_rank_off = 128;
         S0.kext = (int32_t)d;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(gd, T, rp, rp, 128);
         S1.b_map[0] = b.map(down->A, r, n, n, 64);
+        S1.b_rank_off = 128;
         S1.kext = rp;
         P.in0 = e_save;
         P.in1 = u_save;
@@ -1028,7 +1037,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         P.ld_out = d;
         LM_TRY(b.launch("mlp.dX", sms, err, st));
     } else {  // dX = de Wg + du Wu + Gg Ag + Gu Au
-        Builder b(G_STORE_KMN);
+        Builder b(G2_STORE_MN);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
@@ -1039,18 +1048,22 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(de, T, n, n, 128);
         S0.b_map[0] = b.map(gate->W.w, n, d, d, 64);
+        S0.b_rank_off = 128;
         S0.kext = (int32_t)n;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(du, T, n, n, 128);
         S1.b_map[0] = b.map(up->W.w, n, d, d, 64);
+        S1.b_rank_off = 128;
         S1.kext = (int32_t)n;
         Seg& S2 = seg(P, 2);
         S2.a_map = b.map(gg, T, rp, rp, 128);
         S2.b_map[0] = b.map(gate->A, r, d, d, 64);
+        S2.b_rank_off = 128;
         S2.kext = rp;
         Seg& S3 = seg(P, 3);
         S3.a_map = b.map(gu, T, rp, rp, 128);
         S3.b_map[0] = b.map(up->A, r, d, d, 64);
+        S3.b_rank_off = 128;
         S3.kext = rp;
         P.out0 = dX;
         P.ld_out = d;
@@ -1164,7 +1177,7 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         }
         LM_TRY(b.launch("qkv.fwd", sms, err, st));
     } else {
-        Builder b(G_STORE_KK);
+        Builder b(G2_STORE_K);
         const int xmap = b.map(X, T, d, d, 128);
         const int amap = b.map(xa, T, 3 * rp, 3 * rp, 128);
         const lm_lora* Ls[3] = {q, k, v};
@@ -1180,12 +1193,14 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             P.out_col_step = 256;
             Seg& S0 = seg(P, 0);
             S0.a_map = xmap;
-            S0.b_map[0] = b.map(Ls[i]->W.w, ns[i], d, d, 256);
+            S0.b_map[0] = b.map(Ls[i]->W.w, ns[i], d, d, 128);
+            S0.b_rank_off = 128;
             S0.kext = (int32_t)d;
             Seg& S1 = seg(P, 1);
             S1.a_map = amap;
             S1.a_xoff = i * rp;
-            S1.b_map[0] = b.map(Ls[i]->B, ns[i], r, r, 256);
+            S1.b_map[0] = b.map(Ls[i]->B, ns[i], r, r, 128);
+            S1.b_rank_off = 128;
             S1.kext = rp;
             P.out0 = outs[i];
             P.ld_out = ns[i];
@@ -1310,7 +1325,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         P.ld_out = d;
         LM_TRY(b.launch("qkv.dX", sms, err, st));
     } else {  // dX = sum_x dOut_x W_x + G_x A_x
-        Builder b(G_STORE_KMN);
+        Builder b(G2_STORE_MN);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
@@ -1322,12 +1337,14 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             Seg& S = seg(P, i);
             S.a_map = b.map(dOut[i], T, ns[i], ns[i], 128);
             S.b_map[0] = b.map(Ls[i]->W.w, ns[i], d, d, 64);
+            S.b_rank_off = 128;
             S.kext = (int32_t)ns[i];
         }
         for (int i = 0; i < 3; ++i) {
             Seg& S = seg(P, 3 + i);
             S.a_map = b.map(g[i], T, rp, rp, 128);
             S.b_map[0] = b.map(Ls[i]->A, r, d, d, 64);
+            S.b_rank_off = 128;
             S.kext = rp;
         }
         P.out0 = dX;
@@ -1420,7 +1437,7 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         P.ld_out = d_out;
         LM_TRY(b.launch("o.fwd", sms, err, st));
     } else {
-        Builder b(G_STORE_KK);
+        Builder b(G2_STORE_K);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d_out;
@@ -1430,11 +1447,13 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         P.out_col_step = 256;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(X, T, d_in, d_in, 128);
-        S0.b_map[0] = b.map(o->W.w, d_out, d_in, d_in, 256);
+        S0.b_map[0] = b.map(o->W.w, d_out, d_in, d_in, 128);
+        S0.b_rank_off = 128;
         S0.kext = (int32_t)d_in;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(xa, T, rp, rp, 128);
-        S1.b_map[0] = b.map(o->B, d_out, r, r, 256);
+        S1.b_map[0] = b.map(o->B, d_out, r, r, 128);
+        S1.b_rank_off = 128;
         S1.kext = rp;
         P.out0 = Y;
         P.ld_out = d_out;
@@ -1517,7 +1536,7 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         P.ld_out = d_in;
         LM_TRY(b.launch("o.dX", sms, err, st));
     } else {  // dX = dY W + G A
-        Builder b(G_STORE_KMN);
+        Builder b(G2_STORE_MN);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d_in;
@@ -1528,10 +1547,12 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(dY, T, d_out, d_out, 128);
         S0.b_map[0] = b.map(o->W.w, d_out, d_in, d_in, 64);
+        S0.b_rank_off = 128;
         S0.kext = (int32_t)d_out;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(g, T, rp, rp, 128);
         S1.b_map[0] = b.map(o->A, r, d_in, d_in, 64);
+        S1.b_rank_off = 128;
         S1.kext = rp;
         P.out0 = dX;
         P.ld_out = d_in;

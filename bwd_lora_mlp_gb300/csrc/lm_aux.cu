@@ -81,6 +81,35 @@ cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t 
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ block-diagonal rank-r operand
+__global__ void __launch_bounds__(256) blockdiag_kernel(const uint16_t* __restrict__ Bg,
+                                                        const uint16_t* __restrict__ Bu, int64_t n, int r,
+                                                        int rp, uint16_t* __restrict__ out) {
+    const int64_t cols = 2 * rp;
+    const int64_t total = 2 * n * cols;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = idx / cols;
+        const int col = (int)(idx - row * cols);
+        uint16_t v = 0;
+        if (row < n) {
+            if (col < r) v = Bg[row * r + col];
+        } else {
+            const int c = col - rp;
+            if (c >= 0 && c < r) v = Bu[(row - n) * r + c];
+        }
+        out[idx] = v;
+    }
+}
+
+cudaError_t launch_blockdiag(const uint16_t* Bg, const uint16_t* Bu, int64_t n, int r, int rp, uint16_t* out,
+                             cudaStream_t st) {
+    const int64_t total = 2 * n * 2 * rp;
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, 2048);
+    blockdiag_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, st>>>(Bg, Bu, n, r, rp, out);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ NF4
 // The 16 NormalFloat-4 values as printed in the QLoRA paper (Dettmers et al. 2023, appendix
 // "NormalFloat 4-bit data type"); every literal is an exact fp32 value.

@@ -44,6 +44,7 @@ struct Seg {
     int32_t a_xoff;       // added to the K coordinate of A
     int32_t b_nf4[2];     // NF4 kernel: index into Params::nf4 of the weight whose codes b_map[i]
                           // holds (-1: b_map[i] is a bf16 operand loaded as is)
+    int32_t b_rank_off;   // CTA-pair kernel: B rows (K-major) / columns (MN-major) CTA 1 adds
 };
 
 // An NF4-packed base weight as the decode warps of the NF4 GEMM see it.

@@ -22,10 +22,22 @@ enum GemmKind : int {
     G_NF4_STORE_K = 8,   // K-major NF4 B, STORE
     G_NF4_GLU_BWD = 9,   // MN-major NF4 B, GLU_BWD
     G_NF4_STORE_MN = 10, // MN-major NF4 B, STORE
-    G_NUM_KINDS = 11
+    // bf16 base, CTA pair (cta_group::2), 256 x 256 tiles
+    G2_GLU_FWD = 11,     // K-major B, GLU_FWD
+    G2_STORE_K = 12,     // K-major B, STORE
+    G2_GLU_BWD = 13,     // MN-major B, GLU_BWD
+    G2_STORE_MN = 14,    // MN-major B, STORE
+    G_NUM_KINDS = 15
 };
 
-inline bool gemm_is_nf4(GemmKind k) { return k >= G_NF4_GLU_FWD; }
+inline bool gemm_is_nf4(GemmKind k) { return k >= G_NF4_GLU_FWD && k <= G_NF4_STORE_MN; }
+inline bool gemm_is_pair(GemmKind k) { return k >= G2_GLU_FWD && k <= G2_STORE_MN; }
+// Launches at most `max_units` CTA pairs (fewer if fewer pairs fit on the device at once).
+cudaError_t launch_gemm_pair(GemmKind k, const Params& p, int max_units, cudaStream_t st);
+
+// [Bg | 0 ; 0 | Bu]: (2n x 2rp) bf16, the rank-r operand of the CTA-pair gate/up GEMM.
+cudaError_t launch_blockdiag(const uint16_t* Bg, const uint16_t* Bu, int64_t n, int r, int rp, uint16_t* out,
+                             cudaStream_t st);
 cudaError_t launch_gemm_nf4(GemmKind k, const Params& p, int grid, cudaStream_t st);
 
 int gemm_bn_max(GemmKind k);
