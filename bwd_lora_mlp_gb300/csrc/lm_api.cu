@@ -773,8 +773,11 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         // CTA pair: CTA 0 holds the 128 W_g rows of a tile, CTA 1 the matching 128 W_u rows;
         // the rank-r segment multiplies [s XAg | s XAu] by the block-diagonal [Bg | 0 ; 0 | Bu]
         uint16_t* bdiag = at<uint16_t>(ws, PL.bdiag);
-        const cudaError_t be = launch_blockdiag(gate->B, up->B, n, r, rp, bdiag, st);
-        if (be != cudaSuccess) return cuda_fail(be, "rank-r operand launch");
+        {
+            ProfScope prof("mlp.bdiag", st);
+            const cudaError_t be = launch_blockdiag(gate->B, up->B, n, r, rp, bdiag, st);
+            if (be != cudaSuccess) return cuda_fail(be, "rank-r operand launch");
+        }
         Builder b(G2_GLU_FWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;

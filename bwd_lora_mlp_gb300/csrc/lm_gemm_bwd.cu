@@ -1,4 +1,5 @@
-// Instantiations of the backward-pass GEMM variants and the variant dispatcher.
+// Instantiations of the one-CTA split-K GEMMs for the rank-r output-gradient projections and the
+// dA / dB column reductions, and the dispatcher over every GEMM variant.
 #include "lm_internal.h"
 
 namespace lm {
@@ -22,14 +23,8 @@ static cudaError_t launch_variant(const Params& p, int grid, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-int gemm_bn_max(GemmKind k) { return (k == G_PART_KMN || k == G_PART_MNK) ? 64 : 256; }
-bool gemm_a_mn(GemmKind k) { return k == G_PART_MNK; }
-bool gemm_b_mn(GemmKind k) { return k == G_GLU_BWD || k == G_STORE_KMN || k == G_PART_KMN; }
-
 cudaError_t launch_gemm(GemmKind k, const Params& p, int grid, cudaStream_t st) {
     switch (k) {
-        case G_GLU_BWD: return launch_variant<256, false, true, EPI_GLU_BWD>(p, grid, st);
-        case G_STORE_KMN: return launch_variant<256, false, true, EPI_STORE>(p, grid, st);
         case G_PART_KMN: return launch_variant<64, false, true, EPI_PARTIAL>(p, grid, st);
         case G_PART_MNK: return launch_variant<64, true, false, EPI_PARTIAL>(p, grid, st);
         case G_NF4_GLU_FWD:

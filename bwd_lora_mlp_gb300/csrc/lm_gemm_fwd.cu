@@ -1,4 +1,4 @@
-// Instantiations of the forward-pass GEMM variants.
+// Instantiation of the one-CTA split-K GEMM for the rank-r input projections (X A^T, h A^T).
 #include "lm_internal.h"
 
 namespace lm {
@@ -22,8 +22,6 @@ static cudaError_t launch_variant(const Params& p, int grid, cudaStream_t st) {
 
 cudaError_t launch_gemm_fwd(GemmKind k, const Params& p, int grid, cudaStream_t st) {
     switch (k) {
-        case G_GLU_FWD: return launch_variant<256, false, false, EPI_GLU_FWD>(p, grid, st);
-        case G_STORE_KK: return launch_variant<256, false, false, EPI_STORE>(p, grid, st);
         case G_PART_KK: return launch_variant<256, false, false, EPI_PARTIAL>(p, grid, st);
         default: return cudaErrorInvalidValue;
     }

@@ -8,12 +8,8 @@
 
 namespace lm {
 
-// The GEMM variants built (BN_MAX, A major, B major, epilogue).
+// The GEMM variants built.  One-CTA split-K kernels (BN_MAX, A major, B major, epilogue):
 enum GemmKind : int {
-    G_GLU_FWD = 0,   // 256, K, K, GLU_FWD    gate/up forward with fused SwiGLU / GeGLU
-    G_STORE_KK = 1,  // 256, K, K, STORE      down / O / QKV forward
-    G_GLU_BWD = 2,   // 256, K, MN, GLU_BWD   dh = dY Wd (+ rank-r) with fused activation backward
-    G_STORE_KMN = 3, // 256, K, MN, STORE     dX = sum dOut W (+ rank-r)
     G_PART_KK = 4,   // 256, K, K, PARTIAL    X A^T (rank-r input projection), split-K partials
     G_PART_KMN = 5,  //  64, K, MN, PARTIAL   dOut B (rank-r output-gradient projection)
     G_PART_MNK = 6,  //  64, MN, K, PARTIAL   column reductions over T for dA / dB
@@ -40,9 +36,6 @@ cudaError_t launch_blockdiag(const uint16_t* Bg, const uint16_t* Bu, int64_t n, 
                              cudaStream_t st);
 cudaError_t launch_gemm_nf4(GemmKind k, const Params& p, int grid, cudaStream_t st);
 
-int gemm_bn_max(GemmKind k);
-bool gemm_a_mn(GemmKind k);
-bool gemm_b_mn(GemmKind k);
 cudaError_t launch_gemm(GemmKind k, const Params& p, int grid, cudaStream_t st);
 
 // Finalisation of split-K partials of rank-r projections:
