@@ -353,11 +353,11 @@ struct Builder {
 
     explicit Builder(GemmKind k) : kind(k) {
         memset(&p, 0, sizeof p);
-        if (gemm_is_nf4(k)) {
+        if (gemm_is_pair(k)) tile_m = 256;
+        if (gemm_is_pair_nf4(k)) {
             tile_m = 256;
             nf4_codebook_host(p.nf4_code);
         }
-        if (gemm_is_pair(k)) tile_m = 256;
     }
 
     // 2D uint8 tensor (NF4 codes: rows x cols bytes), box = box_w bytes x box_rows rows, no swizzle
@@ -469,8 +469,9 @@ struct Builder {
         const int grid = finish(sms, err);
         if (grid == 0) return LM_OK;
         ProfScope prof(tag, st_);
-        const cudaError_t e = gemm_is_pair(kind) ? launch_gemm_pair(kind, p, p.total_units, st_)
-                                                 : launch_gemm(kind, p, grid, st_);
+        const cudaError_t e = gemm_is_pair(kind)       ? launch_gemm_pair(kind, p, p.total_units, st_)
+                              : gemm_is_pair_nf4(kind) ? launch_gemm_pair_nf4(kind, p, p.total_units, st_)
+                                                       : launch_gemm(kind, p, grid, st_);
         if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
         return LM_OK;
     }
@@ -738,32 +739,35 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(fin_rows("mlp.xa.fin", b, {FinRowJob{part, T * 2 * rp, 0, 2 * rp, rp, {gate->s, up->s, 0.f}, xa, xaT, D.ldT}}, T, st));
     }
     if (nf4) {
-        // NF4 base: 256 x 128 tiles of 64 gate + 64 up columns, codes decoded in the mainloop
-        Builder b(G_NF4_GLU_FWD);
+        // NF4 base, CTA pair: CTA 0 decodes 128 W_g rows of a tile, CTA 1 the matching W_u rows;
+        // the rank-r segment multiplies [s XAg | s XAu] by the block-diagonal [Bg | 0 ; 0 | Bu]
+        uint16_t* bdiag = at<uint16_t>(ws, PL.bdiag);
+        {
+            ProfScope prof("mlp.bdiag", st);
+            const cudaError_t be = launch_blockdiag(gate->B, up->B, n, r, rp, bdiag, st);
+            if (be != cudaSuccess) return cuda_fail(be, "rank-r operand launch");
+        }
+        Builder b(G2N_GLU_FWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)n;
-        P.bn = 128;
-        P.tiles_n = (int32_t)((n + 63) / 64);
-        P.n_step = 64;
-        P.out_col_step = 64;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((n + 127) / 128);
+        P.n_step = 128;
+        P.out_col_step = 128;
         P.act = act;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(X, T, d, d, 128);
-        S0.b_map[0] = b.codes_k(gate->W, 64);
-        S0.b_map[1] = b.codes_k(up->W, 64);
+        S0.b_map[0] = b.codes_k(gate->W, 128);
+        S0.b_map[1] = b.codes_k(up->W, 128);
         S0.b_nf4[0] = b.nf4src(gate->W);
         S0.b_nf4[1] = b.nf4src(up->W);
-        S0.b_rows = 64;
         S0.kext = (int32_t)d;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(xa, T, 2 * rp, 2 * rp, 128);
-        S1.b_map[0] = b.map(gate->B, n, r, r, 64);
-        S1.b_map[1] = b.map(up->B, n, r, r, 64);
-        S1.b_xoff[1] = -rp;
-        S1.b_rows = 64;
+        S1.b_map[0] = b.map(bdiag, n, 2 * rp, 2 * rp, 128);
+        S1.b_map[1] = b.map(bdiag + (size_t)n * 2 * rp, n, 2 * rp, 2 * rp, 128);
         S1.kext = 2 * rp;
-        S1.dual_split = rp;
         P.out0 = e_save;
         P.out1 = u_save;
         P.out2 = h_save;
@@ -810,22 +814,24 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(fin_rows("mlp.ha.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, ha, haT, D.ldT}}, T, st));
     }
     if (nf4) {
-        Builder b(G_NF4_STORE_K);
+        Builder b(G2N_STORE_K);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
-        P.bn = 128;
-        P.tiles_n = (int32_t)((d + 127) / 128);
-        P.n_step = 128;
-        P.out_col_step = 128;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((d + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(h_save, T, n, n, 128);
         S0.b_map[0] = b.codes_k(down->W, 128);
         S0.b_nf4[0] = b.nf4src(down->W);
+        S0.b_rank_off = 128;
         S0.kext = (int32_t)n;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(ha, T, rp, rp, 128);
         S1.b_map[0] = b.map(down->B, d, r, r, 128);
+        S1.b_rank_off = 128;
         S1.kext = rp;
         P.out0 = y;
         P.ld_out = d;
@@ -927,23 +933,25 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(fin_rows("mlp.gd.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st));
     }
     if (nf4) {
-        Builder b(G_NF4_GLU_BWD);
+        Builder b(G2N_GLU_BWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)n;
-        P.bn = 128;
-        P.tiles_n = (int32_t)((n + 127) / 128);
-        P.n_step = 128;
-        P.out_col_step = 128;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((n + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
         P.act = act;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(dY, T, d, d, 128);
         S0.b_map[0] = b.codes_mn(down->W);
         S0.b_nf4[0] = b.nf4src(down->W);
+        S0.b_rank_off = 128;
         S0.kext = (int32_t)d;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(gd, T, rp, rp, 128);
         S1.b_map[0] = b.map(down->A, r, n, n, 64);
+        S1.b_rank_off = 128;
         S1.kext = rp;
         P.in0 = e_save;
         P.in1 = u_save;
@@ -1014,14 +1022,14 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(fin_cols("mlp.dAdB.fin", b, js, 6, st));
     }
     if (nf4) {
-        Builder b(G_NF4_STORE_MN);
+        Builder b(G2N_STORE_MN);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
-        P.bn = 128;
-        P.tiles_n = (int32_t)((d + 127) / 128);
-        P.n_step = 128;
-        P.out_col_step = 128;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((d + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
         const lm_lora* Ls[2] = {gate, up};
         const uint16_t* dOut[2] = {de, du};
         const uint16_t* G[2] = {gg, gu};
@@ -1030,10 +1038,12 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
             S.a_map = b.map(dOut[i], T, n, n, 128);
             S.b_map[0] = b.codes_mn(Ls[i]->W);
             S.b_nf4[0] = b.nf4src(Ls[i]->W);
+            S.b_rank_off = 128;
             S.kext = (int32_t)n;
             Seg& R = seg(P, 2 + i);
             R.a_map = b.map(G[i], T, rp, rp, 128);
             R.b_map[0] = b.map(Ls[i]->A, r, d, d, 64);
+            R.b_rank_off = 128;
             R.kext = rp;
         }
         P.out0 = dX;
@@ -1151,7 +1161,7 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         LM_TRY(fin_rows("qkv.xa.fin", b, {FinRowJob{part, T * 3 * rp, 0, 3 * rp, rp, {q->s, k->s, v->s}, xa, xaT, D.ldT}}, T, st));
     }
     if (nf4) {
-        Builder b(G_NF4_STORE_K);
+        Builder b(G2N_STORE_K);
         const int xmap = b.map(X, T, d, d, 128);
         const int amap = b.map(xa, T, 3 * rp, 3 * rp, 128);
         const lm_lora* Ls[3] = {q, k, v};
@@ -1161,19 +1171,21 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             Prob& P = b.prob();
             P.M = (int32_t)T;
             P.N = (int32_t)ns[i];
-            P.bn = 128;
-            P.tiles_n = (int32_t)((ns[i] + 127) / 128);
-            P.n_step = 128;
-            P.out_col_step = 128;
+            P.bn = 256;
+            P.tiles_n = (int32_t)((ns[i] + 255) / 256);
+            P.n_step = 256;
+            P.out_col_step = 256;
             Seg& S0 = seg(P, 0);
             S0.a_map = xmap;
             S0.b_map[0] = b.codes_k(Ls[i]->W, 128);
             S0.b_nf4[0] = b.nf4src(Ls[i]->W);
+            S0.b_rank_off = 128;
             S0.kext = (int32_t)d;
             Seg& S1 = seg(P, 1);
             S1.a_map = amap;
             S1.a_xoff = i * rp;
             S1.b_map[0] = b.map(Ls[i]->B, ns[i], r, r, 128);
+            S1.b_rank_off = 128;
             S1.kext = rp;
             P.out0 = outs[i];
             P.ld_out = ns[i];
@@ -1303,25 +1315,27 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         LM_TRY(fin_cols("qkv.dAdB.fin", b, js, 6, st));
     }
     if (nf4) {  // dX = sum_x dOut_x W_x + G_x A_x
-        Builder b(G_NF4_STORE_MN);
+        Builder b(G2N_STORE_MN);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
-        P.bn = 128;
-        P.tiles_n = (int32_t)((d + 127) / 128);
-        P.n_step = 128;
-        P.out_col_step = 128;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((d + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
         for (int i = 0; i < 3; ++i) {
             Seg& S = seg(P, i);
             S.a_map = b.map(dOut[i], T, ns[i], ns[i], 128);
             S.b_map[0] = b.codes_mn(Ls[i]->W);
             S.b_nf4[0] = b.nf4src(Ls[i]->W);
+            S.b_rank_off = 128;
             S.kext = (int32_t)ns[i];
         }
         for (int i = 0; i < 3; ++i) {
             Seg& S = seg(P, 3 + i);
             S.a_map = b.map(g[i], T, rp, rp, 128);
             S.b_map[0] = b.map(Ls[i]->A, r, d, d, 64);
+            S.b_rank_off = 128;
             S.kext = rp;
         }
         P.out0 = dX;
@@ -1419,22 +1433,24 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         LM_TRY(fin_rows("o.xa.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st));
     }
     if (nf4) {
-        Builder b(G_NF4_STORE_K);
+        Builder b(G2N_STORE_K);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d_out;
-        P.bn = 128;
-        P.tiles_n = (int32_t)((d_out + 127) / 128);
-        P.n_step = 128;
-        P.out_col_step = 128;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((d_out + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(X, T, d_in, d_in, 128);
         S0.b_map[0] = b.codes_k(o->W, 128);
         S0.b_nf4[0] = b.nf4src(o->W);
+        S0.b_rank_off = 128;
         S0.kext = (int32_t)d_in;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(xa, T, rp, rp, 128);
         S1.b_map[0] = b.map(o->B, d_out, r, r, 128);
+        S1.b_rank_off = 128;
         S1.kext = rp;
         P.out0 = Y;
         P.ld_out = d_out;
@@ -1518,22 +1534,24 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         LM_TRY(fin_cols("o.dAdB.fin", b, js, 2, st));
     }
     if (nf4) {  // dX = dY W + G A
-        Builder b(G_NF4_STORE_MN);
+        Builder b(G2N_STORE_MN);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d_in;
-        P.bn = 128;
-        P.tiles_n = (int32_t)((d_in + 127) / 128);
-        P.n_step = 128;
-        P.out_col_step = 128;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((d_in + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(dY, T, d_out, d_out, 128);
         S0.b_map[0] = b.codes_mn(o->W);
         S0.b_nf4[0] = b.nf4src(o->W);
+        S0.b_rank_off = 128;
         S0.kext = (int32_t)d_out;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(g, T, rp, rp, 128);
         S1.b_map[0] = b.map(o->A, r, d_in, d_in, 64);
+        S1.b_rank_off = 128;
         S1.kext = rp;
         P.out0 = dX;
         P.ld_out = d_in;

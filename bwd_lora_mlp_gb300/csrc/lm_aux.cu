@@ -4,6 +4,7 @@
 #include <cmath>
 
 #include "lm_internal.h"
+#include "lm_nf4_table.cuh"
 
 namespace lm {
 
@@ -111,26 +112,7 @@ cudaError_t launch_blockdiag(const uint16_t* Bg, const uint16_t* Bu, int64_t n, 
 }
 
 // ------------------------------------------------------------------ NF4
-// The 16 NormalFloat-4 values as printed in the QLoRA paper (Dettmers et al. 2023, appendix
-// "NormalFloat 4-bit data type"); every literal is an exact fp32 value.
-static const float kNf4Code[16] = {
-    -1.0f,
-    -0.6961928009986877f,
-    -0.5250730514526367f,
-    -0.39491748809814453f,
-    -0.28444138169288635f,
-    -0.18477343022823334f,
-    -0.09105003625154495f,
-    0.0f,
-    0.07958029955625534f,
-    0.16093020141124725f,
-    0.24611230194568634f,
-    0.33791524171829224f,
-    0.44070982933044434f,
-    0.5626170039176941f,
-    0.7229568362236023f,
-    1.0f,
-};
+static const float* const kNf4Code = kNf4Values;
 
 void nf4_codebook_host(float* out16) {
     for (int i = 0; i < 16; ++i) out16[i] = kNf4Code[i];

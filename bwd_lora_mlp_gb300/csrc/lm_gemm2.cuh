@@ -3,7 +3,7 @@
 // A work unit is a 256 x 256 tile.  CTA r of the pair loads rows [128 r, 128 r + 128) of the A
 // tile and half of the B tile (the operand rows that feed accumulator columns
 // [128 r, 128 r + 128)), 32 KB per 64-deep K block instead of the one-CTA kernel's 48 KB, so
-// six stages fit.  CTA 0 issues tcgen05.mma.cta_group::2 with M = 256: the hardware reads A and
+// seven stages fit.  CTA 0 issues tcgen05.mma.cta_group::2 with M = 256: the hardware reads A and
 // B from both CTAs' shared memory at the same offsets and writes each CTA's 128 accumulator rows
 // into that CTA's TMEM.  Both CTAs' TMA loads complete on CTA 0's stage barrier (CTA 0 expects
 // the pair's bytes); MMA completion is multicast to both CTAs' stage-free and tile-ready
@@ -21,7 +21,7 @@ struct Gemm2Cfg {
     static constexpr int A_BYTES = kBM * kBK * 2;   // this CTA's 128 A rows
     static constexpr int B_BYTES = 128 * kBK * 2;   // this CTA's half of the B tile
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = 6;
+    static constexpr int STAGES = 7;
     static constexpr int TMEM_COLS = 512;           // two 256-column accumulators
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
 };

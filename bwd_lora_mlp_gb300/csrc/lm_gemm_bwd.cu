@@ -27,10 +27,6 @@ cudaError_t launch_gemm(GemmKind k, const Params& p, int grid, cudaStream_t st) 
     switch (k) {
         case G_PART_KMN: return launch_variant<64, false, true, EPI_PARTIAL>(p, grid, st);
         case G_PART_MNK: return launch_variant<64, true, false, EPI_PARTIAL>(p, grid, st);
-        case G_NF4_GLU_FWD:
-        case G_NF4_STORE_K:
-        case G_NF4_GLU_BWD:
-        case G_NF4_STORE_MN: return launch_gemm_nf4(k, p, grid, st);
         default: return launch_gemm_fwd(k, p, grid, st);
     }
 }

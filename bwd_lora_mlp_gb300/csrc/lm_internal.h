@@ -13,29 +13,28 @@ enum GemmKind : int {
     G_PART_KK = 4,   // 256, K, K, PARTIAL    X A^T (rank-r input projection), split-K partials
     G_PART_KMN = 5,  //  64, K, MN, PARTIAL   dOut B (rank-r output-gradient projection)
     G_PART_MNK = 6,  //  64, MN, K, PARTIAL   column reductions over T for dA / dB
-    // NF4 base weight decoded in the mainloop; 256 x 128 tiles
-    G_NF4_GLU_FWD = 7,   // K-major NF4 B, GLU_FWD
-    G_NF4_STORE_K = 8,   // K-major NF4 B, STORE
-    G_NF4_GLU_BWD = 9,   // MN-major NF4 B, GLU_BWD
-    G_NF4_STORE_MN = 10, // MN-major NF4 B, STORE
     // bf16 base, CTA pair (cta_group::2), 256 x 256 tiles
     G2_GLU_FWD = 11,     // K-major B, GLU_FWD
     G2_STORE_K = 12,     // K-major B, STORE
     G2_GLU_BWD = 13,     // MN-major B, GLU_BWD
     G2_STORE_MN = 14,    // MN-major B, STORE
-    G_NUM_KINDS = 15
+    // NF4 base decoded in the mainloop, CTA pair, 256 x 256 tiles
+    G2N_GLU_FWD = 15,
+    G2N_STORE_K = 16,
+    G2N_GLU_BWD = 17,
+    G2N_STORE_MN = 18,
+    G_NUM_KINDS = 19
 };
 
-inline bool gemm_is_nf4(GemmKind k) { return k >= G_NF4_GLU_FWD && k <= G_NF4_STORE_MN; }
 inline bool gemm_is_pair(GemmKind k) { return k >= G2_GLU_FWD && k <= G2_STORE_MN; }
-// Launches at most `max_units` CTA pairs (fewer if fewer pairs fit on the device at once).
+inline bool gemm_is_pair_nf4(GemmKind k) { return k >= G2N_GLU_FWD && k <= G2N_STORE_MN; }
+// Launch at most `max_units` CTA pairs (fewer if fewer pairs fit on the device at once).
 cudaError_t launch_gemm_pair(GemmKind k, const Params& p, int max_units, cudaStream_t st);
+cudaError_t launch_gemm_pair_nf4(GemmKind k, const Params& p, int max_units, cudaStream_t st);
 
 // [Bg | 0 ; 0 | Bu]: (2n x 2rp) bf16, the rank-r operand of the CTA-pair gate/up GEMM.
 cudaError_t launch_blockdiag(const uint16_t* Bg, const uint16_t* Bu, int64_t n, int r, int rp, uint16_t* out,
                              cudaStream_t st);
-cudaError_t launch_gemm_nf4(GemmKind k, const Params& p, int grid, cudaStream_t st);
-
 cudaError_t launch_gemm(GemmKind k, const Params& p, int grid, cudaStream_t st);
 
 // Finalisation of split-K partials of rank-r projections:
