@@ -355,7 +355,7 @@ struct Builder {
         memset(&p, 0, sizeof p);
         if (gemm_is_pair(k)) tile_m = 256;
         if (gemm_is_pair_nf4(k)) {
-            tile_m = 256;
+            tile_m = 512;
             nf4_codebook_host(p.nf4_code);
         }
     }

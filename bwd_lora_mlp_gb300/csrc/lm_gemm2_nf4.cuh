@@ -2,9 +2,12 @@
 // ("loralei" README, QLoRA section: unpacking and double-scale reconstruction fused into the
 // matmul).
 //
-// Each CTA of the pair holds 128 A rows and half of the 256-wide B tile per 64-deep K block.  TMA
-// brings the A rows and the raw NF4 codes of that B half (4 KB) into the CTA's own stage and
-// completes on the CTA's own stage barrier; decode warps turn every 64-element NF4 block into a
+// A work unit is a 512 x 256 tile: per 64-deep K block each CTA of the pair holds 2 x 128 A rows
+// (one set per M half) and half of the 256-wide B tile, and CTA 0 issues two M = 256 pair MMAs
+// per K step that share the decoded B tile, so each decoded weight element feeds 512 output rows
+// (decode work per MMA cycle is half that of a 256 x 256 tile).  The accumulator (2 M halves x 256
+// columns) fills TMEM, so it is single-buffered.  TMA brings the A rows and the raw NF4 codes of
+// the CTA's B half (4 KB) into the CTA's own stage and completes on the CTA's own stage barrier; decode warps turn every 64-element NF4 block into a
 // 128-byte swizzled bf16 row of the B tile and then report to CTA 0's decoded barrier, which
 // counts both CTAs' decoders, so CTA 0's MMA thread starts a K block only when both halves of B
 // and both A halves are in place.
@@ -16,8 +19,10 @@
 // each table by the nibble's top bit.  No shared-memory table is read, which keeps the shared
 // memory bandwidth for the MMA operands.
 //
-// Roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer (CTA 0), warps 2-9 decoders in two
-// groups of four that take alternate K blocks (one thread per NF4 block), warps 10-17 epilogue.
+// Roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer (CTA 0), warps 2-9 decoders in four
+// groups of two that take K blocks round-robin, so four K blocks are decoded at once (each thread
+// decodes two NF4 blocks per K block and fetches the scales of its group's next K block while
+// decoding), warps 10-17 epilogue.
 #pragma once
 
 #include "lm_gemm2.cuh"
@@ -26,15 +31,17 @@
 namespace lm {
 
 constexpr int kPairNf4DecodeWarps = 8;
+constexpr int kPairNf4DecodeGroups = 4;   // groups take K blocks round-robin
+constexpr int kPairNf4GroupWarps = kPairNf4DecodeWarps / kPairNf4DecodeGroups;
 constexpr int kPairNf4Threads = 64 + 32 * kPairNf4DecodeWarps + 32 * kNumEpiWarps;
 
 struct Gemm2Nf4Cfg {
-    static constexpr int A_BYTES = kBM * kBK * 2;   // this CTA's 128 A rows
-    static constexpr int B_BYTES = 128 * kBK * 2;   // this CTA's half of B, decoded (or bf16 via TMA)
-    static constexpr int C_BYTES = 4096;            // raw codes of that half
+    static constexpr int A_BYTES = 2 * kBM * kBK * 2;  // this CTA's 2 x 128 A rows (one per M half)
+    static constexpr int B_BYTES = 128 * kBK * 2;      // this CTA's half of B, decoded (or bf16 via TMA)
+    static constexpr int C_BYTES = 4096;               // raw codes of that half
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + C_BYTES;
-    static constexpr int STAGES = 6;
-    static constexpr int TMEM_COLS = 512;
+    static constexpr int STAGES = 4;
+    static constexpr int TMEM_COLS = 512;              // one accumulator: 2 M halves x 256 columns
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
 };
@@ -84,6 +91,67 @@ __device__ __forceinline__ void nf4_decode_block_regs(uint4 c0, uint4 c1, float 
     }
 }
 
+// Walks the (work unit, K segment, K block) sequence every role of a pair kernel follows.
+struct KBlockIter {
+    int u, si, kb;
+    Unit U;
+    __device__ __forceinline__ bool valid(const Params& p) const { return u < p.total_units; }
+    __device__ __forceinline__ void settle(const Params& p, int stride) {
+        while (u < p.total_units) {
+            const Prob& P = p.prob[U.pi];
+            if (si < P.nseg) {
+                if (kb < (P.seg[si].kext + kBK - 1) / kBK) return;
+                ++si;
+                kb = 0;
+                continue;
+            }
+            u += stride;
+            si = 0;
+            kb = 0;
+            if (u < p.total_units) U = decode_unit(p, u);
+        }
+    }
+    __device__ __forceinline__ void start(const Params& p, int first, int stride) {
+        u = first;
+        si = 0;
+        kb = 0;
+        if (u < p.total_units) U = decode_unit(p, u);
+        settle(p, stride);
+    }
+    __device__ __forceinline__ void next(const Params& p, int stride) {
+        ++kb;
+        settle(p, stride);
+    }
+};
+
+// Block scale fp32(q * c) of NF4 block `t` (0..127) of CTA `rank`'s half of the B tile at K block
+// `it`, and whether the block lies inside the weight (false also for bf16 segments).  K-major:
+// block t is B row t; MN-major: K row t & 63, 64-wide N chunk t >> 6.
+template <bool B_MN>
+__device__ __forceinline__ float nf4_block_scale(const Params& p, const KBlockIter& it, uint32_t rank, int t,
+                                                 bool& valid) {
+    valid = false;
+    if (!it.valid(p)) return 0.0f;
+    const Prob& P = p.prob[it.U.pi];
+    const Seg& S = P.seg[it.si];
+    if (S.b_nf4[0] < 0) return 0.0f;
+    const Nf4Src& W = p.nf4[(rank == 1 && S.b_nf4[1] >= 0) ? S.b_nf4[1] : S.b_nf4[0]];
+    const int64_t bcol0 = (int64_t)it.U.nb * P.n_step + (int64_t)rank * S.b_rank_off;
+    int64_t b;
+    if constexpr (B_MN) {
+        const int64_t krow = (int64_t)it.kb * kBK + (t & 63);
+        const int64_t ncol = bcol0 + (t >> 6) * 64;
+        valid = krow < W.rows && ncol < W.cols;
+        b = (krow * W.cols + ncol) >> 6;
+    } else {
+        const int64_t row = bcol0 + t;
+        valid = row < W.rows;
+        b = row * (W.cols >> 6) + it.kb;
+    }
+    if (!valid) return 0.0f;
+    return __fmul_rn((float)__ldg(W.absmax_q + b), __ldg(W.scale + (b >> 8)));
+}
+
 template <bool B_MN, int EPI>
 __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __grid_constant__ Params p) {
     using C = Gemm2Nf4Cfg;
@@ -107,7 +175,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&bready[s]), 2 * (kPairNf4DecodeWarps / 2));
+            mbar_init(smem_u32(&bready[s]), 2 * kPairNf4GroupWarps);
             mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -157,7 +225,8 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                         const uint32_t fb = smem_u32(&full[stage]);
                         const int kx = kb * kBK;
                         mbar_expect_tx(fb, C::A_BYTES + (nf4 ? (uint32_t)p.map_bytes[bmap] : (uint32_t)C::B_BYTES));
-                        tma_load_2d(sA, &p.maps[S.a_map], fb, kx + S.a_xoff, U.mb * 256 + (int)rank * kBM);
+                        tma_load_2d(sA, &p.maps[S.a_map], fb, kx + S.a_xoff, U.mb * 512 + (int)rank * kBM);
+                        tma_load_2d(sA + 16384, &p.maps[S.a_map], fb, kx + S.a_xoff, U.mb * 512 + 256 + (int)rank * kBM);
                         if (nf4) {
                             if constexpr (B_MN) tma_load_2d(sC, &p.maps[bmap], fb, brow / 2, kx);
                             else tma_load_2d(sC, &p.maps[bmap], fb, kx / 2, brow);
@@ -183,18 +252,16 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
         if (lane == 0 && rank == 0) {  // ---------------- MMA issuer (CTA 0 only)
             int stage = 0;
             uint32_t phase = 0;
-            int acc = 0;
-            uint32_t aphase = 0;
+            uint32_t aphase = 0;  // one accumulator: its free / ready phases flip every tile
             bool ok = true;
             for (int u = cid; ok && u < p.total_units; u += ncl) {
                 const Unit U = decode_unit(p, u);
                 const Prob& P = p.prob[U.pi];
-                if (!mbar_wait(smem_u32(&tempty[acc]), aphase ^ 1u, s_abort)) {
+                if (!mbar_wait(smem_u32(&tempty[0]), aphase ^ 1u, s_abort)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d0 = tmem_base + acc * 256;
                 const uint32_t idesc = make_idesc_bf16(256, P.bn, false, B_MN);
                 uint32_t accum = 0;
                 for (int si = 0; ok && si < P.nseg; ++si) {
@@ -211,10 +278,12 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                         const int rem = S.kext - kb * kBK;
                         const int nsteps = rem >= kBK ? 4 : (rem + 15) >> 4;
                         for (int ks = 0; ks < nsteps; ++ks) {
-                            const uint64_t ad = make_sdesc_sw128(sA + ks * 32, 16, 1024);
                             const uint64_t bd = B_MN ? make_sdesc_sw128(sB + ks * 2048, 8192, 1024)
                                                      : make_sdesc_sw128(sB + ks * 32, 16, 1024);
-                            umma_bf16_pair(d0, ad, bd, idesc, accum);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h)  // both M halves share the decoded B tile
+                                umma_bf16_pair(tmem_base + h * 256, make_sdesc_sw128(sA + h * 16384 + ks * 32, 16, 1024),
+                                               bd, idesc, accum);
                             accum = 1;
                         }
                         umma_commit_pair(smem_u32(&empty[stage]), 0x3);
@@ -225,9 +294,8 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair(smem_u32(&tfull[acc]), 0x3);
-                acc ^= 1;
-                if (acc == 0) aphase ^= 1u;
+                umma_commit_pair(smem_u32(&tfull[0]), 0x3);
+                aphase ^= 1u;
             }
             if (!ok) {
                 record_error(p, kErrTimeout, 2);
@@ -239,69 +307,69 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
         }
     } else if (warp < 2 + kPairNf4DecodeWarps) {  // ---------------- decoders (both CTAs)
         const int dw = warp - 2;
-        const int group = dw >> 2;                 // takes K blocks with iteration parity `group`
-        const int t = (dw & 3) * 32 + lane;        // 0..127: one NF4 block per stage
-        int stage = 0;
-        uint32_t phase = 0;
-        uint32_t iter = 0;
+        const int group = dw / kPairNf4GroupWarps;  // takes the K blocks with iter % groups == group
+        const int t0 = (dw % kPairNf4GroupWarps) * 32 + lane;  // blocks t0 and t0 + 64 of each K block
+        auto advance = [&](KBlockIter& it) {
+            for (int g = 0; g < kPairNf4DecodeGroups; ++g) it.next(p, ncl);
+        };
         bool ok = true;
-        for (int u = cid; ok && u < p.total_units; u += ncl) {
-            const Unit U = decode_unit(p, u);
-            const Prob& P = p.prob[U.pi];
-            for (int si = 0; ok && si < P.nseg; ++si) {
-                const Seg& S = P.seg[si];
-                const int nkb = (S.kext + kBK - 1) / kBK;
-                const bool nf4 = S.b_nf4[0] >= 0;
-                const Nf4Src* W = nf4 ? &p.nf4[(rank == 1 && S.b_nf4[1] >= 0) ? S.b_nf4[1] : S.b_nf4[0]] : nullptr;
-                const int bcol0 = U.nb * P.n_step + (int)rank * S.b_rank_off;
-                for (int kb = 0; kb < nkb; ++kb, ++iter) {
-                    if ((int)(iter & 1u) == group) {
-                        // the block scale does not depend on the stage data: fetch it before waiting
-                        bool valid = false;
-                        float amax = 0.0f;
-                        int64_t b = 0;
-                        int kr = 0, c = 0;
-                        if (nf4) {
-                            if constexpr (B_MN) {
-                                kr = t & 63;
-                                c = t >> 6;
-                                const int64_t krow = (int64_t)kb * kBK + kr;
-                                const int64_t ncol = (int64_t)bcol0 + c * 64;
-                                valid = krow < W->rows && ncol < W->cols;
-                                b = (krow * W->cols + ncol) >> 6;
-                            } else {
-                                const int64_t row = (int64_t)bcol0 + t;
-                                valid = row < W->rows;
-                                b = row * (W->cols >> 6) + kb;
-                            }
-                            if (valid) amax = __fmul_rn((float)__ldg(W->absmax_q + b), __ldg(W->scale + (b >> 8)));
-                        }
-                        if (!mbar_wait(smem_u32(&full[stage]), phase, s_abort)) {
-                            ok = false;
-                            break;
-                        }
-                        if (nf4) {
-                            uint8_t* stg = smem + stage * C::STAGE_BYTES;
-                            const uint32_t sB = smem_u32(stg + C::A_BYTES);
-                            const uint8_t* sC = stg + C::A_BYTES + C::B_BYTES;
-                            if constexpr (B_MN) {
-                                const uint4* src = reinterpret_cast<const uint4*>(sC + kr * 64 + c * 32);
-                                nf4_decode_block_regs(src[0], src[1], amax, valid, sB + c * 8192 + kr * 128, kr & 7);
-                            } else {
-                                const uint4* src = reinterpret_cast<const uint4*>(sC + t * 32);
-                                nf4_decode_block_regs(src[0], src[1], amax, valid, sB + t * 128, t & 7);
-                            }
-                            fence_proxy_async_smem();
-                        }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_remote(bready0 + stage * 8);
-                    }
-                    if (++stage == C::STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
+        KBlockIter cur;
+        cur.start(p, cid, ncl);
+        for (int g = 0; g < group; ++g) cur.next(p, ncl);
+        uint32_t iter = (uint32_t)group;
+        KBlockIter n1 = cur;
+        advance(n1);
+        KBlockIter n2 = n1;
+        advance(n2);
+        // Block scales are fetched two of this group's K blocks ahead, and only after the
+        // release-arrive of the current one: a release waits for the thread's outstanding loads,
+        // so a load issued just before it would put its latency back on the critical path.
+        bool v0 = false, v1 = false, w0 = false, w1 = false;
+        float a0 = nf4_block_scale<B_MN>(p, cur, rank, t0, v0);
+        float a1 = nf4_block_scale<B_MN>(p, cur, rank, t0 + 64, v1);
+        float b0 = nf4_block_scale<B_MN>(p, n1, rank, t0, w0);
+        float b1 = nf4_block_scale<B_MN>(p, n1, rank, t0 + 64, w1);
+        while (ok && cur.valid(p)) {
+            const int stage = (int)(iter % C::STAGES);
+            const uint32_t phase = (iter / C::STAGES) & 1u;
+            if (!mbar_wait(smem_u32(&full[stage]), phase, s_abort)) {
+                ok = false;
+                break;
             }
+            if (p.prob[cur.U.pi].seg[cur.si].b_nf4[0] >= 0) {
+                uint8_t* stg = smem + stage * C::STAGE_BYTES;
+                const uint32_t sB = smem_u32(stg + C::A_BYTES);
+                const uint8_t* sC = stg + C::A_BYTES + C::B_BYTES;
+                if constexpr (B_MN) {
+                    // K row t0 (0..63): both 64-wide N chunks, i.e. blocks t0 and t0 + 64
+                    const uint4* src = reinterpret_cast<const uint4*>(sC + t0 * 64);
+                    nf4_decode_block_regs(src[0], src[1], a0, v0, sB + t0 * 128, t0 & 7);
+                    nf4_decode_block_regs(src[2], src[3], a1, v1, sB + 8192 + t0 * 128, t0 & 7);
+                } else {
+                    const uint4* s0 = reinterpret_cast<const uint4*>(sC + t0 * 32);
+                    const uint4* s1 = reinterpret_cast<const uint4*>(sC + (t0 + 64) * 32);
+                    nf4_decode_block_regs(s0[0], s0[1], a0, v0, sB + t0 * 128, t0 & 7);
+                    nf4_decode_block_regs(s1[0], s1[1], a1, v1, sB + (t0 + 64) * 128, t0 & 7);
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(bready0 + stage * 8);
+            bool x0 = false, x1 = false;
+            const float c0 = nf4_block_scale<B_MN>(p, n2, rank, t0, x0);
+            const float c1 = nf4_block_scale<B_MN>(p, n2, rank, t0 + 64, x1);
+            cur = n1;
+            n1 = n2;
+            advance(n2);
+            a0 = b0;
+            a1 = b1;
+            v0 = w0;
+            v1 = w1;
+            b0 = c0;
+            b1 = c1;
+            w0 = x0;
+            w1 = x1;
+            iter += kPairNf4DecodeGroups;
         }
         if (!ok && lane == 0) {
             record_error(p, kErrTimeout, 4);
@@ -310,26 +378,27 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
     } else {  // ---------------- epilogue warps (both CTAs)
         const int ew = warp - 2 - kPairNf4DecodeWarps;
         const int q = warp & 3;
-        const int hh = ew >> 2;
-        int acc = 0;
+        const int hh = ew >> 2;  // M half
         uint32_t aphase = 0;
         bool ok = true;
         for (int u = cid; u < p.total_units; u += ncl) {
             const Unit U = decode_unit(p, u);
             const Prob& P = p.prob[U.pi];
-            if (!mbar_wait(smem_u32(&tfull[acc]), aphase, s_abort)) {
+            if (!mbar_wait(smem_u32(&tfull[0]), aphase, s_abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
-            const int64_t m = (int64_t)U.mb * 256 + (int64_t)rank * kBM + q * 32 + lane;
-            epilogue_tile<EPI>(P, U, tacc, hh, m, m < P.M);
+            const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + hh * 256;
+            const int64_t m = (int64_t)U.mb * 512 + hh * 256 + (int64_t)rank * kBM + q * 32 + lane;
+            if constexpr (EPI == EPI_GLU_FWD)
+                epilogue_cols<EPI>(P, U, tacc, 0, P.bn >> 1, 16, m, m < P.M);
+            else
+                epilogue_cols<EPI>(P, U, tacc, 0, P.bn, 16, m, m < P.M);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(tempty0 + acc * 8);
-            acc ^= 1;
-            if (acc == 0) aphase ^= 1u;
+            if (lane == 0) mbar_arrive_remote(tempty0);
+            aphase ^= 1u;
         }
         if (!ok && lane == 0) {
             record_error(p, kErrTimeout, 3);
