@@ -349,35 +349,59 @@ def main():
                     "peak_source": peak_src + " sustained bf16", "flops_per_launch": kf,
                     "ms_per_launch": per_launch_ms}
 
-    # ---- end to end through the C ABI from pinned host buffers
+    # ---- end to end through the C ABI from pinned host buffers: every step copies its inputs in
+    # and its results out; the copies of neighbouring steps run on their own streams and overlap
+    # the current step's kernels (inputs and outputs are double-buffered on the device)
     hX, hdY = host_pinned(inp["X"]), host_pinned(inp["dY"])
-    host_out = {"y": torch.empty_like(fw["y"], device="cpu").pin_memory(),
-                "dX": torch.empty_like(bw["dX"], device="cpu").pin_memory()}
-    host_g = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in bw.items() if k != "dX"}
-    Xd, dYd = torch.empty_like(X), torch.empty_like(dY)
-    e2e_steps = max(3, min(args.steps, 20))
+    gkeys = [k for k in bw if k != "dX"]
+    host_out = [{"y": torch.empty_like(fw["y"], device="cpu").pin_memory(),
+                 "dX": torch.empty_like(bw["dX"], device="cpu").pin_memory(),
+                 **{k: torch.empty_like(bw[k], device="cpu").pin_memory() for k in gkeys}} for _ in range(2)]
+    dev_in = [(torch.empty_like(X), torch.empty_like(dY)) for _ in range(2)]
+    dev_out = [{"y": torch.empty_like(fw["y"]), "dX": torch.empty_like(bw["dX"]),
+                **{k: torch.empty_like(bw[k]) for k in gkeys}} for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    for e_ in out_done + comp_done:
+        e_.record(stream)
 
-    def e2e_step():
-        Xd.copy_(hX, non_blocking=True)
-        dYd.copy_(hdY, non_blocking=True)
-        step(Xd, dYd)
-        host_out["y"].copy_(fw["y"], non_blocking=True)
-        host_out["dX"].copy_(bw["dX"], non_blocking=True)
-        for k, v in host_g.items():
-            v.copy_(bw[k], non_blocking=True)
+    def e2e_run(nsteps):
+        for i in range(nsteps):
+            b = i & 1
+            with torch.cuda.stream(s_in):          # inputs of step i (after step i-2 stopped reading them)
+                s_in.wait_event(comp_done[b])
+                dev_in[b][0].copy_(hX, non_blocking=True)
+                dev_in[b][1].copy_(hdY, non_blocking=True)
+                in_done[b].record(s_in)
+            stream.wait_event(in_done[b])           # step i's kernels
+            stream.wait_event(out_done[b])          # after step i-2's results were copied out
+            o = dev_out[b]
+            L.lora_mlp_fwd(dev_in[b][0], gate, up, down, act=w.act, y=o["y"], e=fw["e"], u=fw["u"], h=fw["h"],
+                           saved=fw["saved"], ws=fw["ws"])
+            L.lora_mlp_bwd(dev_in[b][0], dev_in[b][1], fw, gate, up, down, act=w.act, dX=o["dX"],
+                           grads={k: o[k] for k in gkeys})
+            comp_done[b].record(stream)
+            with torch.cuda.stream(s_out):         # results of step i
+                s_out.wait_event(comp_done[b])
+                for k, v in host_out[b].items():
+                    v.copy_(o[k], non_blocking=True)
+                out_done[b].record(s_out)
 
-    e2e_step()
+    e2e_steps = max(4, min(args.steps, 20))
+    e2e_run(2)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    s_in.wait_stream(stream)
+    e2e_run(e2e_steps)
+    stream.wait_stream(s_out)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
     h2d = (hX.numel() + hdY.numel()) * 2
-    d2h = (host_out["y"].numel() + host_out["dX"].numel()) * 2 + sum(v.numel() * 4 for v in host_g.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

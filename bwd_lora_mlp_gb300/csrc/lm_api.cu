@@ -437,7 +437,12 @@ struct Builder {
     // tiles, split-K and work-unit numbering; returns the grid size
     int finish(int sms, int32_t* err) {
         p.err = err;
-        const bool partial = (kind == G_PART_KK || kind == G_PART_KMN || kind == G_PART_MNK);
+        if (kind == G_PART_KK) {  // the narrower stage layout keeps twice the bytes in flight
+            bool narrow = true;
+            for (int i = 0; i < p.nprob; ++i) narrow = narrow && p.prob[i].bn <= 64;
+            if (narrow) kind = G_PART_KK64;
+        }
+        const bool partial = (kind == G_PART_KK || kind == G_PART_KK64 || kind == G_PART_KMN || kind == G_PART_MNK);
         int64_t tiles = 0;
         for (int i = 0; i < p.nprob; ++i) {
             Prob& P = p.prob[i];

@@ -27,6 +27,7 @@ cudaError_t launch_gemm(GemmKind k, const Params& p, int grid, cudaStream_t st) 
     switch (k) {
         case G_PART_KMN: return launch_variant<64, false, true, EPI_PARTIAL>(p, grid, st);
         case G_PART_MNK: return launch_variant<64, true, false, EPI_PARTIAL>(p, grid, st);
+        case G_PART_KK64:
         default: return launch_gemm_fwd(k, p, grid, st);
     }
 }

@@ -1,4 +1,5 @@
-// Instantiation of the one-CTA split-K GEMM for the rank-r input projections (X A^T, h A^T).
+// Instantiations of the one-CTA split-K GEMM for the rank-r input projections (X A^T, h A^T):
+// a 64-wide B stage (eight 24 KB stages) when the projection is at most 64 wide, else 256-wide.
 #include "lm_internal.h"
 
 namespace lm {
@@ -23,6 +24,7 @@ static cudaError_t launch_variant(const Params& p, int grid, cudaStream_t st) {
 cudaError_t launch_gemm_fwd(GemmKind k, const Params& p, int grid, cudaStream_t st) {
     switch (k) {
         case G_PART_KK: return launch_variant<256, false, false, EPI_PARTIAL>(p, grid, st);
+        case G_PART_KK64: return launch_variant<64, false, false, EPI_PARTIAL>(p, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }

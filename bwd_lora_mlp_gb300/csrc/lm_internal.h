@@ -13,6 +13,7 @@ enum GemmKind : int {
     G_PART_KK = 4,   // 256, K, K, PARTIAL    X A^T (rank-r input projection), split-K partials
     G_PART_KMN = 5,  //  64, K, MN, PARTIAL   dOut B (rank-r output-gradient projection)
     G_PART_MNK = 6,  //  64, MN, K, PARTIAL   column reductions over T for dA / dB
+    G_PART_KK64 = 7, //  64, K, K, PARTIAL    G_PART_KK for projections at most 64 wide
     // bf16 base, CTA pair (cta_group::2), 256 x 256 tiles
     G2_GLU_FWD = 11,     // K-major B, GLU_FWD
     G2_STORE_K = 12,     // K-major B, STORE
