@@ -31,6 +31,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "LoRA-MLP fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300"
+METRICS = {"mlp": METRIC,
+           "qkv": "LoRA-QKV fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300",
+           "o": "LoRA-O fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300"}
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -41,14 +44,31 @@ def mlp_flops(T, d, n, r):
     return 12 * T * d * n + 18 * T * r * (d + n)
 
 
-def kernel_flops(tag, T, d, n, r):
-    """Algorithmic flops of one launch of the tagged GEMM kernel (rank-r terms at rank r)."""
-    return {
-        "mlp.gateup": 2 * T * d * 2 * n + 2 * 2 * T * r * n,
-        "mlp.down": 2 * T * n * d + 2 * T * r * d,
-        "mlp.dh": 2 * T * d * n + 2 * T * r * n,
-        "mlp.dX": 2 * T * 2 * n * d + 2 * 2 * T * r * d,
-    }.get(tag)
+def proj_flops(T, d_in, d_out, r):
+    """One LoRA projection fwd + bwd: base GEMMs X W^T and dOut W, rank-r products of both passes."""
+    return 4 * T * d_in * d_out + 6 * T * r * (d_in + d_out)
+
+
+def workload_flops(w):
+    return sum(proj_flops(w.T, p.d_in, p.d_out, w.r) for p in w.projs)
+
+
+def kernel_flops(tag, w):
+    """Algorithmic flops of one launch of the tagged base-GEMM kernel (rank-r terms at rank r)."""
+    T, r = w.T, w.r
+    if w.kind == "mlp":
+        d, n = w.projs[0].d_in, w.projs[0].d_out
+        return {
+            "mlp.gateup": 2 * T * d * 2 * n + 2 * 2 * T * r * n,
+            "mlp.down": 2 * T * n * d + 2 * T * r * d,
+            "mlp.dh": 2 * T * d * n + 2 * T * r * n,
+            "mlp.dX": 2 * T * 2 * n * d + 2 * 2 * T * r * d,
+        }.get(tag)
+    base = sum(2 * T * p.d_in * p.d_out for p in w.projs)
+    rank_out = sum(2 * T * r * p.d_out for p in w.projs)
+    rank_in = sum(2 * T * r * p.d_in for p in w.projs)
+    return {"qkv.fwd": base + rank_out, "qkv.dX": base + rank_in,
+            "o.fwd": base + rank_out, "o.dX": base + rank_in}.get(tag)
 
 
 def load_peaks():
@@ -258,11 +278,11 @@ def main():
 
     from bwd_lora_mlp_gb300 import synth
     w = synth.WORKLOADS[args.workload]
-    assert w.kind == "mlp", "bench.py times the LoRA MLP workloads"
     if args.tokens:
         w = synth.scaled_workload(w, T=args.tokens)
     world, rank, local = dist_setup()
     if args.impl == "reference":
+        assert w.kind == "mlp", "the reference arm times the MLP oracle"
         rc = run_reference(args, w, world, rank)
         if world > 1:
             import torch.distributed as dist
@@ -274,7 +294,7 @@ def main():
     __graft_entry__.build()
     from bwd_lora_mlp_gb300 import lib as L
 
-    T, d, n, r = w.T, w.projs[0].d_in, w.projs[0].d_out, w.r
+    T, r = w.T, w.r
     inp = synth.make_inputs(w)
 
     def dev(bits):
@@ -289,21 +309,52 @@ def main():
             W = L.nf4_pack(W)
         return L.Lora(W, dev(inp["A_" + t]), dev(inp["B_" + t]), w.s)
 
-    gate, up, down = mk("gate"), mk("up"), mk("down")
+    projs = {p.name: mk(p.name) for p in w.projs}
     torch.cuda.synchronize()
-    X, dY = dev(inp["X"]), dev(inp["dY"])
-    fw = L.lora_mlp_fwd(X, gate, up, down, act=w.act)
-    bw = L.lora_mlp_bwd(X, dY, fw, gate, up, down, act=w.act)
     stream = torch.cuda.current_stream()
+    # the step's inputs, in the order run() takes them
+    in_names = ["X", "dY_q", "dY_k", "dY_v"] if w.kind == "qkv" else ["X", "dY"]
+    ins = [dev(inp[k]) for k in in_names]
 
-    def step(Xs, dYs):
-        L.lora_mlp_fwd(Xs, gate, up, down, act=w.act, y=fw["y"], e=fw["e"], u=fw["u"], h=fw["h"],
-                       saved=fw["saved"], ws=fw["ws"])
-        L.lora_mlp_bwd(Xs, dYs, fw, gate, up, down, act=w.act, dX=bw["dX"],
-                       grads={k: v for k, v in bw.items() if k != "dX"})
+    if w.kind == "mlp":
+        gate, up, down = projs["gate"], projs["up"], projs["down"]
+        fw = L.lora_mlp_fwd(ins[0], gate, up, down, act=w.act)
+        bw = L.lora_mlp_bwd(ins[0], ins[1], fw, gate, up, down, act=w.act)
+        out_keys = ["y"]
+
+        def run(xs, outs):
+            L.lora_mlp_fwd(xs[0], gate, up, down, act=w.act, y=outs["y"], e=fw["e"], u=fw["u"], h=fw["h"],
+                           saved=fw["saved"], ws=fw["ws"])
+            L.lora_mlp_bwd(xs[0], xs[1], fw, gate, up, down, act=w.act, dX=outs["dX"],
+                           grads={k: outs[k] for k in outs if k not in ("y", "dX")})
+    elif w.kind == "qkv":
+        q, k_, v = projs["q"], projs["k"], projs["v"]
+        fw = L.lora_qkv_fwd(ins[0], q, k_, v)
+        bw = L.lora_qkv_bwd(ins[0], ins[1], ins[2], ins[3], fw, q, k_, v)
+        out_keys = ["Q", "K", "V"]
+
+        def run(xs, outs):
+            L.lora_qkv_fwd(xs[0], q, k_, v, out={t: outs[t] for t in ("Q", "K", "V")}, saved=fw["saved"],
+                           ws=fw["ws"])
+            L.lora_qkv_bwd(xs[0], xs[1], xs[2], xs[3], fw, q, k_, v, dX=outs["dX"],
+                           grads={t: outs[t] for t in ("dA_q", "dB_q", "dA_k", "dB_k", "dA_v", "dB_v")})
+    else:
+        o = projs["o"]
+        fw = L.lora_o_fwd(ins[0], o)
+        bw = L.lora_o_bwd(ins[0], ins[1], fw, o)
+        out_keys = ["Y"]
+
+        def run(xs, outs):
+            L.lora_o_fwd(xs[0], o, Y=outs["Y"], saved=fw["saved"], ws=fw["ws"])
+            L.lora_o_bwd(xs[0], xs[1], fw, o, dX=outs["dX"], dA=outs["dA"], dB=outs["dB"])
+
+    dev_outs = {**{k: fw[k] for k in out_keys}, **bw}
+
+    def step():
+        run(ins, dev_outs)
 
     for _ in range(args.warmup):
-        step(X, dY)
+        step()
     torch.cuda.synchronize()
     L.lm_workspace_check(fw["ws"])
 
@@ -319,7 +370,7 @@ def main():
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
-        step(X, dY)
+        step()
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -331,7 +382,7 @@ def main():
     ms = max_over_ranks(ms, world)
 
     peaks, peak_src = load_peaks()
-    flops = mlp_flops(T, d, n, r)
+    flops = workload_flops(w)
     value = world * T / (ms / 1e3)
     tflops = world * flops / (ms / 1e3) / 1e12
     launches = sum(c for c, _ in prof.values())
@@ -339,7 +390,7 @@ def main():
     dom = max(prof.items(), key=lambda kv: kv[1][1])
     dom_tag, (dom_n, dom_ms) = dom
     per_launch_ms = dom_ms / dom_n
-    kf = kernel_flops(dom_tag, T, d, n, r)
+    kf = kernel_flops(dom_tag, w)
     roofline = None
     if kf is not None:
         ach = kf / (per_launch_ms / 1e3) / 1e12
@@ -352,14 +403,10 @@ def main():
     # ---- end to end through the C ABI from pinned host buffers: every step copies its inputs in
     # and its results out; the copies of neighbouring steps run on their own streams and overlap
     # the current step's kernels (inputs and outputs are double-buffered on the device)
-    hX, hdY = host_pinned(inp["X"]), host_pinned(inp["dY"])
-    gkeys = [k for k in bw if k != "dX"]
-    host_out = [{"y": torch.empty_like(fw["y"], device="cpu").pin_memory(),
-                 "dX": torch.empty_like(bw["dX"], device="cpu").pin_memory(),
-                 **{k: torch.empty_like(bw[k], device="cpu").pin_memory() for k in gkeys}} for _ in range(2)]
-    dev_in = [(torch.empty_like(X), torch.empty_like(dY)) for _ in range(2)]
-    dev_out = [{"y": torch.empty_like(fw["y"]), "dX": torch.empty_like(bw["dX"]),
-                **{k: torch.empty_like(bw[k]) for k in gkeys}} for _ in range(2)]
+    host_in = [host_pinned(inp[k]) for k in in_names]
+    host_out = [{k: torch.empty_like(v, device="cpu").pin_memory() for k, v in dev_outs.items()} for _ in range(2)]
+    dev_in = [[torch.empty_like(t) for t in ins] for _ in range(2)]
+    dev_out = [{k: torch.empty_like(v) for k, v in dev_outs.items()} for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
     in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
@@ -371,21 +418,17 @@ def main():
             b = i & 1
             with torch.cuda.stream(s_in):          # inputs of step i (after step i-2 stopped reading them)
                 s_in.wait_event(comp_done[b])
-                dev_in[b][0].copy_(hX, non_blocking=True)
-                dev_in[b][1].copy_(hdY, non_blocking=True)
+                for dst, src in zip(dev_in[b], host_in):
+                    dst.copy_(src, non_blocking=True)
                 in_done[b].record(s_in)
             stream.wait_event(in_done[b])           # step i's kernels
             stream.wait_event(out_done[b])          # after step i-2's results were copied out
-            o = dev_out[b]
-            L.lora_mlp_fwd(dev_in[b][0], gate, up, down, act=w.act, y=o["y"], e=fw["e"], u=fw["u"], h=fw["h"],
-                           saved=fw["saved"], ws=fw["ws"])
-            L.lora_mlp_bwd(dev_in[b][0], dev_in[b][1], fw, gate, up, down, act=w.act, dX=o["dX"],
-                           grads={k: o[k] for k in gkeys})
+            run(dev_in[b], dev_out[b])
             comp_done[b].record(stream)
             with torch.cuda.stream(s_out):         # results of step i
                 s_out.wait_event(comp_done[b])
                 for k, v in host_out[b].items():
-                    v.copy_(o[k], non_blocking=True)
+                    v.copy_(dev_out[b][k], non_blocking=True)
                 out_done[b].record(s_out)
 
     e2e_steps = max(4, min(args.steps, 20))
@@ -400,22 +443,28 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
-    h2d = (hX.numel() + hdY.numel()) * 2
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and w.kind == "mlp":
         cpu = cpu_baseline(w, inp)
 
+    d_in, d_out = w.projs[0].d_in, w.projs[-1].d_out
+    cfg = {"workload": w.name, "T": T, "r": r, "alpha": w.alpha, "base": "nf4" if w.nf4 else "bf16"}
+    if w.kind == "mlp":
+        cfg.update(d=d_in, n=w.projs[0].d_out, act=w.act)
+    else:
+        cfg.update(projections={p.name: [p.d_in, p.d_out] for p in w.projs})
+    cfg.update(parallelism="replicas" if world > 1 else "single",
+               l2="no flush: the working set (weights, activations and saved tensors of the step) exceeds the "
+                  "129 MB L2")
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRICS[w.kind], "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded W~N(0,0.02), A~U(+-1/sqrt(in)), B~N(0,0.02), X~N(0,1), dY~N(0,0.01), bf16",
-        "config": {"workload": w.name, "T": T, "d": d, "n": n, "r": r, "alpha": w.alpha, "act": w.act,
-                   "base": "nf4" if w.nf4 else "bf16", "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "no flush: the working set (weights 336 MiB, X/dY/y/dX 256 MiB, e/u/h/de/du 1.1 GiB) "
-                         "exceeds the 129 MB L2"},
+        "config": cfg,
         "tflops": tflops,
         "roofline_step": {"bound": "tensor", "achieved": tflops / world, "peak": peaks["bf16_tflops_sustained"],
                           "unit": "TFLOP/s", "frac": tflops / world / peaks["bf16_tflops_sustained"],
