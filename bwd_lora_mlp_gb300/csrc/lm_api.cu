@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -231,7 +232,7 @@ struct Bump {
     }
 };
 
-constexpr int kMaxSplits = 8;
+constexpr int kMaxSplits = 16;
 
 struct Dims {
     int64_t T, ldT;
@@ -450,7 +451,25 @@ struct Builder {
             tiles += (int64_t)P.tiles_m * P.tiles_n;
         }
         int S = 1;
-        if (partial) S = (int)std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, (2 * sms + tiles - 1) / tiles));
+        if (partial) {
+            // split count with the fewest K blocks on the busiest CTA: waves x blocks per unit
+            int64_t best = INT64_MAX;
+            for (int cand = 1; cand <= kMaxSplits; ++cand) {
+                int64_t units_c = 0, kbps_max = 0;
+                for (int i = 0; i < p.nprob; ++i) {
+                    const Prob& P = p.prob[i];
+                    const int64_t nkb = (P.seg[0].kext + kBK - 1) / kBK;
+                    const int64_t kbps = (nkb + cand - 1) / cand;
+                    units_c += (int64_t)P.tiles_m * P.tiles_n * ((nkb + kbps - 1) / kbps);
+                    kbps_max = std::max(kbps_max, kbps);
+                }
+                const int64_t cost = (units_c + sms - 1) / sms * kbps_max;
+                if (cost < best) {
+                    best = cost;
+                    S = cand;
+                }
+            }
+        }
         int64_t units = 0;
         for (int i = 0; i < p.nprob; ++i) {
             Prob& P = p.prob[i];
