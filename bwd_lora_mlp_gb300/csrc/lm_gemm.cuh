@@ -9,8 +9,10 @@
 // Roles (320 threads):
 //   warp 0 lane 0  TMA producer: fills a ring of shared-memory stages (A tile 128 x 64,
 //                  B tile bn x 64, both 128-byte swizzled, K-major or MN-major).
-//   warp 1 lane 0  MMA issuer: tcgen05.mma kind::f16 (bf16 in, fp32 accumulate), commits
+//   warp 1         MMA issuer: tcgen05.mma kind::f16 (bf16 in, fp32 accumulate), commits
 //                  each stage back to the producer and each finished tile to the epilogue.
+//                  The whole warp runs the issue loop (warp-uniform operands) and lane 0
+//                  issues; each stage is a fixed, unrolled four-MMA body.
 //   warps 2..9     epilogue: TMEM -> registers (tcgen05.ld) -> fused epilogue -> global.
 // Two TMEM accumulators alternate so the epilogue of one tile overlaps the mainloop of the
 // next.  Every wait is bounded: on timeout the kernel records an error and returns.
@@ -412,7 +414,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {  // ---------------- MMA issuer
+        {  // ---------------- MMA issuer: the whole warp, lane 0 issues
+            const bool leader = lane == 0;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -421,7 +424,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
             for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
                 const Unit U = decode_unit(p, u);
                 const Prob& P = p.prob[U.pi];
-                if (!mbar_wait(smem_u32(&tempty[acc]), aphase ^ 1u, s_abort)) {
+                if (!mbar_wait_warp(smem_u32(&tempty[acc]), aphase ^ 1u, s_abort)) {
                     ok = false;
                     break;
                 }
@@ -438,8 +441,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
                         kb0 = U.ks * P.kb_per_split;
                         kb1 = min(nkb, kb0 + P.kb_per_split);
                     }
+                    const bool dual = !B_MN && S.dual_split > 0;
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!mbar_wait(smem_u32(&full[stage]), phase, s_abort)) {
+                        if (!mbar_wait_warp(smem_u32(&full[stage]), phase, s_abort)) {
                             ok = false;
                             break;
                         }
@@ -448,21 +452,27 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
                         const uint32_t sB = sA + C::A_BYTES;
                         const int rem = S.kext - kb * kBK;
                         const int nsteps = rem >= kBK ? 4 : (rem + 15) >> 4;
-                        for (int ks = 0; ks < nsteps; ++ks) {
-                            const uint64_t ad = A_MN ? make_sdesc_sw128(sA + ks * 2048, 8192, 1024)
-                                                     : make_sdesc_sw128(sA + ks * 32, 16, 1024);
-                            if (!B_MN && S.dual_split > 0) {
+                        // fixed four-step body; a short last K block masks its tail steps.
+                        // Descriptor addresses are in 16-byte units: a K step is 32 bytes along a
+                        // K-major row or 16 rows (2048 bytes) of an MN-major tile.
+                        const uint64_t ad0 = A_MN ? make_sdesc_sw128(sA, 8192, 1024) : make_sdesc_sw128(sA, 16, 1024);
+                        const uint64_t bd0 = B_MN ? make_sdesc_sw128(sB, 8192, 1024) : make_sdesc_sw128(sB, 16, 1024);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t ad = ad0 + (uint64_t)(A_MN ? ks * 128 : ks * 2);
+                            const bool go = leader && ks < nsteps;
+                            const uint32_t ac = ks == 0 ? accum : 1u;
+                            if (dual) {
                                 const int hf = (kb * kBK + ks * 16) >= S.dual_split ? 1 : 0;
-                                const uint32_t bo = sB + hf * (P.bn >> 1) * 128 + ks * 32;
-                                umma_bf16(d0 + hf * (P.bn >> 1), ad, make_sdesc_sw128(bo, 16, 1024), idesc_h, accum);
+                                const uint64_t bd = bd0 + (uint64_t)((hf * (P.bn >> 1) * 128) >> 4) + (uint64_t)(ks * 2);
+                                umma_bf16_if(d0 + hf * (P.bn >> 1), ad, bd, idesc_h, ac, go);
                             } else {
-                                const uint64_t bd = B_MN ? make_sdesc_sw128(sB + ks * 2048, 8192, 1024)
-                                                         : make_sdesc_sw128(sB + ks * 32, 16, 1024);
-                                umma_bf16(d0, ad, bd, idesc, accum);
+                                const uint64_t bd = bd0 + (uint64_t)(B_MN ? ks * 128 : ks * 2);
+                                umma_bf16_if(d0, ad, bd, idesc, ac, go);
                             }
-                            accum = 1;
                         }
-                        umma_commit(smem_u32(&empty[stage]));
+                        accum = 1;
+                        umma_commit_if(smem_u32(&empty[stage]), leader);
                         if (++stage == C::STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -470,18 +480,19 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
                     }
                 }
                 if (!ok) break;
-                umma_commit(smem_u32(&tfull[acc]));
+                umma_commit_if(smem_u32(&tfull[acc]), leader);
                 acc ^= 1;
                 if (acc == 0) aphase ^= 1u;
             }
-            if (!ok) {
+            if (!ok && leader) {
                 record_error(p, kErrTimeout, 2);
                 *s_abort = 1;
             }
-            // wait until every MMA this thread issued has finished before TMEM is released
-            umma_commit(smem_u32(drain));
+            // wait until every MMA the leader issued has finished before TMEM is released
+            umma_commit_if(smem_u32(drain), leader);
             volatile int never = 0;
             mbar_wait(smem_u32(drain), 0, &never);
+            __syncwarp();
         }
     } else {  // ---------------- epilogue warps
         const int ew = warp - 2;

@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {  // ---------------- MMA issuer (CTA 0 only)
+        if (rank == 0) {  // ---------------- MMA issuer (CTA 0 only): the whole warp, lane 0 issues
+            const bool leader = lane == 0;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
             for (int u = cid; ok && u < p.total_units; u += ncl) {
                 const Unit U = decode_unit(p, u);
                 const Prob& P = p.prob[U.pi];
-                if (!mbar_wait(smem_u32(&tempty[acc]), aphase ^ 1u, s_abort)) {
+                if (!mbar_wait_warp(smem_u32(&tempty[acc]), aphase ^ 1u, s_abort)) {
                     ok = false;
                     break;
                 }
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
                     const Seg& S = P.seg[si];
                     const int nkb = (S.kext + kBK - 1) / kBK;
                     for (int kb = 0; kb < nkb; ++kb) {
-                        if (!mbar_wait(smem_u32(&full[stage]), phase, s_abort)) {
+                        if (!mbar_wait_warp(smem_u32(&full[stage]), phase, s_abort)) {
                             ok = false;
                             break;
                         }
@@ -145,14 +146,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
                         const uint32_t sB = sA + C::A_BYTES;
                         const int rem = S.kext - kb * kBK;
                         const int nsteps = rem >= kBK ? 4 : (rem + 15) >> 4;
-                        for (int ks = 0; ks < nsteps; ++ks) {
-                            const uint64_t ad = make_sdesc_sw128(sA + ks * 32, 16, 1024);
-                            const uint64_t bd = B_MN ? make_sdesc_sw128(sB + ks * 2048, 8192, 1024)
-                                                     : make_sdesc_sw128(sB + ks * 32, 16, 1024);
-                            umma_bf16_pair(d0, ad, bd, idesc, accum);
-                            accum = 1;
+                        // a fixed four-step body (a short last K block of a segment masks its
+                        // tail steps): a loop with a run-time trip count here starves the tensor pipe
+                        const uint64_t ad0 = make_sdesc_sw128(sA, 16, 1024);
+                        const uint64_t bd0 = B_MN ? make_sdesc_sw128(sB, 8192, 1024) : make_sdesc_sw128(sB, 16, 1024);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            // 16 K elements = 32 bytes along a K-major row or 16 rows (2048 bytes) of an
+                            // MN-major tile; the descriptor holds the address in 16-byte units
+                            const uint64_t ad = ad0 + (uint64_t)(ks * 2);
+                            const uint64_t bd = bd0 + (uint64_t)(B_MN ? ks * 128 : ks * 2);
+                            umma_bf16_pair_if(d0, ad, bd, idesc, ks == 0 ? accum : 1u, leader && ks < nsteps);
                         }
-                        umma_commit_pair(smem_u32(&empty[stage]), 0x3);
+                        accum = 1;
+                        umma_commit_pair_if(smem_u32(&empty[stage]), 0x3, leader);
                         if (++stage == C::STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -160,17 +167,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair(smem_u32(&tfull[acc]), 0x3);
+                umma_commit_pair_if(smem_u32(&tfull[acc]), 0x3, leader);
                 acc ^= 1;
                 if (acc == 0) aphase ^= 1u;
             }
-            if (!ok) {
+            if (!ok && leader) {
                 record_error(p, kErrTimeout, 2);
                 *s_abort = 1;
             }
-            umma_commit_pair(smem_u32(drain), 0x1);
+            umma_commit_pair_if(smem_u32(drain), 0x1, leader);
             volatile int never = 0;
             mbar_wait(smem_u32(drain), 0, &never);
+            __syncwarp();
         }
     } else {  // ---------------- epilogue warps (both CTAs)
         const int ew = warp - 2;

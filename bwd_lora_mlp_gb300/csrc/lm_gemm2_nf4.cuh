@@ -249,7 +249,8 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {  // ---------------- MMA issuer (CTA 0 only)
+        if (rank == 0) {  // ---------------- MMA issuer (CTA 0 only): the whole warp, lane 0 issues
+            const bool leader = lane == 0;
             int stage = 0;
             uint32_t phase = 0;
             uint32_t aphase = 0;  // one accumulator: its free / ready phases flip every tile
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
             for (int u = cid; ok && u < p.total_units; u += ncl) {
                 const Unit U = decode_unit(p, u);
                 const Prob& P = p.prob[U.pi];
-                if (!mbar_wait(smem_u32(&tempty[0]), aphase ^ 1u, s_abort)) {
+                if (!mbar_wait_warp(smem_u32(&tempty[0]), aphase ^ 1u, s_abort)) {
                     ok = false;
                     break;
                 }
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     const Seg& S = P.seg[si];
                     const int nkb = (S.kext + kBK - 1) / kBK;
                     for (int kb = 0; kb < nkb; ++kb) {
-                        if (!mbar_wait(smem_u32(&bready[stage]), phase, s_abort)) {
+                        if (!mbar_wait_warp(smem_u32(&bready[stage]), phase, s_abort)) {
                             ok = false;
                             break;
                         }
@@ -277,16 +278,19 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                         const uint32_t sB = sA + C::A_BYTES;
                         const int rem = S.kext - kb * kBK;
                         const int nsteps = rem >= kBK ? 4 : (rem + 15) >> 4;
-                        for (int ks = 0; ks < nsteps; ++ks) {
-                            const uint64_t bd = B_MN ? make_sdesc_sw128(sB + ks * 2048, 8192, 1024)
-                                                     : make_sdesc_sw128(sB + ks * 32, 16, 1024);
+                        // fixed four-step body; a short last K block masks its tail steps
+                        const uint64_t ad0 = make_sdesc_sw128(sA, 16, 1024);
+                        const uint64_t bd0 = B_MN ? make_sdesc_sw128(sB, 8192, 1024) : make_sdesc_sw128(sB, 16, 1024);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t bd = bd0 + (uint64_t)(B_MN ? ks * 128 : ks * 2);
 #pragma unroll
                             for (int h = 0; h < 2; ++h)  // both M halves share the decoded B tile
-                                umma_bf16_pair(tmem_base + h * 256, make_sdesc_sw128(sA + h * 16384 + ks * 32, 16, 1024),
-                                               bd, idesc, accum);
-                            accum = 1;
+                                umma_bf16_pair_if(tmem_base + h * 256, ad0 + (uint64_t)(h * 1024 + ks * 2), bd, idesc,
+                                                  ks == 0 ? accum : 1u, leader && ks < nsteps);
                         }
-                        umma_commit_pair(smem_u32(&empty[stage]), 0x3);
+                        accum = 1;
+                        umma_commit_pair_if(smem_u32(&empty[stage]), 0x3, leader);
                         if (++stage == C::STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -294,16 +298,17 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair(smem_u32(&tfull[0]), 0x3);
+                umma_commit_pair_if(smem_u32(&tfull[0]), 0x3, leader);
                 aphase ^= 1u;
             }
-            if (!ok) {
+            if (!ok && leader) {
                 record_error(p, kErrTimeout, 2);
                 *s_abort = 1;
             }
-            umma_commit_pair(smem_u32(drain), 0x1);
+            umma_commit_pair_if(smem_u32(drain), 0x1, leader);
             volatile int never = 0;
             mbar_wait(smem_u32(drain), 0, &never);
+            __syncwarp();
         }
     } else if (warp < 2 + kPairNf4DecodeWarps) {  // ---------------- decoders (both CTAs)
         const int dw = warp - 2;
