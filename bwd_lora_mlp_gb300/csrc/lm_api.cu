@@ -268,6 +268,7 @@ struct MlpPlan {
     RankBuf gd, gg, gu;     // s*dY Bd, s*de Bg, s*du Bu
     size_t de, du;
     size_t bdiag;           // [Bg | 0 ; 0 | Bu] (2n x 2rp) for the CTA-pair gate/up GEMM
+    size_t sc[3];           // NF4 base: fp32 block-scale tables of W_gate, W_up, W_down
     size_t ws_total;
 };
 
@@ -289,6 +290,7 @@ MlpPlan plan_mlp(int64_t T, int64_t d, int64_t n, int32_t r) {
     P.de = w.take((size_t)T * n * 2);
     P.du = w.take((size_t)T * n * 2);
     P.bdiag = w.take((size_t)2 * n * 2 * rp * 2);
+    for (int i = 0; i < 3; ++i) P.sc[i] = w.take((size_t)n * d / 64 * 4);
     P.ws_total = w.off;
     return P;
 }
@@ -299,6 +301,7 @@ struct QkvPlan {
     size_t saved_total;
     size_t part;
     RankBuf g[3];
+    size_t sc[3];           // NF4 base: fp32 block-scale tables of W_q, W_k, W_v
     size_t ws_total;
 };
 
@@ -314,6 +317,8 @@ QkvPlan plan_qkv(int64_t T, int64_t d, int64_t nq, int64_t nk, int64_t nv, int32
     const int64_t part_elems = std::max<int64_t>(T * 3 * rp, (3 * d + nq + nk + nv) * rp);
     P.part = w.take((size_t)kMaxSplits * part_elems * 4);
     for (int i = 0; i < 3; ++i) P.g[i] = take_rank(w, P.D, rp);
+    const int64_t nout[3] = {nq, nk, nv};
+    for (int i = 0; i < 3; ++i) P.sc[i] = w.take((size_t)nout[i] * d / 64 * 4);
     P.ws_total = w.off;
     return P;
 }
@@ -324,6 +329,7 @@ struct OPlan {
     size_t saved_total;
     size_t part;
     RankBuf g;
+    size_t sc;              // NF4 base: fp32 block-scale table of W_o
     size_t ws_total;
 };
 
@@ -339,15 +345,22 @@ OPlan plan_o(int64_t T, int64_t d_in, int64_t d_out, int32_t r) {
     const int64_t part_elems = std::max<int64_t>(T * rp, (d_in + d_out) * rp);
     P.part = w.take((size_t)kMaxSplits * part_elems * 4);
     P.g = take_rank(w, P.D, rp);
+    P.sc = w.take((size_t)d_out * d_in / 64 * 4);
     P.ws_total = w.off;
     return P;
+}
+
+// fp32 block-scale table of an NF4 weight for the NF4 GEMMs (traced under `tag`)
+lm_status scale_table(const char* tag, const lm_weight& W, float* table, cudaStream_t st) {
+    ProfScope prof(tag, st);
+    const cudaError_t e = launch_nf4_scale_table(W.absmax_q, W.group_scale, W.rows, W.cols, table, st);
+    return e == cudaSuccess ? LM_OK : cuda_fail(e, "NF4 scale table launch");
 }
 
 // ------------------------------------------------------------------ GEMM launch builder
 struct Builder {
     Params p;
     int nmaps = 0;
-    int nnf4 = 0;
     int tile_m = kBM;
     lm_status st = LM_OK;
     GemmKind kind;
@@ -390,14 +403,30 @@ struct Builder {
     // codes map of an NF4 weight read MN-major (input gradient: box 64 bytes = 128 elements x 64 rows)
     int codes_mn(const lm_weight& W) { return map_u8(W.codes, W.rows, W.cols / 2, W.cols / 2, 64, 64); }
 
-    int nf4src(const lm_weight& W) {
-        if (st != LM_OK) return -1;
-        if (nnf4 >= 4) {
-            st = fail(LM_ERR_UNSUPPORTED, "too many NF4 weights in one launch");
-            return -1;
+    // fp32 block-scale table of an NF4 weight ([cols / 64][rows], see launch_nf4_scale_table):
+    // box 128 rows x 1 K block (weight read K-major) or 64 rows x 2 column blocks (MN-major);
+    // rows outside the weight read 0
+    int scales(const float* table, const lm_weight& W, bool mn) {
+        if (st != LM_OK) return 0;
+        if (nmaps >= kMaxMaps) {
+            st = fail(LM_ERR_UNSUPPORTED, "too many tensor maps in one launch");
+            return 0;
         }
-        p.nf4[nnf4] = Nf4Src{W.absmax_q, W.group_scale, W.rows, W.cols};
-        return nnf4++;
+        cuuint64_t dims[2] = {(cuuint64_t)W.rows, (cuuint64_t)(W.cols / 64)};
+        cuuint64_t strides[1] = {(cuuint64_t)W.rows * 4};
+        cuuint32_t box[2] = {mn ? 64u : 128u, mn ? 2u : 1u};
+        cuuint32_t es[2] = {1u, 1u};
+        const CUresult r = g_encode(&p.maps[nmaps], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(table), dims,
+                                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            st = fail(LM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for an NF4 scale table %lld x %lld", (int)r,
+                      (long long)W.rows, (long long)(W.cols / 64));
+            return 0;
+        }
+        p.map_bytes[nmaps] = 512u;
+        p.map_w[nmaps] = (int32_t)W.rows;
+        return nmaps++;
     }
 
     // 2D bf16 tensor (rows x cols, row stride ld elements), box = 64 columns x box_rows rows
@@ -430,7 +459,7 @@ struct Builder {
         P.splits = 1;
         for (int s = 0; s < kMaxSegs; ++s) {
             for (int i = 0; i < 3; ++i) P.seg[s].b_map[i] = -1;
-            P.seg[s].b_nf4[0] = P.seg[s].b_nf4[1] = -1;
+            P.seg[s].b_scale[0] = P.seg[s].b_scale[1] = -1;
         }
         return P;
     }
@@ -751,6 +780,12 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     const int rp = D.rp;
     int32_t* err = static_cast<int32_t*>(ws);
     float* part = at<float>(ws, PL.part);
+    float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
+    if (nf4) {  // the NF4 GEMMs read per-K-block fp32 block scales of W_gate, W_up, W_down
+        LM_TRY(scale_table("mlp.nf4s", gate->W, sc[0], st));
+        LM_TRY(scale_table("mlp.nf4s", up->W, sc[1], st));
+        LM_TRY(scale_table("mlp.nf4s", down->W, sc[2], st));
+    }
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
     uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     uint16_t* ha = at<uint16_t>(saved, PL.ha.rows_off);
@@ -784,8 +819,8 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         S0.a_map = b.map(X, T, d, d, 128);
         S0.b_map[0] = b.codes_k(gate->W, 128);
         S0.b_map[1] = b.codes_k(up->W, 128);
-        S0.b_nf4[0] = b.nf4src(gate->W);
-        S0.b_nf4[1] = b.nf4src(up->W);
+        S0.b_scale[0] = b.scales(sc[0], gate->W, false);
+        S0.b_scale[1] = b.scales(sc[1], up->W, false);
         S0.kext = (int32_t)d;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(xa, T, 2 * rp, 2 * rp, 128);
@@ -849,7 +884,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(h_save, T, n, n, 128);
         S0.b_map[0] = b.codes_k(down->W, 128);
-        S0.b_nf4[0] = b.nf4src(down->W);
+        S0.b_scale[0] = b.scales(sc[2], down->W, false);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)n;
         Seg& S1 = seg(P, 1);
@@ -939,6 +974,12 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     const int rp = D.rp;
     int32_t* err = static_cast<int32_t*>(ws);
     float* part = at<float>(ws, PL.part);
+    float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
+    if (nf4) {
+        LM_TRY(scale_table("mlp.nf4s", gate->W, sc[0], st));
+        LM_TRY(scale_table("mlp.nf4s", up->W, sc[1], st));
+        LM_TRY(scale_table("mlp.nf4s", down->W, sc[2], st));
+    }
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     const uint16_t* haT = at<uint16_t>(saved, PL.ha.t_off);
     uint16_t* gd = at<uint16_t>(ws, PL.gd.rows_off);
@@ -969,7 +1010,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(dY, T, d, d, 128);
         S0.b_map[0] = b.codes_mn(down->W);
-        S0.b_nf4[0] = b.nf4src(down->W);
+        S0.b_scale[0] = b.scales(sc[2], down->W, true);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)d;
         Seg& S1 = seg(P, 1);
@@ -1061,7 +1102,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
             Seg& S = seg(P, i);
             S.a_map = b.map(dOut[i], T, n, n, 128);
             S.b_map[0] = b.codes_mn(Ls[i]->W);
-            S.b_nf4[0] = b.nf4src(Ls[i]->W);
+            S.b_scale[0] = b.scales(sc[i], Ls[i]->W, true);
             S.b_rank_off = 128;
             S.kext = (int32_t)n;
             Seg& R = seg(P, 2 + i);
@@ -1176,6 +1217,12 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     const int rp = D.rp;
     int32_t* err = static_cast<int32_t*>(ws);
     float* part = at<float>(ws, PL.part);
+    float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
+    if (nf4) {  // the NF4 GEMMs read per-K-block fp32 block scales of W_q, W_k, W_v
+        LM_TRY(scale_table("qkv.nf4s", q->W, sc[0], st));
+        LM_TRY(scale_table("qkv.nf4s", k->W, sc[1], st));
+        LM_TRY(scale_table("qkv.nf4s", v->W, sc[2], st));
+    }
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
     uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     {
@@ -1202,7 +1249,7 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             Seg& S0 = seg(P, 0);
             S0.a_map = xmap;
             S0.b_map[0] = b.codes_k(Ls[i]->W, 128);
-            S0.b_nf4[0] = b.nf4src(Ls[i]->W);
+            S0.b_scale[0] = b.scales(sc[i], Ls[i]->W, false);
             S0.b_rank_off = 128;
             S0.kext = (int32_t)d;
             Seg& S1 = seg(P, 1);
@@ -1297,6 +1344,12 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     const int rp = D.rp;
     int32_t* err = static_cast<int32_t*>(ws);
     float* part = at<float>(ws, PL.part);
+    float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
+    if (nf4) {
+        LM_TRY(scale_table("qkv.nf4s", q->W, sc[0], st));
+        LM_TRY(scale_table("qkv.nf4s", k->W, sc[1], st));
+        LM_TRY(scale_table("qkv.nf4s", v->W, sc[2], st));
+    }
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     const lm_lora* Ls[3] = {q, k, v};
     const uint16_t* dOut[3] = {dQ, dK, dV};
@@ -1351,7 +1404,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             Seg& S = seg(P, i);
             S.a_map = b.map(dOut[i], T, ns[i], ns[i], 128);
             S.b_map[0] = b.codes_mn(Ls[i]->W);
-            S.b_nf4[0] = b.nf4src(Ls[i]->W);
+            S.b_scale[0] = b.scales(sc[i], Ls[i]->W, true);
             S.b_rank_off = 128;
             S.kext = (int32_t)ns[i];
         }
@@ -1448,6 +1501,8 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     const int rp = D.rp;
     int32_t* err = static_cast<int32_t*>(ws);
     float* part = at<float>(ws, PL.part);
+    float* sc = at<float>(ws, PL.sc);
+    if (nf4) LM_TRY(scale_table("o.nf4s", o->W, sc, st));  // per-K-block fp32 block scales of W_o
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
     uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     {
@@ -1468,7 +1523,7 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(X, T, d_in, d_in, 128);
         S0.b_map[0] = b.codes_k(o->W, 128);
-        S0.b_nf4[0] = b.nf4src(o->W);
+        S0.b_scale[0] = b.scales(sc, o->W, false);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)d_in;
         Seg& S1 = seg(P, 1);
@@ -1538,6 +1593,8 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     const int rp = D.rp;
     int32_t* err = static_cast<int32_t*>(ws);
     float* part = at<float>(ws, PL.part);
+    float* sc = at<float>(ws, PL.sc);
+    if (nf4) LM_TRY(scale_table("o.nf4s", o->W, sc, st));
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     uint16_t* g = at<uint16_t>(ws, PL.g.rows_off);
     uint16_t* gT = at<uint16_t>(ws, PL.g.t_off);
@@ -1569,7 +1626,7 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(dY, T, d_out, d_out, 128);
         S0.b_map[0] = b.codes_mn(o->W);
-        S0.b_nf4[0] = b.nf4src(o->W);
+        S0.b_scale[0] = b.scales(sc, o->W, true);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)d_out;
         Seg& S1 = seg(P, 1);

@@ -257,4 +257,32 @@ cudaError_t launch_nf4_dequant(const uint8_t* codes, const int8_t* absmax_q, con
     return cudaGetLastError();
 }
 
+// Block-scale table of an NF4 weight (rows x cols): table[kb * rows + row] = fp32(absmax_q[b] *
+// group_scale[b / 256]) with b = row * (cols / 64) + kb, the scale of 64-element block kb of row
+// `row` (QLoRA, "Double Quantization").  Laid out K-block-major so that one TMA box brings a
+// stage's scales next to its codes: 128 rows of one K block (weight read K-major), or 64 rows of
+// two 64-wide column blocks (weight read MN-major).
+__global__ void __launch_bounds__(256) nf4_scale_table_kernel(const int8_t* __restrict__ absmax_q,
+                                                              const float* __restrict__ scale, int64_t rows,
+                                                              int64_t kblocks, float* __restrict__ table) {
+    const int64_t n = rows * kblocks;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t kb = i / rows, row = i - kb * rows;
+        const int64_t b = row * kblocks + kb;
+        table[i] = __fmul_rn((float)__ldg(absmax_q + b), __ldg(scale + (b >> 8)));
+    }
+}
+
+cudaError_t launch_nf4_scale_table(const int8_t* absmax_q, const float* scale, int64_t rows, int64_t cols,
+                                   float* table, cudaStream_t st) {
+    const int64_t n = rows * (cols / 64);
+    if (n == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)sms * 8);
+    nf4_scale_table_kernel<<<(unsigned)blocks, 256, 0, st>>>(absmax_q, scale, rows, cols / 64, table);
+    return cudaGetLastError();
+}
+
 }  // namespace lm

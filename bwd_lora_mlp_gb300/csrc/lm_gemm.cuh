@@ -44,16 +44,9 @@ struct Seg {
     int32_t dual_split;   // > 0: K steps with k < dual_split use B block 0 and the first bn/2
                           // accumulator columns, the others B block 1 and the second half
     int32_t a_xoff;       // added to the K coordinate of A
-    int32_t b_nf4[2];     // NF4 kernel: index into Params::nf4 of the weight whose codes b_map[i]
-                          // holds (-1: b_map[i] is a bf16 operand loaded as is)
+    int32_t b_scale[2];   // NF4 kernel: tensor map of the fp32 block-scale table of the weight
+                          // whose codes b_map[i] holds (-1: b_map[i] is a bf16 operand loaded as is)
     int32_t b_rank_off;   // CTA-pair kernel: B rows (K-major) / columns (MN-major) CTA 1 adds
-};
-
-// An NF4-packed base weight as the decode warps of the NF4 GEMM see it.
-struct Nf4Src {
-    const int8_t* absmax_q;   // rows * cols / 64 block scales
-    const float* scale;       // rows * cols / 16384 group scales
-    int64_t rows, cols;       // of the weight (out x in)
 };
 
 struct Prob {
@@ -81,7 +74,6 @@ struct Params {  // CUtensorMap members carry their own 128-byte alignment
     uint32_t map_bytes[kMaxMaps];   // bytes one box of the map delivers
     int32_t map_w[kMaxMaps];        // inner (K or MN) extent of the map, elements
     Prob prob[kMaxProbs];
-    Nf4Src nf4[4];
     float nf4_code[16];             // the NF4 values (NF4 kernel only)
     int32_t nprob;
     int32_t total_units;

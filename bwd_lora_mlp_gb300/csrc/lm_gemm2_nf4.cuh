@@ -6,11 +6,13 @@
 // (one set per M half) and half of the 256-wide B tile, and CTA 0 issues two M = 256 pair MMAs
 // per K step that share the decoded B tile, so each decoded weight element feeds 512 output rows
 // (decode work per MMA cycle is half that of a 256 x 256 tile).  The accumulator (2 M halves x 256
-// columns) fills TMEM, so it is single-buffered.  TMA brings the A rows and the raw NF4 codes of
-// the CTA's B half (4 KB) into the CTA's own stage and completes on the CTA's own stage barrier; decode warps turn every 64-element NF4 block into a
-// 128-byte swizzled bf16 row of the B tile and then report to CTA 0's decoded barrier, which
-// counts both CTAs' decoders, so CTA 0's MMA thread starts a K block only when both halves of B
-// and both A halves are in place.
+// columns) fills TMEM, so it is single-buffered.  TMA brings the A rows, the raw NF4 codes of
+// the CTA's B half (4 KB) and their 128 fp32 block scales (512 bytes, from a per-call table of
+// fp32(q * c) laid out K-block-major) into the CTA's own stage and completes on the CTA's own
+// stage barrier; decode warps turn every 64-element NF4 block into a 128-byte swizzled bf16 row of
+// the B tile and then report to CTA 0's decoded barrier, which counts both CTAs' decoders, so
+// CTA 0's MMA thread starts a K block only when both halves of B and both A halves are in place.
+// The decode warps issue no global loads: their release-arrive would wait for them.
 //
 // Decoding keeps everything in registers: for a block with scale amax' = fp32(q * c) the thread
 // forms the 16 products bf16(fp32(code_i * amax')) (the values nf4_dequant writes), splits them
@@ -21,8 +23,7 @@
 //
 // Roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer (CTA 0), warps 2-9 decoders in four
 // groups of two that take K blocks round-robin, so four K blocks are decoded at once (each thread
-// decodes two NF4 blocks per K block and fetches the scales of its group's next K block while
-// decoding), warps 10-17 epilogue.
+// decodes two NF4 blocks per K block), warps 10-17 epilogue.
 #pragma once
 
 #include "lm_gemm2.cuh"
@@ -39,7 +40,9 @@ struct Gemm2Nf4Cfg {
     static constexpr int A_BYTES = 2 * kBM * kBK * 2;  // this CTA's 2 x 128 A rows (one per M half)
     static constexpr int B_BYTES = 128 * kBK * 2;      // this CTA's half of B, decoded (or bf16 via TMA)
     static constexpr int C_BYTES = 4096;               // raw codes of that half
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + C_BYTES;
+    static constexpr int S_BYTES = 512;                // their 128 fp32 block scales
+    static constexpr int S_OFF = A_BYTES + B_BYTES + C_BYTES;
+    static constexpr int STAGE_BYTES = (S_OFF + S_BYTES + 1023) / 1024 * 1024;
     static constexpr int STAGES = 4;
     static constexpr int TMEM_COLS = 512;              // one accumulator: 2 M halves x 256 columns
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
@@ -55,12 +58,11 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // Decode one NF4 block (32 code bytes c0, c1; element 2i in the high nibble of byte i) with
 // block scale amax into a 128-byte row of the swizzled B tile at dst_row (16-byte chunk j stored
 // at chunk j ^ swz).
-__device__ __forceinline__ void nf4_decode_block_regs(uint4 c0, uint4 c1, float amax, bool valid, uint32_t dst_row,
-                                                      int swz) {
+__device__ __forceinline__ void nf4_decode_block_regs(uint4 c0, uint4 c1, float amax, uint32_t dst_row, int swz) {
     uint32_t T[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-        T[i] = valid ? pack_bf16x2(__fmul_rn(nf4_value(2 * i), amax), __fmul_rn(nf4_value(2 * i + 1), amax)) : 0u;
+        T[i] = pack_bf16x2(__fmul_rn(nf4_value(2 * i), amax), __fmul_rn(nf4_value(2 * i + 1), amax));
     // low / high bytes of the 16 bf16 products, four per register, in code order
     const uint32_t L0 = prmt(T[0], T[1], 0x6420), L1 = prmt(T[2], T[3], 0x6420);
     const uint32_t L2 = prmt(T[4], T[5], 0x6420), L3 = prmt(T[6], T[7], 0x6420);
@@ -124,34 +126,6 @@ struct KBlockIter {
     }
 };
 
-// Block scale fp32(q * c) of NF4 block `t` (0..127) of CTA `rank`'s half of the B tile at K block
-// `it`, and whether the block lies inside the weight (false also for bf16 segments).  K-major:
-// block t is B row t; MN-major: K row t & 63, 64-wide N chunk t >> 6.
-template <bool B_MN>
-__device__ __forceinline__ float nf4_block_scale(const Params& p, const KBlockIter& it, uint32_t rank, int t,
-                                                 bool& valid) {
-    valid = false;
-    if (!it.valid(p)) return 0.0f;
-    const Prob& P = p.prob[it.U.pi];
-    const Seg& S = P.seg[it.si];
-    if (S.b_nf4[0] < 0) return 0.0f;
-    const Nf4Src& W = p.nf4[(rank == 1 && S.b_nf4[1] >= 0) ? S.b_nf4[1] : S.b_nf4[0]];
-    const int64_t bcol0 = (int64_t)it.U.nb * P.n_step + (int64_t)rank * S.b_rank_off;
-    int64_t b;
-    if constexpr (B_MN) {
-        const int64_t krow = (int64_t)it.kb * kBK + (t & 63);
-        const int64_t ncol = bcol0 + (t >> 6) * 64;
-        valid = krow < W.rows && ncol < W.cols;
-        b = (krow * W.cols + ncol) >> 6;
-    } else {
-        const int64_t row = bcol0 + t;
-        valid = row < W.rows;
-        b = row * (W.cols >> 6) + it.kb;
-    }
-    if (!valid) return 0.0f;
-    return __fmul_rn((float)__ldg(W.absmax_q + b), __ldg(W.scale + (b >> 8)));
-}
-
 template <bool B_MN, int EPI>
 __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __grid_constant__ Params p) {
     using C = Gemm2Nf4Cfg;
@@ -211,8 +185,9 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                 for (int si = 0; ok && si < P.nseg; ++si) {
                     const Seg& S = P.seg[si];
                     const int nkb = (S.kext + kBK - 1) / kBK;
-                    const bool nf4 = S.b_nf4[0] >= 0;
+                    const bool nf4 = S.b_scale[0] >= 0;
                     const int bmap = (rank == 1 && S.b_map[1] >= 0) ? S.b_map[1] : S.b_map[0];
+                    const int smap = (rank == 1 && S.b_scale[1] >= 0) ? S.b_scale[1] : S.b_scale[0];
                     const int brow = U.nb * P.n_step + (int)rank * S.b_rank_off;
                     for (int kb = 0; kb < nkb; ++kb) {
                         if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) {
@@ -224,12 +199,21 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                         const uint32_t sC = sB + C::B_BYTES;
                         const uint32_t fb = smem_u32(&full[stage]);
                         const int kx = kb * kBK;
-                        mbar_expect_tx(fb, C::A_BYTES + (nf4 ? (uint32_t)p.map_bytes[bmap] : (uint32_t)C::B_BYTES));
+                        mbar_expect_tx(fb, C::A_BYTES + (nf4 ? (uint32_t)(p.map_bytes[bmap] + p.map_bytes[smap])
+                                                             : (uint32_t)C::B_BYTES));
                         tma_load_2d(sA, &p.maps[S.a_map], fb, kx + S.a_xoff, U.mb * 512 + (int)rank * kBM);
                         tma_load_2d(sA + 16384, &p.maps[S.a_map], fb, kx + S.a_xoff, U.mb * 512 + 256 + (int)rank * kBM);
                         if (nf4) {
-                            if constexpr (B_MN) tma_load_2d(sC, &p.maps[bmap], fb, brow / 2, kx);
-                            else tma_load_2d(sC, &p.maps[bmap], fb, kx / 2, brow);
+                            // scale table [K block][weight row]: K-major, the 128 rows of this
+                            // K block; MN-major, 64 K rows of the two 64-wide column blocks
+                            const uint32_t sS = sA + C::S_OFF;
+                            if constexpr (B_MN) {
+                                tma_load_2d(sC, &p.maps[bmap], fb, brow / 2, kx);
+                                tma_load_2d(sS, &p.maps[smap], fb, kx, brow / 64);
+                            } else {
+                                tma_load_2d(sC, &p.maps[bmap], fb, kx / 2, brow);
+                                tma_load_2d(sS, &p.maps[smap], fb, brow, kb);
+                            }
                         } else if constexpr (B_MN) {
                             tma_load_2d(sB, &p.maps[bmap], fb, brow, kx);
                             tma_load_2d(sB + 8192, &p.maps[bmap], fb, brow + 64, kx);
@@ -322,18 +306,6 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
         cur.start(p, cid, ncl);
         for (int g = 0; g < group; ++g) cur.next(p, ncl);
         uint32_t iter = (uint32_t)group;
-        KBlockIter n1 = cur;
-        advance(n1);
-        KBlockIter n2 = n1;
-        advance(n2);
-        // Block scales are fetched two of this group's K blocks ahead, and only after the
-        // release-arrive of the current one: a release waits for the thread's outstanding loads,
-        // so a load issued just before it would put its latency back on the critical path.
-        bool v0 = false, v1 = false, w0 = false, w1 = false;
-        float a0 = nf4_block_scale<B_MN>(p, cur, rank, t0, v0);
-        float a1 = nf4_block_scale<B_MN>(p, cur, rank, t0 + 64, v1);
-        float b0 = nf4_block_scale<B_MN>(p, n1, rank, t0, w0);
-        float b1 = nf4_block_scale<B_MN>(p, n1, rank, t0 + 64, w1);
         while (ok && cur.valid(p)) {
             const int stage = (int)(iter % C::STAGES);
             const uint32_t phase = (iter / C::STAGES) & 1u;
@@ -341,39 +313,30 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                 ok = false;
                 break;
             }
-            if (p.prob[cur.U.pi].seg[cur.si].b_nf4[0] >= 0) {
+            if (p.prob[cur.U.pi].seg[cur.si].b_scale[0] >= 0) {
                 uint8_t* stg = smem + stage * C::STAGE_BYTES;
                 const uint32_t sB = smem_u32(stg + C::A_BYTES);
                 const uint8_t* sC = stg + C::A_BYTES + C::B_BYTES;
+                // block t's scale sits at index t in both layouts (K-major: row t; MN-major:
+                // column block t >> 6, K row t & 63); rows outside the weight read 0
+                const float* sS = reinterpret_cast<const float*>(stg + C::S_OFF);
+                const float amax0 = sS[t0], amax1 = sS[t0 + 64];
                 if constexpr (B_MN) {
                     // K row t0 (0..63): both 64-wide N chunks, i.e. blocks t0 and t0 + 64
                     const uint4* src = reinterpret_cast<const uint4*>(sC + t0 * 64);
-                    nf4_decode_block_regs(src[0], src[1], a0, v0, sB + t0 * 128, t0 & 7);
-                    nf4_decode_block_regs(src[2], src[3], a1, v1, sB + 8192 + t0 * 128, t0 & 7);
+                    nf4_decode_block_regs(src[0], src[1], amax0, sB + t0 * 128, t0 & 7);
+                    nf4_decode_block_regs(src[2], src[3], amax1, sB + 8192 + t0 * 128, t0 & 7);
                 } else {
                     const uint4* s0 = reinterpret_cast<const uint4*>(sC + t0 * 32);
                     const uint4* s1 = reinterpret_cast<const uint4*>(sC + (t0 + 64) * 32);
-                    nf4_decode_block_regs(s0[0], s0[1], a0, v0, sB + t0 * 128, t0 & 7);
-                    nf4_decode_block_regs(s1[0], s1[1], a1, v1, sB + (t0 + 64) * 128, t0 & 7);
+                    nf4_decode_block_regs(s0[0], s0[1], amax0, sB + t0 * 128, t0 & 7);
+                    nf4_decode_block_regs(s1[0], s1[1], amax1, sB + (t0 + 64) * 128, t0 & 7);
                 }
                 fence_proxy_async_smem();
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(bready0 + stage * 8);
-            bool x0 = false, x1 = false;
-            const float c0 = nf4_block_scale<B_MN>(p, n2, rank, t0, x0);
-            const float c1 = nf4_block_scale<B_MN>(p, n2, rank, t0 + 64, x1);
-            cur = n1;
-            n1 = n2;
-            advance(n2);
-            a0 = b0;
-            a1 = b1;
-            v0 = w0;
-            v1 = w1;
-            b0 = c0;
-            b1 = c1;
-            w0 = x0;
-            w1 = x1;
+            advance(cur);
             iter += kPairNf4DecodeGroups;
         }
         if (!ok && lane == 0) {

@@ -73,6 +73,9 @@ cudaError_t launch_nf4_pack(const uint16_t* W, int64_t numel, uint8_t* codes, in
                             float* scale, cudaStream_t st);
 cudaError_t launch_nf4_dequant(const uint8_t* codes, const int8_t* absmax_q, const float* scale,
                                int64_t numel, bool bf16_out, void* out, cudaStream_t st);
+// fp32 block scales of an NF4 weight, K-block-major: table[kb * rows + row] (rows * cols / 64)
+cudaError_t launch_nf4_scale_table(const int8_t* absmax_q, const float* scale, int64_t rows, int64_t cols,
+                                   float* table, cudaStream_t st);
 void nf4_codebook_host(float* out16);
 
 }  // namespace lm

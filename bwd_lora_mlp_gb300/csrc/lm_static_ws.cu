@@ -10,7 +10,7 @@
 //
 // The scratch is kStaticWsBytes (16 MiB) of __device__ memory per GPU that loads the library,
 // held until the process exits.  It covers the O-projection shapes whose lora_o_workspace_size
-// is at most that (for example T = 8192 tokens, 4096 -> 4096, r = 16 needs about 8.5 MiB);
+// is at most that (for example T = 8192 tokens, 4096 -> 4096, r = 16 needs about 9.5 MiB);
 // larger shapes are rejected with LM_ERR_WORKSPACE before anything is enqueued.
 //
 // Sharing: every call, from any thread or stream, uses the same array, and the array keeps what
