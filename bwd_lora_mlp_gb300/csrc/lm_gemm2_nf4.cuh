@@ -21,9 +21,11 @@
 // each table by the nibble's top bit.  No shared-memory table is read, which keeps the shared
 // memory bandwidth for the MMA operands.
 //
-// Roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer (CTA 0), warps 2-9 decoders in four
-// groups of two that take K blocks round-robin, so four K blocks are decoded at once (each thread
-// decodes two NF4 blocks per K block), warps 10-17 epilogue.
+// Roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer (CTA 0), warps 2-9 decoders in
+// kPairNf4DecodeGroups groups that take K blocks round-robin (with two groups of four warps, two K
+// blocks are decoded at once and each thread decodes one NF4 block of each), warps 10-17
+// epilogue.  The producer tags every stage for the decoders (bf16, NF4, or end of work), so they
+// follow the stage ring without walking the work-unit sequence themselves.
 #pragma once
 
 #include "lm_gemm2.cuh"
@@ -32,8 +34,10 @@
 namespace lm {
 
 constexpr int kPairNf4DecodeWarps = 8;
-constexpr int kPairNf4DecodeGroups = 4;   // groups take K blocks round-robin
+constexpr int kPairNf4DecodeGroups = 2;   // groups take K blocks round-robin
 constexpr int kPairNf4GroupWarps = kPairNf4DecodeWarps / kPairNf4DecodeGroups;
+constexpr int kPairNf4BlocksPerThread = 128 / (32 * kPairNf4GroupWarps);  // NF4 blocks per thread per K block
+static_assert(kPairNf4BlocksPerThread == 1 || kPairNf4BlocksPerThread == 2, "decode split");
 constexpr int kPairNf4Threads = 64 + 32 * kPairNf4DecodeWarps + 32 * kNumEpiWarps;
 
 struct Gemm2Nf4Cfg {
@@ -93,39 +97,6 @@ __device__ __forceinline__ void nf4_decode_block_regs(uint4 c0, uint4 c1, float 
     }
 }
 
-// Walks the (work unit, K segment, K block) sequence every role of a pair kernel follows.
-struct KBlockIter {
-    int u, si, kb;
-    Unit U;
-    __device__ __forceinline__ bool valid(const Params& p) const { return u < p.total_units; }
-    __device__ __forceinline__ void settle(const Params& p, int stride) {
-        while (u < p.total_units) {
-            const Prob& P = p.prob[U.pi];
-            if (si < P.nseg) {
-                if (kb < (P.seg[si].kext + kBK - 1) / kBK) return;
-                ++si;
-                kb = 0;
-                continue;
-            }
-            u += stride;
-            si = 0;
-            kb = 0;
-            if (u < p.total_units) U = decode_unit(p, u);
-        }
-    }
-    __device__ __forceinline__ void start(const Params& p, int first, int stride) {
-        u = first;
-        si = 0;
-        kb = 0;
-        if (u < p.total_units) U = decode_unit(p, u);
-        settle(p, stride);
-    }
-    __device__ __forceinline__ void next(const Params& p, int stride) {
-        ++kb;
-        settle(p, stride);
-    }
-};
-
 template <bool B_MN, int EPI>
 __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __grid_constant__ Params p) {
     using C = Gemm2Nf4Cfg;
@@ -139,6 +110,9 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // what each stage holds, written by this CTA's producer before the stage's loads: 0 bf16 B
+    // (nothing to decode), 1 NF4 codes, 2 no more K blocks (one such stage per decode group)
+    volatile int32_t* stage_kind = reinterpret_cast<volatile int32_t*>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -199,6 +173,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                         const uint32_t sC = sB + C::B_BYTES;
                         const uint32_t fb = smem_u32(&full[stage]);
                         const int kx = kb * kBK;
+                        stage_kind[stage] = nf4 ? 1 : 0;
                         mbar_expect_tx(fb, C::A_BYTES + (nf4 ? (uint32_t)(p.map_bytes[bmap] + p.map_bytes[smap])
                                                              : (uint32_t)C::B_BYTES));
                         tma_load_2d(sA, &p.maps[S.a_map], fb, kx + S.a_xoff, U.mb * 512 + (int)rank * kBM);
@@ -225,6 +200,19 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                             phase ^= 1u;
                         }
                     }
+                }
+            }
+            // one end-of-work stage for each decode group (the next stage in its round-robin)
+            for (int g = 0; ok && g < kPairNf4DecodeGroups; ++g) {
+                if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) {
+                    ok = false;
+                    break;
+                }
+                stage_kind[stage] = 2;
+                mbar_arrive(smem_u32(&full[stage]));
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
             if (!ok) {
@@ -297,47 +285,42 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
     } else if (warp < 2 + kPairNf4DecodeWarps) {  // ---------------- decoders (both CTAs)
         const int dw = warp - 2;
         const int group = dw / kPairNf4GroupWarps;  // takes the K blocks with iter % groups == group
-        const int t0 = (dw % kPairNf4GroupWarps) * 32 + lane;  // blocks t0 and t0 + 64 of each K block
-        auto advance = [&](KBlockIter& it) {
-            for (int g = 0; g < kPairNf4DecodeGroups; ++g) it.next(p, ncl);
-        };
+        // blocks t0 (and t0 + 64 with two per thread) of each K block
+        const int t0 = (dw % kPairNf4GroupWarps) * 32 + lane;
         bool ok = true;
-        KBlockIter cur;
-        cur.start(p, cid, ncl);
-        for (int g = 0; g < group; ++g) cur.next(p, ncl);
-        uint32_t iter = (uint32_t)group;
-        while (ok && cur.valid(p)) {
+        for (uint32_t iter = (uint32_t)group;; iter += kPairNf4DecodeGroups) {
             const int stage = (int)(iter % C::STAGES);
             const uint32_t phase = (iter / C::STAGES) & 1u;
             if (!mbar_wait(smem_u32(&full[stage]), phase, s_abort)) {
                 ok = false;
                 break;
             }
-            if (p.prob[cur.U.pi].seg[cur.si].b_scale[0] >= 0) {
+            const int kind = stage_kind[stage];
+            if (kind == 2) break;
+            if (kind == 1) {
                 uint8_t* stg = smem + stage * C::STAGE_BYTES;
                 const uint32_t sB = smem_u32(stg + C::A_BYTES);
                 const uint8_t* sC = stg + C::A_BYTES + C::B_BYTES;
-                // block t's scale sits at index t in both layouts (K-major: row t; MN-major:
+                // block t's scale sits at index t in both layouts (K-major: B row t; MN-major:
                 // column block t >> 6, K row t & 63); rows outside the weight read 0
                 const float* sS = reinterpret_cast<const float*>(stg + C::S_OFF);
-                const float amax0 = sS[t0], amax1 = sS[t0 + 64];
-                if constexpr (B_MN) {
-                    // K row t0 (0..63): both 64-wide N chunks, i.e. blocks t0 and t0 + 64
-                    const uint4* src = reinterpret_cast<const uint4*>(sC + t0 * 64);
-                    nf4_decode_block_regs(src[0], src[1], amax0, sB + t0 * 128, t0 & 7);
-                    nf4_decode_block_regs(src[2], src[3], amax1, sB + 8192 + t0 * 128, t0 & 7);
-                } else {
-                    const uint4* s0 = reinterpret_cast<const uint4*>(sC + t0 * 32);
-                    const uint4* s1 = reinterpret_cast<const uint4*>(sC + (t0 + 64) * 32);
-                    nf4_decode_block_regs(s0[0], s0[1], amax0, sB + t0 * 128, t0 & 7);
-                    nf4_decode_block_regs(s1[0], s1[1], amax1, sB + (t0 + 64) * 128, t0 & 7);
+#pragma unroll
+                for (int j = 0; j < kPairNf4BlocksPerThread; ++j) {
+                    const int t = t0 + 64 * j;
+                    const float amax = sS[t];
+                    if constexpr (B_MN) {
+                        // K row t & 63, 64-wide N chunk t >> 6: 32 code bytes of a 64-byte K row
+                        const uint4* src = reinterpret_cast<const uint4*>(sC + (t & 63) * 64 + (t >> 6) * 32);
+                        nf4_decode_block_regs(src[0], src[1], amax, sB + (t >> 6) * 8192 + (t & 63) * 128, t & 7);
+                    } else {
+                        const uint4* src = reinterpret_cast<const uint4*>(sC + t * 32);
+                        nf4_decode_block_regs(src[0], src[1], amax, sB + t * 128, t & 7);
+                    }
                 }
                 fence_proxy_async_smem();
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(bready0 + stage * 8);
-            advance(cur);
-            iter += kPairNf4DecodeGroups;
+            if (lane == 0) mbar_arrive_peer(bready0 + stage * 8);
         }
         if (!ok && lane == 0) {
             record_error(p, kErrTimeout, 4);
