@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                 epilogue_cols<EPI>(P, U, tacc, 0, P.bn, 16, m, m < P.M);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(tempty0);
+            if (lane == 0) mbar_arrive_peer(tempty0);  // this CTA's TMEM reads are complete (wait::ld)
             aphase ^= 1u;
         }
         if (!ok && lane == 0) {
