@@ -51,6 +51,11 @@ struct Gemm2Nf4Cfg {
     static constexpr int TMEM_COLS = 512;              // one accumulator: 2 M halves x 256 columns
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+    // Each stage slot must always be decoded by the same group: a group waits on a slot's full
+    // barrier by phase parity, and if the slot's previous K block belonged to another group whose
+    // TMA had not landed yet (loads of different stages complete in any order), the barrier would
+    // still be one phase behind and the parity wait would pass at once.
+    static_assert(STAGES % kPairNf4DecodeGroups == 0, "decode groups must divide the stage count");
 };
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
