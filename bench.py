@@ -82,9 +82,9 @@ def load_peaks():
 
 
 def src_digest():
-    """Digest of the sources of the GEMM kernel template (the kernels the traffic figures are for)."""
+    """Digest of the sources of the GEMM kernel templates (the kernels the traffic figures are for)."""
     h = hashlib.sha256()
-    for f in [os.path.join(ROOT, "bwd_lora_mlp_gb300", "csrc", x) for x in ("lm_gemm.cuh", "lm_gemm2.cuh", "lm_ptx.cuh")]:
+    for f in [os.path.join(ROOT, "bwd_lora_mlp_gb300", "csrc", x) for x in ("lm_gemm.cuh", "lm_gemm2.cuh", "lm_gemm2_nf4.cuh", "lm_ptx.cuh")]:
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -478,6 +478,17 @@ struct Builder {
             Prob& P = p.prob[i];
             P.tiles_m = (int32_t)((P.M + tile_m - 1) / tile_m);
             tiles += (int64_t)P.tiles_m * P.tiles_n;
+            P.group_m = 16;
+            if (gemm_is_pair_nf4(kind)) {
+                // about 16 MiB of A rows (bf16, all K segments) per raster group: the NF4 stage
+                // ring is bound by load latency, and with 16 M tiles of 512 rows per group every
+                // N column re-reads all of A from DRAM once the output stream has evicted it
+                // (measured: 4-6 % per NF4 GEMM; the bf16 pair kernels are indifferent)
+                int64_t k = 0;
+                for (int si = 0; si < P.nseg; ++si) k += P.seg[si].kext;
+                const int64_t per_tile = std::max<int64_t>(1, (int64_t)tile_m * k * 2);
+                P.group_m = (int32_t)std::max<int64_t>(1, std::min<int64_t>(P.tiles_m, (16ll << 20) / per_tile));
+            }
         }
         int S = 1;
         if (partial) {

@@ -59,6 +59,7 @@ struct Prob {
     int32_t n_step;             // B rows (K-major) / B columns (MN-major) per N tile
     int32_t out_col_step;       // output columns per N tile
     int32_t act;
+    int32_t group_m;            // M tiles per raster group (units run M-fastest within a group)
     Seg seg[kMaxSegs];
     void* out0;
     void* out1;
@@ -105,8 +106,9 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     r.pi = pi;
     r.ks = local % P.splits;
     local /= P.splits;
-    // rasterise in groups of 16 M tiles so concurrently running tiles share B panels
-    const int GM = 16;
+    // rasterise in groups of group_m M tiles (M fastest): the tiles running at once share B
+    // panels, and a group's A rows stay small enough to be re-read from L2 for every N column
+    const int GM = P.group_m > 0 ? P.group_m : 16;
     const int per_group = GM * P.tiles_n;
     const int g = local / per_group, w = local % per_group;
     const int gm = min(GM, P.tiles_m - g * GM);
