@@ -13,21 +13,40 @@ struct FinRowJobs {
     FinRowJob j[3];
 };
 
+// One thread per (16-column chunk, row): per split a contiguous 64-byte read of the row's chunk,
+// one 32-byte write of the bf16 row chunk, and 16 transposed writes that are coalesced across the
+// threads of a warp (consecutive rows).  ncols and group are multiples of 16.
 __global__ void __launch_bounds__(256) fin_rowproj_kernel(FinRowJobs jobs, int64_t T) {
     const FinRowJob& J = jobs.j[blockIdx.y];
-    const int64_t total = (int64_t)J.ncols * T;
+    const int nchunk = J.ncols / 16;
+    const int64_t total = (int64_t)nchunk * T;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        const int col = (int)(idx / T);
-        const int64_t t = idx - (int64_t)col * T;
-        const float* src = J.part + t * J.ncols + col;
-        float acc = 0.0f;
-        for (int ks = 0; ks < J.splits; ++ks) acc += src[(int64_t)ks * J.split_stride];
-        const float v = acc * J.s[col / J.group];
-        const __nv_bfloat16 b = __float2bfloat16_rn(v);
-        const uint16_t bits = *reinterpret_cast<const uint16_t*>(&b);
-        J.out[t * J.ncols + col] = bits;
-        J.outT[(int64_t)col * J.ldT + t] = bits;
+        const int ch = (int)(idx / T);
+        const int64_t t = idx - (int64_t)ch * T;
+        const int c0 = ch * 16;
+        const float4* src = reinterpret_cast<const float4*>(J.part + t * J.ncols + c0);
+        float4 a0 = src[0], a1 = src[1], a2 = src[2], a3 = src[3];
+        for (int ks = 1; ks < J.splits; ++ks) {
+            const float4* q = reinterpret_cast<const float4*>(J.part + (int64_t)ks * J.split_stride + t * J.ncols + c0);
+            const float4 b0 = q[0], b1 = q[1], b2 = q[2], b3 = q[3];
+            a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
+            a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
+            a2.x += b2.x; a2.y += b2.y; a2.z += b2.z; a2.w += b2.w;
+            a3.x += b3.x; a3.y += b3.y; a3.z += b3.z; a3.w += b3.w;
+        }
+        const float sc = J.s[c0 / J.group];
+        const float v[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
+                             a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[2 * i] * sc, v[2 * i + 1] * sc);
+        uint4* dst = reinterpret_cast<uint4*>(J.out + t * J.ncols + c0);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            J.outT[(int64_t)(c0 + i) * J.ldT + t] = (uint16_t)((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu));
     }
 }
 
@@ -36,7 +55,7 @@ cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cuda
     int64_t most = 0;
     for (int i = 0; i < njobs; ++i) {
         js.j[i] = jobs[i];
-        most = std::max<int64_t>(most, (int64_t)jobs[i].ncols * T);
+        most = std::max<int64_t>(most, (int64_t)(jobs[i].ncols / 16) * T);
     }
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>((most + threads - 1) / threads, 4096);
@@ -48,24 +67,41 @@ struct FinColJobs {
     FinColJob j[6];
 };
 
+// One thread per (16-wide chunk of j, column c), c fastest: per split a contiguous 64-byte read;
+// the transposed output out[j][c] is written coalesced across the warp, out[c][j] as a run of
+// the row.  rp is a multiple of 16.
 __global__ void __launch_bounds__(256) fin_colreduce_kernel(FinColJobs jobs) {
     const FinColJob& J = jobs.j[blockIdx.y];
-    const int64_t total = J.C * J.r;
+    const int nchunk = J.rp / 16;
+    const int64_t total = J.C * nchunk;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        int64_t c;
-        int j;
-        if (J.transposed) {  // out[j][c], consecutive threads -> consecutive c
-            j = (int)(idx / J.C);
-            c = idx - (int64_t)j * J.C;
-        } else {             // out[c][j]
-            c = idx / J.r;
-            j = (int)(idx - c * J.r);
+        const int ch = (int)(idx / J.C);
+        const int64_t c = idx - (int64_t)ch * J.C;
+        const int j0 = ch * 16;
+        if (j0 >= J.r) continue;
+        const float4* src = reinterpret_cast<const float4*>(J.part + c * J.rp + j0);
+        float4 a0 = src[0], a1 = src[1], a2 = src[2], a3 = src[3];
+        for (int ks = 1; ks < J.splits; ++ks) {
+            const float4* q = reinterpret_cast<const float4*>(J.part + (int64_t)ks * J.split_stride + c * J.rp + j0);
+            const float4 b0 = q[0], b1 = q[1], b2 = q[2], b3 = q[3];
+            a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
+            a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
+            a2.x += b2.x; a2.y += b2.y; a2.z += b2.z; a2.w += b2.w;
+            a3.x += b3.x; a3.y += b3.y; a3.z += b3.z; a3.w += b3.w;
         }
-        const float* src = J.part + c * J.rp + j;
-        float acc = 0.0f;
-        for (int ks = 0; ks < J.splits; ++ks) acc += src[(int64_t)ks * J.split_stride];
-        J.out[idx] = acc;
+        const float v[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
+                             a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+        const int nj = min(16, J.r - j0);
+        if (J.transposed) {  // out[j][c]
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (i < nj) J.out[(int64_t)(j0 + i) * J.C + c] = v[i];
+        } else {             // out[c][j]
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (i < nj) J.out[c * J.r + j0 + i] = v[i];
+        }
     }
 }
 
@@ -74,7 +110,7 @@ cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t 
     int64_t most = 0;
     for (int i = 0; i < njobs; ++i) {
         js.j[i] = jobs[i];
-        most = std::max<int64_t>(most, jobs[i].C * jobs[i].r);
+        most = std::max<int64_t>(most, jobs[i].C * (jobs[i].rp / 16));
     }
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>((most + threads - 1) / threads, 4096);
