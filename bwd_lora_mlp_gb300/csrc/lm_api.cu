@@ -473,6 +473,8 @@ struct Builder {
             if (narrow) kind = G_PART_KK64;
         }
         const bool partial = (kind == G_PART_KK || kind == G_PART_KK64 || kind == G_PART_KMN || kind == G_PART_MNK);
+        // resident CTAs of the one-CTA kernel: two per SM for the 64-wide variants
+        const int slots = (kind == G_PART_KK64 || kind == G_PART_KMN || kind == G_PART_MNK) ? 2 * sms : sms;
         int64_t tiles = 0;
         for (int i = 0; i < p.nprob; ++i) {
             Prob& P = p.prob[i];
@@ -503,7 +505,7 @@ struct Builder {
                     units_c += (int64_t)P.tiles_m * P.tiles_n * ((nkb + kbps - 1) / kbps);
                     kbps_max = std::max(kbps_max, kbps);
                 }
-                const int64_t cost = (units_c + sms - 1) / sms * kbps_max;
+                const int64_t cost = (units_c + slots - 1) / slots * kbps_max;
                 if (cost < best) {
                     best = cost;
                     S = cand;
@@ -525,7 +527,7 @@ struct Builder {
             units += (int64_t)P.tiles_m * P.tiles_n * P.splits;
         }
         p.total_units = (int32_t)units;
-        return (int)std::min<int64_t>(units, sms);
+        return (int)std::min<int64_t>(units, partial ? slots : sms);
     }
 
     lm_status launch(const char* tag, int sms, int32_t* err, cudaStream_t st_) {

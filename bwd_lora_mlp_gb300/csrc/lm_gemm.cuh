@@ -86,7 +86,10 @@ struct GemmCfg {
     static constexpr int A_BYTES = kBM * kBK * 2;
     static constexpr int B_BYTES = (BN_MAX < 64 ? 64 : BN_MAX) * kBK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
+    // the narrow (rank-r wide) variants stream A through a tiny B: two CTAs per SM, two
+    // independent load pipelines, the same bytes in flight per SM
+    static constexpr int CTAS_PER_SM = BN_MAX <= 64 ? 2 : 1;
+    static constexpr int STAGES = (196608 / CTAS_PER_SM / STAGE_BYTES) > 8 ? 8 : (196608 / CTAS_PER_SM / STAGE_BYTES);
     static constexpr int TMEM_COLS = 2 * BN_MAX < 32 ? 32 : 2 * BN_MAX;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns must be a power of two");
@@ -294,7 +297,7 @@ __device__ __forceinline__ void epilogue_tile(const Prob& P, const Unit& U, uint
 
 // ---------------------------------------------------------------- the kernel
 template <int BN_MAX, bool A_MN, bool B_MN, int EPI>
-__global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kNumThreads, BN_MAX <= 64 ? 2 : 1) gemm_kernel(const __grid_constant__ Params p) {
     using C = GemmCfg<BN_MAX, A_MN, B_MN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
