@@ -13,40 +13,46 @@ struct FinRowJobs {
     FinRowJob j[3];
 };
 
-// One thread per (16-column chunk, row): per split a contiguous 64-byte read of the row's chunk,
-// one 32-byte write of the bf16 row chunk, and 16 transposed writes that are coalesced across the
-// threads of a warp (consecutive rows).  ncols and group are multiples of 16.
+// Sum of split slices in slice order, with the loads of up to eight slices issued before their
+// additions (the order of the additions, and so the result, is that of a plain loop).
+__device__ __forceinline__ float4 sum_splits(const float* p0, int64_t stride, int splits) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < splits; k0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (k0 + i < splits) v[i] = *reinterpret_cast<const float4*>(p0 + (int64_t)(k0 + i) * stride);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (k0 + i < splits) {
+                acc.x += v[i].x;
+                acc.y += v[i].y;
+                acc.z += v[i].z;
+                acc.w += v[i].w;
+            }
+    }
+    return acc;
+}
+
+// One thread per (4-column chunk, row), rows fastest: the transposed writes are coalesced across
+// a warp, the row write is 8 contiguous bytes.  ncols and group are multiples of 4.
 __global__ void __launch_bounds__(256) fin_rowproj_kernel(FinRowJobs jobs, int64_t T) {
     const FinRowJob& J = jobs.j[blockIdx.y];
-    const int nchunk = J.ncols / 16;
+    const int nchunk = J.ncols / 4;
     const int64_t total = (int64_t)nchunk * T;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
         const int ch = (int)(idx / T);
         const int64_t t = idx - (int64_t)ch * T;
-        const int c0 = ch * 16;
-        const float4* src = reinterpret_cast<const float4*>(J.part + t * J.ncols + c0);
-        float4 a0 = src[0], a1 = src[1], a2 = src[2], a3 = src[3];
-        for (int ks = 1; ks < J.splits; ++ks) {
-            const float4* q = reinterpret_cast<const float4*>(J.part + (int64_t)ks * J.split_stride + t * J.ncols + c0);
-            const float4 b0 = q[0], b1 = q[1], b2 = q[2], b3 = q[3];
-            a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
-            a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
-            a2.x += b2.x; a2.y += b2.y; a2.z += b2.z; a2.w += b2.w;
-            a3.x += b3.x; a3.y += b3.y; a3.z += b3.z; a3.w += b3.w;
-        }
+        const int c0 = ch * 4;
+        const float4 a = sum_splits(J.part + t * J.ncols + c0, J.split_stride, J.splits);
         const float sc = J.s[c0 / J.group];
-        const float v[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
-                             a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[2 * i] * sc, v[2 * i + 1] * sc);
-        uint4* dst = reinterpret_cast<uint4*>(J.out + t * J.ncols + c0);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            J.outT[(int64_t)(c0 + i) * J.ldT + t] = (uint16_t)((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu));
+        const uint32_t w0 = pack_bf16x2(a.x * sc, a.y * sc), w1 = pack_bf16x2(a.z * sc, a.w * sc);
+        *reinterpret_cast<uint2*>(J.out + t * J.ncols + c0) = make_uint2(w0, w1);
+        J.outT[(int64_t)(c0 + 0) * J.ldT + t] = (uint16_t)(w0 & 0xFFFFu);
+        J.outT[(int64_t)(c0 + 1) * J.ldT + t] = (uint16_t)(w0 >> 16);
+        J.outT[(int64_t)(c0 + 2) * J.ldT + t] = (uint16_t)(w1 & 0xFFFFu);
+        J.outT[(int64_t)(c0 + 3) * J.ldT + t] = (uint16_t)(w1 >> 16);
     }
 }
 
@@ -55,7 +61,7 @@ cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cuda
     int64_t most = 0;
     for (int i = 0; i < njobs; ++i) {
         js.j[i] = jobs[i];
-        most = std::max<int64_t>(most, (int64_t)(jobs[i].ncols / 16) * T);
+        most = std::max<int64_t>(most, (int64_t)(jobs[i].ncols / 4) * T);
     }
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>((most + threads - 1) / threads, 4096);
@@ -67,41 +73,27 @@ struct FinColJobs {
     FinColJob j[6];
 };
 
-// One thread per (16-wide chunk of j, column c), c fastest: per split a contiguous 64-byte read;
-// the transposed output out[j][c] is written coalesced across the warp, out[c][j] as a run of
-// the row.  rp is a multiple of 16.
+// One thread per (column c, 4-wide chunk of j), chunk fastest: the partial reads of a warp are
+// contiguous, and so are the writes of out[c][j]; rp is a multiple of 4.
 __global__ void __launch_bounds__(256) fin_colreduce_kernel(FinColJobs jobs) {
     const FinColJob& J = jobs.j[blockIdx.y];
-    const int nchunk = J.rp / 16;
+    const int nchunk = J.rp / 4;
     const int64_t total = J.C * nchunk;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        const int ch = (int)(idx / J.C);
-        const int64_t c = idx - (int64_t)ch * J.C;
-        const int j0 = ch * 16;
+        const int64_t c = idx / nchunk;
+        const int ch = (int)(idx - c * nchunk);
+        const int j0 = ch * 4;
         if (j0 >= J.r) continue;
-        const float4* src = reinterpret_cast<const float4*>(J.part + c * J.rp + j0);
-        float4 a0 = src[0], a1 = src[1], a2 = src[2], a3 = src[3];
-        for (int ks = 1; ks < J.splits; ++ks) {
-            const float4* q = reinterpret_cast<const float4*>(J.part + (int64_t)ks * J.split_stride + c * J.rp + j0);
-            const float4 b0 = q[0], b1 = q[1], b2 = q[2], b3 = q[3];
-            a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
-            a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
-            a2.x += b2.x; a2.y += b2.y; a2.z += b2.z; a2.w += b2.w;
-            a3.x += b3.x; a3.y += b3.y; a3.z += b3.z; a3.w += b3.w;
-        }
-        const float v[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
-                             a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
-        const int nj = min(16, J.r - j0);
-        if (J.transposed) {  // out[j][c]
+        const float4 a = sum_splits(J.part + c * J.rp + j0, J.split_stride, J.splits);
+        const float v[4] = {a.x, a.y, a.z, a.w};
+        const int nj = min(4, J.r - j0);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (i < nj) J.out[(int64_t)(j0 + i) * J.C + c] = v[i];
-        } else {             // out[c][j]
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (i < nj) J.out[c * J.r + j0 + i] = v[i];
-        }
+        for (int i = 0; i < 4; ++i)
+            if (i < nj) {
+                if (J.transposed) J.out[(int64_t)(j0 + i) * J.C + c] = v[i];  // out[j][c]
+                else J.out[c * J.r + j0 + i] = v[i];                          // out[c][j]
+            }
     }
 }
 
@@ -110,7 +102,7 @@ cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t 
     int64_t most = 0;
     for (int i = 0; i < njobs; ++i) {
         js.j[i] = jobs[i];
-        most = std::max<int64_t>(most, jobs[i].C * (jobs[i].rp / 16));
+        most = std::max<int64_t>(most, jobs[i].C * (jobs[i].rp / 4));
     }
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>((most + threads - 1) / threads, 4096);
@@ -119,29 +111,35 @@ cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t 
 }
 
 // ------------------------------------------------------------------ block-diagonal rank-r operand
+// [Bg | 0 ; 0 | Bu] (2n x 2rp bf16): one thread per 8 consecutive columns of a row (one 16-byte
+// store); 2rp is a multiple of 32.
 __global__ void __launch_bounds__(256) blockdiag_kernel(const uint16_t* __restrict__ Bg,
                                                         const uint16_t* __restrict__ Bu, int64_t n, int r,
                                                         int rp, uint16_t* __restrict__ out) {
-    const int64_t cols = 2 * rp;
-    const int64_t total = 2 * n * cols;
+    const int groups = (2 * rp) / 8;
+    const int64_t total = 2 * n * groups;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t row = idx / cols;
-        const int col = (int)(idx - row * cols);
-        uint16_t v = 0;
-        if (row < n) {
-            if (col < r) v = Bg[row * r + col];
-        } else {
-            const int c = col - rp;
-            if (c >= 0 && c < r) v = Bu[(row - n) * r + c];
+        const int64_t row = idx / groups;
+        const int c0 = (int)(idx - row * groups) * 8;
+        const bool upper = row < n;
+        const uint16_t* src = upper ? Bg + row * r : Bu + (row - n) * r;
+        const int off = upper ? 0 : rp;  // first output column of this row's block
+        uint16_t v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = c0 + i - off;
+            v[i] = (c >= 0 && c < r) ? src[c] : (uint16_t)0;
         }
-        out[idx] = v;
+        *reinterpret_cast<uint4*>(out + row * 2 * rp + c0) =
+            make_uint4(v[0] | ((uint32_t)v[1] << 16), v[2] | ((uint32_t)v[3] << 16), v[4] | ((uint32_t)v[5] << 16),
+                       v[6] | ((uint32_t)v[7] << 16));
     }
 }
 
 cudaError_t launch_blockdiag(const uint16_t* Bg, const uint16_t* Bu, int64_t n, int r, int rp, uint16_t* out,
                              cudaStream_t st) {
-    const int64_t total = 2 * n * 2 * rp;
+    const int64_t total = 2 * n * (2 * rp / 8);
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, 2048);
     blockdiag_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, st>>>(Bg, Bu, n, r, rp, out);
     return cudaGetLastError();
