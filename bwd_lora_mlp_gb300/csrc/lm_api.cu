@@ -233,6 +233,10 @@ struct Bump {
 };
 
 constexpr int kMaxSplits = 16;
+// Split tail tiles of a plain-store NF4 pair GEMM: at most this many fp32 partial tiles
+// (512 x 256 each) per launch, in a workspace slot of kTailParts * 512 KiB.
+constexpr int kTailParts = 80;
+constexpr size_t kTailBytes = (size_t)kTailParts * 512 * 256 * 4;
 
 struct Dims {
     int64_t T, ldT;
@@ -269,6 +273,7 @@ struct MlpPlan {
     size_t de, du;
     size_t bdiag;           // [Bg | 0 ; 0 | Bu] (2n x 2rp) for the CTA-pair gate/up GEMM
     size_t sc[3];           // NF4 base: fp32 block-scale tables of W_gate, W_up, W_down
+    size_t tail;            // NF4 base: split tail tiles of the down and dX GEMMs
     size_t ws_total;
 };
 
@@ -291,6 +296,7 @@ MlpPlan plan_mlp(int64_t T, int64_t d, int64_t n, int32_t r) {
     P.du = w.take((size_t)T * n * 2);
     P.bdiag = w.take((size_t)2 * n * 2 * rp * 2);
     for (int i = 0; i < 3; ++i) P.sc[i] = w.take((size_t)n * d / 64 * 4);
+    P.tail = w.take(kTailBytes);
     P.ws_total = w.off;
     return P;
 }
@@ -302,6 +308,7 @@ struct QkvPlan {
     size_t part;
     RankBuf g[3];
     size_t sc[3];           // NF4 base: fp32 block-scale tables of W_q, W_k, W_v
+    size_t tail;            // NF4 base: split tail tiles of the dX GEMM
     size_t ws_total;
 };
 
@@ -319,6 +326,7 @@ QkvPlan plan_qkv(int64_t T, int64_t d, int64_t nq, int64_t nk, int64_t nv, int32
     for (int i = 0; i < 3; ++i) P.g[i] = take_rank(w, P.D, rp);
     const int64_t nout[3] = {nq, nk, nv};
     for (int i = 0; i < 3; ++i) P.sc[i] = w.take((size_t)nout[i] * d / 64 * 4);
+    P.tail = w.take(kTailBytes);
     P.ws_total = w.off;
     return P;
 }
@@ -330,6 +338,7 @@ struct OPlan {
     size_t part;
     RankBuf g;
     size_t sc;              // NF4 base: fp32 block-scale table of W_o
+    size_t tail;            // NF4 base: split tail tiles of the O and dX GEMMs
     size_t ws_total;
 };
 
@@ -346,6 +355,7 @@ OPlan plan_o(int64_t T, int64_t d_in, int64_t d_out, int32_t r) {
     P.part = w.take((size_t)kMaxSplits * part_elems * 4);
     P.g = take_rank(w, P.D, rp);
     P.sc = w.take((size_t)d_out * d_in / 64 * 4);
+    P.tail = w.take(kTailBytes);
     P.ws_total = w.off;
     return P;
 }
@@ -360,6 +370,7 @@ lm_status scale_table(const char* tag, const lm_weight& W, float* table, cudaStr
 // ------------------------------------------------------------------ GEMM launch builder
 struct Builder {
     Params p;
+    float* tail_buf = nullptr;  // workspace slot for split tail tiles (NF4 plain-store GEMMs)
     int nmaps = 0;
     int tile_m = kBM;
     lm_status st = LM_OK;
@@ -527,18 +538,65 @@ struct Builder {
             units += (int64_t)P.tiles_m * P.tiles_n * P.splits;
         }
         p.total_units = (int32_t)units;
-        return (int)std::min<int64_t>(units, partial ? slots : sms);
+        // NF4 plain-store GEMM whose last wave is partly idle: split each tile of that wave over
+        // its K blocks into the number of parts that finishes the tail soonest
+        int ncl = 0;
+        if (tail_buf && (kind == G2N_STORE_K || kind == G2N_STORE_MN) && p.nprob == 1 &&
+            pair_nf4_clusters(kind, &ncl) == cudaSuccess && ncl > 1) {
+            Prob& P = p.prob[0];
+            const int tiles = P.tiles_m * P.tiles_n;
+            const int full = tiles / ncl * ncl, tail = tiles - full;
+            int best = 1;
+            double best_t = 1.0;  // the tail's makespan in tile times
+            for (int S = 2; S <= 4 && full > 0 && tail > 0; ++S) {
+                if (tail * S > kTailParts) break;
+                const double t = (double)((tail * S + ncl - 1) / ncl) / S;
+                if (t < best_t - 1e-9) {
+                    best_t = t;
+                    best = S;
+                }
+            }
+            if (best > 1) {
+                P.tail_begin = full;
+                P.tail_splits = best;
+                P.tail_part = tail_buf;
+                p.total_units = full + tail * best;
+            }
+        }
+        return (int)std::min<int64_t>(p.total_units, partial ? slots : sms);
     }
 
     lm_status launch(const char* tag, int sms, int32_t* err, cudaStream_t st_) {
         if (st != LM_OK) return st;
         const int grid = finish(sms, err);
         if (grid == 0) return LM_OK;
-        ProfScope prof(tag, st_);
-        const cudaError_t e = gemm_is_pair(kind)       ? launch_gemm_pair(kind, p, p.total_units, st_)
-                              : gemm_is_pair_nf4(kind) ? launch_gemm_pair_nf4(kind, p, p.total_units, st_)
-                                                       : launch_gemm(kind, p, grid, st_);
-        if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
+        {
+            ProfScope prof(tag, st_);
+            const cudaError_t e = gemm_is_pair(kind)       ? launch_gemm_pair(kind, p, p.total_units, st_)
+                                  : gemm_is_pair_nf4(kind) ? launch_gemm_pair_nf4(kind, p, p.total_units, st_)
+                                                           : launch_gemm(kind, p, grid, st_);
+            if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
+        }
+        const Prob& P = p.prob[0];
+        if (P.tail_splits > 1) {
+            ProfScope prof("tail.fin", st_);
+            TailFin f{};
+            f.part = P.tail_part;
+            f.out = static_cast<uint16_t*>(P.out0);
+            f.M = P.M;
+            f.N = P.N;
+            f.ld_out = P.ld_out;
+            f.out_col_step = P.out_col_step;
+            f.ntail = P.tiles_m * P.tiles_n - P.tail_begin;
+            f.splits = P.tail_splits;
+            f.bn = P.bn;
+            f.tail_begin = P.tail_begin;
+            f.tiles_m = P.tiles_m;
+            f.tiles_n = P.tiles_n;
+            f.group_m = P.group_m;
+            const cudaError_t e = launch_tail_fin(f, st_);
+            if (e != cudaSuccess) return cuda_fail(e, "tail finalisation launch");
+        }
         return LM_OK;
     }
 };
@@ -887,6 +945,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     }
     if (nf4) {
         Builder b(G2N_STORE_K);
+        b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
@@ -1101,6 +1160,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     }
     if (nf4) {
         Builder b(G2N_STORE_MN);
+        b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
@@ -1246,6 +1306,7 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     }
     if (nf4) {
         Builder b(G2N_STORE_K);
+        b.tail_buf = at<float>(ws, PL.tail);
         const int xmap = b.map(X, T, d, d, 128);
         const int amap = b.map(xa, T, 3 * rp, 3 * rp, 128);
         const lm_lora* Ls[3] = {q, k, v};
@@ -1406,6 +1467,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     }
     if (nf4) {  // dX = sum_x dOut_x W_x + G_x A_x
         Builder b(G2N_STORE_MN);
+        b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
@@ -1526,6 +1588,7 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     }
     if (nf4) {
         Builder b(G2N_STORE_K);
+        b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d_out;
@@ -1629,6 +1692,7 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     }
     if (nf4) {  // dX = dY W + G A
         Builder b(G2N_STORE_MN);
+        b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d_in;

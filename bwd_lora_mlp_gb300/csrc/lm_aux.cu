@@ -110,6 +110,44 @@ cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t 
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ split tail tiles
+// One thread per 4 columns of a tail-tile row; 512-row tiles, bn and N multiples of 4.
+__global__ void __launch_bounds__(256) tail_fin_kernel(TailFin f) {
+    const int c4n = f.bn / 4;
+    const int64_t total = (int64_t)f.ntail * 512 * c4n;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int c4 = (int)(idx % c4n);
+        const int64_t rt = idx / c4n;
+        const int row = (int)(rt % 512);
+        const int t = (int)(rt / 512);
+        int mb, nb;
+        raster_tile(f.tail_begin + t, f.tiles_m, f.tiles_n, f.group_m, mb, nb);
+        const int64_t m = (int64_t)mb * 512 + row;
+        const int64_t gcol = (int64_t)nb * f.out_col_step + c4 * 4;
+        if (m >= f.M || gcol >= f.N) continue;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < f.splits; ++k) {
+            const float4 v =
+                *reinterpret_cast<const float4*>(f.part + ((int64_t)(t * f.splits + k) * 512 + row) * f.bn + c4 * 4);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        *reinterpret_cast<uint2*>(f.out + m * f.ld_out + gcol) =
+            make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    }
+}
+
+cudaError_t launch_tail_fin(const TailFin& f, cudaStream_t st) {
+    const int64_t total = (int64_t)f.ntail * 512 * (f.bn / 4);
+    if (total == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, 4096);
+    tail_fin_kernel<<<(unsigned)blocks, 256, 0, st>>>(f);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ block-diagonal rank-r operand
 // [Bg | 0 ; 0 | Bu] (2n x 2rp bf16): one thread per 8 consecutive columns of a row (one 16-byte
 // store); 2rp is a multiple of 32.

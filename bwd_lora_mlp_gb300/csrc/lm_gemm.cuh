@@ -68,6 +68,12 @@ struct Prob {
     const void* in1;
     int64_t ld_out, ld_in;      // elements
     int64_t split_stride;       // PARTIAL: elements between split slices
+    // Tail splitting (NF4 pair kernel, plain-store epilogue): tiles from tail_begin on are each
+    // run as tail_splits units over consecutive slices of their K-block sequence; each writes its
+    // fp32 accumulator to tail_part[(tile - tail_begin) * tail_splits + part] (tile-sized
+    // row-major blocks of rows x bn) and a finalisation kernel sums the parts in order.
+    int32_t tail_begin, tail_splits;
+    float* tail_part;
 };
 
 struct Params {  // CUtensorMap members carry their own 128-byte alignment
@@ -98,7 +104,18 @@ struct GemmCfg {
 
 struct Unit {
     int pi, mb, nb, ks;
+    int tail;    // >= 0: index of a split tail tile (then ks is its part); -1 otherwise
 };
+
+// (mb, nb) of tile `t` of a problem: groups of `group_m` M tiles, M fastest within a group
+__host__ __device__ inline void raster_tile(int t, int tiles_m, int tiles_n, int group_m, int& mb, int& nb) {
+    const int GM = group_m > 0 ? group_m : 16;
+    const int per_group = GM * tiles_n;
+    const int g = t / per_group, w = t % per_group;
+    const int gm = (tiles_m - g * GM) < GM ? (tiles_m - g * GM) : GM;
+    mb = g * GM + w % gm;
+    nb = w / gm;
+}
 
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     Unit r;
@@ -107,17 +124,34 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     const Prob& P = p.prob[pi];
     int local = u - P.unit_begin;
     r.pi = pi;
-    r.ks = local % P.splits;
-    local /= P.splits;
+    r.tail = -1;
+    if (P.tail_splits > 1 && local >= P.tail_begin) {
+        const int q = local - P.tail_begin;
+        r.tail = q / P.tail_splits;
+        r.ks = q % P.tail_splits;
+        local = P.tail_begin + r.tail;
+    } else {
+        r.ks = local % P.splits;
+        local /= P.splits;
+    }
     // rasterise in groups of group_m M tiles (M fastest): the tiles running at once share B
     // panels, and a group's A rows stay small enough to be re-read from L2 for every N column
-    const int GM = P.group_m > 0 ? P.group_m : 16;
-    const int per_group = GM * P.tiles_n;
-    const int g = local / per_group, w = local % per_group;
-    const int gm = min(GM, P.tiles_m - g * GM);
-    r.mb = g * GM + w % gm;
-    r.nb = w / gm;
+    raster_tile(local, P.tiles_m, P.tiles_n, P.group_m, r.mb, r.nb);
     return r;
+}
+
+// K-block slice [g0, g1) of unit U over the concatenated K blocks of all its segments: all of
+// them, or part U.ks of tail_splits for a split tail tile.
+__device__ __forceinline__ void unit_kslice(const Prob& P, const Unit& U, int& g0, int& g1) {
+    int total = 0;
+    for (int si = 0; si < P.nseg; ++si) total += (P.seg[si].kext + kBK - 1) / kBK;
+    if (U.tail >= 0) {
+        g0 = (int)((int64_t)U.ks * total / P.tail_splits);
+        g1 = (int)((int64_t)(U.ks + 1) * total / P.tail_splits);
+    } else {
+        g0 = 0;
+        g1 = total;
+    }
 }
 
 __device__ __forceinline__ void record_error(const Params& p, int code, int where) {

@@ -5,41 +5,71 @@
 namespace lm {
 
 template <bool B_MN, int EPI>
-static cudaError_t launch_pair_nf4_variant(const Params& p, int max_units, cudaStream_t st) {
-    constexpr int smem = Gemm2Nf4Cfg::SMEM_BYTES;
-    auto k = gemm2_nf4_kernel<B_MN, EPI>;
-    static int clusters[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+static cudaLaunchConfig_t pair_nf4_config(cudaLaunchAttribute* attr, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(kPairNf4Threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = Gemm2Nf4Cfg::SMEM_BYTES;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (dev < 64 && clusters[dev] == 0) {
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return cfg;
+}
+
+// resident clusters of the variant on the current device (queried once per device)
+template <bool B_MN, int EPI>
+static cudaError_t pair_nf4_variant_clusters(int* out) {
+    auto k = gemm2_nf4_kernel<B_MN, EPI>;
+    static int clusters[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || clusters[dev] == 0) {
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Gemm2Nf4Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         int sms = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = pair_nf4_config<B_MN, EPI>(attr, nullptr);
         cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
         int n = 0;
         e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
         if (e != cudaSuccess) return e;
-        clusters[dev] = n > 0 ? n : 1;
+        n = n > 0 ? n : 1;
+        if (dev < 64) clusters[dev] = n;
+        *out = n;
+        return cudaSuccess;
     }
-    const int ncl = std::min(max_units, dev < 64 ? clusters[dev] : 1);
+    *out = clusters[dev];
+    return cudaSuccess;
+}
+
+template <bool B_MN, int EPI>
+static cudaError_t launch_pair_nf4_variant(const Params& p, int max_units, cudaStream_t st) {
+    int n = 0;
+    cudaError_t e = pair_nf4_variant_clusters<B_MN, EPI>(&n);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_nf4_config<B_MN, EPI>(attr, st);
+    const int ncl = std::min(max_units, n);
     cfg.gridDim = dim3(2 * ncl, 1, 1);
-    e = cudaLaunchKernelEx(&cfg, k, p);
+    e = cudaLaunchKernelEx(&cfg, gemm2_nf4_kernel<B_MN, EPI>, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+cudaError_t pair_nf4_clusters(GemmKind k, int* n) {
+    switch (k) {
+        case G2N_GLU_FWD: return pair_nf4_variant_clusters<false, EPI_GLU_FWD>(n);
+        case G2N_STORE_K: return pair_nf4_variant_clusters<false, EPI_STORE>(n);
+        case G2N_GLU_BWD: return pair_nf4_variant_clusters<true, EPI_GLU_BWD>(n);
+        case G2N_STORE_MN: return pair_nf4_variant_clusters<true, EPI_STORE>(n);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_gemm_pair_nf4(GemmKind k, const Params& p, int max_units, cudaStream_t st) {

@@ -161,14 +161,18 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
             for (int u = cid; ok && u < p.total_units; u += ncl) {
                 const Unit U = decode_unit(p, u);
                 const Prob& P = p.prob[U.pi];
-                for (int si = 0; ok && si < P.nseg; ++si) {
+                int g0, g1;
+                unit_kslice(P, U, g0, g1);
+                for (int si = 0, g = 0; ok && si < P.nseg; ++si) {
                     const Seg& S = P.seg[si];
                     const int nkb = (S.kext + kBK - 1) / kBK;
+                    const int kb0 = max(0, g0 - g), kb1 = min(nkb, g1 - g);
+                    g += nkb;
                     const bool nf4 = S.b_scale[0] >= 0;
                     const int bmap = (rank == 1 && S.b_map[1] >= 0) ? S.b_map[1] : S.b_map[0];
                     const int smap = (rank == 1 && S.b_scale[1] >= 0) ? S.b_scale[1] : S.b_scale[0];
                     const int brow = U.nb * P.n_step + (int)rank * S.b_rank_off;
-                    for (int kb = 0; kb < nkb; ++kb) {
+                    for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) {
                             ok = false;
                             break;
@@ -242,10 +246,14 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                 tc_fence_after();
                 const uint32_t idesc = make_idesc_bf16(256, P.bn, false, B_MN);
                 uint32_t accum = 0;
-                for (int si = 0; ok && si < P.nseg; ++si) {
+                int g0, g1;
+                unit_kslice(P, U, g0, g1);
+                for (int si = 0, g = 0; ok && si < P.nseg; ++si) {
                     const Seg& S = P.seg[si];
                     const int nkb = (S.kext + kBK - 1) / kBK;
-                    for (int kb = 0; kb < nkb; ++kb) {
+                    const int kb0 = max(0, g0 - g), kb1 = min(nkb, g1 - g);
+                    g += nkb;
+                    for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait_warp(smem_u32(&bready[stage]), phase, s_abort)) {
                             ok = false;
                             break;
@@ -347,10 +355,30 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
             tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + hh * 256;
             const int64_t m = (int64_t)U.mb * 512 + hh * 256 + (int64_t)rank * kBM + q * 32 + lane;
-            if constexpr (EPI == EPI_GLU_FWD)
+            if constexpr (EPI == EPI_GLU_FWD) {
                 epilogue_cols<EPI>(P, U, tacc, 0, P.bn >> 1, 16, m, m < P.M);
-            else
+            } else if (EPI == EPI_STORE && U.tail >= 0) {
+                // part U.ks of a split tail tile: the raw fp32 accumulator row to its block
+                float* dst = P.tail_part +
+                             ((int64_t)(U.tail * P.tail_splits + U.ks) * 512 + (m - (int64_t)U.mb * 512)) * P.bn;
+#pragma unroll 1
+                for (int c = 0; c < P.bn; c += 32) {
+                    uint32_t a[16], b[16];
+                    tmem_ld_x16(tacc + c, a);
+                    tmem_ld_x16(tacc + c + 16, b);
+                    tmem_ld_wait32(a, b);
+                    float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        d4[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
+                                            __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
+                        d4[4 + i] = make_float4(__uint_as_float(b[4 * i]), __uint_as_float(b[4 * i + 1]),
+                                                __uint_as_float(b[4 * i + 2]), __uint_as_float(b[4 * i + 3]));
+                    }
+                }
+            } else {
                 epilogue_cols<EPI>(P, U, tacc, 0, P.bn, 16, m, m < P.M);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_peer(tempty0);  // this CTA's TMEM reads are complete (wait::ld)

@@ -73,6 +73,18 @@ cudaError_t launch_nf4_pack(const uint16_t* W, int64_t numel, uint8_t* codes, in
                             float* scale, cudaStream_t st);
 cudaError_t launch_nf4_dequant(const uint8_t* codes, const int8_t* absmax_q, const float* scale,
                                int64_t numel, bool bf16_out, void* out, cudaStream_t st);
+// Finalisation of split tail tiles of a plain-store NF4 pair GEMM: out[m][n] = bf16(sum over parts
+// in order of part[(t * splits + k) * 512 + row][col]) for the tiles tail_begin + t.
+struct TailFin {
+    const float* part;
+    uint16_t* out;
+    int64_t M, N, ld_out, out_col_step;
+    int32_t ntail, splits, bn, tail_begin, tiles_m, tiles_n, group_m;
+};
+cudaError_t launch_tail_fin(const TailFin& f, cudaStream_t st);
+// clusters the NF4 pair GEMM of kind k runs with on the current device
+cudaError_t pair_nf4_clusters(GemmKind k, int* n);
+
 // fp32 block scales of an NF4 weight, K-block-major: table[kb * rows + row] (rows * cols / 64)
 cudaError_t launch_nf4_scale_table(const int8_t* absmax_q, const float* scale, int64_t rows, int64_t cols,
                                    float* table, cudaStream_t st);

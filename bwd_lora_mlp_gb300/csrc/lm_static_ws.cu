@@ -8,9 +8,9 @@
 // its inputs and outputs; this entry point allocates nothing (no cudaMalloc, cudaFree or
 // allocating library routine) and runs the same kernels as lora_o_bwd.
 //
-// The scratch is kStaticWsBytes (16 MiB) of __device__ memory per GPU that loads the library,
+// The scratch is kStaticWsBytes (64 MiB) of __device__ memory per GPU that loads the library,
 // held until the process exits.  It covers the O-projection shapes whose lora_o_workspace_size
-// is at most that (for example T = 8192 tokens, 4096 -> 4096, r = 16 needs about 9.5 MiB);
+// is at most that (for example T = 8192 tokens, 4096 -> 4096, r = 16 needs about 49.5 MiB);
 // larger shapes are rejected with LM_ERR_WORKSPACE before anything is enqueued.
 //
 // Sharing: every call, from any thread or stream, uses the same array, and the array keeps what
@@ -34,7 +34,7 @@ lm_status report_error(lm_status s, const char* fmt, ...);
 
 namespace {
 
-constexpr size_t kStaticWsBytes = size_t(16) << 20;
+constexpr size_t kStaticWsBytes = size_t(64) << 20;
 
 static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 

@@ -196,9 +196,9 @@ LM_API lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const uint16
  * plugin whose host framework owns the device memory pool, a process under a hard device-memory
  * cap, or a latency-critical loop that cannot afford cudaFree's device-wide wait).  The web pages
  * have no counterpart: this is a deployment variant, not a step of the method.  The arguments and
- * results are those of lora_o_bwd without ws / ws_bytes: the scratch is a 16 MiB __device__ array
+ * results are those of lora_o_bwd without ws / ws_bytes: the scratch is a 64 MiB __device__ array
  * inside the library, held by every GPU that loads it until the process exits.  Shapes whose
- * lora_o_workspace_size exceeds 16 MiB are rejected with LM_ERR_WORKSPACE before any device work.
+ * lora_o_workspace_size exceeds 64 MiB are rejected with LM_ERR_WORKSPACE before any device work.
  * The call allocates nothing.  All calls share the one array and it keeps the last call's contents;
  * each call clears the error word on its stream, so calls whose kernels overlap on the GPU race and
  * must be ordered by the caller.  The first call on a device (that device current) looks up the
