@@ -126,11 +126,12 @@ lm_status ready(int* sms) {
 }
 
 // ------------------------------------------------------------------ validation
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// 32 bytes: TMA wants 16, the epilogues read and write 32-byte chunks of rows
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 lm_status need_ptr(const void* p, const char* name) {
     if (!p) return fail(LM_ERR_NULL, "%s is NULL", name);
-    if (!aligned16(p)) return fail(LM_ERR_ALIGN, "%s is not 16-byte aligned", name);
+    if (!aligned32(p)) return fail(LM_ERR_ALIGN, "%s is not 32-byte aligned", name);
     return LM_OK;
 }
 

@@ -199,28 +199,15 @@ __device__ __forceinline__ void epilogue_cols(const Prob& P, const Unit& U, uint
             tmem_ld_wait32(a, b);
             const int64_t gcol = (int64_t)U.nb * P.out_col_step + col;
             if (mvalid && gcol < P.N) {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out0) + m * P.ld_out + gcol);
-                uint4 v0, v1, v2, v3;
-                v0.x = pack_bf16x2(__uint_as_float(a[0]), __uint_as_float(a[1]));
-                v0.y = pack_bf16x2(__uint_as_float(a[2]), __uint_as_float(a[3]));
-                v0.z = pack_bf16x2(__uint_as_float(a[4]), __uint_as_float(a[5]));
-                v0.w = pack_bf16x2(__uint_as_float(a[6]), __uint_as_float(a[7]));
-                v1.x = pack_bf16x2(__uint_as_float(a[8]), __uint_as_float(a[9]));
-                v1.y = pack_bf16x2(__uint_as_float(a[10]), __uint_as_float(a[11]));
-                v1.z = pack_bf16x2(__uint_as_float(a[12]), __uint_as_float(a[13]));
-                v1.w = pack_bf16x2(__uint_as_float(a[14]), __uint_as_float(a[15]));
-                v2.x = pack_bf16x2(__uint_as_float(b[0]), __uint_as_float(b[1]));
-                v2.y = pack_bf16x2(__uint_as_float(b[2]), __uint_as_float(b[3]));
-                v2.z = pack_bf16x2(__uint_as_float(b[4]), __uint_as_float(b[5]));
-                v2.w = pack_bf16x2(__uint_as_float(b[6]), __uint_as_float(b[7]));
-                v3.x = pack_bf16x2(__uint_as_float(b[8]), __uint_as_float(b[9]));
-                v3.y = pack_bf16x2(__uint_as_float(b[10]), __uint_as_float(b[11]));
-                v3.z = pack_bf16x2(__uint_as_float(b[12]), __uint_as_float(b[13]));
-                v3.w = pack_bf16x2(__uint_as_float(b[14]), __uint_as_float(b[15]));
-                dst[0] = v0;
-                dst[1] = v1;
-                dst[2] = v2;
-                dst[3] = v3;
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    w[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+                    w[8 + i] = pack_bf16x2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
+                }
+                uint16_t* dst = static_cast<uint16_t*>(P.out0) + m * P.ld_out + gcol;
+                st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
             }
         }
     } else if constexpr (EPI == EPI_GLU_FWD) {
@@ -245,15 +232,9 @@ __device__ __forceinline__ void epilogue_cols(const Prob& P, const Unit& U, uint
                     ho[i] = pack_bf16x2(act_fwd(P.act, e0) * u0, act_fwd(P.act, e1) * u1);
                 }
                 const int64_t off = m * P.ld_out + gcol;
-                uint4* de = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out0) + off);
-                uint4* du = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out1) + off);
-                uint4* dh = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out2) + off);
-                de[0] = make_uint4(eo[0], eo[1], eo[2], eo[3]);
-                de[1] = make_uint4(eo[4], eo[5], eo[6], eo[7]);
-                du[0] = make_uint4(uo[0], uo[1], uo[2], uo[3]);
-                du[1] = make_uint4(uo[4], uo[5], uo[6], uo[7]);
-                dh[0] = make_uint4(ho[0], ho[1], ho[2], ho[3]);
-                dh[1] = make_uint4(ho[4], ho[5], ho[6], ho[7]);
+                st_global_v8(static_cast<uint16_t*>(P.out0) + off, eo[0], eo[1], eo[2], eo[3], eo[4], eo[5], eo[6], eo[7]);
+                st_global_v8(static_cast<uint16_t*>(P.out1) + off, uo[0], uo[1], uo[2], uo[3], uo[4], uo[5], uo[6], uo[7]);
+                st_global_v8(static_cast<uint16_t*>(P.out2) + off, ho[0], ho[1], ho[2], ho[3], ho[4], ho[5], ho[6], ho[7]);
             }
         }
     } else if constexpr (EPI == EPI_GLU_BWD) {
@@ -262,21 +243,15 @@ __device__ __forceinline__ void epilogue_cols(const Prob& P, const Unit& U, uint
         for (int col = c_lo; col < c_hi; col += 16) {
             const int64_t gcol = (int64_t)U.nb * P.out_col_step + col;
             const bool ok = mvalid && gcol < P.N;
-            uint4 e4[2], u4[2];
+            uint32_t ev[8], uv[8];
             if (ok) {
-                const uint4* pe = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(P.in0) + m * P.ld_in + gcol);
-                const uint4* pu = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(P.in1) + m * P.ld_in + gcol);
-                e4[0] = __ldg(pe);
-                e4[1] = __ldg(pe + 1);
-                u4[0] = __ldg(pu);
-                u4[1] = __ldg(pu + 1);
+                ld_global_nc_v8(static_cast<const uint16_t*>(P.in0) + m * P.ld_in + gcol, ev);
+                ld_global_nc_v8(static_cast<const uint16_t*>(P.in1) + m * P.ld_in + gcol, uv);
             }
             uint32_t a[16];
             tmem_ld_x16(tacc + col, a);
             tmem_ld_wait16(a);
             if (ok) {
-                const uint32_t ev[8] = {e4[0].x, e4[0].y, e4[0].z, e4[0].w, e4[1].x, e4[1].y, e4[1].z, e4[1].w};
-                const uint32_t uv[8] = {u4[0].x, u4[0].y, u4[0].z, u4[0].w, u4[1].x, u4[1].y, u4[1].z, u4[1].w};
                 uint32_t deo[8], duo[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -290,12 +265,10 @@ __device__ __forceinline__ void epilogue_cols(const Prob& P, const Unit& U, uint
                     duo[i] = pack_bf16x2(h0 * f0, h1 * f1);
                 }
                 const int64_t off = m * P.ld_out + gcol;
-                uint4* pde = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out0) + off);
-                uint4* pdu = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out1) + off);
-                pde[0] = make_uint4(deo[0], deo[1], deo[2], deo[3]);
-                pde[1] = make_uint4(deo[4], deo[5], deo[6], deo[7]);
-                pdu[0] = make_uint4(duo[0], duo[1], duo[2], duo[3]);
-                pdu[1] = make_uint4(duo[4], duo[5], duo[6], duo[7]);
+                st_global_v8(static_cast<uint16_t*>(P.out0) + off, deo[0], deo[1], deo[2], deo[3], deo[4], deo[5], deo[6],
+                             deo[7]);
+                st_global_v8(static_cast<uint16_t*>(P.out1) + off, duo[0], duo[1], duo[2], duo[3], duo[4], duo[5], duo[6],
+                             duo[7]);
             }
         }
     } else {  // EPI_PARTIAL: raw fp32 accumulator to out0[ks][m][0..bn)
@@ -305,12 +278,9 @@ __device__ __forceinline__ void epilogue_cols(const Prob& P, const Unit& U, uint
             tmem_ld_x16(tacc + c, a);
             tmem_ld_wait16(a);
             if (mvalid) {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(P.out0) + (int64_t)U.ks * P.split_stride +
-                                                        m * P.ld_out + c);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dst[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
-                                         __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
+                float* dst = static_cast<float*>(P.out0) + (int64_t)U.ks * P.split_stride + m * P.ld_out + c;
+                st_global_v8(dst, a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7]);
+                st_global_v8(dst + 8, a[8], a[9], a[10], a[11], a[12], a[13], a[14], a[15]);
             }
         }
     }

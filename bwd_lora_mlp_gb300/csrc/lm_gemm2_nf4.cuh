@@ -367,14 +367,10 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     tmem_ld_x16(tacc + c, a);
                     tmem_ld_x16(tacc + c + 16, b);
                     tmem_ld_wait32(a, b);
-                    float4* d4 = reinterpret_cast<float4*>(dst + c);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        d4[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
-                                            __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
-                        d4[4 + i] = make_float4(__uint_as_float(b[4 * i]), __uint_as_float(b[4 * i + 1]),
-                                                __uint_as_float(b[4 * i + 2]), __uint_as_float(b[4 * i + 3]));
-                    }
+                    st_global_v8(dst + c, a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7]);
+                    st_global_v8(dst + c + 8, a[8], a[9], a[10], a[11], a[12], a[13], a[14], a[15]);
+                    st_global_v8(dst + c + 16, b[0], b[1], b[2], b[3], b[4], b[5], b[6], b[7]);
+                    st_global_v8(dst + c + 24, b[8], b[9], b[10], b[11], b[12], b[13], b[14], b[15]);
                 }
             } else {
                 epilogue_cols<EPI>(P, U, tacc, 0, P.bn, 16, m, m < P.M);

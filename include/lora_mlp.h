@@ -32,7 +32,8 @@
  *    default stream) and never synchronises.  Calls that share a workspace or a saved buffer
  *    must be ordered (same stream or explicit events).
  *  - Sizes: T >= 0 (T == 0 is a no-op), feature sizes > 0 and multiples of 32 ([LL]), 8 <= r <= 64
- *    with r a multiple of 8.  Base pointers must be 16-byte aligned (TMA).  Outputs must not
+ *    with r a multiple of 8.  Base pointers must be 32-byte aligned (TMA wants 16 bytes; the
+ *    epilogues move 32-byte chunks of rows).  Outputs must not
  *    overlap inputs (the in-place dX of [UN] is not offered).
  *  - Errors: every call returns an lm_status; no exception or abort crosses the ABI.  Argument
  *    errors are detected on the host before anything is enqueued.  Kernels never trap: a
@@ -63,7 +64,7 @@ typedef enum lm_status {
     LM_OK = 0,
     LM_ERR_NULL = 1,        /* a required pointer is NULL */
     LM_ERR_SHAPE = 2,       /* a size breaks the rules above */
-    LM_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    LM_ERR_ALIGN = 3,       /* a pointer is not 32-byte aligned */
     LM_ERR_DTYPE = 4,       /* unknown weight kind, activation or output dtype */
     LM_ERR_ALIAS = 5,       /* an output overlaps an input or another output */
     LM_ERR_WORKSPACE = 6,   /* workspace or saved buffer smaller than the size query returns */

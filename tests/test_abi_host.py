@@ -98,6 +98,7 @@ def test_mlp_fwd_argument_errors(so):
     assert _fwd(_mlp_args(X=None)) == L.LM_ERR_NULL
     a = _mlp_args()
     assert _fwd(dict(a, X=a["X"] + 2)) == L.LM_ERR_ALIGN
+    assert _fwd(dict(a, X=a["X"] + 16)) == L.LM_ERR_ALIGN  # 32-byte rule
     assert _fwd(dict(a, y=a["X"])) == L.LM_ERR_ALIAS                       # in-place not offered
     assert _fwd(dict(a, h=a["e"] + 64)) == L.LM_ERR_ALIAS                  # two outputs overlap
     assert _fwd(dict(a, ws_bytes=a["ws_bytes"] - 1)) == L.LM_ERR_WORKSPACE
@@ -138,7 +139,7 @@ def test_nf4_argument_errors(so):
     W, c, q, s = f(16384 * 2), f(8192), f(256), f(64)
     assert L.call_status("nf4_pack", W, 16384 + 64, c, q, s, None) == L.LM_ERR_SHAPE
     assert L.call_status("nf4_pack", W, 16384, None, q, s, None) == L.LM_ERR_NULL
-    assert L.call_status("nf4_pack", W, 16384, W + 16, q, s, None) == L.LM_ERR_ALIAS
+    assert L.call_status("nf4_pack", W, 16384, W + 32, q, s, None) == L.LM_ERR_ALIAS
     assert L.call_status("nf4_pack", W, 0, c, q, s, None) == L.LM_OK
     assert L.call_status("nf4_dequant", c, q, s, 16384, 9, f(65536), None) == L.LM_ERR_DTYPE
     assert L.call_status("nf4_dequant", c, q, s, 16384, L.LM_OUT_F32, c, None) == L.LM_ERR_ALIAS
