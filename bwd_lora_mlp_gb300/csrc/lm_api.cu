@@ -542,14 +542,16 @@ struct Builder {
         // NF4 plain-store GEMM whose last wave is partly idle: split each tile of that wave over
         // its K blocks into the number of parts that finishes the tail soonest
         int ncl = 0;
-        if (tail_buf && (kind == G2N_STORE_K || kind == G2N_STORE_MN) && p.nprob == 1 &&
+        if (tail_buf && (kind == G2N_STORE_K || kind == G2N_STORE_MN) &&
             pair_nf4_clusters(kind, &ncl) == cudaSuccess && ncl > 1) {
-            Prob& P = p.prob[0];
-            const int tiles = P.tiles_m * P.tiles_n;
-            const int full = tiles / ncl * ncl, tail = tiles - full;
+            // the tail must lie inside the last problem (units run problem by problem)
+            Prob& P = p.prob[p.nprob - 1];
+            const int all = (int)units, tiles = P.tiles_m * P.tiles_n;
+            const int full_all = all / ncl * ncl, tail = all - full_all;
+            const int full = tiles - tail;  // the last problem's first tail tile
             int best = 1;
             double best_t = 1.0;  // the tail's makespan in tile times
-            for (int S = 2; S <= 4 && full > 0 && tail > 0; ++S) {
+            for (int S = 2; S <= 4 && full_all > 0 && tail > 0 && full >= 0; ++S) {
                 if (tail * S > kTailParts) break;
                 const double t = (double)((tail * S + ncl - 1) / ncl) / S;
                 if (t < best_t - 1e-9) {
@@ -557,11 +559,11 @@ struct Builder {
                     best = S;
                 }
             }
-            if (best > 1) {
+            if (best > 1 && full >= 0) {
                 P.tail_begin = full;
                 P.tail_splits = best;
                 P.tail_part = tail_buf;
-                p.total_units = full + tail * best;
+                p.total_units = full_all + tail * best;
             }
         }
         return (int)std::min<int64_t>(p.total_units, partial ? slots : sms);
@@ -578,7 +580,7 @@ struct Builder {
                                                            : launch_gemm(kind, p, grid, st_);
             if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
         }
-        const Prob& P = p.prob[0];
+        const Prob& P = p.prob[p.nprob - 1];
         if (P.tail_splits > 1) {
             ProfScope prof("tail.fin", st_);
             TailFin f{};
