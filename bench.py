@@ -303,10 +303,14 @@ def main():
     def host_pinned(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()
 
+    ab32 = synth.fp32_ab(w) if w.ab_f32 else None  # fp32 LoRA parameters: each call rounds them to bf16
+
     def mk(t):
         W = dev(inp["W_" + t])
         if w.nf4:  # quantise the frozen base on the device; packing is not part of the step
             W = L.nf4_pack(W)
+        if ab32 is not None:
+            return L.Lora(W, torch.from_numpy(ab32["A_" + t]).cuda(), torch.from_numpy(ab32["B_" + t]).cuda(), w.s)
         return L.Lora(W, dev(inp["A_" + t]), dev(inp["B_" + t]), w.s)
 
     projs = {p.name: mk(p.name) for p in w.projs}
@@ -451,7 +455,7 @@ def main():
         cpu = cpu_baseline(w, inp)
 
     d_in, d_out = w.projs[0].d_in, w.projs[-1].d_out
-    cfg = {"workload": w.name, "T": T, "r": r, "alpha": w.alpha, "base": "nf4" if w.nf4 else "bf16"}
+    cfg = {"workload": w.name, "T": T, "r": r, "alpha": w.alpha, "base": "nf4" if w.nf4 else "bf16", "lora_params": "fp32" if w.ab_f32 else "bf16"}
     if w.kind == "mlp":
         cfg.update(d=d_in, n=w.projs[0].d_out, act=w.act)
     else:

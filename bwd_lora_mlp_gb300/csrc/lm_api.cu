@@ -174,12 +174,18 @@ lm_status check_lora(const lm_lora* L, const char* name, int64_t in, int64_t out
     } else {
         return fail(LM_ERR_DTYPE, "%s.W.kind = %d is not a known weight kind", name, L->W.kind);
     }
+    if (L->ab_dtype != LM_AB_BF16 && L->ab_dtype != LM_AB_F32)
+        return fail(LM_ERR_DTYPE, "%s.ab_dtype = %d is not a known A/B dtype", name, L->ab_dtype);
     snprintf(buf, sizeof buf, "%s.A", name);
     LM_TRY(need_ptr(L->A, buf));
     snprintf(buf, sizeof buf, "%s.B", name);
     LM_TRY(need_ptr(L->B, buf));
     return LM_OK;
 }
+
+// bytes of `elems` elements of a LoRA A or B matrix
+size_t ab_bytes(const lm_lora* L, int64_t elems) { return (size_t)elems * (L->ab_dtype == LM_AB_F32 ? 4 : 2); }
+inline const uint16_t* bf(const void* p) { return static_cast<const uint16_t*>(p); }
 
 struct Span {
     const void* p;
@@ -222,6 +228,8 @@ lm_status same_kind(std::initializer_list<const lm_lora*> Ls, bool* nf4) {
 
 // ------------------------------------------------------------------ workspace planning
 int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+// bf16 elements of the converted A and B of one projection (fp32 LoRA parameters)
+int64_t ab_elems(int64_t r, int64_t in, int64_t out) { return round_up(r * in, 128) + round_up(out * r, 128); }
 
 struct Bump {
     size_t off = 0;
@@ -275,6 +283,7 @@ struct MlpPlan {
     size_t bdiag;           // [Bg | 0 ; 0 | Bu] (2n x 2rp) for the CTA-pair gate/up GEMM
     size_t sc[3];           // NF4 base: fp32 block-scale tables of W_gate, W_up, W_down
     size_t tail;            // NF4 base: split tail tiles of the down and dX GEMMs
+    size_t abc;             // bf16 copies of fp32 LoRA A and B
     size_t ws_total;
 };
 
@@ -298,6 +307,7 @@ MlpPlan plan_mlp(int64_t T, int64_t d, int64_t n, int32_t r) {
     P.bdiag = w.take((size_t)2 * n * 2 * rp * 2);
     for (int i = 0; i < 3; ++i) P.sc[i] = w.take((size_t)n * d / 64 * 4);
     P.tail = w.take(kTailBytes);
+    P.abc = w.take((size_t)(2 * ab_elems(r, d, n) + ab_elems(r, n, d)) * 2);
     P.ws_total = w.off;
     return P;
 }
@@ -310,6 +320,7 @@ struct QkvPlan {
     RankBuf g[3];
     size_t sc[3];           // NF4 base: fp32 block-scale tables of W_q, W_k, W_v
     size_t tail;            // NF4 base: split tail tiles of the dX GEMM
+    size_t abc;             // bf16 copies of fp32 LoRA A and B
     size_t ws_total;
 };
 
@@ -328,6 +339,7 @@ QkvPlan plan_qkv(int64_t T, int64_t d, int64_t nq, int64_t nk, int64_t nv, int32
     const int64_t nout[3] = {nq, nk, nv};
     for (int i = 0; i < 3; ++i) P.sc[i] = w.take((size_t)nout[i] * d / 64 * 4);
     P.tail = w.take(kTailBytes);
+    P.abc = w.take((size_t)(ab_elems(r, d, nq) + ab_elems(r, d, nk) + ab_elems(r, d, nv)) * 2);
     P.ws_total = w.off;
     return P;
 }
@@ -340,6 +352,7 @@ struct OPlan {
     RankBuf g;
     size_t sc;              // NF4 base: fp32 block-scale table of W_o
     size_t tail;            // NF4 base: split tail tiles of the O and dX GEMMs
+    size_t abc;             // bf16 copies of fp32 LoRA A and B
     size_t ws_total;
 };
 
@@ -357,6 +370,7 @@ OPlan plan_o(int64_t T, int64_t d_in, int64_t d_out, int32_t r) {
     P.g = take_rank(w, P.D, rp);
     P.sc = w.take((size_t)d_out * d_in / 64 * 4);
     P.tail = w.take(kTailBytes);
+    P.abc = w.take((size_t)ab_elems(r, d_in, d_out) * 2);
     P.ws_total = w.off;
     return P;
 }
@@ -366,6 +380,33 @@ lm_status scale_table(const char* tag, const lm_weight& W, float* table, cudaStr
     ProfScope prof(tag, st);
     const cudaError_t e = launch_nf4_scale_table(W.absmax_q, W.group_scale, W.rows, W.cols, table, st);
     return e == cudaSuccess ? LM_OK : cuda_fail(e, "NF4 scale table launch");
+}
+
+// fp32 LoRA parameters ([LO] "FP32 LoRA gradients"): A (r x in) and B (out x r) of every fp32
+// projection rounded to bf16 (RNE) into `dst`, one launch; each copy then points at its bf16
+// matrices.  bf16 parameters are used as they are.
+struct AbProj {
+    lm_lora* L;
+    int64_t in, out;
+};
+lm_status ab_to_bf16(const char* tag, std::initializer_list<AbProj> projs, uint16_t* dst, cudaStream_t st) {
+    CvtJobs jobs{};
+    int nj = 0;
+    for (const AbProj& a : projs) {
+        if (a.L->ab_dtype != LM_AB_F32) continue;
+        const int64_t na = (int64_t)a.L->r * a.in, nb = a.out * (int64_t)a.L->r;
+        jobs.j[nj++] = CvtJob{static_cast<const float*>(a.L->A), dst, na};
+        a.L->A = dst;
+        dst += round_up(na, 128);
+        jobs.j[nj++] = CvtJob{static_cast<const float*>(a.L->B), dst, nb};
+        a.L->B = dst;
+        dst += round_up(nb, 128);
+        a.L->ab_dtype = LM_AB_BF16;
+    }
+    if (nj == 0) return LM_OK;
+    ProfScope prof(tag, st);
+    const cudaError_t e = launch_f32_to_bf16(jobs, nj, st);
+    return e == cudaSuccess ? LM_OK : cuda_fail(e, "fp32 -> bf16 launch");
 }
 
 // ------------------------------------------------------------------ GEMM launch builder
@@ -611,7 +652,7 @@ Seg& seg(Prob& P, int i) {
 
 // rank-r input projection, K-major B made of stacked A matrices:
 //   part[ks][t][i*rp + j] = sum_k Z[t][k] * A_i[j][k]
-void add_rowproj_in(Builder& b, const uint16_t* Z, int64_t T, int64_t K, std::initializer_list<const uint16_t*> As,
+void add_rowproj_in(Builder& b, const uint16_t* Z, int64_t T, int64_t K, std::initializer_list<const void*> As,
                     const Dims& D, float* part) {
     Prob& P = b.prob();
     const int cnt = (int)As.size();
@@ -622,7 +663,7 @@ void add_rowproj_in(Builder& b, const uint16_t* Z, int64_t T, int64_t K, std::in
     Seg& S = seg(P, 0);
     S.a_map = b.map(Z, T, K, K, 128);
     int i = 0;
-    for (const uint16_t* A : As) S.b_map[i++] = b.map(A, D.r, K, K, D.rp);
+    for (const void* A : As) S.b_map[i++] = b.map(A, D.r, K, K, D.rp);
     S.b_rows = D.rp;
     S.kext = (int32_t)K;
     P.out0 = part;
@@ -631,7 +672,7 @@ void add_rowproj_in(Builder& b, const uint16_t* Z, int64_t T, int64_t K, std::in
 }
 
 // rank-r output-gradient projection, MN-major B:  part[ks][t][j] = sum_c dO[t][c] * Bm[c][j]
-void add_rowproj_out(Builder& b, const uint16_t* dO, int64_t T, int64_t C, const uint16_t* Bm, const Dims& D,
+void add_rowproj_out(Builder& b, const uint16_t* dO, int64_t T, int64_t C, const void* Bm, const Dims& D,
                      float* part) {
     Prob& P = b.prob();
     P.M = (int32_t)T;
@@ -843,9 +884,9 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     LM_TRY(check_alias({{y, td, "y"}, {e_save, tn, "e_save"}, {u_save, tn, "u_save"}, {h_save, tn, "h_save"},
                         {saved, PL.saved_total, "saved"}, {ws, PL.ws_total, "ws"}},
                        {{X, td, "X"}, wspan(gate, "gate.W"), wspan(up, "up.W"), wspan(down, "down.W"),
-                        {gate->A, (size_t)r * d * 2, "gate.A"}, {gate->B, (size_t)n * r * 2, "gate.B"},
-                        {up->A, (size_t)r * d * 2, "up.A"}, {up->B, (size_t)n * r * 2, "up.B"},
-                        {down->A, (size_t)r * n * 2, "down.A"}, {down->B, (size_t)d * r * 2, "down.B"}}));
+                        {gate->A, ab_bytes(gate, r * d), "gate.A"}, {gate->B, ab_bytes(gate, n * r), "gate.B"},
+                        {up->A, ab_bytes(up, r * d), "up.A"}, {up->B, ab_bytes(up, n * r), "up.B"},
+                        {down->A, ab_bytes(down, r * n), "down.A"}, {down->B, ab_bytes(down, d * r), "down.B"}}));
     if (T == 0) return LM_OK;
     int sms = 0;
     LM_TRY(ready(&sms));
@@ -854,6 +895,11 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     const int rp = D.rp;
     int32_t* err = static_cast<int32_t*>(ws);
     float* part = at<float>(ws, PL.part);
+    lm_lora gate_c = *gate, up_c = *up, down_c = *down;
+    LM_TRY(ab_to_bf16("mlp.ab", {{&gate_c, d, n}, {&up_c, d, n}, {&down_c, n, d}}, at<uint16_t>(ws, PL.abc), st));
+    gate = &gate_c;
+    up = &up_c;
+    down = &down_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
     if (nf4) {  // the NF4 GEMMs read per-K-block fp32 block scales of W_gate, W_up, W_down
         LM_TRY(scale_table("mlp.nf4s", gate->W, sc[0], st));
@@ -877,7 +923,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         uint16_t* bdiag = at<uint16_t>(ws, PL.bdiag);
         {
             ProfScope prof("mlp.bdiag", st);
-            const cudaError_t be = launch_blockdiag(gate->B, up->B, n, r, rp, bdiag, st);
+            const cudaError_t be = launch_blockdiag(bf(gate->B), bf(up->B), n, r, rp, bdiag, st);
             if (be != cudaSuccess) return cuda_fail(be, "rank-r operand launch");
         }
         Builder b(G2N_GLU_FWD);
@@ -912,7 +958,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         uint16_t* bdiag = at<uint16_t>(ws, PL.bdiag);
         {
             ProfScope prof("mlp.bdiag", st);
-            const cudaError_t be = launch_blockdiag(gate->B, up->B, n, r, rp, bdiag, st);
+            const cudaError_t be = launch_blockdiag(bf(gate->B), bf(up->B), n, r, rp, bdiag, st);
             if (be != cudaSuccess) return cuda_fail(be, "rank-r operand launch");
         }
         Builder b(G2_GLU_FWD);
@@ -1049,6 +1095,11 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     const int rp = D.rp;
     int32_t* err = static_cast<int32_t*>(ws);
     float* part = at<float>(ws, PL.part);
+    lm_lora gate_c = *gate, up_c = *up, down_c = *down;
+    LM_TRY(ab_to_bf16("mlp.ab", {{&gate_c, d, n}, {&up_c, d, n}, {&down_c, n, d}}, at<uint16_t>(ws, PL.abc), st));
+    gate = &gate_c;
+    up = &up_c;
+    down = &down_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
     if (nf4) {
         LM_TRY(scale_table("mlp.nf4s", gate->W, sc[0], st));
@@ -1293,6 +1344,11 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     const int rp = D.rp;
     int32_t* err = static_cast<int32_t*>(ws);
     float* part = at<float>(ws, PL.part);
+    lm_lora q_c = *q, k_c = *k, v_c = *v;
+    LM_TRY(ab_to_bf16("qkv.ab", {{&q_c, d, nq}, {&k_c, d, nk}, {&v_c, d, nv}}, at<uint16_t>(ws, PL.abc), st));
+    q = &q_c;
+    k = &k_c;
+    v = &v_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
     if (nf4) {  // the NF4 GEMMs read per-K-block fp32 block scales of W_q, W_k, W_v
         LM_TRY(scale_table("qkv.nf4s", q->W, sc[0], st));
@@ -1421,6 +1477,11 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     const int rp = D.rp;
     int32_t* err = static_cast<int32_t*>(ws);
     float* part = at<float>(ws, PL.part);
+    lm_lora q_c = *q, k_c = *k, v_c = *v;
+    LM_TRY(ab_to_bf16("qkv.ab", {{&q_c, d, nq}, {&k_c, d, nk}, {&v_c, d, nv}}, at<uint16_t>(ws, PL.abc), st));
+    q = &q_c;
+    k = &k_c;
+    v = &v_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
     if (nf4) {
         LM_TRY(scale_table("qkv.nf4s", q->W, sc[0], st));
@@ -1579,6 +1640,9 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     const int rp = D.rp;
     int32_t* err = static_cast<int32_t*>(ws);
     float* part = at<float>(ws, PL.part);
+    lm_lora o_c = *o;
+    LM_TRY(ab_to_bf16("o.ab", {{&o_c, d_in, d_out}}, at<uint16_t>(ws, PL.abc), st));
+    o = &o_c;
     float* sc = at<float>(ws, PL.sc);
     if (nf4) LM_TRY(scale_table("o.nf4s", o->W, sc, st));  // per-K-block fp32 block scales of W_o
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
@@ -1672,6 +1736,9 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     const int rp = D.rp;
     int32_t* err = static_cast<int32_t*>(ws);
     float* part = at<float>(ws, PL.part);
+    lm_lora o_c = *o;
+    LM_TRY(ab_to_bf16("o.ab", {{&o_c, d_in, d_out}}, at<uint16_t>(ws, PL.abc), st));
+    o = &o_c;
     float* sc = at<float>(ws, PL.sc);
     if (nf4) LM_TRY(scale_table("o.nf4s", o->W, sc, st));
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);

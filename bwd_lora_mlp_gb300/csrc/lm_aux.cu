@@ -110,6 +110,26 @@ cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t 
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ fp32 LoRA parameters
+// fp32 -> bf16 bits, round to nearest even (the GEMM input precision of fp32 LoRA parameters);
+// blockIdx.y picks the matrix
+__global__ void __launch_bounds__(256) f32_to_bf16_kernel(CvtJobs jobs) {
+    const CvtJob& J = jobs.j[blockIdx.y];
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < J.n; i += (int64_t)gridDim.x * blockDim.x) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(J.in[i]);
+        J.out[i] = *reinterpret_cast<const uint16_t*>(&b);
+    }
+}
+
+cudaError_t launch_f32_to_bf16(const CvtJobs& jobs, int njobs, cudaStream_t st) {
+    int64_t most = 0;
+    for (int i = 0; i < njobs; ++i) most = std::max<int64_t>(most, jobs.j[i].n);
+    if (njobs == 0 || most == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((most + 255) / 256, 256);
+    f32_to_bf16_kernel<<<dim3((unsigned)blocks, (unsigned)njobs), 256, 0, st>>>(jobs);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ split tail tiles
 // One thread per 4 columns of a tail-tile row; 512-row tiles, bn and N multiples of 4.
 __global__ void __launch_bounds__(256) tail_fin_kernel(TailFin f) {

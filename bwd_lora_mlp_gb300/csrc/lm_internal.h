@@ -82,6 +82,16 @@ struct TailFin {
     int32_t ntail, splits, bn, tail_begin, tiles_m, tiles_n, group_m;
 };
 cudaError_t launch_tail_fin(const TailFin& f, cudaStream_t st);
+// fp32 -> bf16 bits (RNE) of up to six matrices in one launch
+struct CvtJob {
+    const float* in;
+    uint16_t* out;
+    int64_t n;
+};
+struct CvtJobs {
+    CvtJob j[6];
+};
+cudaError_t launch_f32_to_bf16(const CvtJobs& jobs, int njobs, cudaStream_t st);
 // clusters the NF4 pair GEMM of kind k runs with on the current device
 cudaError_t pair_nf4_clusters(GemmKind k, int* n);
 

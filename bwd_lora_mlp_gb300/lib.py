@@ -28,6 +28,7 @@ STATUS_NAMES = {0: "LM_OK", 1: "LM_ERR_NULL", 2: "LM_ERR_SHAPE", 3: "LM_ERR_ALIG
 LM_WEIGHT_BF16, LM_WEIGHT_NF4 = 0, 1
 LM_ACT_SWIGLU, LM_ACT_GEGLU_ERF = 0, 1
 LM_OUT_F32, LM_OUT_BF16 = 0, 1
+LM_AB_BF16, LM_AB_F32 = 0, 1
 ACTS = {"swiglu": LM_ACT_SWIGLU, "geglu": LM_ACT_GEGLU_ERF}
 
 
@@ -45,7 +46,7 @@ class lm_weight(ctypes.Structure):
 
 class lm_lora(ctypes.Structure):
     _fields_ = [("W", lm_weight), ("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("r", ctypes.c_int32),
-                ("s", ctypes.c_float)]
+                ("s", ctypes.c_float), ("ab_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -160,7 +161,9 @@ class NF4Weight:
 
 @dataclass
 class Lora:
-    """One adapted projection: W (out, in) bf16 tensor or NF4Weight, A (r, in), B (out, r), s."""
+    """One adapted projection: W (out, in) bf16 tensor or NF4Weight, A (r, in), B (out, r), s.
+
+    A and B are both bf16 or both fp32 (fp32 LoRA parameters; each call rounds them to bf16)."""
     W: object
     A: torch.Tensor
     B: torch.Tensor
@@ -184,8 +187,14 @@ class Lora:
             w.w = _ptr(self.W, torch.bfloat16, "W")
         L = lm_lora()
         L.W = w
-        L.A = _ptr(self.A, torch.bfloat16, "A")
-        L.B = _ptr(self.B, torch.bfloat16, "B")
+        if self.A.dtype == torch.float32 and self.B.dtype == torch.float32:
+            L.ab_dtype = LM_AB_F32
+            L.A = _ptr(self.A, torch.float32, "A")
+            L.B = _ptr(self.B, torch.float32, "B")
+        else:
+            L.ab_dtype = LM_AB_BF16
+            L.A = _ptr(self.A, torch.bfloat16, "A")
+            L.B = _ptr(self.B, torch.bfloat16, "B")
         L.r = self.r
         L.s = float(self.s)
         return L

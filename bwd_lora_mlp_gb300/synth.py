@@ -52,6 +52,19 @@ def uniform_bf16(shape, bound: float, seed: int) -> np.ndarray:
     return f32_to_bf16_bits(x)
 
 
+def fp32_ab(w: "Workload", seed: int = 4321) -> dict:
+    """fp32 LoRA parameters for every projection of ``w`` (fp32 LoRA-parameter runs): A ~
+    U(+-1/sqrt(in)), B ~ N(0, 0.02), drawn in fp32 and kept in fp32 (most are not bf16 values).
+    Returns ``A_<name>``, ``B_<name>`` as float32 arrays."""
+    out = {}
+    for i, p in enumerate(w.projs):
+        out["A_" + p.name] = _rng(seed + 2 * i).uniform(-1.0 / math.sqrt(p.d_in), 1.0 / math.sqrt(p.d_in),
+                                                        size=(w.r, p.d_in)).astype(np.float32)
+        out["B_" + p.name] = (_rng(seed + 2 * i + 1).standard_normal(size=(p.d_out, w.r), dtype=np.float32)
+                              * np.float32(0.02))
+    return out
+
+
 @dataclass
 class ProjSpec:
     """One LoRA projection: out = X W^T + s (X A^T) B^T, W (out, in)."""
@@ -71,6 +84,7 @@ class Workload:
     projs: list = field(default_factory=list)
     act: str = "swiglu"  # mlp only: "swiglu" or "geglu"
     nf4: bool = False
+    ab_f32: bool = False  # LoRA A, B passed as fp32 parameters
 
     @property
     def s(self) -> float:
@@ -106,6 +120,11 @@ WORKLOADS = {
     "llama3_70b_mlp_nf4_geglu": mlp_workload("llama3_70b_mlp_nf4_geglu", 4096, 8192, 28672, 64, 128.0,
                                              act="geglu", nf4=True),
 }
+# the 8B MLP with fp32 LoRA parameters (bf16 and NF4 base)
+for _b in ("bf16", "nf4"):
+    _w = mlp_workload("llama3_8b_mlp_%s_ab32" % _b, 8192, 4096, 14336, 16, 32.0, nf4=_b == "nf4")
+    _w.ab_f32 = True
+    WORKLOADS[_w.name] = _w
 
 
 def make_inputs(w: Workload, seed: int = BASE_SEED, zero_W: bool = False, zero_B: bool = False,

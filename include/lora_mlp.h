@@ -22,9 +22,11 @@
  *    W is (out, in) row-major; LoRA A is (r, in); LoRA B is (out, r); activations are (T, in)
  *    or (T, out) row-major with T = batch * sequence flattened.  The LoRA term of a projection
  *    is s * (X A^T) B^T with s = alpha / r (or alpha / sqrt(r) for rsLoRA: the caller passes s).
- *  - bf16 tensors are passed as uint16_t bit patterns.  Activations, A and B are bf16; LoRA
- *    gradients are fp32 and are written in parameter layout (dA: r x in, dB: out x r),
- *    overwriting the destination ([UN]: the weight-gradient GEMMs use beta = 0).
+ *  - bf16 tensors are passed as uint16_t bit patterns.  Activations are bf16; A and B are bf16
+ *    or fp32 (lm_lora.ab_dtype: fp32 LoRA parameters, [LO] "FP32 LoRA gradients", enter the
+ *    GEMMs rounded to bf16, round-to-nearest-even); LoRA gradients are fp32 and are written in
+ *    parameter layout (dA: r x in, dB: out x r), overwriting the destination ([UN]: the
+ *    weight-gradient GEMMs use beta = 0).
  *  - Every pointer argument is a DEVICE pointer unless stated otherwise.  The caller owns every
  *    buffer, including the workspace; the library allocates no device memory and keeps no state
  *    other than a per-thread last-error string and cached function pointers.
@@ -76,6 +78,7 @@ typedef enum lm_status {
 typedef enum lm_weight_kind { LM_WEIGHT_BF16 = 0, LM_WEIGHT_NF4 = 1 } lm_weight_kind;
 typedef enum lm_act { LM_ACT_SWIGLU = 0, LM_ACT_GEGLU_ERF = 1 } lm_act;
 typedef enum lm_out_dtype { LM_OUT_F32 = 0, LM_OUT_BF16 = 1 } lm_out_dtype;
+typedef enum lm_ab_dtype { LM_AB_BF16 = 0, LM_AB_F32 = 1 } lm_ab_dtype;
 
 /* A frozen base weight W (out x in).  kind == LM_WEIGHT_BF16: `w` holds rows*cols bf16.
  * kind == LM_WEIGHT_NF4 ([LL]): `codes` holds rows*cols/2 bytes (element 2i in the high nibble
@@ -94,13 +97,18 @@ typedef struct lm_weight {
     const float* group_scale;
 } lm_weight;
 
-/* One adapted projection: base W, A (r x in), B (out x r), rank r and scale s. */
+/* One adapted projection: base W, A (r x in), B (out x r), rank r and scale s.  A and B hold
+ * bf16 bits (ab_dtype LM_AB_BF16) or fp32 values (LM_AB_F32: [LO] "FP32 LoRA gradients" keeps
+ * the trainable parameters in fp32; each call rounds them to bf16 into its workspace, RNE, and
+ * every GEMM reads the bf16 copy).  Any other ab_dtype is LM_ERR_DTYPE. */
 typedef struct lm_lora {
     lm_weight W;
-    const uint16_t* A;
-    const uint16_t* B;
+    const void* A;
+    const void* B;
     int32_t r;
     float s;
+    int32_t ab_dtype;
+    int32_t reserved;
 } lm_lora;
 
 /* ---- utilities ------------------------------------------------------------------------- */

@@ -28,6 +28,21 @@ def from_bf16(bits: np.ndarray) -> np.ndarray:
     return u.view(np.float32).astype(np.float64)
 
 
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of fp32 values, round to nearest with ties to even.
+
+    fp32 LoRA parameters ("LoRA Optimizations", FP32 LoRA gradients: the trainable parameters
+    stay fp32, the GEMMs take bf16 inputs) enter the computation as these bf16 values.  bf16 is
+    the top 16 bits of an fp32; the dropped 16 bits decide the rounding: above half an ulp
+    rounds up, below rounds down, exactly half rounds to the even (last kept bit 0) neighbour.
+    Finite inputs only (an fp32 that rounds past the largest bf16 becomes infinity).
+    """
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    hi, lo = u >> np.uint64(16), u & np.uint64(0xFFFF)
+    up = (lo > 0x8000) | ((lo == 0x8000) & ((hi & np.uint64(1)) == 1))
+    return (hi + up.astype(np.uint64)).astype(np.uint16)
+
+
 # ----------------------------------------------------------------------------------------------
 # Gated activations ("LoRA Optimizations", Triton kernels: SwiGLU and GeGLU forward / backward).
 # SiLU(x) = x * sigmoid(x); GELU is the exact-erf form 0.5 x (1 + erf(x / sqrt 2)).

@@ -118,6 +118,10 @@ def test_mlp_fwd_argument_errors(so):
     z["gate"].s = float("nan")
     assert _fwd(z) == L.LM_ERR_SHAPE
     assert "gate.s" in L.last_error()
+    t = _mlp_args()
+    t["up"].ab_dtype = 7                                                   # neither bf16 nor fp32 A/B
+    assert _fwd(t) == L.LM_ERR_DTYPE
+    assert "up.ab_dtype" in L.last_error()
 
 
 def test_empty_token_count_is_a_no_op(so):

@@ -219,3 +219,33 @@ def test_lora_grads_without_dX_equal_full_backward():
     part = O.lora_w_lora_grads(X, dY, p["Aq"], p["Bq"], p["sq"])
     np.testing.assert_allclose(part["dA"], full["dA"], rtol=1e-13, atol=1e-16)
     np.testing.assert_allclose(part["dB"], full["dB"], rtol=1e-13, atol=1e-16)
+
+
+def test_to_bf16_bits_rounds_to_nearest_even():
+    """fp32 -> bf16 of fp32 LoRA parameters ("LoRA Optimizations", FP32 LoRA gradients: bf16 GEMM
+    inputs): values fixed by the bf16 format, then brute force against the nearest neighbour."""
+    f = lambda v: np.array(v, dtype=np.float32)
+    # representable values are unchanged
+    exact = np.array([0x3F80, 0xC020, 0x0000, 0x7F7F, 0x0001, 0x8001], dtype=np.uint16)
+    back = (exact.astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(O.to_bf16_bits(back), exact)
+    # 1 + 2^-8 lies halfway between 1 (0x3F80, even) and 1 + 2^-7 (0x3F81): ties go to even
+    assert O.to_bf16_bits(f([1 + 2.0 ** -8]))[0] == 0x3F80
+    assert O.to_bf16_bits(f([-(1 + 2.0 ** -8)]))[0] == 0xBF80
+    # 1 + 3 * 2^-8 lies halfway between 0x3F81 (odd) and 0x3F82 (even)
+    assert O.to_bf16_bits(f([1 + 3 * 2.0 ** -8]))[0] == 0x3F82
+    assert O.to_bf16_bits(f([-(1 + 3 * 2.0 ** -8)]))[0] == 0xBF82
+    # just above / below half an ulp
+    assert O.to_bf16_bits(f([1 + 2.0 ** -8 + 2.0 ** -20]))[0] == 0x3F81
+    assert O.to_bf16_bits(f([1 + 2.0 ** -8 - 2.0 ** -20]))[0] == 0x3F80
+    # the largest finite fp32 is above the largest bf16 by more than half an ulp: infinity
+    assert O.to_bf16_bits(f([np.finfo(np.float32).max]))[0] == 0x7F80
+    # brute force: the nearer of the two bf16 neighbours (fp64 distances), ties to the even one
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(20000) * np.exp2(rng.integers(-30, 30, 20000))).astype(np.float32)
+    down = (x.view(np.uint32) >> 16).astype(np.uint16)
+    up = (down.astype(np.uint32) + 1).astype(np.uint16)
+    vd, vu, vx = O.from_bf16(down), O.from_bf16(up), x.astype(np.float64)
+    dd, du = np.abs(vx - vd), np.abs(vu - vx)
+    want = np.where(dd < du, down, np.where(du < dd, up, np.where(down % 2 == 0, down, up)))
+    assert np.array_equal(O.to_bf16_bits(x), want)
