@@ -33,7 +33,8 @@ if ROOT not in sys.path:
 METRIC = "LoRA-MLP fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300"
 METRICS = {"mlp": METRIC,
            "qkv": "LoRA-QKV fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300",
-           "o": "LoRA-O fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300"}
+           "o": "LoRA-O fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300",
+           "relu2": "LoRA ReLU^2-MLP fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300"}
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -67,6 +68,14 @@ def kernel_flops(tag, w):
     base = sum(2 * T * p.d_in * p.d_out for p in w.projs)
     rank_out = sum(2 * T * r * p.d_out for p in w.projs)
     rank_in = sum(2 * T * r * p.d_in for p in w.projs)
+    if w.kind == "relu2":
+        d, n = w.projs[0].d_in, w.projs[0].d_out
+        return {
+            "relu2.up": 2 * T * d * n + 2 * T * r * n,
+            "relu2.down": 2 * T * n * d + 2 * T * r * d,
+            "relu2.dh": 2 * T * d * n + 2 * T * r * n,
+            "relu2.dX": 2 * T * n * d + 2 * T * r * d,
+        }.get(tag)
     return {"qkv.fwd": base + rank_out, "qkv.dX": base + rank_in,
             "o.fwd": base + rank_out, "o.dX": base + rank_in}.get(tag)
 
@@ -331,6 +340,16 @@ def main():
                            saved=fw["saved"], ws=fw["ws"])
             L.lora_mlp_bwd(xs[0], xs[1], fw, gate, up, down, act=w.act, dX=outs["dX"],
                            grads={k: outs[k] for k in outs if k not in ("y", "dX")})
+    elif w.kind == "relu2":
+        up, down = projs["up"], projs["down"]
+        fw = L.lora_relu2_mlp_fwd(ins[0], up, down)
+        bw = L.lora_relu2_mlp_bwd(ins[0], ins[1], fw, up, down)
+        out_keys = ["y"]
+
+        def run(xs, outs):
+            L.lora_relu2_mlp_fwd(xs[0], up, down, y=outs["y"], u=fw["u"], h=fw["h"], saved=fw["saved"], ws=fw["ws"])
+            L.lora_relu2_mlp_bwd(xs[0], xs[1], fw, up, down, dX=outs["dX"],
+                                 grads={k: outs[k] for k in outs if k not in ("y", "dX")})
     elif w.kind == "qkv":
         q, k_, v = projs["q"], projs["k"], projs["v"]
         fw = L.lora_qkv_fwd(ins[0], q, k_, v)
@@ -456,7 +475,7 @@ def main():
 
     d_in, d_out = w.projs[0].d_in, w.projs[-1].d_out
     cfg = {"workload": w.name, "T": T, "r": r, "alpha": w.alpha, "base": "nf4" if w.nf4 else "bf16", "lora_params": "fp32" if w.ab_f32 else "bf16"}
-    if w.kind == "mlp":
+    if w.kind in ("mlp", "relu2"):
         cfg.update(d=d_in, n=w.projs[0].d_out, act=w.act)
     else:
         cfg.update(projections={p.name: [p.d_in, p.d_out] for p in w.projs})

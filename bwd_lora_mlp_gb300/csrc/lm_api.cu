@@ -1278,6 +1278,347 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
 }
 
 // ====================================================================== LoRA QKV
+// ====================================================================== non-gated ReLU^2 MLP
+// [LO] "FP32 LoRA gradients": dense ReLU^2 MLPs with up/down LoRA projections and a fused ReLU^2
+// activation derivative.  u = X Wu^T + su (X Au^T) Bu^T, h = max(u, 0)^2, y = h Wd^T + sd (h Ad^T) Bd^T.
+struct Relu2Plan {
+    Dims D;
+    RankBuf xa, ha;         // saved: s_u X Au^T (T x rp), s_d h Ad^T (T x rp)
+    size_t saved_total;
+    size_t part;            // workspace
+    RankBuf gd, gu;         // s_d dY Bd, s_u du Bu
+    size_t du;
+    size_t sc[2];           // NF4 base: fp32 block-scale tables of W_up, W_down
+    size_t tail;            // NF4 base: split tail tiles of the down and dX GEMMs
+    size_t abc;             // bf16 copies of fp32 LoRA A and B
+    size_t ws_total;
+};
+
+Relu2Plan plan_relu2(int64_t T, int64_t d, int64_t n, int32_t r) {
+    Relu2Plan P;
+    P.D = make_dims(T, r);
+    const int64_t rp = P.D.rp;
+    Bump s;
+    P.xa = take_rank(s, P.D, rp);
+    P.ha = take_rank(s, P.D, rp);
+    P.saved_total = s.off;
+    Bump w;
+    w.take(256);  // error word
+    const int64_t part_elems = std::max<int64_t>(T * rp, 2 * (n + d) * rp);
+    P.part = w.take((size_t)kMaxSplits * part_elems * 4);
+    P.gd = take_rank(w, P.D, rp);
+    P.gu = take_rank(w, P.D, rp);
+    P.du = w.take((size_t)T * n * 2);
+    P.sc[0] = w.take((size_t)n * d / 64 * 4);
+    P.sc[1] = w.take((size_t)d * n / 64 * 4);
+    P.tail = w.take(kTailBytes);
+    P.abc = w.take((size_t)(ab_elems(r, d, n) + ab_elems(r, n, d)) * 2);
+    P.ws_total = w.off;
+    return P;
+}
+
+extern "C" lm_status lora_relu2_mlp_saved_size(int64_t T, int32_t r, size_t* bytes) {
+    if (!bytes) return fail(LM_ERR_NULL, "bytes is NULL");
+    LM_TRY(check_T(T));
+    LM_TRY(check_r(r));
+    *bytes = plan_relu2(T, 32, 32, r).saved_total;
+    return LM_OK;
+}
+
+extern "C" lm_status lora_relu2_mlp_workspace_size(int64_t T, int64_t d, int64_t n, int32_t r, size_t* bytes) {
+    if (!bytes) return fail(LM_ERR_NULL, "bytes is NULL");
+    LM_TRY(check_T(T));
+    LM_TRY(check_dim(d, "d"));
+    LM_TRY(check_dim(n, "n"));
+    LM_TRY(check_r(r));
+    *bytes = plan_relu2(T, d, n, r).ws_total;
+    return LM_OK;
+}
+
+static lm_status check_relu2_common(int64_t T, int64_t d, int64_t n, const lm_lora* up, const lm_lora* down) {
+    LM_TRY(check_T(T));
+    LM_TRY(check_dim(d, "d"));
+    LM_TRY(check_dim(n, "n"));
+    if (!up) return fail(LM_ERR_NULL, "up is NULL");
+    LM_TRY(check_r(up->r));
+    LM_TRY(check_lora(up, "up", d, n, up->r));
+    LM_TRY(check_lora(down, "down", n, d, up->r));
+    bool nf4 = false;
+    LM_TRY(same_kind({up, down}, &nf4));
+    return LM_OK;
+}
+
+extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const uint16_t* X, const lm_lora* up,
+                                        const lm_lora* down, uint16_t* y, uint16_t* u_save, uint16_t* h_save,
+                                        void* saved, size_t saved_bytes, void* ws, size_t ws_bytes, lm_stream stream) {
+    LM_TRY(check_relu2_common(T, d, n, up, down));
+    LM_TRY(need_ptr(X, "X"));
+    LM_TRY(need_ptr(y, "y"));
+    LM_TRY(need_ptr(u_save, "u_save"));
+    LM_TRY(need_ptr(h_save, "h_save"));
+    LM_TRY(need_ptr(saved, "saved"));
+    LM_TRY(need_ptr(ws, "ws"));
+    const int32_t r = up->r;
+    const bool nf4 = up->W.kind == LM_WEIGHT_NF4;
+    const Relu2Plan PL = plan_relu2(T, d, n, r);
+    if (saved_bytes < PL.saved_total)
+        return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
+    if (ws_bytes < PL.ws_total) return fail(LM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, PL.ws_total);
+    const size_t td = (size_t)T * d * 2, tn = (size_t)T * n * 2;
+    LM_TRY(check_alias({{y, td, "y"}, {u_save, tn, "u_save"}, {h_save, tn, "h_save"}, {saved, PL.saved_total, "saved"},
+                        {ws, PL.ws_total, "ws"}},
+                       {{X, td, "X"}, wspan(up, "up.W"), wspan(down, "down.W"), {up->A, ab_bytes(up, r * d), "up.A"},
+                        {up->B, ab_bytes(up, n * r), "up.B"}, {down->A, ab_bytes(down, r * n), "down.A"},
+                        {down->B, ab_bytes(down, d * r), "down.B"}}));
+    if (T == 0) return LM_OK;
+    int sms = 0;
+    LM_TRY(ready(&sms));
+    cudaStream_t st = (cudaStream_t)stream;
+    const Dims& D = PL.D;
+    const int rp = D.rp;
+    int32_t* err = static_cast<int32_t*>(ws);
+    float* part = at<float>(ws, PL.part);
+    lm_lora up_c = *up, down_c = *down;
+    LM_TRY(ab_to_bf16("relu2.ab", {{&up_c, d, n}, {&down_c, n, d}}, at<uint16_t>(ws, PL.abc), st));
+    up = &up_c;
+    down = &down_c;
+    float* sc[2] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1])};
+    if (nf4) {
+        LM_TRY(scale_table("relu2.nf4s", up->W, sc[0], st));
+        LM_TRY(scale_table("relu2.nf4s", down->W, sc[1], st));
+    }
+    uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
+    uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
+    uint16_t* ha = at<uint16_t>(saved, PL.ha.rows_off);
+    uint16_t* haT = at<uint16_t>(saved, PL.ha.t_off);
+    {  // s_u X Au^T
+        Builder b(G_PART_KK);
+        add_rowproj_in(b, X, T, d, {up->A}, D, part);
+        LM_TRY(b.launch("relu2.xa", sms, err, st));
+        LM_TRY(fin_rows("relu2.xa.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {up->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st));
+    }
+    {  // u = X Wu^T + (s_u X Au^T) Bu^T; the epilogue writes u and h = relu(u)^2
+        Builder b(nf4 ? G2N_ACT_FWD : G2_ACT_FWD);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)n;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((n + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
+        P.act = ACT_RELU2;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(X, T, d, d, 128);
+        if (nf4) {
+            S0.b_map[0] = b.codes_k(up->W, 128);
+            S0.b_scale[0] = b.scales(sc[0], up->W, false);
+        } else {
+            S0.b_map[0] = b.map(up->W.w, n, d, d, 128);
+        }
+        S0.b_rank_off = 128;
+        S0.kext = (int32_t)d;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(xa, T, rp, rp, 128);
+        S1.b_map[0] = b.map(up->B, n, r, r, 128);
+        S1.b_rank_off = 128;
+        S1.kext = rp;
+        P.out0 = u_save;
+        P.out1 = h_save;
+        P.ld_out = n;
+        LM_TRY(b.launch("relu2.up", sms, err, st));
+    }
+    {  // s_d h Ad^T
+        Builder b(G_PART_KK);
+        add_rowproj_in(b, h_save, T, n, {down->A}, D, part);
+        LM_TRY(b.launch("relu2.ha", sms, err, st));
+        LM_TRY(fin_rows("relu2.ha.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, ha, haT, D.ldT}}, T, st));
+    }
+    {  // y = h Wd^T + (s_d h Ad^T) Bd^T
+        Builder b(nf4 ? G2N_STORE_K : G2_STORE_K);
+        if (nf4) b.tail_buf = at<float>(ws, PL.tail);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)d;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((d + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(h_save, T, n, n, 128);
+        if (nf4) {
+            S0.b_map[0] = b.codes_k(down->W, 128);
+            S0.b_scale[0] = b.scales(sc[1], down->W, false);
+        } else {
+            S0.b_map[0] = b.map(down->W.w, d, n, n, 128);
+        }
+        S0.b_rank_off = 128;
+        S0.kext = (int32_t)n;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(ha, T, rp, rp, 128);
+        S1.b_map[0] = b.map(down->B, d, r, r, 128);
+        S1.b_rank_off = 128;
+        S1.kext = rp;
+        P.out0 = y;
+        P.ld_out = d;
+        LM_TRY(b.launch("relu2.down", sms, err, st));
+    }
+    return LM_OK;
+}
+
+extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const uint16_t* X, const uint16_t* dY,
+                                        const uint16_t* u_save, const uint16_t* h_save, const void* saved,
+                                        size_t saved_bytes, const lm_lora* up, const lm_lora* down, uint16_t* dX,
+                                        float* dA_up, float* dB_up, float* dA_down, float* dB_down, void* ws,
+                                        size_t ws_bytes, lm_stream stream) {
+    LM_TRY(check_relu2_common(T, d, n, up, down));
+    LM_TRY(need_ptr(X, "X"));
+    LM_TRY(need_ptr(dY, "dY"));
+    LM_TRY(need_ptr(u_save, "u_save"));
+    LM_TRY(need_ptr(h_save, "h_save"));
+    LM_TRY(need_ptr(saved, "saved"));
+    LM_TRY(need_ptr(dX, "dX"));
+    LM_TRY(need_ptr(dA_up, "dA_up"));
+    LM_TRY(need_ptr(dB_up, "dB_up"));
+    LM_TRY(need_ptr(dA_down, "dA_down"));
+    LM_TRY(need_ptr(dB_down, "dB_down"));
+    LM_TRY(need_ptr(ws, "ws"));
+    const int32_t r = up->r;
+    const bool nf4 = up->W.kind == LM_WEIGHT_NF4;
+    const Relu2Plan PL = plan_relu2(T, d, n, r);
+    if (saved_bytes < PL.saved_total)
+        return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
+    if (ws_bytes < PL.ws_total) return fail(LM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, PL.ws_total);
+    const size_t td = (size_t)T * d * 2, tn = (size_t)T * n * 2;
+    const size_t ad = (size_t)r * d * 4, an = (size_t)r * n * 4;
+    LM_TRY(check_alias({{dX, td, "dX"}, {dA_up, ad, "dA_up"}, {dB_up, an, "dB_up"}, {dA_down, an, "dA_down"},
+                        {dB_down, ad, "dB_down"}, {ws, PL.ws_total, "ws"}},
+                       {{X, td, "X"}, {dY, td, "dY"}, {u_save, tn, "u_save"}, {h_save, tn, "h_save"},
+                        {saved, PL.saved_total, "saved"}, wspan(up, "up.W"), wspan(down, "down.W")}));
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T == 0) {
+        LM_CUDA(cudaMemsetAsync(dA_up, 0, ad, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dB_up, 0, an, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dA_down, 0, an, st), "cudaMemsetAsync");
+        LM_CUDA(cudaMemsetAsync(dB_down, 0, ad, st), "cudaMemsetAsync");
+        return LM_OK;
+    }
+    int sms = 0;
+    LM_TRY(ready(&sms));
+    const Dims& D = PL.D;
+    const int rp = D.rp;
+    int32_t* err = static_cast<int32_t*>(ws);
+    float* part = at<float>(ws, PL.part);
+    lm_lora up_c = *up, down_c = *down;
+    LM_TRY(ab_to_bf16("relu2.ab", {{&up_c, d, n}, {&down_c, n, d}}, at<uint16_t>(ws, PL.abc), st));
+    up = &up_c;
+    down = &down_c;
+    float* sc[2] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1])};
+    if (nf4) {
+        LM_TRY(scale_table("relu2.nf4s", up->W, sc[0], st));
+        LM_TRY(scale_table("relu2.nf4s", down->W, sc[1], st));
+    }
+    const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
+    const uint16_t* haT = at<uint16_t>(saved, PL.ha.t_off);
+    uint16_t* gd = at<uint16_t>(ws, PL.gd.rows_off);
+    uint16_t* gdT = at<uint16_t>(ws, PL.gd.t_off);
+    uint16_t* gu = at<uint16_t>(ws, PL.gu.rows_off);
+    uint16_t* guT = at<uint16_t>(ws, PL.gu.t_off);
+    uint16_t* du = at<uint16_t>(ws, PL.du);
+
+    {  // Gd = s_d dY Bd, formed once (feeds dh and dA_down)
+        Builder b(G_PART_KMN);
+        add_rowproj_out(b, dY, T, d, down->B, D, part);
+        LM_TRY(b.launch("relu2.gd", sms, err, st));
+        LM_TRY(fin_rows("relu2.gd.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st));
+    }
+    {  // dh = dY Wd + Gd Ad with the ReLU^2 derivative in the epilogue: du = dh * 2 relu(u)
+        Builder b(nf4 ? G2N_ACT_BWD : G2_ACT_BWD);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)n;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((n + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
+        P.act = ACT_RELU2;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(dY, T, d, d, 128);
+        if (nf4) {
+            S0.b_map[0] = b.codes_mn(down->W);
+            S0.b_scale[0] = b.scales(sc[1], down->W, true);
+        } else {
+            S0.b_map[0] = b.map(down->W.w, d, n, n, 64);
+        }
+        S0.b_rank_off = 128;
+        S0.kext = (int32_t)d;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(gd, T, rp, rp, 128);
+        S1.b_map[0] = b.map(down->A, r, n, n, 64);
+        S1.b_rank_off = 128;
+        S1.kext = rp;
+        P.in0 = u_save;
+        P.ld_in = n;
+        P.out0 = du;
+        P.ld_out = n;
+        LM_TRY(b.launch("relu2.dh", sms, err, st));
+    }
+    {  // Gu = s_u du Bu, formed once (feeds dA_up and dX)
+        Builder b(G_PART_KMN);
+        add_rowproj_out(b, du, T, n, up->B, D, part);
+        LM_TRY(b.launch("relu2.gu", sms, err, st));
+        LM_TRY(fin_rows("relu2.gu.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {up->s, 0.f, 0.f}, gu, guT, D.ldT}}, T, st));
+    }
+    {  // the four LoRA gradients as column reductions over the tokens
+        Builder b(G_PART_MNK);
+        float* p0 = part;
+        float* p1 = p0 + (size_t)kMaxSplits * n * rp;   // dB_down  (C = d)
+        float* p2 = p1 + (size_t)kMaxSplits * d * rp;   // dA_up    (C = d)
+        float* p3 = p2 + (size_t)kMaxSplits * d * rp;   // dB_up    (C = n)
+        add_colreduce(b, h_save, T, n, gdT, D, p0);  // dA_down^T = h^T Gd
+        add_colreduce(b, dY, T, d, haT, D, p1);      // dB_down   = dY^T (s h Ad^T)
+        add_colreduce(b, X, T, d, guT, D, p2);       // dA_up^T   = X^T Gu
+        add_colreduce(b, du, T, n, xaT, D, p3);      // dB_up     = du^T (s X Au^T)
+        LM_TRY(b.launch("relu2.dAdB", sms, err, st));
+        FinColJob js[4] = {
+            {p0, n * rp, n, 0, rp, r, 1, dA_down},
+            {p1, d * rp, d, 0, rp, r, 0, dB_down},
+            {p2, d * rp, d, 0, rp, r, 1, dA_up},
+            {p3, n * rp, n, 0, rp, r, 0, dB_up},
+        };
+        LM_TRY(fin_cols("relu2.dAdB.fin", b, js, 4, st));
+    }
+    {  // dX = du Wu + Gu Au
+        Builder b(nf4 ? G2N_STORE_MN : G2_STORE_MN);
+        if (nf4) b.tail_buf = at<float>(ws, PL.tail);
+        Prob& P = b.prob();
+        P.M = (int32_t)T;
+        P.N = (int32_t)d;
+        P.bn = 256;
+        P.tiles_n = (int32_t)((d + 255) / 256);
+        P.n_step = 256;
+        P.out_col_step = 256;
+        Seg& S0 = seg(P, 0);
+        S0.a_map = b.map(du, T, n, n, 128);
+        if (nf4) {
+            S0.b_map[0] = b.codes_mn(up->W);
+            S0.b_scale[0] = b.scales(sc[0], up->W, true);
+        } else {
+            S0.b_map[0] = b.map(up->W.w, n, d, d, 64);
+        }
+        S0.b_rank_off = 128;
+        S0.kext = (int32_t)n;
+        Seg& S1 = seg(P, 1);
+        S1.a_map = b.map(gu, T, rp, rp, 128);
+        S1.b_map[0] = b.map(up->A, r, d, d, 64);
+        S1.b_rank_off = 128;
+        S1.kext = rp;
+        P.out0 = dX;
+        P.ld_out = d;
+        LM_TRY(b.launch("relu2.dX", sms, err, st));
+    }
+    return LM_OK;
+}
+
 extern "C" lm_status lora_qkv_saved_size(int64_t T, int32_t r, size_t* bytes) {
     if (!bytes) return fail(LM_ERR_NULL, "bytes is NULL");
     LM_TRY(check_T(T));

@@ -22,8 +22,8 @@
 
 namespace lm {
 
-enum : int { EPI_STORE = 0, EPI_GLU_FWD = 1, EPI_GLU_BWD = 2, EPI_PARTIAL = 3 };
-enum : int { ACT_SWIGLU = 0, ACT_GEGLU = 1 };
+enum : int { EPI_STORE = 0, EPI_GLU_FWD = 1, EPI_GLU_BWD = 2, EPI_PARTIAL = 3, EPI_ACT_FWD = 4, EPI_ACT_BWD = 5 };
+enum : int { ACT_SWIGLU = 0, ACT_GEGLU = 1, ACT_RELU2 = 2 };
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
@@ -167,6 +167,7 @@ __device__ __forceinline__ float act_fwd(int act, float x) {
     // fast division (reciprocal times numerator, ~2 ulp), far below the bf16 rounding of the
     // outputs; for x below about -88 the denominator is inf and the quotient 0, the limit
     if (act == ACT_SWIGLU) return __fdividef(x, 1.0f + __expf(-x));
+    if (act == ACT_RELU2) return x > 0.0f ? x * x : 0.0f;  // squared ReLU
     return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
 }
 // returns act(x) and act'(x)
@@ -175,6 +176,10 @@ __device__ __forceinline__ void act_fwd_bwd(int act, float x, float& f, float& d
         const float sg = __fdividef(1.0f, 1.0f + __expf(-x));
         f = x * sg;
         df = sg * (1.0f + x * (1.0f - sg));
+    } else if (act == ACT_RELU2) {  // relu(x)^2 and 2 relu(x)
+        const float rx = x > 0.0f ? x : 0.0f;
+        f = rx * rx;
+        df = 2.0f * rx;
     } else {
         const float cdf = 0.5f * (1.0f + erff(x * 0.70710678118654752f));
         const float pdf = 0.39894228040143268f * __expf(-0.5f * x * x);
@@ -269,6 +274,51 @@ __device__ __forceinline__ void epilogue_cols(const Prob& P, const Unit& U, uint
                              deo[7]);
                 st_global_v8(static_cast<uint16_t*>(P.out1) + off, duo[0], duo[1], duo[2], duo[3], duo[4], duo[5], duo[6],
                              duo[7]);
+            }
+        }
+    } else if constexpr (EPI == EPI_ACT_FWD) {
+        // non-gated activation: the accumulator is u; write u and h = act(u), h taken from the
+        // bf16 u (the value the backward reads)
+#pragma unroll 1
+        for (int col = c_lo; col < c_hi; col += 16) {
+            uint32_t a[16];
+            tmem_ld_x16(tacc + col, a);
+            tmem_ld_wait16(a);
+            const int64_t gcol = (int64_t)U.nb * P.out_col_step + col;
+            if (mvalid && gcol < P.N) {
+                uint32_t uo[8], ho[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    uo[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+                    ho[i] = pack_bf16x2(act_fwd(P.act, bf16lo(uo[i])), act_fwd(P.act, bf16hi(uo[i])));
+                }
+                const int64_t off = m * P.ld_out + gcol;
+                st_global_v8(static_cast<uint16_t*>(P.out0) + off, uo[0], uo[1], uo[2], uo[3], uo[4], uo[5], uo[6], uo[7]);
+                st_global_v8(static_cast<uint16_t*>(P.out1) + off, ho[0], ho[1], ho[2], ho[3], ho[4], ho[5], ho[6], ho[7]);
+            }
+        }
+    } else if constexpr (EPI == EPI_ACT_BWD) {
+        // accumulator = dh; with the saved u:  du = dh * act'(u)
+#pragma unroll 1
+        for (int col = c_lo; col < c_hi; col += 16) {
+            const int64_t gcol = (int64_t)U.nb * P.out_col_step + col;
+            const bool ok = mvalid && gcol < P.N;
+            uint32_t uv[8];
+            if (ok) ld_global_nc_v8(static_cast<const uint16_t*>(P.in0) + m * P.ld_in + gcol, uv);
+            uint32_t a[16];
+            tmem_ld_x16(tacc + col, a);
+            tmem_ld_wait16(a);
+            if (ok) {
+                uint32_t duo[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float f0, df0, f1, df1;
+                    act_fwd_bwd(P.act, bf16lo(uv[i]), f0, df0);
+                    act_fwd_bwd(P.act, bf16hi(uv[i]), f1, df1);
+                    duo[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * df0, __uint_as_float(a[2 * i + 1]) * df1);
+                }
+                st_global_v8(static_cast<uint16_t*>(P.out0) + m * P.ld_out + gcol, duo[0], duo[1], duo[2], duo[3], duo[4],
+                             duo[5], duo[6], duo[7]);
             }
         }
     } else {  // EPI_PARTIAL: raw fp32 accumulator to out0[ks][m][0..bn)

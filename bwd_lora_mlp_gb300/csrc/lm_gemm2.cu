@@ -48,6 +48,8 @@ cudaError_t launch_gemm_pair(GemmKind k, const Params& p, int max_units, cudaStr
         case G2_STORE_K: return launch_pair_variant<false, EPI_STORE>(p, max_units, st);
         case G2_GLU_BWD: return launch_pair_variant<true, EPI_GLU_BWD>(p, max_units, st);
         case G2_STORE_MN: return launch_pair_variant<true, EPI_STORE>(p, max_units, st);
+        case G2_ACT_FWD: return launch_pair_variant<false, EPI_ACT_FWD>(p, max_units, st);
+        case G2_ACT_BWD: return launch_pair_variant<true, EPI_ACT_BWD>(p, max_units, st);
         default: return cudaErrorInvalidValue;
     }
 }

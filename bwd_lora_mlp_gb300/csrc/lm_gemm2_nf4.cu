@@ -68,6 +68,8 @@ cudaError_t pair_nf4_clusters(GemmKind k, int* n) {
         case G2N_STORE_K: return pair_nf4_variant_clusters<false, EPI_STORE>(n);
         case G2N_GLU_BWD: return pair_nf4_variant_clusters<true, EPI_GLU_BWD>(n);
         case G2N_STORE_MN: return pair_nf4_variant_clusters<true, EPI_STORE>(n);
+        case G2N_ACT_FWD: return pair_nf4_variant_clusters<false, EPI_ACT_FWD>(n);
+        case G2N_ACT_BWD: return pair_nf4_variant_clusters<true, EPI_ACT_BWD>(n);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -78,6 +80,8 @@ cudaError_t launch_gemm_pair_nf4(GemmKind k, const Params& p, int max_units, cud
         case G2N_STORE_K: return launch_pair_nf4_variant<false, EPI_STORE>(p, max_units, st);
         case G2N_GLU_BWD: return launch_pair_nf4_variant<true, EPI_GLU_BWD>(p, max_units, st);
         case G2N_STORE_MN: return launch_pair_nf4_variant<true, EPI_STORE>(p, max_units, st);
+        case G2N_ACT_FWD: return launch_pair_nf4_variant<false, EPI_ACT_FWD>(p, max_units, st);
+        case G2N_ACT_BWD: return launch_pair_nf4_variant<true, EPI_ACT_BWD>(p, max_units, st);
         default: return cudaErrorInvalidValue;
     }
 }

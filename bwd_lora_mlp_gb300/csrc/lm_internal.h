@@ -19,16 +19,20 @@ enum GemmKind : int {
     G2_STORE_K = 12,     // K-major B, STORE
     G2_GLU_BWD = 13,     // MN-major B, GLU_BWD
     G2_STORE_MN = 14,    // MN-major B, STORE
-    // NF4 base decoded in the mainloop, CTA pair, 256 x 256 tiles
-    G2N_GLU_FWD = 15,
-    G2N_STORE_K = 16,
-    G2N_GLU_BWD = 17,
-    G2N_STORE_MN = 18,
-    G_NUM_KINDS = 19
+    G2_ACT_FWD = 15,     // K-major B, ACT_FWD (non-gated activation: u and act(u))
+    G2_ACT_BWD = 16,     // MN-major B, ACT_BWD (du = dh * act'(u))
+    // NF4 base decoded in the mainloop, CTA pair, 512 x 256 tiles
+    G2N_GLU_FWD = 21,
+    G2N_STORE_K = 22,
+    G2N_GLU_BWD = 23,
+    G2N_STORE_MN = 24,
+    G2N_ACT_FWD = 25,
+    G2N_ACT_BWD = 26,
+    G_NUM_KINDS = 27
 };
 
-inline bool gemm_is_pair(GemmKind k) { return k >= G2_GLU_FWD && k <= G2_STORE_MN; }
-inline bool gemm_is_pair_nf4(GemmKind k) { return k >= G2N_GLU_FWD && k <= G2N_STORE_MN; }
+inline bool gemm_is_pair(GemmKind k) { return k >= G2_GLU_FWD && k <= G2_ACT_BWD; }
+inline bool gemm_is_pair_nf4(GemmKind k) { return k >= G2N_GLU_FWD && k <= G2N_ACT_BWD; }
 // Launch at most `max_units` CTA pairs (fewer if fewer pairs fit on the device at once).
 cudaError_t launch_gemm_pair(GemmKind k, const Params& p, int max_units, cudaStream_t st);
 cudaError_t launch_gemm_pair_nf4(GemmKind k, const Params& p, int max_units, cudaStream_t st);

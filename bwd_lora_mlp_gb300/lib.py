@@ -65,6 +65,11 @@ _SIGS = {
     "lm_profile_reset": ([], _I32),
     "lm_profile_summary": ([ctypes.c_char_p, _SZ], _I32),
     "lora_mlp_saved_size": ([_I64, _I32, _SZP], _I32),
+    "lora_relu2_mlp_saved_size": ([_I64, _I32, _SZP], _I32),
+    "lora_relu2_mlp_workspace_size": ([_I64, _I64, _I64, _I32, _SZP], _I32),
+    "lora_relu2_mlp_fwd": ([_I64, _I64, _I64, _P, _LP, _LP, _P, _P, _P, _P, _SZ, _P, _SZ, _P], _I32),
+    "lora_relu2_mlp_bwd": ([_I64, _I64, _I64, _P, _P, _P, _P, _P, _SZ, _LP, _LP, _P, _P, _P, _P, _P, _P, _SZ, _P],
+                           _I32),
     "lora_mlp_workspace_size": ([_I64, _I64, _I64, _I32, _SZP], _I32),
     "lora_mlp_fwd": ([_I64, _I64, _I64, _I32, _P, _LP, _LP, _LP, _P, _P, _P, _P, _P, _SZ, _P, _SZ, _P], _I32),
     "lora_mlp_bwd": ([_I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _SZ, _LP, _LP, _LP, _P, _P, _P, _P, _P,
@@ -298,6 +303,56 @@ def lora_mlp_bwd(X, dY, fwd: dict, gate: Lora, up: Lora, down: Lora, act="swiglu
           _ptr(g["dA_gate"], f32, "dA_gate"), _ptr(g["dB_gate"], f32, "dB_gate"), _ptr(g["dA_up"], f32, "dA_up"),
           _ptr(g["dB_up"], f32, "dB_up"), _ptr(g["dA_down"], f32, "dA_down"), _ptr(g["dB_down"], f32, "dB_down"),
           _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+    return {"dX": dX, **grads}
+
+
+def lora_relu2_mlp_saved_size(T: int, r: int) -> int:
+    return _size("lora_relu2_mlp_saved_size", T, r)
+
+
+def lora_relu2_mlp_workspace_size(T: int, d: int, n: int, r: int) -> int:
+    return _size("lora_relu2_mlp_workspace_size", T, d, n, r)
+
+
+def lora_relu2_mlp_fwd(X, up: Lora, down: Lora, y=None, u=None, h=None, saved=None, ws=None, stream=None) -> dict:
+    T, d = X.shape
+    n = up.W.rows if isinstance(up.W, NF4Weight) else up.W.shape[0]
+    r = up.r
+    dev = X.device
+    bf = torch.bfloat16
+    y = torch.empty((T, d), dtype=bf, device=dev) if y is None else y
+    u = torch.empty((T, n), dtype=bf, device=dev) if u is None else u
+    h = torch.empty((T, n), dtype=bf, device=dev) if h is None else h
+    saved = torch.empty(lora_relu2_mlp_saved_size(T, r), dtype=torch.uint8, device=dev) if saved is None else saved
+    ws = workspace(lora_relu2_mlp_workspace_size(T, d, n, r), dev) if ws is None else ws
+    Lu, Ld = up.c_struct(), down.c_struct()
+    _call("lora_relu2_mlp_fwd", T, d, n, _ptr(X, bf, "X"), ctypes.byref(Lu), ctypes.byref(Ld), _ptr(y, bf, "y"),
+          _ptr(u, bf, "u"), _ptr(h, bf, "h"), _ptr(saved, torch.uint8, "saved"), saved.numel(),
+          _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+    return {"y": y, "u": u, "h": h, "saved": saved, "ws": ws}
+
+
+def lora_relu2_mlp_bwd(X, dY, fwd: dict, up: Lora, down: Lora, dX=None, grads=None, ws=None, stream=None) -> dict:
+    T, d = X.shape
+    n = fwd["u"].shape[1]
+    r = up.r
+    dev = X.device
+    bf, f32 = torch.bfloat16, torch.float32
+    dX = torch.empty((T, d), dtype=bf, device=dev) if dX is None else dX
+    if grads is None:
+        grads = {"dA_up": torch.empty((r, d), dtype=f32, device=dev),
+                 "dB_up": torch.empty((n, r), dtype=f32, device=dev),
+                 "dA_down": torch.empty((r, n), dtype=f32, device=dev),
+                 "dB_down": torch.empty((d, r), dtype=f32, device=dev)}
+    ws = fwd["ws"] if ws is None else ws
+    saved = fwd["saved"]
+    Lu, Ld = up.c_struct(), down.c_struct()
+    g = grads
+    _call("lora_relu2_mlp_bwd", T, d, n, _ptr(X, bf, "X"), _ptr(dY, bf, "dY"), _ptr(fwd["u"], bf, "u"),
+          _ptr(fwd["h"], bf, "h"), _ptr(saved, torch.uint8, "saved"), saved.numel(), ctypes.byref(Lu),
+          ctypes.byref(Ld), _ptr(dX, bf, "dX"), _ptr(g["dA_up"], f32, "dA_up"), _ptr(g["dB_up"], f32, "dB_up"),
+          _ptr(g["dA_down"], f32, "dA_down"), _ptr(g["dB_down"], f32, "dB_down"), _ptr(ws, torch.uint8, "ws"),
+          ws.numel(), _stream(stream))
     return {"dX": dX, **grads}
 
 

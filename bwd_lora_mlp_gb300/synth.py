@@ -77,7 +77,7 @@ class ProjSpec:
 class Workload:
     """A named workload: the projections of one block plus the token count."""
     name: str
-    kind: str            # "mlp", "qkv", "o"
+    kind: str            # "mlp", "relu2", "qkv", "o"
     T: int
     r: int
     alpha: float
@@ -95,6 +95,12 @@ def mlp_workload(name, T, d, n, r, alpha, act="swiglu", nf4=False) -> Workload:
     return Workload(name, "mlp", T, r, alpha,
                     [ProjSpec("gate", d, n), ProjSpec("up", d, n), ProjSpec("down", n, d)],
                     act=act, nf4=nf4)
+
+
+def relu2_workload(name, T, d, n, r, alpha, nf4=False) -> Workload:
+    """Non-gated ReLU^2 MLP: up (d -> n) and down (n -> d) projections."""
+    return Workload(name, "relu2", T, r, alpha, [ProjSpec("up", d, n), ProjSpec("down", n, d)], act="relu2",
+                    nf4=nf4)
 
 
 def qkv_workload(name, T, d, q, kv, r, alpha, nf4=False) -> Workload:
@@ -120,6 +126,10 @@ WORKLOADS = {
     "llama3_70b_mlp_nf4_geglu": mlp_workload("llama3_70b_mlp_nf4_geglu", 4096, 8192, 28672, 64, 128.0,
                                              act="geglu", nf4=True),
 }
+# the non-gated ReLU^2 MLP at the 8B MLP sizes (the pages give no sizes for it)
+WORKLOADS["tiny_relu2_mlp"] = relu2_workload("tiny_relu2_mlp", 512, 256, 704, 8, 16.0)
+WORKLOADS["relu2_mlp_8b_bf16"] = relu2_workload("relu2_mlp_8b_bf16", 8192, 4096, 14336, 16, 32.0)
+WORKLOADS["relu2_mlp_8b_nf4"] = relu2_workload("relu2_mlp_8b_nf4", 8192, 4096, 14336, 16, 32.0, nf4=True)
 # the 8B MLP with fp32 LoRA parameters (bf16 and NF4 base)
 for _b in ("bf16", "nf4"):
     _w = mlp_workload("llama3_8b_mlp_%s_ab32" % _b, 8192, 4096, 14336, 16, 32.0, nf4=_b == "nf4")

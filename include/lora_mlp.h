@@ -167,6 +167,28 @@ LM_API lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act,
                        float* dB_up, float* dA_down, float* dB_down,
                        void* ws, size_t ws_bytes, lm_stream stream);
 
+/* ---- non-gated ReLU^2 MLP with LoRA up / down projections ([LO] "FP32 LoRA gradients":
+ * dense ReLU^2 MLPs use up/down LoRA projections and a fused ReLU^2 activation derivative) ----
+ *   u = X Wu^T + su (X Au^T) Bu^T,   h = max(u, 0)^2,   y = h Wd^T + sd (h Ad^T) Bd^T.
+ * The backward hoists Gd = sd dY Bd and Gu = su du Bu and fuses the activation derivative into
+ * the dh GEMM's epilogue:  dh = dY Wd + Gd Ad,  du = dh * 2 max(u, 0),  dX = du Wu + Gu Au,
+ * dAd = Gd^T h, dBd = sd dY^T (h Ad^T), dAu = Gu^T X, dBu = su du^T (X Au^T).  up is d -> n,
+ * down is n -> d, same r; bf16 or NF4 base (both the same kind).  X, y, dX (T x d); u_save,
+ * h_save (T x n) are written by the forward (u = pre-activation, h = activation, bf16, h taken
+ * from the bf16 u) and read by the backward; saved (lora_relu2_mlp_saved_size bytes) holds the
+ * rank-r products.  dA_up (r x d), dB_up (n x r), dA_down (r x n), dB_down (d x r) fp32. */
+LM_API lm_status lora_relu2_mlp_saved_size(int64_t T, int32_t r, size_t* bytes);
+LM_API lm_status lora_relu2_mlp_workspace_size(int64_t T, int64_t d, int64_t n, int32_t r, size_t* bytes);
+LM_API lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const uint16_t* X, const lm_lora* up,
+                                    const lm_lora* down, uint16_t* y, uint16_t* u_save, uint16_t* h_save,
+                                    void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                                    lm_stream stream);
+LM_API lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const uint16_t* X, const uint16_t* dY,
+                                    const uint16_t* u_save, const uint16_t* h_save, const void* saved,
+                                    size_t saved_bytes, const lm_lora* up, const lm_lora* down, uint16_t* dX,
+                                    float* dA_up, float* dB_up, float* dA_down, float* dB_down, void* ws,
+                                    size_t ws_bytes, lm_stream stream);
+
 /* ---- LoRA QKV ([LO] query/key/value function; [UN] LoRA_QKV) ---------------------------
  * Q = X Wq^T + sq (X Aq^T) Bq^T, and likewise K (nk columns) and V (nv columns); one read of
  * X feeds all three.  The backward sums the three input gradients into dX.  q, k, v must have

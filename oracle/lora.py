@@ -170,6 +170,59 @@ def mlp_backward(X, dY, p, act="swiglu"):
             "de": de, "du": du, "dh": dh, "Gg": Gg, "Gu": Gu, "Gd": Gd, **fw}
 
 
+# ----------------------------------------------------------------------------------------------
+# Non-gated ReLU^2 MLP ("LoRA Optimizations", FP32 LoRA gradients: dense ReLU^2 MLPs with up/down
+# LoRA projections and a fused ReLU^2 activation derivative).  ReLU^2(x) = max(x, 0)^2, its
+# derivative 2 max(x, 0).
+# ----------------------------------------------------------------------------------------------
+
+def relu2(x):
+    return np.square(np.maximum(x, 0.0))
+
+
+def relu2_grad(x):
+    return 2.0 * np.maximum(x, 0.0)
+
+
+def relu2_mlp_forward(X, p):
+    """p: dict with Wu, Au, Bu, su, Wd, Ad, Bd, sd.  u = X Wu^T + su (X Au^T) Bu^T, h = relu(u)^2,
+    y = h Wd^T + sd (h Ad^T) Bd^T."""
+    XAu = X @ p["Au"].T
+    u = X @ p["Wu"].T + p["su"] * (XAu @ p["Bu"].T)
+    h = relu2(u)
+    hA = h @ p["Ad"].T
+    y = h @ p["Wd"].T + p["sd"] * (hA @ p["Bd"].T)
+    return {"u": u, "h": h, "y": y, "XAu": XAu, "hA": hA}
+
+
+def relu2_mlp_backward(X, dY, p):
+    """Gradients of L = <dY, y> for X and the four LoRA factors.
+
+    Down: Gd = dY Bd (hoisted), dh = dY Wd + sd Gd Ad, dAd = sd Gd^T h, dBd = sd dY^T (h Ad^T).
+    Activation: du = dh * 2 relu(u).
+    Up: Gu = du Bu (hoisted), dAu = su Gu^T X, dBu = su du^T (X Au^T), dX = du Wu + su Gu Au.
+    """
+    fw = relu2_mlp_forward(X, p)
+    u, h = fw["u"], fw["h"]
+    Gd = dY @ p["Bd"]
+    dh = dY @ p["Wd"] + p["sd"] * (Gd @ p["Ad"])
+    dAd = p["sd"] * (Gd.T @ h)
+    dBd = p["sd"] * (dY.T @ fw["hA"])
+    du = dh * relu2_grad(u)
+    Gu = du @ p["Bu"]
+    dAu = p["su"] * (Gu.T @ X)
+    dBu = p["su"] * (du.T @ fw["XAu"])
+    dX = du @ p["Wu"] + p["su"] * (Gu @ p["Au"])
+    return {"dX": dX, "dAu": dAu, "dBu": dBu, "dAd": dAd, "dBd": dBd, "du": du, "dh": dh, "Gu": Gu,
+            "Gd": Gd, **fw}
+
+
+def relu2_mlp_flops(T, d, n, r):
+    """Algorithmic flops of one fwd+bwd of the ReLU^2 MLP: the up and down projections as two
+    LoRA projections (base 4 T in out each, fwd + dX) plus the rank-r terms."""
+    return lora_proj_flops(T, d, n, r) + lora_proj_flops(T, n, d, r)
+
+
 def mlp_backward_columns(X, dY, p, cols, act="swiglu"):
     """dB_gate[cols], dB_up[cols] and dA_down[:, cols] of mlp_backward, for a subset of the n
     intermediate features.  Column c of e, u, h, dh, de, du depends only on row c of W_g, W_u, B_g,
