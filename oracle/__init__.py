@@ -17,6 +17,7 @@ Sources (web pages the method is described on):
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test against
 something other than itself (finite differences, closed forms, the merge
-identity, NF4 invariants, the published NF4 table, the adapter parameter count
+identity, NF4 invariants, the published NF4 table, int4 grid round trips and
+nearest-level checks, the adapter parameter count
 printed on the "LoRA Optimizations" page).  No function is "parity unpinned".
 """
