@@ -171,6 +171,16 @@ lm_status check_lora(const lm_lora* L, const char* name, int64_t in, int64_t out
         LM_TRY(need_ptr(L->W.absmax_q, buf));
         snprintf(buf, sizeof buf, "%s.W.group_scale", name);
         LM_TRY(need_ptr(L->W.group_scale, buf));
+    } else if (L->W.kind == LM_WEIGHT_INT4) {
+        const int32_t G = L->W.group;
+        if (G != 32 && G != 64 && G != 128 && G != 256)
+            return fail(LM_ERR_SHAPE, "%s.W.group = %d: an int4 group holds 32, 64, 128 or 256 elements", name, G);
+        if (L->W.cols % 64 != 0 || L->W.cols % G != 0)
+            return fail(LM_ERR_SHAPE, "%s: an int4 weight needs cols %% 64 == 0 and cols %% group == 0", name);
+        snprintf(buf, sizeof buf, "%s.W.codes", name);
+        LM_TRY(need_ptr(L->W.codes, buf));
+        snprintf(buf, sizeof buf, "%s.W.scale_zero", name);
+        LM_TRY(need_ptr(L->W.scale_zero, buf));
     } else {
         return fail(LM_ERR_DTYPE, "%s.W.kind = %d is not a known weight kind", name, L->W.kind);
     }
@@ -212,17 +222,19 @@ lm_status check_alias(std::initializer_list<Span> outs, std::initializer_list<Sp
 }
 
 Span wspan(const lm_lora* L, const char* name) {
-    if (L->W.kind == LM_WEIGHT_NF4) return Span{L->W.codes, (size_t)(L->W.rows * L->W.cols / 2), name};
+    if (L->W.kind != LM_WEIGHT_BF16) return Span{L->W.codes, (size_t)(L->W.rows * L->W.cols / 2), name};
     return Span{L->W.w, (size_t)(L->W.rows * L->W.cols * 2), name};
 }
 
 // every projection of one call must use the same kind of base weight
-lm_status same_kind(std::initializer_list<const lm_lora*> Ls, bool* nf4) {
+// (*q4: a packed 4-bit base, NF4 or int4, decoded inside the GEMM mainloop)
+lm_status same_kind(std::initializer_list<const lm_lora*> Ls, bool* q4) {
     const lm_lora* first = *Ls.begin();
     for (const lm_lora* L : Ls)
         if (L->W.kind != first->W.kind)
-            return fail(LM_ERR_UNSUPPORTED, "the projections of one call mix bf16 and NF4 base weights");
-    *nf4 = first->W.kind == LM_WEIGHT_NF4;
+            return fail(LM_ERR_UNSUPPORTED, "the projections of one call mix base weight kinds (%d and %d)",
+                        first->W.kind, L->W.kind);
+    *q4 = first->W.kind != LM_WEIGHT_BF16;
     return LM_OK;
 }
 
@@ -376,7 +388,9 @@ OPlan plan_o(int64_t T, int64_t d_in, int64_t d_out, int32_t r) {
 }
 
 // fp32 block-scale table of an NF4 weight for the NF4 GEMMs (traced under `tag`)
+// (an int4 weight needs none: its (scale, zero) words are read where they are)
 lm_status scale_table(const char* tag, const lm_weight& W, float* table, cudaStream_t st) {
+    if (W.kind != LM_WEIGHT_NF4) return LM_OK;
     ProfScope prof(tag, st);
     const cudaError_t e = launch_nf4_scale_table(W.absmax_q, W.group_scale, W.rows, W.cols, table, st);
     return e == cudaSuccess ? LM_OK : cuda_fail(e, "NF4 scale table launch");
@@ -459,11 +473,34 @@ struct Builder {
     // fp32 block-scale table of an NF4 weight ([cols / 64][rows], see launch_nf4_scale_table):
     // box 128 rows x 1 K block (weight read K-major) or 64 rows x 2 column blocks (MN-major);
     // rows outside the weight read 0
+    // An int4 weight instead maps its (scale, zero) words ([cols / G][rows] 32-bit words): box
+    // 128 rows x (G == 32 ? 2 : 1) groups (K-major: the groups of one 64-wide K block) or 64 rows x
+    // max(1, 128 / G) groups (MN-major: the groups of 128 columns).
     int scales(const float* table, const lm_weight& W, bool mn) {
         if (st != LM_OK) return 0;
         if (nmaps >= kMaxMaps) {
             st = fail(LM_ERR_UNSUPPORTED, "too many tensor maps in one launch");
             return 0;
+        }
+        if (W.kind == LM_WEIGHT_INT4) {
+            const int G = W.group;
+            cuuint64_t dims[2] = {(cuuint64_t)W.rows, (cuuint64_t)(W.cols / G)};
+            cuuint64_t strides[1] = {(cuuint64_t)W.rows * 4};
+            cuuint32_t box[2] = {mn ? 64u : 128u, mn ? (cuuint32_t)std::max(1, 128 / G) : (G == 32 ? 2u : 1u)};
+            cuuint32_t es[2] = {1u, 1u};
+            const CUresult r = g_encode(&p.maps[nmaps], CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
+                                        const_cast<uint16_t*>(W.scale_zero), dims, strides, box, es,
+                                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) {
+                st = fail(LM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for int4 scales %lld x %lld", (int)r,
+                          (long long)W.rows, (long long)(W.cols / G));
+                return 0;
+            }
+            p.map_bytes[nmaps] = 4u * box[0] * box[1];
+            p.map_w[nmaps] = (int32_t)W.rows;
+            p.map_group[nmaps] = G;
+            return nmaps++;
         }
         cuuint64_t dims[2] = {(cuuint64_t)W.rows, (cuuint64_t)(W.cols / 64)};
         cuuint64_t strides[1] = {(cuuint64_t)W.rows * 4};
@@ -857,8 +894,8 @@ static lm_status check_mlp_common(int64_t T, int64_t d, int64_t n, int32_t act, 
     LM_TRY(check_lora(gate, "gate", d, n, gate->r));
     LM_TRY(check_lora(up, "up", d, n, gate->r));
     LM_TRY(check_lora(down, "down", n, d, gate->r));
-    bool nf4 = false;
-    LM_TRY(same_kind({gate, up, down}, &nf4));
+    bool q4 = false;
+    LM_TRY(same_kind({gate, up, down}, &q4));
     return LM_OK;
 }
 
@@ -875,7 +912,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     LM_TRY(need_ptr(saved, "saved"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = gate->r;
-    const bool nf4 = gate->W.kind == LM_WEIGHT_NF4;
+    const bool q4 = gate->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
     const MlpPlan PL = plan_mlp(T, d, n, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -901,7 +938,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     up = &up_c;
     down = &down_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
-    if (nf4) {  // the NF4 GEMMs read per-K-block fp32 block scales of W_gate, W_up, W_down
+    if (q4) {  // the NF4 GEMMs read per-K-block fp32 block scales of W_gate, W_up, W_down
         LM_TRY(scale_table("mlp.nf4s", gate->W, sc[0], st));
         LM_TRY(scale_table("mlp.nf4s", up->W, sc[1], st));
         LM_TRY(scale_table("mlp.nf4s", down->W, sc[2], st));
@@ -917,7 +954,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(b.launch("mlp.xa", sms, err, st));
         LM_TRY(fin_rows("mlp.xa.fin", b, {FinRowJob{part, T * 2 * rp, 0, 2 * rp, rp, {gate->s, up->s, 0.f}, xa, xaT, D.ldT}}, T, st));
     }
-    if (nf4) {
+    if (q4) {
         // NF4 base, CTA pair: CTA 0 decodes 128 W_g rows of a tile, CTA 1 the matching W_u rows;
         // the rank-r segment multiplies [s XAg | s XAu] by the block-diagonal [Bg | 0 ; 0 | Bu]
         uint16_t* bdiag = at<uint16_t>(ws, PL.bdiag);
@@ -992,7 +1029,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(b.launch("mlp.ha", sms, err, st));
         LM_TRY(fin_rows("mlp.ha.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, ha, haT, D.ldT}}, T, st));
     }
-    if (nf4) {
+    if (q4) {
         Builder b(G2N_STORE_K);
         b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
@@ -1064,7 +1101,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     LM_TRY(need_ptr(dB_down, "dB_down"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = gate->r;
-    const bool nf4 = gate->W.kind == LM_WEIGHT_NF4;
+    const bool q4 = gate->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
     const MlpPlan PL = plan_mlp(T, d, n, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1101,7 +1138,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     up = &up_c;
     down = &down_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
-    if (nf4) {
+    if (q4) {
         LM_TRY(scale_table("mlp.nf4s", gate->W, sc[0], st));
         LM_TRY(scale_table("mlp.nf4s", up->W, sc[1], st));
         LM_TRY(scale_table("mlp.nf4s", down->W, sc[2], st));
@@ -1123,7 +1160,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(b.launch("mlp.gd", sms, err, st));
         LM_TRY(fin_rows("mlp.gd.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st));
     }
-    if (nf4) {
+    if (q4) {
         Builder b(G2N_GLU_BWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;
@@ -1212,7 +1249,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         };
         LM_TRY(fin_cols("mlp.dAdB.fin", b, js, 6, st));
     }
-    if (nf4) {
+    if (q4) {
         Builder b(G2N_STORE_MN);
         b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
@@ -1343,8 +1380,8 @@ static lm_status check_relu2_common(int64_t T, int64_t d, int64_t n, const lm_lo
     LM_TRY(check_r(up->r));
     LM_TRY(check_lora(up, "up", d, n, up->r));
     LM_TRY(check_lora(down, "down", n, d, up->r));
-    bool nf4 = false;
-    LM_TRY(same_kind({up, down}, &nf4));
+    bool q4 = false;
+    LM_TRY(same_kind({up, down}, &q4));
     return LM_OK;
 }
 
@@ -1359,7 +1396,7 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
     LM_TRY(need_ptr(saved, "saved"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = up->r;
-    const bool nf4 = up->W.kind == LM_WEIGHT_NF4;
+    const bool q4 = up->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
     const Relu2Plan PL = plan_relu2(T, d, n, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1383,7 +1420,7 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
     up = &up_c;
     down = &down_c;
     float* sc[2] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1])};
-    if (nf4) {
+    if (q4) {
         LM_TRY(scale_table("relu2.nf4s", up->W, sc[0], st));
         LM_TRY(scale_table("relu2.nf4s", down->W, sc[1], st));
     }
@@ -1398,7 +1435,7 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
         LM_TRY(fin_rows("relu2.xa.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {up->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st));
     }
     {  // u = X Wu^T + (s_u X Au^T) Bu^T; the epilogue writes u and h = relu(u)^2
-        Builder b(nf4 ? G2N_ACT_FWD : G2_ACT_FWD);
+        Builder b(q4 ? G2N_ACT_FWD : G2_ACT_FWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)n;
@@ -1409,7 +1446,7 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
         P.act = ACT_RELU2;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(X, T, d, d, 128);
-        if (nf4) {
+        if (q4) {
             S0.b_map[0] = b.codes_k(up->W, 128);
             S0.b_scale[0] = b.scales(sc[0], up->W, false);
         } else {
@@ -1434,8 +1471,8 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
         LM_TRY(fin_rows("relu2.ha.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, ha, haT, D.ldT}}, T, st));
     }
     {  // y = h Wd^T + (s_d h Ad^T) Bd^T
-        Builder b(nf4 ? G2N_STORE_K : G2_STORE_K);
-        if (nf4) b.tail_buf = at<float>(ws, PL.tail);
+        Builder b(q4 ? G2N_STORE_K : G2_STORE_K);
+        if (q4) b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
@@ -1445,7 +1482,7 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
         P.out_col_step = 256;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(h_save, T, n, n, 128);
-        if (nf4) {
+        if (q4) {
             S0.b_map[0] = b.codes_k(down->W, 128);
             S0.b_scale[0] = b.scales(sc[1], down->W, false);
         } else {
@@ -1483,7 +1520,7 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
     LM_TRY(need_ptr(dB_down, "dB_down"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = up->r;
-    const bool nf4 = up->W.kind == LM_WEIGHT_NF4;
+    const bool q4 = up->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
     const Relu2Plan PL = plan_relu2(T, d, n, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1513,7 +1550,7 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
     up = &up_c;
     down = &down_c;
     float* sc[2] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1])};
-    if (nf4) {
+    if (q4) {
         LM_TRY(scale_table("relu2.nf4s", up->W, sc[0], st));
         LM_TRY(scale_table("relu2.nf4s", down->W, sc[1], st));
     }
@@ -1532,7 +1569,7 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
         LM_TRY(fin_rows("relu2.gd.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st));
     }
     {  // dh = dY Wd + Gd Ad with the ReLU^2 derivative in the epilogue: du = dh * 2 relu(u)
-        Builder b(nf4 ? G2N_ACT_BWD : G2_ACT_BWD);
+        Builder b(q4 ? G2N_ACT_BWD : G2_ACT_BWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)n;
@@ -1543,7 +1580,7 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
         P.act = ACT_RELU2;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(dY, T, d, d, 128);
-        if (nf4) {
+        if (q4) {
             S0.b_map[0] = b.codes_mn(down->W);
             S0.b_scale[0] = b.scales(sc[1], down->W, true);
         } else {
@@ -1588,8 +1625,8 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
         LM_TRY(fin_cols("relu2.dAdB.fin", b, js, 4, st));
     }
     {  // dX = du Wu + Gu Au
-        Builder b(nf4 ? G2N_STORE_MN : G2_STORE_MN);
-        if (nf4) b.tail_buf = at<float>(ws, PL.tail);
+        Builder b(q4 ? G2N_STORE_MN : G2_STORE_MN);
+        if (q4) b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
@@ -1599,7 +1636,7 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
         P.out_col_step = 256;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(du, T, n, n, 128);
-        if (nf4) {
+        if (q4) {
             S0.b_map[0] = b.codes_mn(up->W);
             S0.b_scale[0] = b.scales(sc[0], up->W, true);
         } else {
@@ -1652,8 +1689,8 @@ static lm_status check_qkv_common(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     LM_TRY(check_lora(q, "q", d, nq, q->r));
     LM_TRY(check_lora(k, "k", d, nk, q->r));
     LM_TRY(check_lora(v, "v", d, nv, q->r));
-    bool nf4 = false;
-    LM_TRY(same_kind({q, k, v}, &nf4));
+    bool q4 = false;
+    LM_TRY(same_kind({q, k, v}, &q4));
     return LM_OK;
 }
 
@@ -1669,7 +1706,7 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     LM_TRY(need_ptr(saved, "saved"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = q->r;
-    const bool nf4 = q->W.kind == LM_WEIGHT_NF4;
+    const bool q4 = q->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
     const QkvPlan PL = plan_qkv(T, d, nq, nk, nv, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1691,7 +1728,7 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     k = &k_c;
     v = &v_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
-    if (nf4) {  // the NF4 GEMMs read per-K-block fp32 block scales of W_q, W_k, W_v
+    if (q4) {  // the NF4 GEMMs read per-K-block fp32 block scales of W_q, W_k, W_v
         LM_TRY(scale_table("qkv.nf4s", q->W, sc[0], st));
         LM_TRY(scale_table("qkv.nf4s", k->W, sc[1], st));
         LM_TRY(scale_table("qkv.nf4s", v->W, sc[2], st));
@@ -1704,7 +1741,7 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         LM_TRY(b.launch("qkv.xa", sms, err, st));
         LM_TRY(fin_rows("qkv.xa.fin", b, {FinRowJob{part, T * 3 * rp, 0, 3 * rp, rp, {q->s, k->s, v->s}, xa, xaT, D.ldT}}, T, st));
     }
-    if (nf4) {
+    if (q4) {
         Builder b(G2N_STORE_K);
         b.tail_buf = at<float>(ws, PL.tail);
         const int xmap = b.map(X, T, d, d, 128);
@@ -1790,7 +1827,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     LM_TRY(need_ptr(dB_v, "dB_v"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = q->r;
-    const bool nf4 = q->W.kind == LM_WEIGHT_NF4;
+    const bool q4 = q->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
     const QkvPlan PL = plan_qkv(T, d, nq, nk, nv, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1824,7 +1861,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     k = &k_c;
     v = &v_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
-    if (nf4) {
+    if (q4) {
         LM_TRY(scale_table("qkv.nf4s", q->W, sc[0], st));
         LM_TRY(scale_table("qkv.nf4s", k->W, sc[1], st));
         LM_TRY(scale_table("qkv.nf4s", v->W, sc[2], st));
@@ -1870,7 +1907,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         LM_TRY(b.launch("qkv.dAdB", sms, err, st));
         LM_TRY(fin_cols("qkv.dAdB.fin", b, js, 6, st));
     }
-    if (nf4) {  // dX = sum_x dOut_x W_x + G_x A_x
+    if (q4) {  // dX = sum_x dOut_x W_x + G_x A_x
         Builder b(G2N_STORE_MN);
         b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
@@ -1966,7 +2003,7 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(need_ptr(saved, "saved"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = o->r;
-    const bool nf4 = o->W.kind == LM_WEIGHT_NF4;
+    const bool q4 = o->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
     const OPlan PL = plan_o(T, d_in, d_out, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1985,7 +2022,7 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(ab_to_bf16("o.ab", {{&o_c, d_in, d_out}}, at<uint16_t>(ws, PL.abc), st));
     o = &o_c;
     float* sc = at<float>(ws, PL.sc);
-    if (nf4) LM_TRY(scale_table("o.nf4s", o->W, sc, st));  // per-K-block fp32 block scales of W_o
+    if (q4) LM_TRY(scale_table("o.nf4s", o->W, sc, st));  // per-K-block fp32 block scales of W_o
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
     uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     {
@@ -1994,7 +2031,7 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         LM_TRY(b.launch("o.xa", sms, err, st));
         LM_TRY(fin_rows("o.xa.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st));
     }
-    if (nf4) {
+    if (q4) {
         Builder b(G2N_STORE_K);
         b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
@@ -2056,7 +2093,7 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(need_ptr(dB, "dB"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = o->r;
-    const bool nf4 = o->W.kind == LM_WEIGHT_NF4;
+    const bool q4 = o->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
     const OPlan PL = plan_o(T, d_in, d_out, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -2081,7 +2118,7 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(ab_to_bf16("o.ab", {{&o_c, d_in, d_out}}, at<uint16_t>(ws, PL.abc), st));
     o = &o_c;
     float* sc = at<float>(ws, PL.sc);
-    if (nf4) LM_TRY(scale_table("o.nf4s", o->W, sc, st));
+    if (q4) LM_TRY(scale_table("o.nf4s", o->W, sc, st));
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     uint16_t* g = at<uint16_t>(ws, PL.g.rows_off);
     uint16_t* gT = at<uint16_t>(ws, PL.g.t_off);
@@ -2101,7 +2138,7 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         FinColJob js[2] = {{p0, d_in * rp, d_in, 0, rp, r, 1, dA}, {p1, d_out * rp, d_out, 0, rp, r, 0, dB}};
         LM_TRY(fin_cols("o.dAdB.fin", b, js, 2, st));
     }
-    if (nf4) {  // dX = dY W + G A
+    if (q4) {  // dX = dY W + G A
         Builder b(G2N_STORE_MN);
         b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
@@ -2191,5 +2228,56 @@ extern "C" lm_status nf4_dequant(const uint8_t* codes, const int8_t* absmax_q, c
     const cudaError_t e =
         launch_nf4_dequant(codes, absmax_q, group_scale, numel, out_dtype == LM_OUT_BF16, out, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "nf4_dequant launch");
+    return LM_OK;
+}
+
+// ====================================================================== int4
+namespace {
+lm_status check_int4_shape(int64_t rows, int64_t cols, int32_t group) {
+    if (group != 32 && group != 64 && group != 128 && group != 256)
+        return fail(LM_ERR_SHAPE, "group = %d: an int4 group holds 32, 64, 128 or 256 elements", group);
+    if (rows < 0 || cols < 0 || cols % group != 0 || rows > (int64_t(1) << 24) || cols > (int64_t(1) << 24))
+        return fail(LM_ERR_SHAPE, "an int4 weight of %lld x %lld needs cols a multiple of the group (%d)",
+                    (long long)rows, (long long)cols, group);
+    return LM_OK;
+}
+}  // namespace
+
+extern "C" lm_status int4_pack(const uint16_t* W, int64_t rows, int64_t cols, int32_t group, uint8_t* codes,
+                               uint16_t* scale_zero, lm_stream stream) {
+    LM_TRY(check_int4_shape(rows, cols, group));
+    LM_TRY(need_ptr(W, "W"));
+    LM_TRY(need_ptr(codes, "codes"));
+    LM_TRY(need_ptr(scale_zero, "scale_zero"));
+    const int64_t numel = rows * cols;
+    LM_TRY(check_alias({{codes, (size_t)numel / 2, "codes"}, {scale_zero, (size_t)(numel / group) * 4, "scale_zero"}},
+                       {{W, (size_t)numel * 2, "W"}}));
+    if (numel == 0) return LM_OK;
+    int sms = 0;
+    LM_TRY(device_sms(&sms));
+    const cudaError_t e = launch_int4_pack(W, rows, cols, group, codes, reinterpret_cast<uint32_t*>(scale_zero),
+                                           (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "int4_pack launch");
+    return LM_OK;
+}
+
+extern "C" lm_status int4_dequant(const uint8_t* codes, const uint16_t* scale_zero, int64_t rows, int64_t cols,
+                                  int32_t group, int32_t out_dtype, void* out, lm_stream stream) {
+    LM_TRY(check_int4_shape(rows, cols, group));
+    if (out_dtype != LM_OUT_F32 && out_dtype != LM_OUT_BF16)
+        return fail(LM_ERR_DTYPE, "out_dtype = %d is not known", out_dtype);
+    LM_TRY(need_ptr(codes, "codes"));
+    LM_TRY(need_ptr(scale_zero, "scale_zero"));
+    LM_TRY(need_ptr(out, "out"));
+    const int64_t numel = rows * cols;
+    const size_t ob = (size_t)numel * (out_dtype == LM_OUT_F32 ? 4 : 2);
+    LM_TRY(check_alias({{out, ob, "out"}}, {{codes, (size_t)numel / 2, "codes"},
+                                            {scale_zero, (size_t)(numel / group) * 4, "scale_zero"}}));
+    if (numel == 0) return LM_OK;
+    int sms = 0;
+    LM_TRY(device_sms(&sms));
+    const cudaError_t e = launch_int4_dequant(codes, reinterpret_cast<const uint32_t*>(scale_zero), rows, cols, group,
+                                              out_dtype == LM_OUT_BF16, out, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "int4_dequant launch");
     return LM_OK;
 }

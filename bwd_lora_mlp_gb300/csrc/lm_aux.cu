@@ -377,4 +377,120 @@ cudaError_t launch_nf4_scale_table(const int8_t* absmax_q, const float* scale, i
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ int4 groupwise base
+// "loralei" README, QLoRA section (int4 base, groups of 32 to 256 elements of a row): asymmetric
+// min/max quantisation with a bf16 scale s and a bf16 zero z (the value of the middle code 8):
+//   s = bf16(fp32((mx - mn) / 15)), z = bf16(fp32(mn + 8 s)),
+//   q = clamp(rint(fp32(fp32(x - z) / s)) + 8, 0, 15)   (q = 8 when s == 0),
+// codes packed as for NF4, (s, z) stored as one 32-bit word (s low, z high) at sz[g * rows + row].
+
+__device__ __forceinline__ uint32_t bf16_bits_rn(float x) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// one thread per group; two passes over the group's bf16 values (range, then codes)
+__global__ void __launch_bounds__(256) int4_pack_kernel(const uint16_t* __restrict__ W, int64_t rows,
+                                                        int64_t cols, int group, uint8_t* __restrict__ codes,
+                                                        uint32_t* __restrict__ sz) {
+    const int64_t ng = cols / group;
+    const int64_t n = rows * ng;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / ng, g = i - row * ng;
+        const int64_t e0 = row * cols + g * group;
+        const uint4* src = reinterpret_cast<const uint4*>(W + e0);
+        float mn = INFINITY, mx = -INFINITY;
+        for (int c = 0; c < group / 8; ++c) {
+            const uint4 v = __ldg(src + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                mn = fminf(mn, fminf(bf16lo(w[k]), bf16hi(w[k])));
+                mx = fmaxf(mx, fmaxf(bf16lo(w[k]), bf16hi(w[k])));
+            }
+        }
+        const uint32_t sb = bf16_bits_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.0f));
+        const float s = __uint_as_float(sb << 16);
+        const uint32_t zb = bf16_bits_rn(__fadd_rn(mn, __fmul_rn(8.0f, s)));
+        const float z = __uint_as_float(zb << 16);
+        sz[g * rows + row] = sb | (zb << 16);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(codes + e0 / 2);
+        for (int c = 0; c < group / 8; ++c) {
+            const uint4 v = __ldg(src + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t packed = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float x = (e & 1) ? bf16hi(w[e >> 1]) : bf16lo(w[e >> 1]);
+                uint32_t q = 8;
+                if (s > 0.0f) {
+                    const float r = rintf(__fdiv_rn(__fsub_rn(x, z), s)) + 8.0f;
+                    q = (uint32_t)fminf(fmaxf(r, 0.0f), 15.0f);
+                }
+                // element 2i -> high nibble of byte i; byte i at bits 8 * i of the word
+                packed |= ((e & 1) ? q : (q << 4)) << (8 * (e >> 1));
+            }
+            dst[c] = packed;
+        }
+    }
+}
+
+cudaError_t launch_int4_pack(const uint16_t* W, int64_t rows, int64_t cols, int group, uint8_t* codes,
+                             uint32_t* sz, cudaStream_t st) {
+    const int64_t n = rows * (cols / group);
+    if (n == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)sms * 8);
+    int4_pack_kernel<<<(unsigned)blocks, 256, 0, st>>>(W, rows, cols, group, codes, sz);
+    return cudaGetLastError();
+}
+
+// Each thread decodes 8 elements (4 code bytes) of one group: w = fp32((q - 8) s + z), one
+// rounding ((q - 8) s is exact).
+__global__ void __launch_bounds__(256) int4_dequant_kernel(const uint32_t* __restrict__ codes,
+                                                           const uint32_t* __restrict__ sz, int64_t rows,
+                                                           int64_t cols, int group, int bf16_out, void* out) {
+    const int64_t n8 = rows * cols / 8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t e0 = i * 8, row = e0 / cols, g = (e0 - row * cols) / group;
+        const uint32_t word = __ldg(sz + g * rows + row);
+        const float s = __uint_as_float(word << 16), z = __uint_as_float(word & 0xFFFF0000u);
+        const uint32_t c4 = __ldg(codes + i);
+        float w[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t byte = (c4 >> (8 * k)) & 0xFFu;
+            w[2 * k] = __fmaf_rn((float)((int)(byte >> 4) - 8), s, z);
+            w[2 * k + 1] = __fmaf_rn((float)((int)(byte & 15u) - 8), s, z);
+        }
+        if (bf16_out) {
+            uint4 v;
+            v.x = pack_bf16x2(w[0], w[1]);
+            v.y = pack_bf16x2(w[2], w[3]);
+            v.z = pack_bf16x2(w[4], w[5]);
+            v.w = pack_bf16x2(w[6], w[7]);
+            reinterpret_cast<uint4*>(out)[i] = v;
+        } else {
+            float4* o = reinterpret_cast<float4*>(out) + 2 * i;
+            o[0] = make_float4(w[0], w[1], w[2], w[3]);
+            o[1] = make_float4(w[4], w[5], w[6], w[7]);
+        }
+    }
+}
+
+cudaError_t launch_int4_dequant(const uint8_t* codes, const uint32_t* sz, int64_t rows, int64_t cols, int group,
+                                bool bf16_out, void* out, cudaStream_t st) {
+    const int64_t n8 = rows * cols / 8;
+    if (n8 == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, (int64_t)sms * 8);
+    int4_dequant_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(codes), sz, rows, cols,
+                                                           group, bf16_out ? 1 : 0, out);
+    return cudaGetLastError();
+}
+
 }  // namespace lm

@@ -44,8 +44,10 @@ struct Seg {
     int32_t dual_split;   // > 0: K steps with k < dual_split use B block 0 and the first bn/2
                           // accumulator columns, the others B block 1 and the second half
     int32_t a_xoff;       // added to the K coordinate of A
-    int32_t b_scale[2];   // NF4 kernel: tensor map of the fp32 block-scale table of the weight
-                          // whose codes b_map[i] holds (-1: b_map[i] is a bf16 operand loaded as is)
+    int32_t b_scale[2];   // packed 4-bit kernel: tensor map of the scales of the weight whose
+                          // codes b_map[i] holds -- the fp32 block-scale table of an NF4 weight or
+                          // the (scale, zero) words of an int4 one (-1: b_map[i] is a bf16
+                          // operand loaded as is)
     int32_t b_rank_off;   // CTA-pair kernel: B rows (K-major) / columns (MN-major) CTA 1 adds
 };
 
@@ -80,6 +82,8 @@ struct Params {  // CUtensorMap members carry their own 128-byte alignment
     CUtensorMap maps[kMaxMaps];
     uint32_t map_bytes[kMaxMaps];   // bytes one box of the map delivers
     int32_t map_w[kMaxMaps];        // inner (K or MN) extent of the map, elements
+    int32_t map_group[kMaxMaps];    // scale map of a packed 4-bit weight: 0 NF4 block scales,
+                                    // G > 0 int4 (scale, zero) words of groups of G elements
     Prob prob[kMaxProbs];
     float nf4_code[16];             // the NF4 values (NF4 kernel only)
     int32_t nprob;

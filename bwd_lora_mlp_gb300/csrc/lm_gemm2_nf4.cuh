@@ -44,7 +44,8 @@ struct Gemm2Nf4Cfg {
     static constexpr int A_BYTES = 2 * kBM * kBK * 2;  // this CTA's 2 x 128 A rows (one per M half)
     static constexpr int B_BYTES = 128 * kBK * 2;      // this CTA's half of B, decoded (or bf16 via TMA)
     static constexpr int C_BYTES = 4096;               // raw codes of that half
-    static constexpr int S_BYTES = 512;                // their 128 fp32 block scales
+    static constexpr int S_BYTES = 1024;               // their scales: 128 fp32 NF4 block scales,
+                                                       // or up to 256 int4 (scale, zero) words
     static constexpr int S_OFF = A_BYTES + B_BYTES + C_BYTES;
     static constexpr int STAGE_BYTES = (S_OFF + S_BYTES + 1023) / 1024 * 1024;
     static constexpr int STAGES = 4;
@@ -64,22 +65,55 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
-// Decode one NF4 block (32 code bytes c0, c1; element 2i in the high nibble of byte i) with
-// block scale amax into a 128-byte row of the swizzled B tile at dst_row (16-byte chunk j stored
-// at chunk j ^ swz).
-__device__ __forceinline__ void nf4_decode_block_regs(uint4 c0, uint4 c1, float amax, uint32_t dst_row, int swz) {
+// The 16 bf16 values of a 4-bit code as low-byte and high-byte tables of four registers each,
+// in code order.
+struct Q4Tab {
+    uint32_t L0, L1, L2, L3, H0, H1, H2, H3;
+};
+
+// T[i] holds the bf16 values of codes 2i (low half) and 2i + 1 (high half)
+__device__ __forceinline__ Q4Tab q4_tab(const uint32_t (&T)[8]) {
+    Q4Tab t;
+    t.L0 = prmt(T[0], T[1], 0x6420);
+    t.L1 = prmt(T[2], T[3], 0x6420);
+    t.L2 = prmt(T[4], T[5], 0x6420);
+    t.L3 = prmt(T[6], T[7], 0x6420);
+    t.H0 = prmt(T[0], T[1], 0x7531);
+    t.H1 = prmt(T[2], T[3], 0x7531);
+    t.H2 = prmt(T[4], T[5], 0x7531);
+    t.H3 = prmt(T[6], T[7], 0x7531);
+    return t;
+}
+
+// NF4 block with scale amax: code i -> bf16(fp32(nf4[i] * amax))
+__device__ __forceinline__ Q4Tab nf4_tab(float amax) {
     uint32_t T[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         T[i] = pack_bf16x2(__fmul_rn(nf4_value(2 * i), amax), __fmul_rn(nf4_value(2 * i + 1), amax));
-    // low / high bytes of the 16 bf16 products, four per register, in code order
-    const uint32_t L0 = prmt(T[0], T[1], 0x6420), L1 = prmt(T[2], T[3], 0x6420);
-    const uint32_t L2 = prmt(T[4], T[5], 0x6420), L3 = prmt(T[6], T[7], 0x6420);
-    const uint32_t H0 = prmt(T[0], T[1], 0x7531), H1 = prmt(T[2], T[3], 0x7531);
-    const uint32_t H2 = prmt(T[4], T[5], 0x7531), H3 = prmt(T[6], T[7], 0x7531);
-    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    return q4_tab(T);
+}
+
+// int4 group with the (scale, zero) word sz (bf16 s in the low half, bf16 z in the high half):
+// code q -> bf16(fp32((q - 8) * s + z)); (q - 8) * s is exact, so the fused multiply-add rounds
+// once, as the separate product and sum would.
+__device__ __forceinline__ Q4Tab int4_tab(uint32_t sz) {
+    const float s = __uint_as_float(sz << 16), z = __uint_as_float(sz & 0xFFFF0000u);
+    uint32_t T[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int i = 0; i < 8; ++i)
+        T[i] = pack_bf16x2(__fmaf_rn((float)(2 * i - 8), s, z), __fmaf_rn((float)(2 * i - 7), s, z));
+    return q4_tab(T);
+}
+
+// Decode the 16-byte output chunks J0..J1-1 (8 elements each, from code word j) of one 64-element
+// block into a 128-byte row of the swizzled B tile at dst_row (chunk j stored at chunk j ^ swz).
+// Code words hold element 2i in the high nibble of byte i.
+template <int J0, int J1>
+__device__ __forceinline__ void q4_decode_chunks(const Q4Tab& t, const uint32_t (&words)[8], uint32_t dst_row,
+                                                 int swz) {
+#pragma unroll
+    for (int j = J0; j < J1; ++j) {
         uint32_t o[4];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -90,8 +124,8 @@ __device__ __forceinline__ void nf4_decode_block_regs(uint4 c0, uint4 c1, float 
             const uint32_t z = prmt(x, 0u, 0x1100);                  // bytes x.b0 x.b0 x.b1 x.b1
             const uint32_t y = ((z << 4) & 0x00800080u) | (z & ~0x00800080u);  // bit 7 of byte k = bit 3 of n_k
             const uint32_t m = prmt(y, y, 0xBA98);                   // 0xFF where n_k >= 8
-            const uint32_t lw = (prmt(L2, L3, sel) & m) | (prmt(L0, L1, sel) & ~m);
-            const uint32_t hw = (prmt(H2, H3, sel) & m) | (prmt(H0, H1, sel) & ~m);
+            const uint32_t lw = (prmt(t.L2, t.L3, sel) & m) | (prmt(t.L0, t.L1, sel) & ~m);
+            const uint32_t hw = (prmt(t.H2, t.H3, sel) & m) | (prmt(t.H0, t.H1, sel) & ~m);
             o[2 * h] = prmt(lw, hw, 0x4051);      // bf16 of n1 (low half), n0 (high half)
             o[2 * h + 1] = prmt(lw, hw, 0x6273);  // bf16 of n3, n2
         }
@@ -100,6 +134,12 @@ __device__ __forceinline__ void nf4_decode_block_regs(uint4 c0, uint4 c1, float 
                      "r"(o[3])
                      : "memory");
     }
+}
+
+__device__ __forceinline__ void q4_words(const uint4* src, uint32_t (&w)[8]) {
+    const uint4 c0 = src[0], c1 = src[1];
+    w[0] = c0.x; w[1] = c0.y; w[2] = c0.z; w[3] = c0.w;
+    w[4] = c1.x; w[5] = c1.y; w[6] = c1.z; w[7] = c1.w;
 }
 
 template <bool B_MN, int EPI>
@@ -171,6 +211,9 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     const bool nf4 = S.b_scale[0] >= 0;
                     const int bmap = (rank == 1 && S.b_map[1] >= 0) ? S.b_map[1] : S.b_map[0];
                     const int smap = (rank == 1 && S.b_scale[1] >= 0) ? S.b_scale[1] : S.b_scale[0];
+                    // int4 group size (0: NF4); the decoders read it from the stage tag
+                    const int q4g = nf4 ? p.map_group[smap] : 0;
+                    const int32_t tag = !nf4 ? 0 : (q4g ? (3 | (q4g << 8)) : 1);
                     const int brow = U.nb * P.n_step + (int)rank * S.b_rank_off;
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) {
@@ -182,21 +225,23 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                         const uint32_t sC = sB + C::B_BYTES;
                         const uint32_t fb = smem_u32(&full[stage]);
                         const int kx = kb * kBK;
-                        stage_kind[stage] = nf4 ? 1 : 0;
+                        stage_kind[stage] = tag;
                         mbar_expect_tx(fb, C::A_BYTES + (nf4 ? (uint32_t)(p.map_bytes[bmap] + p.map_bytes[smap])
                                                              : (uint32_t)C::B_BYTES));
                         tma_load_2d(sA, &p.maps[S.a_map], fb, kx + S.a_xoff, U.mb * 512 + (int)rank * kBM);
                         tma_load_2d(sA + 16384, &p.maps[S.a_map], fb, kx + S.a_xoff, U.mb * 512 + 256 + (int)rank * kBM);
                         if (nf4) {
-                            // scale table [K block][weight row]: K-major, the 128 rows of this
-                            // K block; MN-major, 64 K rows of the two 64-wide column blocks
+                            // NF4 scale table [K block][weight row]: K-major, the 128 rows of
+                            // this K block; MN-major, 64 K rows of the two 64-wide column blocks.
+                            // int4 (scale, zero) words [group][weight row]: the groups that the
+                            // stage's 64 (K-major) or 128 (MN-major) weight columns fall in.
                             const uint32_t sS = sA + C::S_OFF;
                             if constexpr (B_MN) {
                                 tma_load_2d(sC, &p.maps[bmap], fb, brow / 2, kx);
-                                tma_load_2d(sS, &p.maps[smap], fb, kx, brow / 64);
+                                tma_load_2d(sS, &p.maps[smap], fb, kx, q4g ? brow / q4g : brow / 64);
                             } else {
                                 tma_load_2d(sC, &p.maps[bmap], fb, kx / 2, brow);
-                                tma_load_2d(sS, &p.maps[smap], fb, brow, kb);
+                                tma_load_2d(sS, &p.maps[smap], fb, brow, q4g ? kx / q4g : kb);
                             }
                         } else if constexpr (B_MN) {
                             tma_load_2d(sB, &p.maps[bmap], fb, brow, kx);
@@ -320,14 +365,41 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
 #pragma unroll
                 for (int j = 0; j < kPairNf4BlocksPerThread; ++j) {
                     const int t = t0 + 64 * j;
-                    const float amax = sS[t];
-                    if constexpr (B_MN) {
-                        // K row t & 63, 64-wide N chunk t >> 6: 32 code bytes of a 64-byte K row
-                        const uint4* src = reinterpret_cast<const uint4*>(sC + (t & 63) * 64 + (t >> 6) * 32);
-                        nf4_decode_block_regs(src[0], src[1], amax, sB + (t >> 6) * 8192 + (t & 63) * 128, t & 7);
+                    // MN-major: K row t & 63, 64-wide N chunk t >> 6 (32 code bytes of a 64-byte K
+                    // row); K-major: B row t
+                    const uint4* src = B_MN ? reinterpret_cast<const uint4*>(sC + (t & 63) * 64 + (t >> 6) * 32)
+                                            : reinterpret_cast<const uint4*>(sC + t * 32);
+                    const uint32_t dst = B_MN ? sB + (t >> 6) * 8192 + (t & 63) * 128 : sB + t * 128;
+                    uint32_t words[8];
+                    q4_words(src, words);
+                    q4_decode_chunks<0, 8>(nf4_tab(sS[t]), words, dst, t & 7);
+                }
+                fence_proxy_async_smem();
+            } else if (kind != 0) {
+                // int4: the (scale, zero) words of this stage, [group][row] as loaded; a block's
+                // first and second 32 elements share a word unless groups hold 32 elements
+                uint8_t* stg = smem + stage * C::STAGE_BYTES;
+                const uint32_t sB = smem_u32(stg + C::A_BYTES);
+                const uint8_t* sC = stg + C::A_BYTES + C::B_BYTES;
+                const uint32_t* sW = reinterpret_cast<const uint32_t*>(stg + C::S_OFF);
+                const int gsh = 31 - __clz(kind >> 8);  // log2 of the group size
+#pragma unroll
+                for (int j = 0; j < kPairNf4BlocksPerThread; ++j) {
+                    const int t = t0 + 64 * j;
+                    const uint4* src = B_MN ? reinterpret_cast<const uint4*>(sC + (t & 63) * 64 + (t >> 6) * 32)
+                                            : reinterpret_cast<const uint4*>(sC + t * 32);
+                    const uint32_t dst = B_MN ? sB + (t >> 6) * 8192 + (t & 63) * 128 : sB + t * 128;
+                    // MN-major: groups along the stage's 128 columns, 64 K rows each; K-major: one
+                    // group per row (two when groups hold 32 elements), 128 rows each
+                    const int lo = B_MN ? (((t >> 6) * 64) >> gsh) * 64 + (t & 63) : t;
+                    const int hi = B_MN ? (((t >> 6) * 64 + 32) >> gsh) * 64 + (t & 63) : (gsh == 5 ? 128 + t : t);
+                    uint32_t words[8];
+                    q4_words(src, words);
+                    if (gsh == 5) {
+                        q4_decode_chunks<0, 4>(int4_tab(sW[lo]), words, dst, t & 7);
+                        q4_decode_chunks<4, 8>(int4_tab(sW[hi]), words, dst, t & 7);
                     } else {
-                        const uint4* src = reinterpret_cast<const uint4*>(sC + t * 32);
-                        nf4_decode_block_regs(src[0], src[1], amax, sB + t * 128, t & 7);
+                        q4_decode_chunks<0, 8>(int4_tab(sW[lo]), words, dst, t & 7);
                     }
                 }
                 fence_proxy_async_smem();

@@ -103,5 +103,10 @@ cudaError_t pair_nf4_clusters(GemmKind k, int* n);
 cudaError_t launch_nf4_scale_table(const int8_t* absmax_q, const float* scale, int64_t rows, int64_t cols,
                                    float* table, cudaStream_t st);
 void nf4_codebook_host(float* out16);
+// int4 groupwise base: codes (rows * cols / 2 bytes) and (scale, zero) words sz[g * rows + row]
+cudaError_t launch_int4_pack(const uint16_t* W, int64_t rows, int64_t cols, int group, uint8_t* codes,
+                             uint32_t* sz, cudaStream_t st);
+cudaError_t launch_int4_dequant(const uint8_t* codes, const uint32_t* sz, int64_t rows, int64_t cols, int group,
+                                bool bf16_out, void* out, cudaStream_t st);
 
 }  // namespace lm

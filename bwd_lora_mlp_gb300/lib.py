@@ -25,7 +25,7 @@ LM_ERR_WORKSPACE, LM_ERR_CUDA, LM_ERR_TIMEOUT, LM_ERR_UNSUPPORTED = 6, 7, 8, 9
 STATUS_NAMES = {0: "LM_OK", 1: "LM_ERR_NULL", 2: "LM_ERR_SHAPE", 3: "LM_ERR_ALIGN", 4: "LM_ERR_DTYPE",
                 5: "LM_ERR_ALIAS", 6: "LM_ERR_WORKSPACE", 7: "LM_ERR_CUDA", 8: "LM_ERR_TIMEOUT",
                 9: "LM_ERR_UNSUPPORTED"}
-LM_WEIGHT_BF16, LM_WEIGHT_NF4 = 0, 1
+LM_WEIGHT_BF16, LM_WEIGHT_NF4, LM_WEIGHT_INT4 = 0, 1, 2
 LM_ACT_SWIGLU, LM_ACT_GEGLU_ERF = 0, 1
 LM_OUT_F32, LM_OUT_BF16 = 0, 1
 LM_AB_BF16, LM_AB_F32 = 0, 1
@@ -39,9 +39,9 @@ class LmError(RuntimeError):
 
 
 class lm_weight(ctypes.Structure):
-    _fields_ = [("kind", ctypes.c_int32), ("reserved", ctypes.c_int32), ("rows", ctypes.c_int64),
+    _fields_ = [("kind", ctypes.c_int32), ("group", ctypes.c_int32), ("rows", ctypes.c_int64),
                 ("cols", ctypes.c_int64), ("w", ctypes.c_void_p), ("codes", ctypes.c_void_p),
-                ("absmax_q", ctypes.c_void_p), ("group_scale", ctypes.c_void_p)]
+                ("absmax_q", ctypes.c_void_p), ("group_scale", ctypes.c_void_p), ("scale_zero", ctypes.c_void_p)]
 
 
 class lm_lora(ctypes.Structure):
@@ -86,6 +86,8 @@ _SIGS = {
     "lora_o_bwd_static": ([_I64, _I64, _I64, _P, _P, _P, _SZ, _LP, _P, _P, _P, _P], _I32),
     "nf4_pack": ([_P, _I64, _P, _P, _P, _P], _I32),
     "nf4_dequant": ([_P, _P, _P, _I64, _I32, _P, _P], _I32),
+    "int4_pack": ([_P, _I64, _I64, _I32, _P, _P, _P], _I32),
+    "int4_dequant": ([_P, _P, _I64, _I64, _I32, _I32, _P, _P], _I32),
 }
 
 _lib = None
@@ -165,8 +167,21 @@ class NF4Weight:
 
 
 @dataclass
+class Int4Weight:
+    """A groupwise int4 base weight (see int4_pack)."""
+    codes: torch.Tensor        # uint8, rows*cols/2
+    scale_zero: torch.Tensor   # bfloat16, (cols/group, rows, 2): scale, zero
+    rows: int
+    cols: int
+    group: int
+
+
+_PACKED = (NF4Weight, Int4Weight)
+
+
+@dataclass
 class Lora:
-    """One adapted projection: W (out, in) bf16 tensor or NF4Weight, A (r, in), B (out, r), s.
+    """One adapted projection: W (out, in) bf16 tensor, NF4Weight or Int4Weight, A (r, in), B (out, r), s.
 
     A and B are both bf16 or both fp32 (fp32 LoRA parameters; each call rounds them to bf16)."""
     W: object
@@ -186,6 +201,11 @@ class Lora:
             w.codes = _ptr(self.W.codes, torch.uint8, "codes")
             w.absmax_q = _ptr(self.W.absmax_q, torch.int8, "absmax_q")
             w.group_scale = _ptr(self.W.group_scale, torch.float32, "group_scale")
+        elif isinstance(self.W, Int4Weight):
+            w.kind = LM_WEIGHT_INT4
+            w.rows, w.cols, w.group = self.W.rows, self.W.cols, self.W.group
+            w.codes = _ptr(self.W.codes, torch.uint8, "codes")
+            w.scale_zero = _ptr(self.W.scale_zero, torch.bfloat16, "scale_zero")
         else:
             w.kind = LM_WEIGHT_BF16
             w.rows, w.cols = int(self.W.shape[0]), int(self.W.shape[1])
@@ -260,7 +280,7 @@ def lora_mlp_workspace_size(T: int, d: int, n: int, r: int) -> int:
 def lora_mlp_fwd(X, gate: Lora, up: Lora, down: Lora, act="swiglu", y=None, e=None, u=None, h=None,
                  saved=None, ws=None, stream=None) -> dict:
     T, d = X.shape
-    n = gate.W.rows if isinstance(gate.W, NF4Weight) else gate.W.shape[0]
+    n = gate.W.rows if isinstance(gate.W, _PACKED) else gate.W.shape[0]
     r = gate.r
     dev = X.device
     bf = torch.bfloat16
@@ -316,7 +336,7 @@ def lora_relu2_mlp_workspace_size(T: int, d: int, n: int, r: int) -> int:
 
 def lora_relu2_mlp_fwd(X, up: Lora, down: Lora, y=None, u=None, h=None, saved=None, ws=None, stream=None) -> dict:
     T, d = X.shape
-    n = up.W.rows if isinstance(up.W, NF4Weight) else up.W.shape[0]
+    n = up.W.rows if isinstance(up.W, _PACKED) else up.W.shape[0]
     r = up.r
     dev = X.device
     bf = torch.bfloat16
@@ -365,7 +385,7 @@ def lora_qkv_workspace_size(T, d, nq, nk, nv, r) -> int:
 
 
 def _rows(L: Lora) -> int:
-    return L.W.rows if isinstance(L.W, NF4Weight) else int(L.W.shape[0])
+    return L.W.rows if isinstance(L.W, _PACKED) else int(L.W.shape[0])
 
 
 def lora_qkv_fwd(X, q: Lora, k: Lora, v: Lora, out=None, saved=None, ws=None, stream=None) -> dict:
@@ -482,4 +502,22 @@ def nf4_dequant(w: NF4Weight, out_dtype=torch.float32, out=None, stream=None) ->
     _call("nf4_dequant", _ptr(w.codes, torch.uint8, "codes"), _ptr(w.absmax_q, torch.int8, "absmax_q"),
           _ptr(w.group_scale, torch.float32, "group_scale"), numel, code, _ptr(out, out_dtype, "out"),
           _stream(stream))
+    return out
+
+
+def int4_pack(W: torch.Tensor, group: int = 128, stream=None) -> Int4Weight:
+    rows, cols = int(W.shape[0]), int(W.shape[1])
+    dev = W.device
+    codes = torch.empty(rows * cols // 2, dtype=torch.uint8, device=dev)
+    sz = torch.empty((cols // group if group > 0 else 0, rows, 2), dtype=torch.bfloat16, device=dev)
+    _call("int4_pack", _ptr(W, torch.bfloat16, "W"), rows, cols, int(group), _ptr(codes, torch.uint8, "codes"),
+          _ptr(sz, torch.bfloat16, "scale_zero"), _stream(stream))
+    return Int4Weight(codes, sz, rows, cols, int(group))
+
+
+def int4_dequant(w: Int4Weight, out_dtype=torch.float32, out=None, stream=None) -> torch.Tensor:
+    code = LM_OUT_F32 if out_dtype == torch.float32 else LM_OUT_BF16
+    out = torch.empty((w.rows, w.cols), dtype=out_dtype, device=w.codes.device) if out is None else out
+    _call("int4_dequant", _ptr(w.codes, torch.uint8, "codes"), _ptr(w.scale_zero, torch.bfloat16, "scale_zero"),
+          w.rows, w.cols, w.group, code, _ptr(out, out_dtype, "out"), _stream(stream))
     return out

@@ -85,6 +85,7 @@ class Workload:
     act: str = "swiglu"  # mlp only: "swiglu" or "geglu"
     nf4: bool = False
     ab_f32: bool = False  # LoRA A, B passed as fp32 parameters
+    int4_group: int = 0   # > 0: groupwise int4 base with groups of this many elements
 
     @property
     def s(self) -> float:
@@ -134,6 +135,14 @@ WORKLOADS["relu2_mlp_8b_nf4"] = relu2_workload("relu2_mlp_8b_nf4", 8192, 4096, 1
 for _b in ("bf16", "nf4"):
     _w = mlp_workload("llama3_8b_mlp_%s_ab32" % _b, 8192, 4096, 14336, 16, 32.0, nf4=_b == "nf4")
     _w.ab_f32 = True
+    WORKLOADS[_w.name] = _w
+# groupwise int4 base: groups of 128 (the pages' example) and of 32 (the smallest offered)
+for _w in (mlp_workload("llama3_8b_mlp_int4", 8192, 4096, 14336, 16, 32.0),
+           mlp_workload("llama3_8b_mlp_int4_g32", 8192, 4096, 14336, 16, 32.0),
+           qkv_workload("llama3_8b_qkv_int4", 8192, 4096, 4096, 1024, 16, 32.0),
+           o_workload("llama3_8b_o_int4", 8192, 4096, 4096, 16, 32.0),
+           relu2_workload("relu2_mlp_8b_int4", 8192, 4096, 14336, 16, 32.0)):
+    _w.int4_group = 32 if _w.name.endswith("_g32") else 128
     WORKLOADS[_w.name] = _w
 
 

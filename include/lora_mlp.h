@@ -14,7 +14,9 @@
  *         matmul_lora; dY.B^T is formed once per projection and reused for dA and dX.
  *   [LL]  "loralei" README, QLoRA section: NF4 base weights with 64-element blocks and
  *         double-quantised block scales (256 blocks per scale), dimensions divisible by 32,
- *         unpacking and double-scale reconstruction fused into the matmul.
+ *         unpacking and double-scale reconstruction fused into the matmul; the alternative
+ *         groupwise int4 base (group sizes 32, 64, 128, 256), input gradients from the packed
+ *         weight.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -75,7 +77,7 @@ typedef enum lm_status {
     LM_ERR_UNSUPPORTED = 9  /* no device of compute capability 10.3, or a combination not built */
 } lm_status;
 
-typedef enum lm_weight_kind { LM_WEIGHT_BF16 = 0, LM_WEIGHT_NF4 = 1 } lm_weight_kind;
+typedef enum lm_weight_kind { LM_WEIGHT_BF16 = 0, LM_WEIGHT_NF4 = 1, LM_WEIGHT_INT4 = 2 } lm_weight_kind;
 typedef enum lm_act { LM_ACT_SWIGLU = 0, LM_ACT_GEGLU_ERF = 1 } lm_act;
 typedef enum lm_out_dtype { LM_OUT_F32 = 0, LM_OUT_BF16 = 1 } lm_out_dtype;
 typedef enum lm_ab_dtype { LM_AB_BF16 = 0, LM_AB_F32 = 1 } lm_ab_dtype;
@@ -85,16 +87,23 @@ typedef enum lm_ab_dtype { LM_AB_BF16 = 0, LM_AB_F32 = 1 } lm_ab_dtype;
  * of byte i), `absmax_q` rows*cols/64 int8 block scales and `group_scale` rows*cols/16384 fp32
  * scales, exactly as nf4_pack writes them; rows*cols must be a multiple of 16384 and cols a
  * multiple of 64.  Element (i, j) decodes to code[idx] * (absmax_q[b] * group_scale[b/256])
- * with b = (i*cols + j)/64, then rounds to bf16 for the matmul. */
+ * with b = (i*cols + j)/64, then rounds to bf16 for the matmul.
+ * kind == LM_WEIGHT_INT4 ([LL] "int4" groupwise base): `codes` as for NF4 and `scale_zero`
+ * 2*rows*cols/group bf16 values, [cols/group][rows][2] (the scale s then the zero z of group g of
+ * row i at index 2*(g*rows + i)), exactly as int4_pack writes them; `group` is 32, 64, 128 or 256
+ * and cols a multiple of 64 and of group.  Element (i, j) with code q decodes to
+ * fp32((q - 8) * s + z) of its group g = j / group, then rounds to bf16 for the matmul.
+ * Unused pointers of a kind are ignored; `group` is ignored unless kind == LM_WEIGHT_INT4. */
 typedef struct lm_weight {
     int32_t kind;
-    int32_t reserved;
+    int32_t group;             /* LM_WEIGHT_INT4: elements per quantisation group */
     int64_t rows;              /* out_features */
     int64_t cols;              /* in_features  */
     const uint16_t* w;
     const uint8_t* codes;
     const int8_t* absmax_q;
     const float* group_scale;
+    const uint16_t* scale_zero;
 } lm_weight;
 
 /* One adapted projection: base W, A (r x in), B (out x r), rank r and scale s.  A and B hold
@@ -254,6 +263,21 @@ LM_API lm_status nf4_pack(const uint16_t* W, int64_t numel, uint8_t* codes, int8
                    float* group_scale, lm_stream stream);
 LM_API lm_status nf4_dequant(const uint8_t* codes, const int8_t* absmax_q, const float* group_scale,
                       int64_t numel, int32_t out_dtype, void* out, lm_stream stream);
+
+/* ---- int4 groupwise base ([LL] QLoRA section: "int4", group sizes 32, 64, 128, 256) --------
+ * int4_pack: quantise a rows x cols bf16 weight W (row-major) in groups of `group` consecutive
+ * elements of a row (group 32, 64, 128 or 256; cols a multiple of group; else LM_ERR_SHAPE).
+ * Per group, with mn and mx its minimum and maximum: s = bf16(fp32((mx - mn) / 15)),
+ * z = bf16(fp32(mn + 8*s)); each element x gets q = clamp(rint(fp32(fp32(x - z) / s)) + 8, 0, 15)
+ * (rint: half to even; q = 8 for every element when s == 0).  Writes codes (rows*cols/2 bytes,
+ * element 2i in the high nibble of byte i) and scale_zero (2*rows*cols/group bf16 values,
+ * [cols/group][rows][2], s before z).  Bit-exact and deterministic.
+ * int4_dequant: w = fp32((q - 8) * s + z) (one rounding: the product is exact), written as fp32
+ * (LM_OUT_F32) or rounded to nearest-even bf16 (LM_OUT_BF16); rows*cols values, row-major. */
+LM_API lm_status int4_pack(const uint16_t* W, int64_t rows, int64_t cols, int32_t group, uint8_t* codes,
+                           uint16_t* scale_zero, lm_stream stream);
+LM_API lm_status int4_dequant(const uint8_t* codes, const uint16_t* scale_zero, int64_t rows, int64_t cols,
+                              int32_t group, int32_t out_dtype, void* out, lm_stream stream);
 
 #ifdef __cplusplus
 }

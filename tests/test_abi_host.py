@@ -19,7 +19,7 @@ def so():
 
 def test_exports_every_header_symbol(so):
     names = L.header_symbols()
-    assert len(names) == 26
+    assert len(names) == 28
     for n in names:
         assert hasattr(so, n), n
     assert set(names) == set(L._SIGS)
@@ -147,6 +147,42 @@ def test_nf4_argument_errors(so):
     assert L.call_status("nf4_pack", W, 0, c, q, s, None) == L.LM_OK
     assert L.call_status("nf4_dequant", c, q, s, 16384, 9, f(65536), None) == L.LM_ERR_DTYPE
     assert L.call_status("nf4_dequant", c, q, s, 16384, L.LM_OUT_F32, c, None) == L.LM_ERR_ALIAS
+
+
+def test_int4_argument_errors(so):
+    f = Fake()
+    W, c, sz = f(256 * 512 * 2), f(256 * 256), f(256 * 512 // 32 * 4)
+    assert L.call_status("int4_pack", W, 256, 512, 16, c, sz, None) == L.LM_ERR_SHAPE      # group
+    assert L.call_status("int4_pack", W, 256, 96, 64, c, sz, None) == L.LM_ERR_SHAPE       # cols % group
+    assert L.call_status("int4_pack", W, 256, 512, 32, None, sz, None) == L.LM_ERR_NULL
+    assert L.call_status("int4_pack", W, 256, 512, 32, c, W + 64, None) == L.LM_ERR_ALIAS
+    assert L.call_status("int4_pack", W, 0, 512, 128, c, sz, None) == L.LM_OK
+    assert L.call_status("int4_dequant", c, sz, 256, 512, 32, 9, f(1 << 20), None) == L.LM_ERR_DTYPE
+    assert L.call_status("int4_dequant", c, sz, 256, 512, 32, L.LM_OUT_F32, sz, None) == L.LM_ERR_ALIAS
+
+
+def _int4(a, t, group):
+    w = a[t].W
+    w.kind, w.group = L.LM_WEIGHT_INT4, group
+    w.codes = w.w
+    w.scale_zero = w.w + (1 << 24)
+
+
+def test_int4_weight_validation(so):
+    # every case fails validation on the host, before any device call
+    b = _mlp_args()
+    for t in ("gate", "up", "down"):
+        _int4(b, t, 64)
+    b["up"].W.group = 48
+    assert _fwd(b) == L.LM_ERR_SHAPE and "up.W.group" in L.last_error()
+    c = _mlp_args()
+    for t in ("gate", "up", "down"):
+        _int4(c, t, 128)
+    c["gate"].W.scale_zero = None
+    assert _fwd(c) == L.LM_ERR_NULL and "gate.W.scale_zero" in L.last_error()
+    m = _mlp_args()
+    _int4(m, "gate", 128)
+    assert _fwd(m) == L.LM_ERR_UNSUPPORTED                                   # kinds mixed in one call
 
 
 def test_profile_summary_empty_without_launches(so):

@@ -1,4 +1,5 @@
-"""Parity at the full workload sizes, in the launch configuration the benchmark times.
+"""Parity at the full workload sizes (bf16, NF4 and int4 bases), in the launch configuration the
+benchmark times.
 
 The oracle cannot run a full-size backward in seconds, so it is checked where it can be
 computed exactly and cheaply:
@@ -18,6 +19,7 @@ import torch
 from bwd_lora_mlp_gb300 import lib as L
 from bwd_lora_mlp_gb300 import synth
 from oracle import lora as O
+from oracle import int4 as oi4
 from oracle import nf4 as onf4
 
 from gpu_util import check, dev_bf16, host64
@@ -27,21 +29,25 @@ pytestmark = pytest.mark.gpu
 _cache = {}
 
 
-def _base64(bits, nf4):
-    if not nf4:
+def _base64(bits, w):
+    if w.int4_group:
+        x = synth.bf16_bits_to_f32(bits).reshape(bits.shape)
+        codes, s, z, _ = oi4.quantize(x, w.int4_group)
+        return oi4.dequantize_bf16(codes, s, z, bits.shape[0], bits.shape[1], w.int4_group).astype(np.float64)
+    if not w.nf4:
         return O.from_bf16(bits)
     x = synth.bf16_bits_to_f32(bits).reshape(-1)
     return onf4.dequantize_bf16(*onf4.quantize(x)).astype(np.float64).reshape(bits.shape)
 
 
 def _inputs(w):
-    key = (tuple((p.d_in, p.d_out) for p in w.projs), w.T, w.r, w.nf4)
+    key = (tuple((p.d_in, p.d_out) for p in w.projs), w.T, w.r, w.nf4, w.int4_group)
     if key not in _cache:
         _cache.clear()
         inp = synth.make_inputs(w)
         p = {}
         for t, k in zip([q.name for q in w.projs], ["g", "u", "d"] if w.kind == "mlp" else [q.name for q in w.projs]):
-            p["W" + k] = _base64(inp["W_" + t], w.nf4)
+            p["W" + k] = _base64(inp["W_" + t], w)
             p["A" + k] = O.from_bf16(inp["A_" + t])
             p["B" + k] = O.from_bf16(inp["B_" + t])
             p["s" + k] = w.s
@@ -53,6 +59,8 @@ def _dev_lora(inp, t, w):
     W = dev_bf16(inp["W_" + t])
     if w.nf4:
         W = L.nf4_pack(W)
+    elif w.int4_group:
+        W = L.int4_pack(W, w.int4_group)
     return L.Lora(W, dev_bf16(inp["A_" + t]), dev_bf16(inp["B_" + t]), w.s)
 
 
@@ -61,7 +69,8 @@ def _rows(T, k=24, seed=0):
     return np.unique(np.concatenate([[0, T - 1], rng.integers(0, T, k)]))
 
 
-MLP = ["llama3_8b_mlp_bf16", "llama3_8b_mlp_nf4", "llama3_70b_mlp_nf4_swiglu", "llama3_70b_mlp_nf4_geglu"]
+MLP = ["llama3_8b_mlp_bf16", "llama3_8b_mlp_nf4", "llama3_70b_mlp_nf4_swiglu", "llama3_70b_mlp_nf4_geglu",
+       "llama3_8b_mlp_int4"]
 
 
 @pytest.mark.parametrize("name", MLP)
@@ -93,9 +102,9 @@ def test_full_size_mlp(name):
         assert abs(a - b) <= 1e-2 * max(abs(a), abs(b)), (t, a, b)
 
 
-@pytest.mark.parametrize("nf4", [False, True], ids=["bf16", "nf4"])
-def test_full_size_qkv_and_o(nf4):
-    w = synth.WORKLOADS["llama3_8b_qkv_nf4" if nf4 else "llama3_8b_qkv_bf16"]
+@pytest.mark.parametrize("base", ["bf16", "nf4", "int4"])
+def test_full_size_qkv_and_o(base):
+    w = synth.WORKLOADS["llama3_8b_qkv_" + base]
     inp, p = _inputs(w)
     Ls = {t: _dev_lora(inp, t, w) for t in ("q", "k", "v")}
     X = dev_bf16(inp["X"])
@@ -117,7 +126,7 @@ def test_full_size_qkv_and_o(nf4):
         check("dA_" + t, host64(bw["dA_" + t]), g["dA"])
         check("dB_" + t, host64(bw["dB_" + t]), g["dB"])
 
-    wo = synth.WORKLOADS["llama3_8b_o_nf4" if nf4 else "llama3_8b_o_bf16"]
+    wo = synth.WORKLOADS["llama3_8b_o_" + base]
     io, po = _inputs(wo)
     o = _dev_lora(io, "o", wo)
     Xd, dYd = dev_bf16(io["X"]), dev_bf16(io["dY"])
