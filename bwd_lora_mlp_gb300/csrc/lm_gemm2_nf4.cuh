@@ -1,6 +1,9 @@
-// The CTA-pair GEMM of lm_gemm2.cuh with an NF4-packed frozen B operand decoded in the mainloop
+// The CTA-pair GEMM of lm_gemm2.cuh with a 4-bit packed frozen B operand decoded in the mainloop
 // ("loralei" README, QLoRA section: unpacking and double-scale reconstruction fused into the
-// matmul).
+// matmul; the same section's groupwise int4 base).  The two formats differ only in the 16-entry
+// table a 64-element block is decoded with: NF4 code_i * amax', or int4 (i - 8) * s + z with the
+// bf16 scale and zero of the block's group (two tables per block for groups of 32), and in the
+// scales a stage carries (see the producer).
 //
 // A work unit is a 512 x 256 tile: per 64-deep K block each CTA of the pair holds 2 x 128 A rows
 // (one set per M half) and half of the 256-wide B tile, and CTA 0 issues two M = 256 pair MMAs
@@ -24,8 +27,9 @@
 // Roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer (CTA 0), warps 2-9 decoders in
 // kPairNf4DecodeGroups groups that take K blocks round-robin (with two groups of four warps, two K
 // blocks are decoded at once and each thread decodes one NF4 block of each), warps 10-17
-// epilogue.  The producer tags every stage for the decoders (bf16, NF4, or end of work), so they
-// follow the stage ring without walking the work-unit sequence themselves.
+// epilogue.  The producer tags every stage for the decoders (bf16, NF4, int4 with its group size,
+// or end of work), so they follow the stage ring without walking the work-unit sequence
+// themselves.
 #pragma once
 
 #include "lm_gemm2.cuh"
