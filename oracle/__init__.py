@@ -13,11 +13,13 @@ Sources (web pages the method is described on):
     (unsloth fast_lora diff): the backward of LoRA_MLP, LoRA_QKV, LoRA_W and
     matmul_lora, with the dY.B^T hoist.
   * "loralei" README, QLoRA section: NF4 base weights, block 64, scaler block 256,
-    double-scale reconstruction.
+    double-scale reconstruction; the groupwise int4 base (groups 32 to 256).
+  * "LoRA Optimizations", FP32 LoRA gradients: weight-only NVFP4 bases (E2M1 codes, E4M3
+    scales per 16 elements, one fp32 scale per tensor).
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test against
 something other than itself (finite differences, closed forms, the merge
-identity, NF4 invariants, the published NF4 table, int4 grid round trips and
-nearest-level checks, the adapter parameter count
-printed on the "LoRA Optimizations" page).  No function is "parity unpinned".
+identity, NF4 invariants, the published NF4 table, int4 and NVFP4 grid round
+trips and nearest-level checks, E4M3 against PyTorch's float8 conversion, the
+adapter parameter count printed on the "LoRA Optimizations" page).  No function is "parity unpinned".
 """
