@@ -320,6 +320,8 @@ def main():
             W = L.nf4_pack(W)
         elif w.int4_group:
             W = L.int4_pack(W, w.int4_group)
+        elif w.nvfp4:
+            W = L.nvfp4_pack(W)
         if ab32 is not None:
             return L.Lora(W, torch.from_numpy(ab32["A_" + t]).cuda(), torch.from_numpy(ab32["B_" + t]).cuda(), w.s)
         return L.Lora(W, dev(inp["A_" + t]), dev(inp["B_" + t]), w.s)
@@ -476,7 +478,7 @@ def main():
         cpu = cpu_baseline(w, inp)
 
     d_in, d_out = w.projs[0].d_in, w.projs[-1].d_out
-    cfg = {"workload": w.name, "T": T, "r": r, "alpha": w.alpha, "base": "nf4" if w.nf4 else ("int4_g%d" % w.int4_group if w.int4_group else "bf16"), "lora_params": "fp32" if w.ab_f32 else "bf16"}
+    cfg = {"workload": w.name, "T": T, "r": r, "alpha": w.alpha, "base": "nf4" if w.nf4 else ("int4_g%d" % w.int4_group if w.int4_group else ("nvfp4" if w.nvfp4 else "bf16")), "lora_params": "fp32" if w.ab_f32 else "bf16"}
     if w.kind in ("mlp", "relu2"):
         cfg.update(d=d_in, n=w.projs[0].d_out, act=w.act)
     else:

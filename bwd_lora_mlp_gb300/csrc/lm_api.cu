@@ -135,6 +135,13 @@ lm_status need_ptr(const void* p, const char* name) {
     return LM_OK;
 }
 
+// a scalar the kernels read with a plain load (no TMA): 4-byte alignment
+lm_status need_ptr4(const void* p, const char* name) {
+    if (!p) return fail(LM_ERR_NULL, "%s is NULL", name);
+    if (reinterpret_cast<uintptr_t>(p) % 4 != 0) return fail(LM_ERR_ALIGN, "%s is not 4-byte aligned", name);
+    return LM_OK;
+}
+
 lm_status check_dim(int64_t v, const char* name) {
     if (v <= 0 || v % 32 != 0 || v > (int64_t(1) << 20))
         return fail(LM_ERR_SHAPE, "%s = %lld must be a positive multiple of 32 (at most 2^20)", name, (long long)v);
@@ -181,6 +188,14 @@ lm_status check_lora(const lm_lora* L, const char* name, int64_t in, int64_t out
         LM_TRY(need_ptr(L->W.codes, buf));
         snprintf(buf, sizeof buf, "%s.W.scale_zero", name);
         LM_TRY(need_ptr(L->W.scale_zero, buf));
+    } else if (L->W.kind == LM_WEIGHT_NVFP4) {
+        if (L->W.cols % 64 != 0) return fail(LM_ERR_SHAPE, "%s: an NVFP4 weight needs cols %% 64 == 0", name);
+        snprintf(buf, sizeof buf, "%s.W.codes", name);
+        LM_TRY(need_ptr(L->W.codes, buf));
+        snprintf(buf, sizeof buf, "%s.W.block_scale", name);
+        LM_TRY(need_ptr(L->W.block_scale, buf));
+        snprintf(buf, sizeof buf, "%s.W.global_scale", name);
+        LM_TRY(need_ptr4(L->W.global_scale, buf));
     } else {
         return fail(LM_ERR_DTYPE, "%s.W.kind = %d is not a known weight kind", name, L->W.kind);
     }
@@ -227,7 +242,7 @@ Span wspan(const lm_lora* L, const char* name) {
 }
 
 // every projection of one call must use the same kind of base weight
-// (*q4: a packed 4-bit base, NF4 or int4, decoded inside the GEMM mainloop)
+// (*q4: a packed 4-bit base, NF4, int4 or NVFP4, decoded inside the GEMM mainloop)
 lm_status same_kind(std::initializer_list<const lm_lora*> Ls, bool* q4) {
     const lm_lora* first = *Ls.begin();
     for (const lm_lora* L : Ls)
@@ -473,7 +488,8 @@ struct Builder {
     // fp32 block-scale table of an NF4 weight ([cols / 64][rows], see launch_nf4_scale_table):
     // box 128 rows x 1 K block (weight read K-major) or 64 rows x 2 column blocks (MN-major);
     // rows outside the weight read 0
-    // An int4 weight instead maps its (scale, zero) words ([cols / G][rows] 32-bit words): box
+    // An NVFP4 weight maps its E4M3 block scales the same way (four per 32-bit word); an int4
+    // weight instead maps its (scale, zero) words ([cols / G][rows] 32-bit words): box
     // 128 rows x (G == 32 ? 2 : 1) groups (K-major: the groups of one 64-wide K block) or 64 rows x
     // max(1, 128 / G) groups (MN-major: the groups of 128 columns).
     int scales(const float* table, const lm_weight& W, bool mn) {
@@ -481,6 +497,26 @@ struct Builder {
         if (nmaps >= kMaxMaps) {
             st = fail(LM_ERR_UNSUPPORTED, "too many tensor maps in one launch");
             return 0;
+        }
+        if (W.kind == LM_WEIGHT_NVFP4) {  // E4M3 scales, four per word: [cols / 64][rows] words
+            cuuint64_t dims[2] = {(cuuint64_t)W.rows, (cuuint64_t)(W.cols / 64)};
+            cuuint64_t strides[1] = {(cuuint64_t)W.rows * 4};
+            cuuint32_t box[2] = {mn ? 64u : 128u, mn ? 2u : 1u};
+            cuuint32_t es[2] = {1u, 1u};
+            const CUresult r = g_encode(&p.maps[nmaps], CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
+                                        const_cast<uint8_t*>(W.block_scale), dims, strides, box, es,
+                                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) {
+                st = fail(LM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for NVFP4 scales %lld x %lld", (int)r,
+                          (long long)W.rows, (long long)(W.cols / 64));
+                return 0;
+            }
+            p.map_bytes[nmaps] = 512u;
+            p.map_w[nmaps] = (int32_t)W.rows;
+            p.map_group[nmaps] = -1;
+            p.map_gscale[nmaps] = W.global_scale;
+            return nmaps++;
         }
         if (W.kind == LM_WEIGHT_INT4) {
             const int G = W.group;
@@ -912,7 +948,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     LM_TRY(need_ptr(saved, "saved"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = gate->r;
-    const bool q4 = gate->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
+    const bool q4 = gate->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4, int4 or NVFP4)
     const MlpPlan PL = plan_mlp(T, d, n, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1101,7 +1137,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     LM_TRY(need_ptr(dB_down, "dB_down"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = gate->r;
-    const bool q4 = gate->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
+    const bool q4 = gate->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4, int4 or NVFP4)
     const MlpPlan PL = plan_mlp(T, d, n, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1396,7 +1432,7 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
     LM_TRY(need_ptr(saved, "saved"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = up->r;
-    const bool q4 = up->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
+    const bool q4 = up->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4, int4 or NVFP4)
     const Relu2Plan PL = plan_relu2(T, d, n, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1520,7 +1556,7 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
     LM_TRY(need_ptr(dB_down, "dB_down"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = up->r;
-    const bool q4 = up->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
+    const bool q4 = up->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4, int4 or NVFP4)
     const Relu2Plan PL = plan_relu2(T, d, n, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1706,7 +1742,7 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     LM_TRY(need_ptr(saved, "saved"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = q->r;
-    const bool q4 = q->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
+    const bool q4 = q->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4, int4 or NVFP4)
     const QkvPlan PL = plan_qkv(T, d, nq, nk, nv, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -1827,7 +1863,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     LM_TRY(need_ptr(dB_v, "dB_v"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = q->r;
-    const bool q4 = q->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
+    const bool q4 = q->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4, int4 or NVFP4)
     const QkvPlan PL = plan_qkv(T, d, nq, nk, nv, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -2003,7 +2039,7 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(need_ptr(saved, "saved"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = o->r;
-    const bool q4 = o->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
+    const bool q4 = o->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4, int4 or NVFP4)
     const OPlan PL = plan_o(T, d_in, d_out, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -2093,7 +2129,7 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(need_ptr(dB, "dB"));
     LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = o->r;
-    const bool q4 = o->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4 or int4)
+    const bool q4 = o->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4, int4 or NVFP4)
     const OPlan PL = plan_o(T, d_in, d_out, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
@@ -2279,5 +2315,52 @@ extern "C" lm_status int4_dequant(const uint8_t* codes, const uint16_t* scale_ze
     const cudaError_t e = launch_int4_dequant(codes, reinterpret_cast<const uint32_t*>(scale_zero), rows, cols, group,
                                               out_dtype == LM_OUT_BF16, out, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "int4_dequant launch");
+    return LM_OK;
+}
+
+// ====================================================================== NVFP4
+extern "C" lm_status nvfp4_pack(const uint16_t* W, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* block_scale,
+                                float* global_scale, lm_stream stream) {
+    if (rows < 0 || cols < 0 || cols % 64 != 0 || rows > (int64_t(1) << 24) || cols > (int64_t(1) << 24))
+        return fail(LM_ERR_SHAPE, "an NVFP4 weight of %lld x %lld needs cols a multiple of 64", (long long)rows,
+                    (long long)cols);
+    LM_TRY(need_ptr(W, "W"));
+    LM_TRY(need_ptr(codes, "codes"));
+    LM_TRY(need_ptr(block_scale, "block_scale"));
+    LM_TRY(need_ptr4(global_scale, "global_scale"));
+    const int64_t numel = rows * cols;
+    LM_TRY(check_alias({{codes, (size_t)numel / 2, "codes"}, {block_scale, (size_t)numel / 16, "block_scale"},
+                        {global_scale, 4, "global_scale"}},
+                       {{W, (size_t)numel * 2, "W"}}));
+    if (numel == 0) return LM_OK;
+    int sms = 0;
+    LM_TRY(device_sms(&sms));
+    const cudaError_t e = launch_nvfp4_pack(W, rows, cols, codes, block_scale, global_scale, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "nvfp4_pack launch");
+    return LM_OK;
+}
+
+extern "C" lm_status nvfp4_dequant(const uint8_t* codes, const uint8_t* block_scale, const float* global_scale,
+                                   int64_t rows, int64_t cols, int32_t out_dtype, void* out, lm_stream stream) {
+    if (rows < 0 || cols < 0 || cols % 64 != 0 || rows > (int64_t(1) << 24) || cols > (int64_t(1) << 24))
+        return fail(LM_ERR_SHAPE, "an NVFP4 weight of %lld x %lld needs cols a multiple of 64", (long long)rows,
+                    (long long)cols);
+    if (out_dtype != LM_OUT_F32 && out_dtype != LM_OUT_BF16)
+        return fail(LM_ERR_DTYPE, "out_dtype = %d is not known", out_dtype);
+    LM_TRY(need_ptr(codes, "codes"));
+    LM_TRY(need_ptr(block_scale, "block_scale"));
+    LM_TRY(need_ptr4(global_scale, "global_scale"));
+    LM_TRY(need_ptr(out, "out"));
+    const int64_t numel = rows * cols;
+    const size_t ob = (size_t)numel * (out_dtype == LM_OUT_F32 ? 4 : 2);
+    LM_TRY(check_alias({{out, ob, "out"}}, {{codes, (size_t)numel / 2, "codes"},
+                                            {block_scale, (size_t)numel / 16, "block_scale"},
+                                            {global_scale, 4, "global_scale"}}));
+    if (numel == 0) return LM_OK;
+    int sms = 0;
+    LM_TRY(device_sms(&sms));
+    const cudaError_t e = launch_nvfp4_dequant(codes, block_scale, global_scale, rows, cols,
+                                               out_dtype == LM_OUT_BF16, out, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "nvfp4_dequant launch");
     return LM_OK;
 }

@@ -493,4 +493,153 @@ cudaError_t launch_int4_dequant(const uint8_t* codes, const uint32_t* sz, int64_
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ NVFP4 weight-only base
+// E2M1 codes (element 2i in the low nibble of byte i), one E4M3 scale per 16 elements of a row
+// stored as sf[((col / 64) * rows + row) * 4 + (col % 64) / 16], and one fp32 tensor scale
+// S_g = amax / (6 * 448) (1 when that is 0).  Per block: s_b = E4M3(fp32(fp32(bmax / 6) / S_g)),
+// nearest, ties to even, saturated at 448; per element: code = E2M1(fp32(x / fp32(s_b * S_g))),
+// nearest, ties to even, saturated at 6, sign of x (all codes 0 when s_b * S_g == 0).
+
+// value of an E4M3 byte (finite encodings; exact)
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+    const float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
+    return (b & 0x80u) ? -mag : mag;
+}
+
+// nearest E4M3 byte of d >= 0, ties to even, saturated at 448 (byte 126)
+__device__ __forceinline__ uint32_t f32_to_e4m3_sat(float d) {
+    if (!(d < 448.0f)) return 126u;
+    if (d < 0.015625f) return (uint32_t)rintf(d * 512.0f);  // subnormal steps of 2^-9 (8 -> 2^-6)
+    uint32_t u = __float_as_uint(d);
+    u += 0x7FFFFu + ((u >> 20) & 1u);                        // round the mantissa to 3 bits, even
+    return min((u >> 20) - 960u, 126u);                      // rebias the exponent from 127 to 7
+}
+
+// nearest E2M1 code of y, ties to even, saturated at 6, sign bit of y
+__device__ __forceinline__ uint32_t f32_to_e2m1_sat(float y) {
+    const float a = fabsf(y);
+    const uint32_t i = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+    return i | (signbit(y) ? 8u : 0u);
+}
+
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+    const float mag = e ? __uint_as_float(((e + 126u) << 23) | (m << 22)) : (m ? 0.5f : 0.0f);
+    return (c & 8u) ? -mag : mag;
+}
+
+__device__ __forceinline__ float nvfp4_tensor_scale(float amax) {
+    const float sg = __fdiv_rn(amax, 2688.0f);
+    return sg > 0.0f ? sg : 1.0f;
+}
+
+__global__ void __launch_bounds__(256) nvfp4_amax_kernel(const uint4* __restrict__ W, int64_t n8,
+                                                         uint32_t* __restrict__ amax_bits) {
+    float m = 0.0f;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 v = __ldg(W + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[k])), fabsf(bf16hi(w[k]))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));  // non-negative: bits order as values
+}
+
+// one thread per 16-element block
+__global__ void __launch_bounds__(256) nvfp4_pack_kernel(const uint16_t* __restrict__ W, int64_t rows, int64_t cols,
+                                                         const uint32_t* __restrict__ amax_bits,
+                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+    const float sg = nvfp4_tensor_scale(__uint_as_float(__ldg(amax_bits)));
+    const int64_t nbr = cols / 16, n = rows * nbr;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / nbr, b = i - row * nbr;
+        const uint4* src = reinterpret_cast<const uint4*>(W + row * cols + b * 16);
+        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        float bmax = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) bmax = fmaxf(bmax, fmaxf(fabsf(bf16lo(w[k])), fabsf(bf16hi(w[k]))));
+        const uint32_t sb = f32_to_e4m3_sat(__fdiv_rn(__fdiv_rn(bmax, 6.0f), sg));
+        const float S = __fmul_rn(e4m3_to_f32(sb), sg);
+        uint32_t packed[2] = {0u, 0u};
+        if (S > 0.0f) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float x = (e & 1) ? bf16hi(w[e >> 1]) : bf16lo(w[e >> 1]);
+                const uint32_t c = f32_to_e2m1_sat(__fdiv_rn(x, S));
+                packed[e >> 3] |= c << (4 * (e & 7));  // element 2i low nibble of byte i
+            }
+        }
+        *reinterpret_cast<uint2*>(codes + (row * cols + b * 16) / 2) = make_uint2(packed[0], packed[1]);
+        sf[((b >> 2) * rows + row) * 4 + (b & 3)] = (uint8_t)sb;
+    }
+}
+
+__global__ void nvfp4_scale_kernel(float* gs) {
+    *gs = nvfp4_tensor_scale(__uint_as_float(*reinterpret_cast<const uint32_t*>(gs)));
+}
+
+cudaError_t launch_nvfp4_pack(const uint16_t* W, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* sf, float* gs,
+                              cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(gs, 0, sizeof(float), st);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t n8 = rows * cols / 8, nb = rows * cols / 16;
+    uint32_t* amax_bits = reinterpret_cast<uint32_t*>(gs);  // holds the tensor amax until the last launch
+    nvfp4_amax_kernel<<<(unsigned)std::min<int64_t>((n8 + 255) / 256, (int64_t)sms * 8), 256, 0, st>>>(
+        reinterpret_cast<const uint4*>(W), n8, amax_bits);
+    nvfp4_pack_kernel<<<(unsigned)std::min<int64_t>((nb + 255) / 256, (int64_t)sms * 8), 256, 0, st>>>(
+        W, rows, cols, amax_bits, codes, sf);
+    nvfp4_scale_kernel<<<1, 1, 0, st>>>(gs);
+    return cudaGetLastError();
+}
+
+// Each thread decodes 8 elements (4 code bytes): w = fp32(e2m1 * fp32(s_b * S_g)).
+__global__ void __launch_bounds__(256) nvfp4_dequant_kernel(const uint32_t* __restrict__ codes,
+                                                            const uint8_t* __restrict__ sf,
+                                                            const float* __restrict__ gs, int64_t rows,
+                                                            int64_t cols, int bf16_out, void* out) {
+    const float sg = __ldg(gs);
+    const int64_t n8 = rows * cols / 8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t e0 = i * 8, row = e0 / cols, col = e0 - row * cols;
+        const float S = __fmul_rn(e4m3_to_f32(__ldg(sf + ((col >> 6) * rows + row) * 4 + ((col & 63) >> 4))), sg);
+        const uint32_t c8 = __ldg(codes + i);
+        float w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = __fmul_rn(e2m1_to_f32((c8 >> (4 * k)) & 15u), S);
+        if (bf16_out) {
+            uint4 v;
+            v.x = pack_bf16x2(w[0], w[1]);
+            v.y = pack_bf16x2(w[2], w[3]);
+            v.z = pack_bf16x2(w[4], w[5]);
+            v.w = pack_bf16x2(w[6], w[7]);
+            reinterpret_cast<uint4*>(out)[i] = v;
+        } else {
+            float4* o = reinterpret_cast<float4*>(out) + 2 * i;
+            o[0] = make_float4(w[0], w[1], w[2], w[3]);
+            o[1] = make_float4(w[4], w[5], w[6], w[7]);
+        }
+    }
+}
+
+cudaError_t launch_nvfp4_dequant(const uint8_t* codes, const uint8_t* sf, const float* gs, int64_t rows, int64_t cols,
+                                 bool bf16_out, void* out, cudaStream_t st) {
+    const int64_t n8 = rows * cols / 8;
+    if (n8 == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, (int64_t)sms * 8);
+    nvfp4_dequant_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(codes), sf, gs, rows,
+                                                            cols, bf16_out ? 1 : 0, out);
+    return cudaGetLastError();
+}
+
 }  // namespace lm

@@ -83,7 +83,9 @@ struct Params {  // CUtensorMap members carry their own 128-byte alignment
     uint32_t map_bytes[kMaxMaps];   // bytes one box of the map delivers
     int32_t map_w[kMaxMaps];        // inner (K or MN) extent of the map, elements
     int32_t map_group[kMaxMaps];    // scale map of a packed 4-bit weight: 0 NF4 block scales,
-                                    // G > 0 int4 (scale, zero) words of groups of G elements
+                                    // G > 0 int4 (scale, zero) words of groups of G elements,
+                                    // -1 NVFP4 E4M3 block scales (four per 32-bit word)
+    const float* map_gscale[kMaxMaps];  // NVFP4 scale map: the weight's fp32 tensor scale (device)
     Prob prob[kMaxProbs];
     float nf4_code[16];             // the NF4 values (NF4 kernel only)
     int32_t nprob;

@@ -146,6 +146,47 @@ __device__ __forceinline__ void q4_words(const uint4* src, uint32_t (&w)[8]) {
     w[4] = c1.x; w[5] = c1.y; w[6] = c1.z; w[7] = c1.w;
 }
 
+// Two E4M3 bytes (low byte first) -> their values as f16x2 (exact: every E4M3 value is an f16)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    uint32_t d;
+    asm("{\n .reg .b16 h;\n mov.b32 {h, _}, %1;\n cvt.rn.f16x2.e4m3x2 %0, h;\n}" : "=r"(d) : "r"(two));
+    return d;
+}
+
+// Four bytes of E2M1 code pairs (element 2i in the low nibble) -> four f16x2 (exact)
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
+__device__ __forceinline__ float f16lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))); }
+__device__ __forceinline__ float f16hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+
+// Decode one 64-element NVFP4 span (8 code words, word j = elements 8j..8j+7; E4M3 scales of its
+// four 16-element blocks in the bytes of sc4) with tensor scale gs into a 128-byte row of the
+// swizzled B tile: w = bf16(fp32(e2m1 * fp32(s_b * gs))).
+__device__ __forceinline__ void nvfp4_decode_block(const uint32_t (&words)[8], uint32_t sc4, float gs,
+                                                   uint32_t dst_row, int swz) {
+    const uint32_t s01 = e4m3x2_to_f16x2(sc4), s23 = e4m3x2_to_f16x2(sc4 >> 16);
+    const float S[4] = {__fmul_rn(f16lo(s01), gs), __fmul_rn(f16hi(s01), gs), __fmul_rn(f16lo(s23), gs),
+                        __fmul_rn(f16hi(s23), gs)};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t h[4], o[4];
+        e2m1x8_to_f16x2(words[j], h);
+        const float Sj = S[j >> 1];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[k] = pack_bf16x2(__fmul_rn(f16lo(h[k]), Sj), __fmul_rn(f16hi(h[k]), Sj));
+        const uint32_t addr = dst_row + ((uint32_t)(j ^ swz) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o[0]), "r"(o[1]), "r"(o[2]),
+                     "r"(o[3])
+                     : "memory");
+    }
+}
+
 template <bool B_MN, int EPI>
 __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __grid_constant__ Params p) {
     using C = Gemm2Nf4Cfg;
@@ -162,6 +203,8 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
     // what each stage holds, written by this CTA's producer before the stage's loads: 0 bf16 B
     // (nothing to decode), 1 NF4 codes, 2 no more K blocks (one such stage per decode group)
     volatile int32_t* stage_kind = reinterpret_cast<volatile int32_t*>(tmem_slot + 2);
+    // fp32 tensor scale of each NVFP4 scale map, read once at launch
+    float* s_gscale = const_cast<float*>(reinterpret_cast<volatile float*>(stage_kind + C::STAGES));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -184,6 +227,10 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
         fence_mbar_init();
         for (int i = 0; i < kMaxMaps; ++i)
             if (p.map_bytes[i]) tma_prefetch_map(&p.maps[i]);
+    }
+    if (threadIdx.x >= 32 && threadIdx.x < 32 + kMaxMaps) {  // published by the cluster barrier below
+        const int i = threadIdx.x - 32;
+        s_gscale[i] = p.map_gscale[i] ? __ldg(p.map_gscale[i]) : 0.0f;
     }
     __syncwarp();
     if (warp == 0) {
@@ -215,9 +262,10 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     const bool nf4 = S.b_scale[0] >= 0;
                     const int bmap = (rank == 1 && S.b_map[1] >= 0) ? S.b_map[1] : S.b_map[0];
                     const int smap = (rank == 1 && S.b_scale[1] >= 0) ? S.b_scale[1] : S.b_scale[0];
-                    // int4 group size (0: NF4); the decoders read it from the stage tag
+                    // int4 group size (0: NF4, -1: NVFP4); the decoders read the format, and the
+                    // int4 group size or the NVFP4 scale map, from the stage tag
                     const int q4g = nf4 ? p.map_group[smap] : 0;
-                    const int32_t tag = !nf4 ? 0 : (q4g ? (3 | (q4g << 8)) : 1);
+                    const int32_t tag = !nf4 ? 0 : q4g > 0 ? (3 | (q4g << 8)) : q4g < 0 ? (4 | (smap << 8)) : 1;
                     const int brow = U.nb * P.n_step + (int)rank * S.b_rank_off;
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) {
@@ -235,17 +283,18 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                         tma_load_2d(sA, &p.maps[S.a_map], fb, kx + S.a_xoff, U.mb * 512 + (int)rank * kBM);
                         tma_load_2d(sA + 16384, &p.maps[S.a_map], fb, kx + S.a_xoff, U.mb * 512 + 256 + (int)rank * kBM);
                         if (nf4) {
-                            // NF4 scale table [K block][weight row]: K-major, the 128 rows of
-                            // this K block; MN-major, 64 K rows of the two 64-wide column blocks.
-                            // int4 (scale, zero) words [group][weight row]: the groups that the
-                            // stage's 64 (K-major) or 128 (MN-major) weight columns fall in.
+                            // NF4 scale table / NVFP4 scale words [64-column span][weight row]:
+                            // K-major, the 128 rows of this K block; MN-major, 64 K rows of the
+                            // two 64-wide column spans.  int4 (scale, zero) words [group][weight
+                            // row]: the groups that the stage's 64 (K-major) or 128 (MN-major)
+                            // weight columns fall in.
                             const uint32_t sS = sA + C::S_OFF;
                             if constexpr (B_MN) {
                                 tma_load_2d(sC, &p.maps[bmap], fb, brow / 2, kx);
-                                tma_load_2d(sS, &p.maps[smap], fb, kx, q4g ? brow / q4g : brow / 64);
+                                tma_load_2d(sS, &p.maps[smap], fb, kx, q4g > 0 ? brow / q4g : brow / 64);
                             } else {
                                 tma_load_2d(sC, &p.maps[bmap], fb, kx / 2, brow);
-                                tma_load_2d(sS, &p.maps[smap], fb, brow, q4g ? kx / q4g : kb);
+                                tma_load_2d(sS, &p.maps[smap], fb, brow, q4g > 0 ? kx / q4g : kb);
                             }
                         } else if constexpr (B_MN) {
                             tma_load_2d(sB, &p.maps[bmap], fb, brow, kx);
@@ -379,7 +428,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     q4_decode_chunks<0, 8>(nf4_tab(sS[t]), words, dst, t & 7);
                 }
                 fence_proxy_async_smem();
-            } else if (kind != 0) {
+            } else if ((kind & 0xFF) == 3) {
                 // int4: the (scale, zero) words of this stage, [group][row] as loaded; a block's
                 // first and second 32 elements share a word unless groups hold 32 elements
                 uint8_t* stg = smem + stage * C::STAGE_BYTES;
@@ -405,6 +454,25 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     } else {
                         q4_decode_chunks<0, 8>(int4_tab(sW[lo]), words, dst, t & 7);
                     }
+                }
+                fence_proxy_async_smem();
+            } else if ((kind & 0xFF) == 4) {
+                // NVFP4: block t's four E4M3 scales (one per 16 elements) sit in word t in both
+                // layouts, as the NF4 block scales do
+                uint8_t* stg = smem + stage * C::STAGE_BYTES;
+                const uint32_t sB = smem_u32(stg + C::A_BYTES);
+                const uint8_t* sC = stg + C::A_BYTES + C::B_BYTES;
+                const uint32_t* sW = reinterpret_cast<const uint32_t*>(stg + C::S_OFF);
+                const float gs = s_gscale[kind >> 8];
+#pragma unroll
+                for (int j = 0; j < kPairNf4BlocksPerThread; ++j) {
+                    const int t = t0 + 64 * j;
+                    const uint4* src = B_MN ? reinterpret_cast<const uint4*>(sC + (t & 63) * 64 + (t >> 6) * 32)
+                                            : reinterpret_cast<const uint4*>(sC + t * 32);
+                    const uint32_t dst = B_MN ? sB + (t >> 6) * 8192 + (t & 63) * 128 : sB + t * 128;
+                    uint32_t words[8];
+                    q4_words(src, words);
+                    nvfp4_decode_block(words, sW[t], gs, dst, t & 7);
                 }
                 fence_proxy_async_smem();
             }

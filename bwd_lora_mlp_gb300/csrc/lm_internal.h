@@ -108,5 +108,11 @@ cudaError_t launch_int4_pack(const uint16_t* W, int64_t rows, int64_t cols, int 
                              uint32_t* sz, cudaStream_t st);
 cudaError_t launch_int4_dequant(const uint8_t* codes, const uint32_t* sz, int64_t rows, int64_t cols, int group,
                                 bool bf16_out, void* out, cudaStream_t st);
+// NVFP4 weight-only base: codes (rows * cols / 2 bytes), E4M3 block scales sf (rows * cols / 16
+// bytes, [cols / 64][rows][4]) and the fp32 tensor scale *gs (device)
+cudaError_t launch_nvfp4_pack(const uint16_t* W, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* sf, float* gs,
+                              cudaStream_t st);
+cudaError_t launch_nvfp4_dequant(const uint8_t* codes, const uint8_t* sf, const float* gs, int64_t rows, int64_t cols,
+                                 bool bf16_out, void* out, cudaStream_t st);
 
 }  // namespace lm

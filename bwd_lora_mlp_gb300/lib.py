@@ -25,7 +25,7 @@ LM_ERR_WORKSPACE, LM_ERR_CUDA, LM_ERR_TIMEOUT, LM_ERR_UNSUPPORTED = 6, 7, 8, 9
 STATUS_NAMES = {0: "LM_OK", 1: "LM_ERR_NULL", 2: "LM_ERR_SHAPE", 3: "LM_ERR_ALIGN", 4: "LM_ERR_DTYPE",
                 5: "LM_ERR_ALIAS", 6: "LM_ERR_WORKSPACE", 7: "LM_ERR_CUDA", 8: "LM_ERR_TIMEOUT",
                 9: "LM_ERR_UNSUPPORTED"}
-LM_WEIGHT_BF16, LM_WEIGHT_NF4, LM_WEIGHT_INT4 = 0, 1, 2
+LM_WEIGHT_BF16, LM_WEIGHT_NF4, LM_WEIGHT_INT4, LM_WEIGHT_NVFP4 = 0, 1, 2, 3
 LM_ACT_SWIGLU, LM_ACT_GEGLU_ERF = 0, 1
 LM_OUT_F32, LM_OUT_BF16 = 0, 1
 LM_AB_BF16, LM_AB_F32 = 0, 1
@@ -41,7 +41,8 @@ class LmError(RuntimeError):
 class lm_weight(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("group", ctypes.c_int32), ("rows", ctypes.c_int64),
                 ("cols", ctypes.c_int64), ("w", ctypes.c_void_p), ("codes", ctypes.c_void_p),
-                ("absmax_q", ctypes.c_void_p), ("group_scale", ctypes.c_void_p), ("scale_zero", ctypes.c_void_p)]
+                ("absmax_q", ctypes.c_void_p), ("group_scale", ctypes.c_void_p), ("scale_zero", ctypes.c_void_p),
+                ("block_scale", ctypes.c_void_p), ("global_scale", ctypes.c_void_p)]
 
 
 class lm_lora(ctypes.Structure):
@@ -88,6 +89,8 @@ _SIGS = {
     "nf4_dequant": ([_P, _P, _P, _I64, _I32, _P, _P], _I32),
     "int4_pack": ([_P, _I64, _I64, _I32, _P, _P, _P], _I32),
     "int4_dequant": ([_P, _P, _I64, _I64, _I32, _I32, _P, _P], _I32),
+    "nvfp4_pack": ([_P, _I64, _I64, _P, _P, _P, _P], _I32),
+    "nvfp4_dequant": ([_P, _P, _P, _I64, _I64, _I32, _P, _P], _I32),
 }
 
 _lib = None
@@ -176,12 +179,23 @@ class Int4Weight:
     group: int
 
 
-_PACKED = (NF4Weight, Int4Weight)
+@dataclass
+class NVFP4Weight:
+    """An NVFP4 weight-only base (see nvfp4_pack)."""
+    codes: torch.Tensor         # uint8, rows*cols/2 (E2M1, element 2i in the low nibble)
+    block_scale: torch.Tensor   # uint8 E4M3, (cols/64, rows, 4)
+    global_scale: torch.Tensor  # float32, (1,)
+    rows: int
+    cols: int
+
+
+_PACKED = (NF4Weight, Int4Weight, NVFP4Weight)
 
 
 @dataclass
 class Lora:
-    """One adapted projection: W (out, in) bf16 tensor, NF4Weight or Int4Weight, A (r, in), B (out, r), s.
+    """One adapted projection: W (out, in) bf16 tensor, NF4Weight, Int4Weight or NVFP4Weight, A (r, in),
+    B (out, r), s.
 
     A and B are both bf16 or both fp32 (fp32 LoRA parameters; each call rounds them to bf16)."""
     W: object
@@ -206,6 +220,12 @@ class Lora:
             w.rows, w.cols, w.group = self.W.rows, self.W.cols, self.W.group
             w.codes = _ptr(self.W.codes, torch.uint8, "codes")
             w.scale_zero = _ptr(self.W.scale_zero, torch.bfloat16, "scale_zero")
+        elif isinstance(self.W, NVFP4Weight):
+            w.kind = LM_WEIGHT_NVFP4
+            w.rows, w.cols = self.W.rows, self.W.cols
+            w.codes = _ptr(self.W.codes, torch.uint8, "codes")
+            w.block_scale = _ptr(self.W.block_scale, torch.uint8, "block_scale")
+            w.global_scale = _ptr(self.W.global_scale, torch.float32, "global_scale")
         else:
             w.kind = LM_WEIGHT_BF16
             w.rows, w.cols = int(self.W.shape[0]), int(self.W.shape[1])
@@ -520,4 +540,24 @@ def int4_dequant(w: Int4Weight, out_dtype=torch.float32, out=None, stream=None) 
     out = torch.empty((w.rows, w.cols), dtype=out_dtype, device=w.codes.device) if out is None else out
     _call("int4_dequant", _ptr(w.codes, torch.uint8, "codes"), _ptr(w.scale_zero, torch.bfloat16, "scale_zero"),
           w.rows, w.cols, w.group, code, _ptr(out, out_dtype, "out"), _stream(stream))
+    return out
+
+
+def nvfp4_pack(W: torch.Tensor, stream=None) -> NVFP4Weight:
+    rows, cols = int(W.shape[0]), int(W.shape[1])
+    dev = W.device
+    codes = torch.empty(rows * cols // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty((cols // 64, rows, 4), dtype=torch.uint8, device=dev)
+    gs = torch.empty(1, dtype=torch.float32, device=dev)
+    _call("nvfp4_pack", _ptr(W, torch.bfloat16, "W"), rows, cols, _ptr(codes, torch.uint8, "codes"),
+          _ptr(sf, torch.uint8, "block_scale"), _ptr(gs, torch.float32, "global_scale"), _stream(stream))
+    return NVFP4Weight(codes, sf, gs, rows, cols)
+
+
+def nvfp4_dequant(w: NVFP4Weight, out_dtype=torch.float32, out=None, stream=None) -> torch.Tensor:
+    code = LM_OUT_F32 if out_dtype == torch.float32 else LM_OUT_BF16
+    out = torch.empty((w.rows, w.cols), dtype=out_dtype, device=w.codes.device) if out is None else out
+    _call("nvfp4_dequant", _ptr(w.codes, torch.uint8, "codes"), _ptr(w.block_scale, torch.uint8, "block_scale"),
+          _ptr(w.global_scale, torch.float32, "global_scale"), w.rows, w.cols, code, _ptr(out, out_dtype, "out"),
+          _stream(stream))
     return out

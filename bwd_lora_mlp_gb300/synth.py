@@ -86,6 +86,7 @@ class Workload:
     nf4: bool = False
     ab_f32: bool = False  # LoRA A, B passed as fp32 parameters
     int4_group: int = 0   # > 0: groupwise int4 base with groups of this many elements
+    nvfp4: bool = False   # NVFP4 weight-only base
 
     @property
     def s(self) -> float:
@@ -143,6 +144,13 @@ for _w in (mlp_workload("llama3_8b_mlp_int4", 8192, 4096, 14336, 16, 32.0),
            o_workload("llama3_8b_o_int4", 8192, 4096, 4096, 16, 32.0),
            relu2_workload("relu2_mlp_8b_int4", 8192, 4096, 14336, 16, 32.0)):
     _w.int4_group = 32 if _w.name.endswith("_g32") else 128
+    WORKLOADS[_w.name] = _w
+# NVFP4 weight-only base
+for _w in (mlp_workload("llama3_8b_mlp_nvfp4", 8192, 4096, 14336, 16, 32.0),
+           qkv_workload("llama3_8b_qkv_nvfp4", 8192, 4096, 4096, 1024, 16, 32.0),
+           o_workload("llama3_8b_o_nvfp4", 8192, 4096, 4096, 16, 32.0),
+           relu2_workload("relu2_mlp_8b_nvfp4", 8192, 4096, 14336, 16, 32.0)):
+    _w.nvfp4 = True
     WORKLOADS[_w.name] = _w
 
 

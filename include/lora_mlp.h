@@ -77,7 +77,12 @@ typedef enum lm_status {
     LM_ERR_UNSUPPORTED = 9  /* no device of compute capability 10.3, or a combination not built */
 } lm_status;
 
-typedef enum lm_weight_kind { LM_WEIGHT_BF16 = 0, LM_WEIGHT_NF4 = 1, LM_WEIGHT_INT4 = 2 } lm_weight_kind;
+typedef enum lm_weight_kind {
+    LM_WEIGHT_BF16 = 0,
+    LM_WEIGHT_NF4 = 1,
+    LM_WEIGHT_INT4 = 2,
+    LM_WEIGHT_NVFP4 = 3
+} lm_weight_kind;
 typedef enum lm_act { LM_ACT_SWIGLU = 0, LM_ACT_GEGLU_ERF = 1 } lm_act;
 typedef enum lm_out_dtype { LM_OUT_F32 = 0, LM_OUT_BF16 = 1 } lm_out_dtype;
 typedef enum lm_ab_dtype { LM_AB_BF16 = 0, LM_AB_F32 = 1 } lm_ab_dtype;
@@ -93,6 +98,13 @@ typedef enum lm_ab_dtype { LM_AB_BF16 = 0, LM_AB_F32 = 1 } lm_ab_dtype;
  * row i at index 2*(g*rows + i)), exactly as int4_pack writes them; `group` is 32, 64, 128 or 256
  * and cols a multiple of 64 and of group.  Element (i, j) with code q decodes to
  * fp32((q - 8) * s + z) of its group g = j / group, then rounds to bf16 for the matmul.
+ * kind == LM_WEIGHT_NVFP4 ([LO] FP32 LoRA gradients: weight-only NVFP4 bases; activations stay
+ * bf16): `codes` rows*cols/2 bytes of E2M1 codes (element 2i in the LOW nibble of byte i),
+ * `block_scale` rows*cols/16 E4M3 bytes, [cols/64][rows][4] (the scale of elements
+ * [16k, 16k+16) of row i at index ((k/4)*rows + i)*4 + k%4), and `global_scale` one fp32 value
+ * on the device (4-byte aligned), exactly as nvfp4_pack writes them; cols a multiple of 64.
+ * Element (i, j) decodes to fp32(e2m1(code) * fp32(s_b * global_scale)) with s_b the E4M3 scale
+ * of its 16-element block, then rounds to bf16 for the matmul.
  * Unused pointers of a kind are ignored; `group` is ignored unless kind == LM_WEIGHT_INT4. */
 typedef struct lm_weight {
     int32_t kind;
@@ -104,6 +116,8 @@ typedef struct lm_weight {
     const int8_t* absmax_q;
     const float* group_scale;
     const uint16_t* scale_zero;
+    const uint8_t* block_scale;
+    const float* global_scale;
 } lm_weight;
 
 /* One adapted projection: base W, A (r x in), B (out x r), rank r and scale s.  A and B hold
@@ -278,6 +292,22 @@ LM_API lm_status int4_pack(const uint16_t* W, int64_t rows, int64_t cols, int32_
                            uint16_t* scale_zero, lm_stream stream);
 LM_API lm_status int4_dequant(const uint8_t* codes, const uint16_t* scale_zero, int64_t rows, int64_t cols,
                               int32_t group, int32_t out_dtype, void* out, lm_stream stream);
+
+/* ---- NVFP4 weight-only base ([LO] FP32 LoRA gradients) --------------------------------------
+ * nvfp4_pack: quantise a rows x cols bf16 weight W (row-major; cols a multiple of 64, else
+ * LM_ERR_SHAPE) to NVFP4 with two-level scaling.  global_scale (one fp32 on the device, 4-byte
+ * aligned) = S_g = fp32(amax / 2688), amax = max |W| (S_g = 1 when that is 0); per 16-element
+ * block of a row, with bmax its max |x|: s_b = E4M3(fp32(fp32(bmax / 6) / S_g)) (nearest, ties to
+ * even, saturated at 448); each element x gets code = E2M1(fp32(x / fp32(s_b * S_g))) (nearest,
+ * ties to even, saturated at 6; the sign bit is the sign of x; every code of the block is 0 when
+ * s_b * S_g == 0).  Writes codes, block_scale and global_scale in the layout of lm_weight above.
+ * Bit-exact and deterministic; three launches (tensor maximum, blocks, tensor scale).
+ * nvfp4_dequant: w = fp32(e2m1(code) * fp32(s_b * S_g)), written as fp32 (LM_OUT_F32) or rounded
+ * to nearest-even bf16 (LM_OUT_BF16); rows*cols values, row-major. */
+LM_API lm_status nvfp4_pack(const uint16_t* W, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* block_scale,
+                            float* global_scale, lm_stream stream);
+LM_API lm_status nvfp4_dequant(const uint8_t* codes, const uint8_t* block_scale, const float* global_scale,
+                               int64_t rows, int64_t cols, int32_t out_dtype, void* out, lm_stream stream);
 
 #ifdef __cplusplus
 }

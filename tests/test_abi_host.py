@@ -19,7 +19,7 @@ def so():
 
 def test_exports_every_header_symbol(so):
     names = L.header_symbols()
-    assert len(names) == 28
+    assert len(names) == 30
     for n in names:
         assert hasattr(so, n), n
     assert set(names) == set(L._SIGS)
@@ -159,6 +159,30 @@ def test_int4_argument_errors(so):
     assert L.call_status("int4_pack", W, 0, 512, 128, c, sz, None) == L.LM_OK
     assert L.call_status("int4_dequant", c, sz, 256, 512, 32, 9, f(1 << 20), None) == L.LM_ERR_DTYPE
     assert L.call_status("int4_dequant", c, sz, 256, 512, 32, L.LM_OUT_F32, sz, None) == L.LM_ERR_ALIAS
+
+
+def test_nvfp4_argument_errors(so):
+    f = Fake()
+    W, c, sf, gs = f(256 * 512 * 2), f(256 * 256), f(256 * 512 // 16), f(64)
+    assert L.call_status("nvfp4_pack", W, 256, 96, c, sf, gs, None) == L.LM_ERR_SHAPE        # cols % 64
+    assert L.call_status("nvfp4_pack", W, 256, 512, c, None, gs, None) == L.LM_ERR_NULL
+    assert L.call_status("nvfp4_pack", W, 256, 512, c, sf, gs + 2, None) == L.LM_ERR_ALIGN
+    assert L.call_status("nvfp4_pack", W, 256, 512, c, sf, W + 64, None) == L.LM_ERR_ALIAS
+    assert L.call_status("nvfp4_pack", W, 0, 512, c, sf, gs, None) == L.LM_OK
+    assert L.call_status("nvfp4_dequant", c, sf, gs, 256, 512, 9, f(1 << 20), None) == L.LM_ERR_DTYPE
+    assert L.call_status("nvfp4_dequant", c, sf, gs, 256, 512, L.LM_OUT_F32, c, None) == L.LM_ERR_ALIAS
+
+
+def test_nvfp4_weight_validation(so):
+    a = _mlp_args()
+    for t in ("gate", "up", "down"):
+        w = a[t].W
+        w.kind, w.codes, w.block_scale, w.global_scale = L.LM_WEIGHT_NVFP4, w.w, w.w + (1 << 24), w.w + (1 << 25)
+    a["down"].W.block_scale = None
+    assert _fwd(a) == L.LM_ERR_NULL and "down.W.block_scale" in L.last_error()
+    a["down"].W.block_scale = a["down"].W.w + (1 << 24)
+    a["up"].W.global_scale += 1                                              # a float needs 4-byte alignment
+    assert _fwd(a) == L.LM_ERR_ALIGN and "up.W.global_scale" in L.last_error()
 
 
 def _int4(a, t, group):

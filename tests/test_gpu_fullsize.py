@@ -1,4 +1,4 @@
-"""Parity at the full workload sizes (bf16, NF4 and int4 bases), in the launch configuration the
+"""Parity at the full workload sizes (bf16, NF4, int4 and NVFP4 bases), in the launch configuration the
 benchmark times.
 
 The oracle cannot run a full-size backward in seconds, so it is checked where it can be
@@ -21,6 +21,7 @@ from bwd_lora_mlp_gb300 import synth
 from oracle import lora as O
 from oracle import int4 as oi4
 from oracle import nf4 as onf4
+from oracle import nvfp4 as onv
 
 from gpu_util import check, dev_bf16, host64
 
@@ -34,6 +35,10 @@ def _base64(bits, w):
         x = synth.bf16_bits_to_f32(bits).reshape(bits.shape)
         codes, s, z, _ = oi4.quantize(x, w.int4_group)
         return oi4.dequantize_bf16(codes, s, z, bits.shape[0], bits.shape[1], w.int4_group).astype(np.float64)
+    if w.nvfp4:
+        x = synth.bf16_bits_to_f32(bits).reshape(bits.shape)
+        codes, sb, sg, _ = onv.quantize(x)
+        return onv.dequantize_bf16(codes, sb, sg, bits.shape[0], bits.shape[1]).astype(np.float64)
     if not w.nf4:
         return O.from_bf16(bits)
     x = synth.bf16_bits_to_f32(bits).reshape(-1)
@@ -41,7 +46,7 @@ def _base64(bits, w):
 
 
 def _inputs(w):
-    key = (tuple((p.d_in, p.d_out) for p in w.projs), w.T, w.r, w.nf4, w.int4_group)
+    key = (tuple((p.d_in, p.d_out) for p in w.projs), w.T, w.r, w.nf4, w.int4_group, w.nvfp4)
     if key not in _cache:
         _cache.clear()
         inp = synth.make_inputs(w)
@@ -61,6 +66,8 @@ def _dev_lora(inp, t, w):
         W = L.nf4_pack(W)
     elif w.int4_group:
         W = L.int4_pack(W, w.int4_group)
+    elif w.nvfp4:
+        W = L.nvfp4_pack(W)
     return L.Lora(W, dev_bf16(inp["A_" + t]), dev_bf16(inp["B_" + t]), w.s)
 
 
@@ -70,7 +77,7 @@ def _rows(T, k=24, seed=0):
 
 
 MLP = ["llama3_8b_mlp_bf16", "llama3_8b_mlp_nf4", "llama3_70b_mlp_nf4_swiglu", "llama3_70b_mlp_nf4_geglu",
-       "llama3_8b_mlp_int4"]
+       "llama3_8b_mlp_int4", "llama3_8b_mlp_nvfp4"]
 
 
 @pytest.mark.parametrize("name", MLP)
@@ -102,7 +109,7 @@ def test_full_size_mlp(name):
         assert abs(a - b) <= 1e-2 * max(abs(a), abs(b)), (t, a, b)
 
 
-@pytest.mark.parametrize("base", ["bf16", "nf4", "int4"])
+@pytest.mark.parametrize("base", ["bf16", "nf4", "int4", "nvfp4"])
 def test_full_size_qkv_and_o(base):
     w = synth.WORKLOADS["llama3_8b_qkv_" + base]
     inp, p = _inputs(w)
