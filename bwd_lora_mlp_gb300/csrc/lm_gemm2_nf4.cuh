@@ -98,18 +98,6 @@ __device__ __forceinline__ Q4Tab nf4_tab(float amax) {
     return q4_tab(T);
 }
 
-// int4 group with the (scale, zero) word sz (bf16 s in the low half, bf16 z in the high half):
-// code q -> bf16(fp32((q - 8) * s + z)); (q - 8) * s is exact, so the fused multiply-add rounds
-// once, as the separate product and sum would.
-__device__ __forceinline__ Q4Tab int4_tab(uint32_t sz) {
-    const float s = __uint_as_float(sz << 16), z = __uint_as_float(sz & 0xFFFF0000u);
-    uint32_t T[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        T[i] = pack_bf16x2(__fmaf_rn((float)(2 * i - 8), s, z), __fmaf_rn((float)(2 * i - 7), s, z));
-    return q4_tab(T);
-}
-
 // Decode the 16-byte output chunks J0..J1-1 (8 elements each, from code word j) of one 64-element
 // block into a 128-byte row of the swizzled B tile at dst_row (chunk j stored at chunk j ^ swz).
 // Code words hold element 2i in the high nibble of byte i.
@@ -144,6 +132,40 @@ __device__ __forceinline__ void q4_words(const uint4* src, uint32_t (&w)[8]) {
     const uint4 c0 = src[0], c1 = src[1];
     w[0] = c0.x; w[1] = c0.y; w[2] = c0.z; w[3] = c0.w;
     w[4] = c1.x; w[5] = c1.y; w[6] = c1.z; w[7] = c1.w;
+}
+
+// Decode one 64-element int4 block (8 code words, element 2i in the high nibble of byte i) into a
+// 128-byte row of the swizzled B tile: w = bf16(fp32((q - 8) * s + z)), with (s, z) of word sz[0]
+// for the first 32 elements and of sz[1] for the rest.  The nibbles become f16 values 1024 + q by
+// OR-ing them into the mantissa of 1024 (two per instruction), an f16 subtraction of 1032 gives
+// q - 8 exactly, and an fp32 fused multiply-add rounds (q - 8) * s + z once -- the arithmetic
+// runs on the FMA pipe instead of a chain of byte permutes on the integer pipe.
+__device__ __forceinline__ void int4_decode_block(const uint32_t (&words)[8], const uint32_t (&sz)[2],
+                                                  uint32_t dst_row, int swz) {
+    const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6408u),
+                                        __ushort_as_half((unsigned short)0x6408u));  // 1032
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t wd = sz[j >> 2];
+        const float s = __uint_as_float(wd << 16), z = __uint_as_float(wd & 0xFFFF0000u);
+        const uint32_t w = words[j];
+        // p_i holds nibbles i (low half) and i + 4 (high half); nibble 2k is element 2k + 1 and
+        // nibble 2k + 1 is element 2k of the word
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t m = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+            const float2 f = __half22float2(__hsub2(*reinterpret_cast<const __half2*>(&m), bias));
+            const int e = (i & 1) ? i - 1 : i + 1;  // element of nibble i
+            v[e] = __fmaf_rn(f.x, s, z);
+            v[e + 4] = __fmaf_rn(f.y, s, z);
+        }
+        const uint32_t o0 = pack_bf16x2(v[0], v[1]), o1 = pack_bf16x2(v[2], v[3]);
+        const uint32_t o2 = pack_bf16x2(v[4], v[5]), o3 = pack_bf16x2(v[6], v[7]);
+        const uint32_t addr = dst_row + ((uint32_t)(j ^ swz) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o0), "r"(o1), "r"(o2), "r"(o3)
+                     : "memory");
+    }
 }
 
 // Two E4M3 bytes (low byte first) -> their values as f16x2 (exact: every E4M3 value is an f16)
@@ -448,12 +470,8 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     const int hi = B_MN ? (((t >> 6) * 64 + 32) >> gsh) * 64 + (t & 63) : (gsh == 5 ? 128 + t : t);
                     uint32_t words[8];
                     q4_words(src, words);
-                    if (gsh == 5) {
-                        q4_decode_chunks<0, 4>(int4_tab(sW[lo]), words, dst, t & 7);
-                        q4_decode_chunks<4, 8>(int4_tab(sW[hi]), words, dst, t & 7);
-                    } else {
-                        q4_decode_chunks<0, 8>(int4_tab(sW[lo]), words, dst, t & 7);
-                    }
+                    const uint32_t sz[2] = {sW[lo], sW[hi]};
+                    int4_decode_block(words, sz, dst, t & 7);
                 }
                 fence_proxy_async_smem();
             } else if ((kind & 0xFF) == 4) {
