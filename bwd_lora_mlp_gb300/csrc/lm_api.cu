@@ -402,12 +402,21 @@ OPlan plan_o(int64_t T, int64_t d_in, int64_t d_out, int32_t r) {
     return P;
 }
 
-// fp32 block-scale table of an NF4 weight for the NF4 GEMMs (traced under `tag`)
-// (an int4 weight needs none: its (scale, zero) words are read where they are)
-lm_status scale_table(const char* tag, const lm_weight& W, float* table, cudaStream_t st) {
-    if (W.kind != LM_WEIGHT_NF4) return LM_OK;
+// fp32 block-scale tables of the NF4 weights among `ws` for the NF4 GEMMs, one launch (traced
+// under `tag`); int4 and NVFP4 weights need none: their scales are read where they are
+struct ScaleTable {
+    const lm_weight* W;
+    float* table;
+};
+lm_status scale_tables(const char* tag, std::initializer_list<ScaleTable> ws, cudaStream_t st) {
+    Nf4ScaleJobs jobs{};
+    int nj = 0;
+    for (const ScaleTable& t : ws)
+        if (t.W->kind == LM_WEIGHT_NF4)
+            jobs.j[nj++] = Nf4ScaleJob{t.W->absmax_q, t.W->group_scale, t.W->rows, t.W->cols / 64, t.table};
+    if (nj == 0) return LM_OK;
     ProfScope prof(tag, st);
-    const cudaError_t e = launch_nf4_scale_table(W.absmax_q, W.group_scale, W.rows, W.cols, table, st);
+    const cudaError_t e = launch_nf4_scale_tables(jobs, nj, st);
     return e == cudaSuccess ? LM_OK : cuda_fail(e, "NF4 scale table launch");
 }
 
@@ -485,7 +494,7 @@ struct Builder {
     // codes map of an NF4 weight read MN-major (input gradient: box 64 bytes = 128 elements x 64 rows)
     int codes_mn(const lm_weight& W) { return map_u8(W.codes, W.rows, W.cols / 2, W.cols / 2, 64, 64); }
 
-    // fp32 block-scale table of an NF4 weight ([cols / 64][rows], see launch_nf4_scale_table):
+    // fp32 block-scale table of an NF4 weight ([cols / 64][rows], see launch_nf4_scale_tables):
     // box 128 rows x 1 K block (weight read K-major) or 64 rows x 2 column blocks (MN-major);
     // rows outside the weight read 0
     // An NVFP4 weight maps its E4M3 block scales the same way (four per 32-bit word); an int4
@@ -553,6 +562,26 @@ struct Builder {
         p.map_bytes[nmaps] = 512u;
         p.map_w[nmaps] = (int32_t)W.rows;
         return nmaps++;
+    }
+
+    // The base-weight operand of a segment of the 512 x 256 pair GEMM: a bf16 W loaded as it is
+    // (K-major box 64 x 128 rows, MN-major 64 x 64), a packed W as its codes plus scales (`table`:
+    // the per-call NF4 block-scale table; unused for the other formats).
+    void base_k(Seg& S, const lm_weight& W, const float* table) {
+        if (W.kind == LM_WEIGHT_BF16) {
+            S.b_map[0] = map(W.w, W.rows, W.cols, W.cols, 128);
+        } else {
+            S.b_map[0] = codes_k(W, 128);
+            S.b_scale[0] = scales(table, W, false);
+        }
+    }
+    void base_mn(Seg& S, const lm_weight& W, const float* table) {
+        if (W.kind == LM_WEIGHT_BF16) {
+            S.b_map[0] = map(W.w, W.rows, W.cols, W.cols, 64);
+        } else {
+            S.b_map[0] = codes_mn(W);
+            S.b_scale[0] = scales(table, W, true);
+        }
     }
 
     // 2D bf16 tensor (rows x cols, row stride ld elements), box = 64 columns x box_rows rows
@@ -975,9 +1004,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     down = &down_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
     if (q4) {  // the NF4 GEMMs read per-K-block fp32 block scales of W_gate, W_up, W_down
-        LM_TRY(scale_table("mlp.nf4s", gate->W, sc[0], st));
-        LM_TRY(scale_table("mlp.nf4s", up->W, sc[1], st));
-        LM_TRY(scale_table("mlp.nf4s", down->W, sc[2], st));
+        LM_TRY(scale_tables("mlp.nf4s", {{&gate->W, sc[0]}, {&up->W, sc[1]}, {&down->W, sc[2]}}, st));
     }
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
     uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
@@ -1065,7 +1092,9 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(b.launch("mlp.ha", sms, err, st));
         LM_TRY(fin_rows("mlp.ha.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, ha, haT, D.ldT}}, T, st));
     }
-    if (q4) {
+    {  // y = h Wd^T + (s_d h Ad^T) Bd^T on 512 x 256 tiles for every base (a bf16 W is loaded as
+       // is, a packed one decoded); with its light plain-store epilogue the single accumulator
+       // costs less than the 256 x 256 kernel's extra operand traffic
         Builder b(G2N_STORE_K);
         b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
@@ -1077,30 +1106,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         P.out_col_step = 256;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(h_save, T, n, n, 128);
-        S0.b_map[0] = b.codes_k(down->W, 128);
-        S0.b_scale[0] = b.scales(sc[2], down->W, false);
-        S0.b_rank_off = 128;
-        S0.kext = (int32_t)n;
-        Seg& S1 = seg(P, 1);
-        S1.a_map = b.map(ha, T, rp, rp, 128);
-        S1.b_map[0] = b.map(down->B, d, r, r, 128);
-        S1.b_rank_off = 128;
-        S1.kext = rp;
-        P.out0 = y;
-        P.ld_out = d;
-        LM_TRY(b.launch("mlp.down", sms, err, st));
-    } else {  // y = h Wd^T + (s_d h Ad^T) Bd^T
-        Builder b(G2_STORE_K);
-        Prob& P = b.prob();
-        P.M = (int32_t)T;
-        P.N = (int32_t)d;
-        P.bn = 256;
-        P.tiles_n = (int32_t)((d + 255) / 256);
-        P.n_step = 256;
-        P.out_col_step = 256;
-        Seg& S0 = seg(P, 0);
-        S0.a_map = b.map(h_save, T, n, n, 128);
-        S0.b_map[0] = b.map(down->W.w, d, n, n, 128);
+        b.base_k(S0, down->W, sc[2]);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)n;
         Seg& S1 = seg(P, 1);
@@ -1175,9 +1181,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     down = &down_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
     if (q4) {
-        LM_TRY(scale_table("mlp.nf4s", gate->W, sc[0], st));
-        LM_TRY(scale_table("mlp.nf4s", up->W, sc[1], st));
-        LM_TRY(scale_table("mlp.nf4s", down->W, sc[2], st));
+        LM_TRY(scale_tables("mlp.nf4s", {{&gate->W, sc[0]}, {&up->W, sc[1]}, {&down->W, sc[2]}}, st));
     }
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     const uint16_t* haT = at<uint16_t>(saved, PL.ha.t_off);
@@ -1208,8 +1212,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         P.act = act;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(dY, T, d, d, 128);
-        S0.b_map[0] = b.codes_mn(down->W);
-        S0.b_scale[0] = b.scales(sc[2], down->W, true);
+        b.base_mn(S0, down->W, sc[2]);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)d;
         Seg& S1 = seg(P, 1);
@@ -1285,7 +1288,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         };
         LM_TRY(fin_cols("mlp.dAdB.fin", b, js, 6, st));
     }
-    if (q4) {
+    {  // dX = de Wg + du Wu + Gg Ag + Gu Au on 512 x 256 tiles for every base
         Builder b(G2N_STORE_MN);
         b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
@@ -1301,8 +1304,7 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         for (int i = 0; i < 2; ++i) {
             Seg& S = seg(P, i);
             S.a_map = b.map(dOut[i], T, n, n, 128);
-            S.b_map[0] = b.codes_mn(Ls[i]->W);
-            S.b_scale[0] = b.scales(sc[i], Ls[i]->W, true);
+            b.base_mn(S, Ls[i]->W, sc[i]);
             S.b_rank_off = 128;
             S.kext = (int32_t)n;
             Seg& R = seg(P, 2 + i);
@@ -1311,38 +1313,6 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
             R.b_rank_off = 128;
             R.kext = rp;
         }
-        P.out0 = dX;
-        P.ld_out = d;
-        LM_TRY(b.launch("mlp.dX", sms, err, st));
-    } else {  // dX = de Wg + du Wu + Gg Ag + Gu Au
-        Builder b(G2_STORE_MN);
-        Prob& P = b.prob();
-        P.M = (int32_t)T;
-        P.N = (int32_t)d;
-        P.bn = 256;
-        P.tiles_n = (int32_t)((d + 255) / 256);
-        P.n_step = 256;
-        P.out_col_step = 256;
-        Seg& S0 = seg(P, 0);
-        S0.a_map = b.map(de, T, n, n, 128);
-        S0.b_map[0] = b.map(gate->W.w, n, d, d, 64);
-        S0.b_rank_off = 128;
-        S0.kext = (int32_t)n;
-        Seg& S1 = seg(P, 1);
-        S1.a_map = b.map(du, T, n, n, 128);
-        S1.b_map[0] = b.map(up->W.w, n, d, d, 64);
-        S1.b_rank_off = 128;
-        S1.kext = (int32_t)n;
-        Seg& S2 = seg(P, 2);
-        S2.a_map = b.map(gg, T, rp, rp, 128);
-        S2.b_map[0] = b.map(gate->A, r, d, d, 64);
-        S2.b_rank_off = 128;
-        S2.kext = rp;
-        Seg& S3 = seg(P, 3);
-        S3.a_map = b.map(gu, T, rp, rp, 128);
-        S3.b_map[0] = b.map(up->A, r, d, d, 64);
-        S3.b_rank_off = 128;
-        S3.kext = rp;
         P.out0 = dX;
         P.ld_out = d;
         LM_TRY(b.launch("mlp.dX", sms, err, st));
@@ -1457,8 +1427,7 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
     down = &down_c;
     float* sc[2] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1])};
     if (q4) {
-        LM_TRY(scale_table("relu2.nf4s", up->W, sc[0], st));
-        LM_TRY(scale_table("relu2.nf4s", down->W, sc[1], st));
+        LM_TRY(scale_tables("relu2.nf4s", {{&up->W, sc[0]}, {&down->W, sc[1]}}, st));
     }
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
     uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
@@ -1482,12 +1451,7 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
         P.act = ACT_RELU2;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(X, T, d, d, 128);
-        if (q4) {
-            S0.b_map[0] = b.codes_k(up->W, 128);
-            S0.b_scale[0] = b.scales(sc[0], up->W, false);
-        } else {
-            S0.b_map[0] = b.map(up->W.w, n, d, d, 128);
-        }
+        b.base_k(S0, up->W, sc[0]);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)d;
         Seg& S1 = seg(P, 1);
@@ -1507,8 +1471,8 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
         LM_TRY(fin_rows("relu2.ha.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, ha, haT, D.ldT}}, T, st));
     }
     {  // y = h Wd^T + (s_d h Ad^T) Bd^T
-        Builder b(q4 ? G2N_STORE_K : G2_STORE_K);
-        if (q4) b.tail_buf = at<float>(ws, PL.tail);
+        Builder b(G2N_STORE_K);  // 512 x 256 tiles for every base
+        b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
@@ -1518,12 +1482,7 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
         P.out_col_step = 256;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(h_save, T, n, n, 128);
-        if (q4) {
-            S0.b_map[0] = b.codes_k(down->W, 128);
-            S0.b_scale[0] = b.scales(sc[1], down->W, false);
-        } else {
-            S0.b_map[0] = b.map(down->W.w, d, n, n, 128);
-        }
+        b.base_k(S0, down->W, sc[1]);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)n;
         Seg& S1 = seg(P, 1);
@@ -1587,8 +1546,7 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
     down = &down_c;
     float* sc[2] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1])};
     if (q4) {
-        LM_TRY(scale_table("relu2.nf4s", up->W, sc[0], st));
-        LM_TRY(scale_table("relu2.nf4s", down->W, sc[1], st));
+        LM_TRY(scale_tables("relu2.nf4s", {{&up->W, sc[0]}, {&down->W, sc[1]}}, st));
     }
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     const uint16_t* haT = at<uint16_t>(saved, PL.ha.t_off);
@@ -1616,12 +1574,7 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
         P.act = ACT_RELU2;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(dY, T, d, d, 128);
-        if (q4) {
-            S0.b_map[0] = b.codes_mn(down->W);
-            S0.b_scale[0] = b.scales(sc[1], down->W, true);
-        } else {
-            S0.b_map[0] = b.map(down->W.w, d, n, n, 64);
-        }
+        b.base_mn(S0, down->W, sc[1]);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)d;
         Seg& S1 = seg(P, 1);
@@ -1661,8 +1614,8 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
         LM_TRY(fin_cols("relu2.dAdB.fin", b, js, 4, st));
     }
     {  // dX = du Wu + Gu Au
-        Builder b(q4 ? G2N_STORE_MN : G2_STORE_MN);
-        if (q4) b.tail_buf = at<float>(ws, PL.tail);
+        Builder b(G2N_STORE_MN);  // 512 x 256 tiles for every base
+        b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
@@ -1672,12 +1625,7 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
         P.out_col_step = 256;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(du, T, n, n, 128);
-        if (q4) {
-            S0.b_map[0] = b.codes_mn(up->W);
-            S0.b_scale[0] = b.scales(sc[0], up->W, true);
-        } else {
-            S0.b_map[0] = b.map(up->W.w, n, d, d, 64);
-        }
+        b.base_mn(S0, up->W, sc[0]);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)n;
         Seg& S1 = seg(P, 1);
@@ -1765,9 +1713,7 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     v = &v_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
     if (q4) {  // the NF4 GEMMs read per-K-block fp32 block scales of W_q, W_k, W_v
-        LM_TRY(scale_table("qkv.nf4s", q->W, sc[0], st));
-        LM_TRY(scale_table("qkv.nf4s", k->W, sc[1], st));
-        LM_TRY(scale_table("qkv.nf4s", v->W, sc[2], st));
+        LM_TRY(scale_tables("qkv.nf4s", {{&q->W, sc[0]}, {&k->W, sc[1]}, {&v->W, sc[2]}}, st));
     }
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
     uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
@@ -1777,6 +1723,9 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         LM_TRY(b.launch("qkv.xa", sms, err, st));
         LM_TRY(fin_rows("qkv.xa.fin", b, {FinRowJob{part, T * 3 * rp, 0, 3 * rp, rp, {q->s, k->s, v->s}, xa, xaT, D.ldT}}, T, st));
     }
+    // A bf16 base keeps the 256 x 256 kernel here: with outputs this narrow (4096 / 1024 columns)
+    // the 512-row tiles leave too few units for the machine (measured at the 8B sizes: QKV 0.614
+    // against 0.628 ms, O 0.425 against 0.467 ms per fwd+bwd).
     if (q4) {
         Builder b(G2N_STORE_K);
         b.tail_buf = at<float>(ws, PL.tail);
@@ -1795,8 +1744,7 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             P.out_col_step = 256;
             Seg& S0 = seg(P, 0);
             S0.a_map = xmap;
-            S0.b_map[0] = b.codes_k(Ls[i]->W, 128);
-            S0.b_scale[0] = b.scales(sc[i], Ls[i]->W, false);
+            b.base_k(S0, Ls[i]->W, sc[i]);
             S0.b_rank_off = 128;
             S0.kext = (int32_t)d;
             Seg& S1 = seg(P, 1);
@@ -1898,9 +1846,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     v = &v_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
     if (q4) {
-        LM_TRY(scale_table("qkv.nf4s", q->W, sc[0], st));
-        LM_TRY(scale_table("qkv.nf4s", k->W, sc[1], st));
-        LM_TRY(scale_table("qkv.nf4s", v->W, sc[2], st));
+        LM_TRY(scale_tables("qkv.nf4s", {{&q->W, sc[0]}, {&k->W, sc[1]}, {&v->W, sc[2]}}, st));
     }
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     const lm_lora* Ls[3] = {q, k, v};
@@ -1956,8 +1902,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         for (int i = 0; i < 3; ++i) {
             Seg& S = seg(P, i);
             S.a_map = b.map(dOut[i], T, ns[i], ns[i], 128);
-            S.b_map[0] = b.codes_mn(Ls[i]->W);
-            S.b_scale[0] = b.scales(sc[i], Ls[i]->W, true);
+            b.base_mn(S, Ls[i]->W, sc[i]);
             S.b_rank_off = 128;
             S.kext = (int32_t)ns[i];
         }
@@ -2058,7 +2003,7 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(ab_to_bf16("o.ab", {{&o_c, d_in, d_out}}, at<uint16_t>(ws, PL.abc), st));
     o = &o_c;
     float* sc = at<float>(ws, PL.sc);
-    if (q4) LM_TRY(scale_table("o.nf4s", o->W, sc, st));  // per-K-block fp32 block scales of W_o
+    if (q4) LM_TRY(scale_tables("o.nf4s", {{&o->W, sc}}, st));  // per-K-block fp32 block scales of W_o
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
     uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     {
@@ -2067,6 +2012,7 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         LM_TRY(b.launch("o.xa", sms, err, st));
         LM_TRY(fin_rows("o.xa.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st));
     }
+    // (a bf16 base keeps the 256 x 256 kernel: see the QKV forward)
     if (q4) {
         Builder b(G2N_STORE_K);
         b.tail_buf = at<float>(ws, PL.tail);
@@ -2079,8 +2025,7 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         P.out_col_step = 256;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(X, T, d_in, d_in, 128);
-        S0.b_map[0] = b.codes_k(o->W, 128);
-        S0.b_scale[0] = b.scales(sc, o->W, false);
+        b.base_k(S0, o->W, sc);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)d_in;
         Seg& S1 = seg(P, 1);
@@ -2154,7 +2099,7 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(ab_to_bf16("o.ab", {{&o_c, d_in, d_out}}, at<uint16_t>(ws, PL.abc), st));
     o = &o_c;
     float* sc = at<float>(ws, PL.sc);
-    if (q4) LM_TRY(scale_table("o.nf4s", o->W, sc, st));
+    if (q4) LM_TRY(scale_tables("o.nf4s", {{&o->W, sc}}, st));
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     uint16_t* g = at<uint16_t>(ws, PL.g.rows_off);
     uint16_t* gT = at<uint16_t>(ws, PL.g.t_off);
@@ -2186,8 +2131,7 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         P.out_col_step = 256;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(dY, T, d_out, d_out, 128);
-        S0.b_map[0] = b.codes_mn(o->W);
-        S0.b_scale[0] = b.scales(sc, o->W, true);
+        b.base_mn(S0, o->W, sc);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)d_out;
         Seg& S1 = seg(P, 1);

@@ -354,26 +354,59 @@ cudaError_t launch_nf4_dequant(const uint8_t* codes, const int8_t* absmax_q, con
 // `row` (QLoRA, "Double Quantization").  Laid out K-block-major so that one TMA box brings a
 // stage's scales next to its codes: 128 rows of one K block (weight read K-major), or 64 rows of
 // two 64-wide column blocks (weight read MN-major).
-__global__ void __launch_bounds__(256) nf4_scale_table_kernel(const int8_t* __restrict__ absmax_q,
-                                                              const float* __restrict__ scale, int64_t rows,
-                                                              int64_t kblocks, float* __restrict__ table) {
-    const int64_t n = rows * kblocks;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t kb = i / rows, row = i - kb * rows;
-        const int64_t b = row * kblocks + kb;
-        table[i] = __fmul_rn((float)__ldg(absmax_q + b), __ldg(scale + (b >> 8)));
+// One CTA per 64-row x 64-K-block tile of one job: the int8 block scales are read along K (64
+// consecutive bytes of a row) and the table is written along rows (64 consecutive floats of a K
+// block), transposed through shared memory, so both sides are coalesced.
+__global__ void __launch_bounds__(256) nf4_scale_table_kernel(Nf4ScaleJobs jobs, int njobs) {
+    __shared__ float tile[64][65];
+    int t = blockIdx.x, j = 0;
+    for (; j < njobs; ++j) {
+        const int tiles = (int)(((jobs.j[j].rows + 63) / 64) * ((jobs.j[j].kblocks + 63) / 64));
+        if (t < tiles) break;
+        t -= tiles;
+    }
+    if (j == njobs) return;
+    const Nf4ScaleJob& J = jobs.j[j];
+    const int64_t tk = (J.kblocks + 63) / 64;
+    const int64_t r0 = (t / tk) * 64, k0 = (t % tk) * 64;
+    // read: rows of 64 consecutive K blocks, four per thread (one 32-bit load when the four are
+    // inside the row and 4-byte aligned, else byte by byte)
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int i = threadIdx.x + 256 * it;
+        const int rr = i >> 4, kk = (i & 15) * 4;
+        const int64_t row = r0 + rr, kb = k0 + kk;
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (row < J.rows) {
+            const int64_t b = row * J.kblocks + kb;
+            if (kb + 4 <= J.kblocks && (b & 3) == 0) {
+                const uint32_t q4 = __ldg(reinterpret_cast<const uint32_t*>(J.absmax_q + b));
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    v[c] = __fmul_rn((float)(int8_t)(q4 >> (8 * c)), __ldg(J.scale + ((b + c) >> 8)));
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (kb + c < J.kblocks)
+                        v[c] = __fmul_rn((float)__ldg(J.absmax_q + b + c), __ldg(J.scale + ((b + c) >> 8)));
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tile[kk + c][rr] = v[c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 64 * 64; i += 256) {  // write: K blocks of 64 consecutive rows
+        const int kk = i >> 6, rr = i & 63;
+        const int64_t row = r0 + rr, kb = k0 + kk;
+        if (row < J.rows && kb < J.kblocks) J.table[kb * J.rows + row] = tile[kk][rr];
     }
 }
 
-cudaError_t launch_nf4_scale_table(const int8_t* absmax_q, const float* scale, int64_t rows, int64_t cols,
-                                   float* table, cudaStream_t st) {
-    const int64_t n = rows * (cols / 64);
-    if (n == 0) return cudaSuccess;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)sms * 8);
-    nf4_scale_table_kernel<<<(unsigned)blocks, 256, 0, st>>>(absmax_q, scale, rows, cols / 64, table);
+cudaError_t launch_nf4_scale_tables(const Nf4ScaleJobs& jobs, int njobs, cudaStream_t st) {
+    int64_t tiles = 0;
+    for (int j = 0; j < njobs; ++j) tiles += ((jobs.j[j].rows + 63) / 64) * ((jobs.j[j].kblocks + 63) / 64);
+    if (tiles == 0) return cudaSuccess;
+    nf4_scale_table_kernel<<<(unsigned)tiles, 256, 0, st>>>(jobs, njobs);
     return cudaGetLastError();
 }
 

@@ -99,9 +99,18 @@ cudaError_t launch_f32_to_bf16(const CvtJobs& jobs, int njobs, cudaStream_t st);
 // clusters the NF4 pair GEMM of kind k runs with on the current device
 cudaError_t pair_nf4_clusters(GemmKind k, int* n);
 
-// fp32 block scales of an NF4 weight, K-block-major: table[kb * rows + row] (rows * cols / 64)
-cudaError_t launch_nf4_scale_table(const int8_t* absmax_q, const float* scale, int64_t rows, int64_t cols,
-                                   float* table, cudaStream_t st);
+// fp32 block scales of up to three NF4 weights in one launch, each K-block-major:
+// table[kb * rows + row] = fp32(absmax_q[b] * scale[b / 256]), b = row * kblocks + kb
+struct Nf4ScaleJob {
+    const int8_t* absmax_q;
+    const float* scale;
+    int64_t rows, kblocks;
+    float* table;
+};
+struct Nf4ScaleJobs {
+    Nf4ScaleJob j[3];
+};
+cudaError_t launch_nf4_scale_tables(const Nf4ScaleJobs& jobs, int njobs, cudaStream_t st);
 void nf4_codebook_host(float* out16);
 // int4 groupwise base: codes (rows * cols / 2 bytes) and (scale, zero) words sz[g * rows + row]
 cudaError_t launch_int4_pack(const uint16_t* W, int64_t rows, int64_t cols, int group, uint8_t* codes,
