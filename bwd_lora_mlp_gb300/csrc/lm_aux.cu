@@ -37,6 +37,8 @@ __device__ __forceinline__ float4 sum_splits(const float* p0, int64_t stride, in
 // One thread per (4-column chunk, row), rows fastest: the transposed writes are coalesced across
 // a warp, the row write is 8 contiguous bytes.  ncols and group are multiples of 4.
 __global__ void __launch_bounds__(256) fin_rowproj_kernel(FinRowJobs jobs, int64_t T) {
+    griddep_launch_dependents();
+    griddep_wait();
     const FinRowJob& J = jobs.j[blockIdx.y];
     const int nchunk = J.ncols / 4;
     const int64_t total = (int64_t)nchunk * T;
@@ -65,8 +67,8 @@ cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cuda
     }
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>((most + threads - 1) / threads, 4096);
-    fin_rowproj_kernel<<<dim3((unsigned)std::max<int64_t>(blocks, 1), njobs), threads, 0, st>>>(js, T);
-    return cudaGetLastError();
+    return launch_pdl(fin_rowproj_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1), njobs), dim3(threads), 0, st, nullptr, 0,
+                      js, T);
 }
 
 struct FinColJobs {
@@ -76,6 +78,8 @@ struct FinColJobs {
 // One thread per (column c, 4-wide chunk of j), chunk fastest: the partial reads of a warp are
 // contiguous, and so are the writes of out[c][j]; rp is a multiple of 4.
 __global__ void __launch_bounds__(256) fin_colreduce_kernel(FinColJobs jobs) {
+    griddep_launch_dependents();
+    griddep_wait();
     const FinColJob& J = jobs.j[blockIdx.y];
     const int nchunk = J.rp / 4;
     const int64_t total = J.C * nchunk;
@@ -106,14 +110,16 @@ cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t 
     }
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>((most + threads - 1) / threads, 4096);
-    fin_colreduce_kernel<<<dim3((unsigned)std::max<int64_t>(blocks, 1), njobs), threads, 0, st>>>(js);
-    return cudaGetLastError();
+    return launch_pdl(fin_colreduce_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1), njobs), dim3(threads), 0, st, nullptr,
+                      0, js);
 }
 
 // ------------------------------------------------------------------ fp32 LoRA parameters
 // fp32 -> bf16 bits, round to nearest even (the GEMM input precision of fp32 LoRA parameters);
 // blockIdx.y picks the matrix
 __global__ void __launch_bounds__(256) f32_to_bf16_kernel(CvtJobs jobs) {
+    griddep_launch_dependents();
+    griddep_wait();
     const CvtJob& J = jobs.j[blockIdx.y];
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < J.n; i += (int64_t)gridDim.x * blockDim.x) {
         const __nv_bfloat16 b = __float2bfloat16_rn(J.in[i]);
@@ -126,13 +132,14 @@ cudaError_t launch_f32_to_bf16(const CvtJobs& jobs, int njobs, cudaStream_t st) 
     for (int i = 0; i < njobs; ++i) most = std::max<int64_t>(most, jobs.j[i].n);
     if (njobs == 0 || most == 0) return cudaSuccess;
     const int64_t blocks = std::min<int64_t>((most + 255) / 256, 256);
-    f32_to_bf16_kernel<<<dim3((unsigned)blocks, (unsigned)njobs), 256, 0, st>>>(jobs);
-    return cudaGetLastError();
+    return launch_pdl(f32_to_bf16_kernel, dim3((unsigned)blocks, (unsigned)njobs), dim3(256), 0, st, nullptr, 0, jobs);
 }
 
 // ------------------------------------------------------------------ split tail tiles
 // One thread per 4 columns of a tail-tile row; 512-row tiles, bn and N multiples of 4.
 __global__ void __launch_bounds__(256) tail_fin_kernel(TailFin f) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int c4n = f.bn / 4;
     const int64_t total = (int64_t)f.ntail * 512 * c4n;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -164,8 +171,7 @@ cudaError_t launch_tail_fin(const TailFin& f, cudaStream_t st) {
     const int64_t total = (int64_t)f.ntail * 512 * (f.bn / 4);
     if (total == 0) return cudaSuccess;
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, 4096);
-    tail_fin_kernel<<<(unsigned)blocks, 256, 0, st>>>(f);
-    return cudaGetLastError();
+    return launch_pdl(tail_fin_kernel, dim3((unsigned)blocks), dim3(256), 0, st, nullptr, 0, f);
 }
 
 // ------------------------------------------------------------------ block-diagonal rank-r operand
@@ -174,6 +180,8 @@ cudaError_t launch_tail_fin(const TailFin& f, cudaStream_t st) {
 __global__ void __launch_bounds__(256) blockdiag_kernel(const uint16_t* __restrict__ Bg,
                                                         const uint16_t* __restrict__ Bu, int64_t n, int r,
                                                         int rp, uint16_t* __restrict__ out) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int groups = (2 * rp) / 8;
     const int64_t total = 2 * n * groups;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -199,8 +207,8 @@ cudaError_t launch_blockdiag(const uint16_t* Bg, const uint16_t* Bu, int64_t n, 
                              cudaStream_t st) {
     const int64_t total = 2 * n * (2 * rp / 8);
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, 2048);
-    blockdiag_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, st>>>(Bg, Bu, n, r, rp, out);
-    return cudaGetLastError();
+    return launch_pdl(blockdiag_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1)), dim3(256), 0, st, nullptr, 0, Bg, Bu, n,
+                      r, rp, out);
 }
 
 // ------------------------------------------------------------------ NF4
@@ -358,6 +366,8 @@ cudaError_t launch_nf4_dequant(const uint8_t* codes, const int8_t* absmax_q, con
 // consecutive bytes of a row) and the table is written along rows (64 consecutive floats of a K
 // block), transposed through shared memory, so both sides are coalesced.
 __global__ void __launch_bounds__(256) nf4_scale_table_kernel(Nf4ScaleJobs jobs, int njobs) {
+    griddep_launch_dependents();
+    griddep_wait();
     __shared__ float tile[64][65];
     int t = blockIdx.x, j = 0;
     for (; j < njobs; ++j) {
@@ -406,8 +416,7 @@ cudaError_t launch_nf4_scale_tables(const Nf4ScaleJobs& jobs, int njobs, cudaStr
     int64_t tiles = 0;
     for (int j = 0; j < njobs; ++j) tiles += ((jobs.j[j].rows + 63) / 64) * ((jobs.j[j].kblocks + 63) / 64);
     if (tiles == 0) return cudaSuccess;
-    nf4_scale_table_kernel<<<(unsigned)tiles, 256, 0, st>>>(jobs, njobs);
-    return cudaGetLastError();
+    return launch_pdl(nf4_scale_table_kernel, dim3((unsigned)tiles), dim3(256), 0, st, nullptr, 0, jobs, njobs);
 }
 
 // ------------------------------------------------------------------ int4 groupwise base

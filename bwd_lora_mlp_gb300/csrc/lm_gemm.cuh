@@ -373,6 +373,7 @@ __global__ void __launch_bounds__(kNumThreads, BN_MAX <= 64 ? 2 : 1) gemm_kernel
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -397,6 +398,7 @@ __global__ void __launch_bounds__(kNumThreads, BN_MAX <= 64 ? 2 : 1) gemm_kernel
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_wait();  // the previous kernel of the stream has completed: its outputs are visible
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {

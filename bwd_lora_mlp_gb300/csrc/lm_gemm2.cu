@@ -36,8 +36,7 @@ static cudaError_t launch_pair_variant(const Params& p, int max_units, cudaStrea
         clusters[dev] = n > 0 ? n : 1;
     }
     const int ncl = std::min(max_units, dev < 64 ? clusters[dev] : 1);
-    cfg.gridDim = dim3(2 * ncl, 1, 1);
-    e = cudaLaunchKernelEx(&cfg, k, p);
+    e = launch_pdl(k, dim3(2 * ncl, 1, 1), cfg.blockDim, smem, st, attr, 1, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

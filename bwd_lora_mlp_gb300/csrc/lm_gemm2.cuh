@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    griddep_launch_dependents();
     const uint32_t rank = cluster_ctarank();
     const int cid = (int)cluster_id_x();
     const int ncl = (int)nclusters_x();
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
     tc_fence_before();
     cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
     tc_fence_after();
+    griddep_wait();  // the previous kernel of the stream has completed: its outputs are visible
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t full0 = map_to_rank(smem_u32(&full[0]), 0);      // CTA 0's stage barriers
     const uint32_t tempty0 = map_to_rank(smem_u32(&tempty[0]), 0);  // CTA 0's accumulator-free barriers

@@ -56,8 +56,8 @@ static cudaError_t launch_pair_nf4_variant(const Params& p, int max_units, cudaS
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pair_nf4_config<B_MN, EPI>(attr, st);
     const int ncl = std::min(max_units, n);
-    cfg.gridDim = dim3(2 * ncl, 1, 1);
-    e = cudaLaunchKernelEx(&cfg, gemm2_nf4_kernel<B_MN, EPI>, p);
+    e = launch_pdl(gemm2_nf4_kernel<B_MN, EPI>, dim3(2 * ncl, 1, 1), cfg.blockDim, cfg.dynamicSmemBytes, st, attr, 1,
+                   p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

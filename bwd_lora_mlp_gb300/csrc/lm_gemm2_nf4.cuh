@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    griddep_launch_dependents();
     const uint32_t rank = cluster_ctarank();
     const int cid = (int)cluster_id_x();
     const int ncl = (int)nclusters_x();
@@ -252,6 +253,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
     }
     if (threadIdx.x >= 32 && threadIdx.x < 32 + kMaxMaps) {  // published by the cluster barrier below
         const int i = threadIdx.x - 32;
+        griddep_wait();  // (a previous kernel of the stream may have written the scale)
         s_gscale[i] = p.map_gscale[i] ? __ldg(p.map_gscale[i]) : 0.0f;
     }
     __syncwarp();
@@ -262,6 +264,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
     tc_fence_before();
     cluster_sync();
     tc_fence_after();
+    griddep_wait();  // the previous kernel of the stream has completed: its outputs are visible
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t bready0 = map_to_rank(smem_u32(&bready[0]), 0);
     const uint32_t tempty0 = map_to_rank(smem_u32(&tempty[0]), 0);

@@ -17,8 +17,7 @@ static cudaError_t launch_variant(const Params& p, int grid, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
-    k<<<grid, kNumThreads, smem, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(grid), dim3(kNumThreads), smem, st, nullptr, 0, p);
 }
 
 cudaError_t launch_gemm_fwd(GemmKind k, const Params& p, int grid, cudaStream_t st) {

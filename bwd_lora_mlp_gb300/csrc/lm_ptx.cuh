@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -311,5 +312,35 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Programmatic dependent launch.  Every kernel of a step lets the next launch of its stream be
+// scheduled as soon as all of its own CTAs have started (launch_dependents), and touches no global
+// memory before griddepcontrol.wait, which returns once the previous grid in the stream has
+// completed and its writes are visible (at once for a launch without the attribute).  A dependent
+// CTA that is already resident thus sets up its barriers and tensor memory while the previous
+// kernel drains.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch with programmatic stream serialisation allowed (the kernel must call griddep_wait before
+// its first global memory access); extra attributes (a cluster shape) may be passed in.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              const cudaLaunchAttribute* extra, int nextra, Args&&... args) {
+    cudaLaunchAttribute attr[4];
+    int n = 0;
+    for (int i = 0; i < nextra && n < 3; ++i) attr[n++] = extra[i];
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = (unsigned)n;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 }  // namespace lm
