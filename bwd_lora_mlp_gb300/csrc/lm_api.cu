@@ -567,12 +567,13 @@ struct Builder {
     // The base-weight operand of a segment of the 512 x 256 pair GEMM: a bf16 W loaded as it is
     // (K-major box 64 x 128 rows, MN-major 64 x 64), a packed W as its codes plus scales (`table`:
     // the per-call NF4 block-scale table; unused for the other formats).
-    void base_k(Seg& S, const lm_weight& W, const float* table) {
+    // (`slot`: which of the segment's B operands; the gate/up GEMM has W_g in 0 and W_u in 1)
+    void base_k(Seg& S, const lm_weight& W, const float* table, int slot = 0) {
         if (W.kind == LM_WEIGHT_BF16) {
-            S.b_map[0] = map(W.w, W.rows, W.cols, W.cols, 128);
+            S.b_map[slot] = map(W.w, W.rows, W.cols, W.cols, 128);
         } else {
-            S.b_map[0] = codes_k(W, 128);
-            S.b_scale[0] = scales(table, W, false);
+            S.b_map[slot] = codes_k(W, 128);
+            S.b_scale[slot] = scales(table, W, false);
         }
     }
     void base_mn(Seg& S, const lm_weight& W, const float* table) {
@@ -1017,8 +1018,8 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(b.launch("mlp.xa", sms, err, st));
         LM_TRY(fin_rows("mlp.xa.fin", b, {FinRowJob{part, T * 2 * rp, 0, 2 * rp, rp, {gate->s, up->s, 0.f}, xa, xaT, D.ldT}}, T, st));
     }
-    if (q4) {
-        // NF4 base, CTA pair: CTA 0 decodes 128 W_g rows of a tile, CTA 1 the matching W_u rows;
+    {  // e, u and h = act(e) * u; the rank-r terms enter the same accumulator
+        // CTA pair: CTA 0 holds (or decodes) the 128 W_g rows of a tile, CTA 1 the matching W_u rows;
         // the rank-r segment multiplies [s XAg | s XAu] by the block-diagonal [Bg | 0 ; 0 | Bu]
         uint16_t* bdiag = at<uint16_t>(ws, PL.bdiag);
         {
@@ -1026,7 +1027,7 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
             const cudaError_t be = launch_blockdiag(bf(gate->B), bf(up->B), n, r, rp, bdiag, st);
             if (be != cudaSuccess) return cuda_fail(be, "rank-r operand launch");
         }
-        Builder b(G2N_GLU_FWD);
+        Builder b(q4 ? G2N_GLU_FWD : G2_GLU_FWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)n;
@@ -1037,43 +1038,8 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         P.act = act;
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(X, T, d, d, 128);
-        S0.b_map[0] = b.codes_k(gate->W, 128);
-        S0.b_map[1] = b.codes_k(up->W, 128);
-        S0.b_scale[0] = b.scales(sc[0], gate->W, false);
-        S0.b_scale[1] = b.scales(sc[1], up->W, false);
-        S0.kext = (int32_t)d;
-        Seg& S1 = seg(P, 1);
-        S1.a_map = b.map(xa, T, 2 * rp, 2 * rp, 128);
-        S1.b_map[0] = b.map(bdiag, n, 2 * rp, 2 * rp, 128);
-        S1.b_map[1] = b.map(bdiag + (size_t)n * 2 * rp, n, 2 * rp, 2 * rp, 128);
-        S1.kext = 2 * rp;
-        P.out0 = e_save;
-        P.out1 = u_save;
-        P.out2 = h_save;
-        P.ld_out = n;
-        LM_TRY(b.launch("mlp.gateup", sms, err, st));
-    } else {  // e, u and h = act(e) * u; the rank-r terms enter the same accumulator
-        // CTA pair: CTA 0 holds the 128 W_g rows of a tile, CTA 1 the matching 128 W_u rows;
-        // the rank-r segment multiplies [s XAg | s XAu] by the block-diagonal [Bg | 0 ; 0 | Bu]
-        uint16_t* bdiag = at<uint16_t>(ws, PL.bdiag);
-        {
-            ProfScope prof("mlp.bdiag", st);
-            const cudaError_t be = launch_blockdiag(bf(gate->B), bf(up->B), n, r, rp, bdiag, st);
-            if (be != cudaSuccess) return cuda_fail(be, "rank-r operand launch");
-        }
-        Builder b(G2_GLU_FWD);
-        Prob& P = b.prob();
-        P.M = (int32_t)T;
-        P.N = (int32_t)n;
-        P.bn = 256;
-        P.tiles_n = (int32_t)((n + 127) / 128);
-        P.n_step = 128;
-        P.out_col_step = 128;
-        P.act = act;
-        Seg& S0 = seg(P, 0);
-        S0.a_map = b.map(X, T, d, d, 128);
-        S0.b_map[0] = b.map(gate->W.w, n, d, d, 128);
-        S0.b_map[1] = b.map(up->W.w, n, d, d, 128);
+        b.base_k(S0, gate->W, sc[0], 0);
+        b.base_k(S0, up->W, sc[1], 1);
         S0.kext = (int32_t)d;
         Seg& S1 = seg(P, 1);
         S1.a_map = b.map(xa, T, 2 * rp, 2 * rp, 128);
@@ -1200,8 +1166,8 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(b.launch("mlp.gd", sms, err, st));
         LM_TRY(fin_rows("mlp.gd.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st));
     }
-    if (q4) {
-        Builder b(G2N_GLU_BWD);
+    {  // dh = dY Wd + Gd Ad with the activation backward in the epilogue: de, du
+        Builder b(q4 ? G2N_GLU_BWD : G2_GLU_BWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)n;
@@ -1213,33 +1179,6 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(dY, T, d, d, 128);
         b.base_mn(S0, down->W, sc[2]);
-        S0.b_rank_off = 128;
-        S0.kext = (int32_t)d;
-        Seg& S1 = seg(P, 1);
-        S1.a_map = b.map(gd, T, rp, rp, 128);
-        S1.b_map[0] = b.map(down->A, r, n, n, 64);
-        S1.b_rank_off = 128;
-        S1.kext = rp;
-        P.in0 = e_save;
-        P.in1 = u_save;
-        P.ld_in = n;
-        P.out0 = de;
-        P.out1 = du;
-        P.ld_out = n;
-        LM_TRY(b.launch("mlp.dh", sms, err, st));
-    } else {  // dh = dY Wd + Gd Ad with the activation backward in the epilogue: de, du
-        Builder b(G2_GLU_BWD);
-        Prob& P = b.prob();
-        P.M = (int32_t)T;
-        P.N = (int32_t)n;
-        P.bn = 256;
-        P.tiles_n = (int32_t)((n + 255) / 256);
-        P.n_step = 256;
-        P.out_col_step = 256;
-        P.act = act;
-        Seg& S0 = seg(P, 0);
-        S0.a_map = b.map(dY, T, d, d, 128);
-        S0.b_map[0] = b.map(down->W.w, d, n, n, 64);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)d;
         Seg& S1 = seg(P, 1);
@@ -1726,9 +1665,9 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     // A bf16 base keeps the 256 x 256 kernel here: with outputs this narrow (4096 / 1024 columns)
     // the 512-row tiles leave too few units for the machine (measured at the 8B sizes: QKV 0.614
     // against 0.628 ms, O 0.425 against 0.467 ms per fwd+bwd).
-    if (q4) {
-        Builder b(G2N_STORE_K);
-        b.tail_buf = at<float>(ws, PL.tail);
+    {
+        Builder b(q4 ? G2N_STORE_K : G2_STORE_K);
+        if (q4) b.tail_buf = at<float>(ws, PL.tail);
         const int xmap = b.map(X, T, d, d, 128);
         const int amap = b.map(xa, T, 3 * rp, 3 * rp, 128);
         const lm_lora* Ls[3] = {q, k, v};
@@ -1745,36 +1684,6 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             Seg& S0 = seg(P, 0);
             S0.a_map = xmap;
             b.base_k(S0, Ls[i]->W, sc[i]);
-            S0.b_rank_off = 128;
-            S0.kext = (int32_t)d;
-            Seg& S1 = seg(P, 1);
-            S1.a_map = amap;
-            S1.a_xoff = i * rp;
-            S1.b_map[0] = b.map(Ls[i]->B, ns[i], r, r, 128);
-            S1.b_rank_off = 128;
-            S1.kext = rp;
-            P.out0 = outs[i];
-            P.ld_out = ns[i];
-        }
-        LM_TRY(b.launch("qkv.fwd", sms, err, st));
-    } else {
-        Builder b(G2_STORE_K);
-        const int xmap = b.map(X, T, d, d, 128);
-        const int amap = b.map(xa, T, 3 * rp, 3 * rp, 128);
-        const lm_lora* Ls[3] = {q, k, v};
-        uint16_t* outs[3] = {Q, K, V};
-        const int64_t ns[3] = {nq, nk, nv};
-        for (int i = 0; i < 3; ++i) {
-            Prob& P = b.prob();
-            P.M = (int32_t)T;
-            P.N = (int32_t)ns[i];
-            P.bn = 256;
-            P.tiles_n = (int32_t)((ns[i] + 255) / 256);
-            P.n_step = 256;
-            P.out_col_step = 256;
-            Seg& S0 = seg(P, 0);
-            S0.a_map = xmap;
-            S0.b_map[0] = b.map(Ls[i]->W.w, ns[i], d, d, 128);
             S0.b_rank_off = 128;
             S0.kext = (int32_t)d;
             Seg& S1 = seg(P, 1);
@@ -1889,9 +1798,9 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         LM_TRY(b.launch("qkv.dAdB", sms, err, st));
         LM_TRY(fin_cols("qkv.dAdB.fin", b, js, 6, st));
     }
-    if (q4) {  // dX = sum_x dOut_x W_x + G_x A_x
-        Builder b(G2N_STORE_MN);
-        b.tail_buf = at<float>(ws, PL.tail);
+    {  // dX = sum_x dOut_x W_x + G_x A_x
+        Builder b(q4 ? G2N_STORE_MN : G2_STORE_MN);
+        if (q4) b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d;
@@ -1903,32 +1812,6 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             Seg& S = seg(P, i);
             S.a_map = b.map(dOut[i], T, ns[i], ns[i], 128);
             b.base_mn(S, Ls[i]->W, sc[i]);
-            S.b_rank_off = 128;
-            S.kext = (int32_t)ns[i];
-        }
-        for (int i = 0; i < 3; ++i) {
-            Seg& S = seg(P, 3 + i);
-            S.a_map = b.map(g[i], T, rp, rp, 128);
-            S.b_map[0] = b.map(Ls[i]->A, r, d, d, 64);
-            S.b_rank_off = 128;
-            S.kext = rp;
-        }
-        P.out0 = dX;
-        P.ld_out = d;
-        LM_TRY(b.launch("qkv.dX", sms, err, st));
-    } else {  // dX = sum_x dOut_x W_x + G_x A_x
-        Builder b(G2_STORE_MN);
-        Prob& P = b.prob();
-        P.M = (int32_t)T;
-        P.N = (int32_t)d;
-        P.bn = 256;
-        P.tiles_n = (int32_t)((d + 255) / 256);
-        P.n_step = 256;
-        P.out_col_step = 256;
-        for (int i = 0; i < 3; ++i) {
-            Seg& S = seg(P, i);
-            S.a_map = b.map(dOut[i], T, ns[i], ns[i], 128);
-            S.b_map[0] = b.map(Ls[i]->W.w, ns[i], d, d, 64);
             S.b_rank_off = 128;
             S.kext = (int32_t)ns[i];
         }
@@ -2013,9 +1896,9 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         LM_TRY(fin_rows("o.xa.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st));
     }
     // (a bf16 base keeps the 256 x 256 kernel: see the QKV forward)
-    if (q4) {
-        Builder b(G2N_STORE_K);
-        b.tail_buf = at<float>(ws, PL.tail);
+    {
+        Builder b(q4 ? G2N_STORE_K : G2_STORE_K);
+        if (q4) b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d_out;
@@ -2026,28 +1909,6 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(X, T, d_in, d_in, 128);
         b.base_k(S0, o->W, sc);
-        S0.b_rank_off = 128;
-        S0.kext = (int32_t)d_in;
-        Seg& S1 = seg(P, 1);
-        S1.a_map = b.map(xa, T, rp, rp, 128);
-        S1.b_map[0] = b.map(o->B, d_out, r, r, 128);
-        S1.b_rank_off = 128;
-        S1.kext = rp;
-        P.out0 = Y;
-        P.ld_out = d_out;
-        LM_TRY(b.launch("o.fwd", sms, err, st));
-    } else {
-        Builder b(G2_STORE_K);
-        Prob& P = b.prob();
-        P.M = (int32_t)T;
-        P.N = (int32_t)d_out;
-        P.bn = 256;
-        P.tiles_n = (int32_t)((d_out + 255) / 256);
-        P.n_step = 256;
-        P.out_col_step = 256;
-        Seg& S0 = seg(P, 0);
-        S0.a_map = b.map(X, T, d_in, d_in, 128);
-        S0.b_map[0] = b.map(o->W.w, d_out, d_in, d_in, 128);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)d_in;
         Seg& S1 = seg(P, 1);
@@ -2119,9 +1980,9 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         FinColJob js[2] = {{p0, d_in * rp, d_in, 0, rp, r, 1, dA}, {p1, d_out * rp, d_out, 0, rp, r, 0, dB}};
         LM_TRY(fin_cols("o.dAdB.fin", b, js, 2, st));
     }
-    if (q4) {  // dX = dY W + G A
-        Builder b(G2N_STORE_MN);
-        b.tail_buf = at<float>(ws, PL.tail);
+    {  // dX = dY W + G A
+        Builder b(q4 ? G2N_STORE_MN : G2_STORE_MN);
+        if (q4) b.tail_buf = at<float>(ws, PL.tail);
         Prob& P = b.prob();
         P.M = (int32_t)T;
         P.N = (int32_t)d_in;
@@ -2132,28 +1993,6 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         Seg& S0 = seg(P, 0);
         S0.a_map = b.map(dY, T, d_out, d_out, 128);
         b.base_mn(S0, o->W, sc);
-        S0.b_rank_off = 128;
-        S0.kext = (int32_t)d_out;
-        Seg& S1 = seg(P, 1);
-        S1.a_map = b.map(g, T, rp, rp, 128);
-        S1.b_map[0] = b.map(o->A, r, d_in, d_in, 64);
-        S1.b_rank_off = 128;
-        S1.kext = rp;
-        P.out0 = dX;
-        P.ld_out = d_in;
-        LM_TRY(b.launch("o.dX", sms, err, st));
-    } else {  // dX = dY W + G A
-        Builder b(G2_STORE_MN);
-        Prob& P = b.prob();
-        P.M = (int32_t)T;
-        P.N = (int32_t)d_in;
-        P.bn = 256;
-        P.tiles_n = (int32_t)((d_in + 255) / 256);
-        P.n_step = 256;
-        P.out_col_step = 256;
-        Seg& S0 = seg(P, 0);
-        S0.a_map = b.map(dY, T, d_out, d_out, 128);
-        S0.b_map[0] = b.map(o->W.w, d_out, d_in, d_in, 64);
         S0.b_rank_off = 128;
         S0.kext = (int32_t)d_out;
         Seg& S1 = seg(P, 1);
