@@ -3,7 +3,8 @@
 * a different LoRA scale s for every projection (a swapped or shared scale shows at once),
 * a single token for every entry point and base,
 * the Llama-3-8B feature sizes with a ragged token count (partial 512-row tiles, split tail
-  tiles and a long K in one launch), checked on sampled rows and columns."""
+  tiles and a long K in one launch), checked on sampled rows and columns,
+* a token count of 50 row tiles with small features, every output against the oracle in full."""
 import numpy as np
 import pytest
 import torch
@@ -161,3 +162,44 @@ def test_8b_features_ragged_tokens(base):
         a = float(np.sum(p["A" + k] * host64(bw["dA_" + t])))
         b = float(np.sum(p["B" + k] * host64(bw["dB_" + t])))
         assert abs(a - b) <= 1e-2 * max(abs(a), abs(b)), (t, a, b)
+
+
+@pytest.mark.parametrize("base", ["bf16", "nf4"])
+def test_fifty_row_tiles_checked_in_full(base):
+    """T = 50 x 128 - 37 tokens (many split-K units per rank-r projection, a ragged last tile) with
+    feature sizes small enough for the oracle to check every output and gradient in full."""
+    T = 50 * 128 - 37
+    w = synth.mlp_workload("rows50", T, 256, 384, 16, 32.0, act="swiglu")
+    inp = synth.make_inputs(w, seed=83)
+    scales = {"gate": 0.75, "up": 2.5, "down": 1.5}
+    fw, bw, p = _mlp(inp, scales, base, "swiglu")
+    ref = O.mlp_backward(O.from_bf16(inp["X"]), O.from_bf16(inp["dY"]), p, "swiglu")
+    for k in ("e", "u", "h", "y"):
+        check(k, host64(fw[k]), ref[k])
+    check("dX", host64(bw["dX"]), ref["dX"])
+    for k, rk in MLP_GRADS:
+        check(k, host64(bw[k]), ref[rk])
+
+    wq = synth.qkv_workload("rows50q", T, 256, 256, 128, 16, 32.0)
+    iq = synth.make_inputs(wq, seed=89)
+    Ls = {t: _dev(iq, t, wq.s, base) for t in ("q", "k", "v")}
+    X = dev_bf16(iq["X"])
+    dO = {t: dev_bf16(iq["dY_" + t]) for t in ("q", "k", "v")}
+    fq = L.lora_qkv_fwd(X, Ls["q"], Ls["k"], Ls["v"])
+    bq = L.lora_qkv_bwd(X, dO["q"], dO["k"], dO["v"], fq, Ls["q"], Ls["k"], Ls["v"])
+    L.lm_workspace_check(fq["ws"])
+    pq = {}
+    for t in ("q", "k", "v"):
+        pq["W" + t] = _base(iq["W_" + t], base)
+        pq["A" + t] = O.from_bf16(iq["A_" + t])
+        pq["B" + t] = O.from_bf16(iq["B_" + t])
+        pq["s" + t] = wq.s
+    Xo = O.from_bf16(iq["X"])
+    rf = O.qkv_forward(Xo, pq)
+    rb = O.qkv_backward(Xo, O.from_bf16(iq["dY_q"]), O.from_bf16(iq["dY_k"]), O.from_bf16(iq["dY_v"]), pq)
+    for t in ("Q", "K", "V"):
+        check(t, host64(fq[t]), rf[t])
+    check("dX", host64(bq["dX"]), rb["dX"])
+    for t in ("q", "k", "v"):
+        check("dA_" + t, host64(bq["dA_" + t]), rb["dA" + t])
+        check("dB_" + t, host64(bq["dB_" + t]), rb["dB" + t])
