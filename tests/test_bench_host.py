@@ -1,0 +1,38 @@
+"""Host checks of bench.py's arithmetic: the algorithmic flop counts behind every TFLOP/s and
+roofline figure it prints agree with the oracle's own counts, and the per-kernel counts of the
+four base GEMMs of the MLP add up to the block's six base GEMMs plus their rank-r terms."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from bwd_lora_mlp_gb300 import synth  # noqa: E402
+from oracle import lora as O  # noqa: E402
+
+
+@pytest.mark.parametrize("name", sorted(synth.WORKLOADS))
+def test_workload_flops_match_the_oracle(name):
+    w = synth.WORKLOADS[name]
+    T, r = w.T, w.r
+    if w.kind == "mlp":
+        want = O.mlp_flops(T, w.projs[0].d_in, w.projs[0].d_out, r)
+    elif w.kind == "relu2":
+        want = O.relu2_mlp_flops(T, w.projs[0].d_in, w.projs[0].d_out, r)
+    else:
+        want = sum(O.lora_proj_flops(T, p.d_in, p.d_out, r) for p in w.projs)
+    assert bench.workload_flops(w) == want
+
+
+def test_base_gemm_kernel_flops_cover_the_six_base_gemms():
+    w = synth.WORKLOADS["llama3_8b_mlp_bf16"]
+    T, d, n, r = w.T, 4096, 14336, w.r
+    tags = ("mlp.gateup", "mlp.down", "mlp.dh", "mlp.dX")
+    total = sum(bench.kernel_flops(t, w) for t in tags)
+    # 6 base GEMMs of 2 T d n each; the rank-r (XA) B^T of gate, up, down in the forward, G_d A_d
+    # inside dh, and G_g A_g + G_u A_u inside dX: 2 T r per output column each
+    assert total == 12 * T * d * n + 2 * T * r * (2 * n + d + n + 2 * d)
+    assert 5.8e12 < bench.workload_flops(w) < 5.83e12       # 710 MFLOP per token at the 8B sizes
