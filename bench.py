@@ -248,7 +248,9 @@ def run_reference(args, w, world, rank):
     from bwd_lora_mlp_gb300 import synth
     inp = synth.make_inputs(w)
     inp64 = oracle_inputs(w, inp)
-    Ts = pick_sample(w, inp64, 2.0)
+    # tokens per step sized so that the warm-up and timed steps together take about two minutes
+    # (at most 2 s a step, at least the 64-token minimum sample)
+    Ts = pick_sample(w, inp64, min(2.0, max(0.1, 120.0 / (args.steps + args.warmup))))
     for _ in range(args.warmup):
         oracle_step(w, inp64, Ts)
     t0 = time.perf_counter()
