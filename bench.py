@@ -91,11 +91,15 @@ def load_peaks():
 
 
 def src_digest():
-    """Digest of the sources of the GEMM kernel templates (the kernels the traffic figures are for)."""
+    """Digest of the code of the GEMM kernel templates (the kernels the traffic figures are for):
+    line comments, trailing blanks and blank lines are left out, so a comment edit keeps it."""
     h = hashlib.sha256()
     for f in [os.path.join(ROOT, "bwd_lora_mlp_gb300", "csrc", x) for x in ("lm_gemm.cuh", "lm_gemm2.cuh", "lm_gemm2_nf4.cuh", "lm_ptx.cuh")]:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

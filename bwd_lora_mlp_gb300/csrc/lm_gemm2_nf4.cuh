@@ -1,23 +1,27 @@
 // The CTA-pair GEMM of lm_gemm2.cuh with a 4-bit packed frozen B operand decoded in the mainloop
 // ("loralei" README, QLoRA section: unpacking and double-scale reconstruction fused into the
-// matmul; the same section's groupwise int4 base).  The two formats differ only in the 16-entry
-// table a 64-element block is decoded with: NF4 code_i * amax', or int4 (i - 8) * s + z with the
-// bf16 scale and zero of the block's group (two tables per block for groups of 32), and in the
-// scales a stage carries (see the producer).
+// matmul, and the same section's groupwise int4 base; "LoRA Optimizations", FP32 LoRA gradients:
+// weight-only NVFP4 bases).  The formats differ only in how a 64-element block of codes becomes
+// bf16 -- NF4 code_i * amax' (a register table built per block), int4 (q - 8) * s + z with the
+// bf16 scale and zero of the block's group (f16 magic-number arithmetic and one fp32 FMA per
+// element), NVFP4 e2m1 * fp32(s_b * S_g) (the hardware E2M1 conversion) -- and in the scales a
+// stage carries (see the producer).  The same kernel also
+// runs plain bf16 GEMMs (every stage loaded as it is), which the MLPs use for their store GEMMs.
 //
 // A work unit is a 512 x 256 tile: per 64-deep K block each CTA of the pair holds 2 x 128 A rows
 // (one set per M half) and half of the 256-wide B tile, and CTA 0 issues two M = 256 pair MMAs
 // per K step that share the decoded B tile, so each decoded weight element feeds 512 output rows
 // (decode work per MMA cycle is half that of a 256 x 256 tile).  The accumulator (2 M halves x 256
-// columns) fills TMEM, so it is single-buffered.  TMA brings the A rows, the raw NF4 codes of
-// the CTA's B half (4 KB) and their 128 fp32 block scales (512 bytes, from a per-call table of
-// fp32(q * c) laid out K-block-major) into the CTA's own stage and completes on the CTA's own
-// stage barrier; decode warps turn every 64-element NF4 block into a 128-byte swizzled bf16 row of
+// columns) fills TMEM, so it is single-buffered.  TMA brings the A rows, the raw 4-bit codes of
+// the CTA's B half (4 KB) and their scales (up to 1 KB: for NF4 128 fp32 block scales from a
+// per-call table of fp32(q * c) laid out K-block-major; for int4 and NVFP4 the stored scale words
+// themselves) into the CTA's own stage and completes on the CTA's own stage barrier; decode warps
+// turn every 64-element block of codes into a 128-byte swizzled bf16 row of
 // the B tile and then report to CTA 0's decoded barrier, which counts both CTAs' decoders, so
 // CTA 0's MMA thread starts a K block only when both halves of B and both A halves are in place.
 // The decode warps issue no global loads: their release-arrive would wait for them.
 //
-// Decoding keeps everything in registers: for a block with scale amax' = fp32(q * c) the thread
+// Decoding keeps everything in registers.  NF4: for a block with scale amax' = fp32(q * c) the thread
 // forms the 16 products bf16(fp32(code_i * amax')) (the values nf4_dequant writes), splits them
 // into low-byte and high-byte tables of four registers each, and assembles every output pair of
 // bf16 with byte permutes (prmt) indexed by the code nibbles, choosing between the two halves of
@@ -26,10 +30,10 @@
 //
 // Roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer (CTA 0), warps 2-9 decoders in
 // kPairNf4DecodeGroups groups that take K blocks round-robin (with two groups of four warps, two K
-// blocks are decoded at once and each thread decodes one NF4 block of each), warps 10-17
+// blocks are decoded at once and each thread decodes one 64-element block of each), warps 10-17
 // epilogue.  The producer tags every stage for the decoders (bf16, NF4, int4 with its group size,
-// or end of work), so they follow the stage ring without walking the work-unit sequence
-// themselves.
+// NVFP4 with its scale map, or end of work), so they follow the stage ring without walking the
+// work-unit sequence themselves.
 #pragma once
 
 #include "lm_gemm2.cuh"
@@ -40,7 +44,7 @@ namespace lm {
 constexpr int kPairNf4DecodeWarps = 8;
 constexpr int kPairNf4DecodeGroups = 2;   // groups take K blocks round-robin
 constexpr int kPairNf4GroupWarps = kPairNf4DecodeWarps / kPairNf4DecodeGroups;
-constexpr int kPairNf4BlocksPerThread = 128 / (32 * kPairNf4GroupWarps);  // NF4 blocks per thread per K block
+constexpr int kPairNf4BlocksPerThread = 128 / (32 * kPairNf4GroupWarps);  // 64-element blocks per thread per K block
 static_assert(kPairNf4BlocksPerThread == 1 || kPairNf4BlocksPerThread == 2, "decode split");
 constexpr int kPairNf4Threads = 64 + 32 * kPairNf4DecodeWarps + 32 * kNumEpiWarps;
 
@@ -223,7 +227,9 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // what each stage holds, written by this CTA's producer before the stage's loads: 0 bf16 B
-    // (nothing to decode), 1 NF4 codes, 2 no more K blocks (one such stage per decode group)
+    // (nothing to decode), 1 NF4 codes, 3 | G << 8 int4 codes with groups of G, 4 | map << 8 NVFP4
+    // codes (map: the scale map, whose tensor scale s_gscale holds), 2 no more K blocks (one such
+    // stage per decode group)
     volatile int32_t* stage_kind = reinterpret_cast<volatile int32_t*>(tmem_slot + 2);
     // fp32 tensor scale of each NVFP4 scale map, read once at launch
     float* s_gscale = const_cast<float*>(reinterpret_cast<volatile float*>(stage_kind + C::STAGES));
