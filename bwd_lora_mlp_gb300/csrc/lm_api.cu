@@ -300,6 +300,16 @@ RankBuf take_rank(Bump& b, const Dims& D, int cols) {
     return r;
 }
 
+// rank-r buffers whose transposes are stacked: buffer i's transpose starts i * cols rows after
+// buffer 0's, so one tensor map over the first covers all of them
+void take_rank_stack(Bump& b, const Dims& D, int cols, std::initializer_list<RankBuf*> bufs) {
+    for (RankBuf* r : bufs) r->rows_off = b.take((size_t)D.T * cols * 2);
+    const size_t block = (size_t)cols * D.ldT * 2;
+    const size_t t0 = b.take(bufs.size() * block);
+    size_t i = 0;
+    for (RankBuf* r : bufs) r->t_off = t0 + (i++) * block;
+}
+
 struct MlpPlan {
     Dims D;
     RankBuf xa, ha;         // saved: s*[X Ag^T | X Au^T] (T x 2rp), s*h Ad^T (T x rp)
@@ -327,8 +337,7 @@ MlpPlan plan_mlp(int64_t T, int64_t d, int64_t n, int32_t r) {
     const int64_t part_elems = std::max<int64_t>(T * 2 * rp, 3 * (n + d) * rp);
     P.part = w.take((size_t)kMaxSplits * part_elems * 4);
     P.gd = take_rank(w, P.D, rp);
-    P.gg = take_rank(w, P.D, rp);
-    P.gu = take_rank(w, P.D, rp);
+    take_rank_stack(w, P.D, rp, {&P.gg, &P.gu});
     P.de = w.take((size_t)T * n * 2);
     P.du = w.take((size_t)T * n * 2);
     P.bdiag = w.take((size_t)2 * n * 2 * rp * 2);
@@ -362,7 +371,7 @@ QkvPlan plan_qkv(int64_t T, int64_t d, int64_t nq, int64_t nk, int64_t nv, int32
     w.take(256);
     const int64_t part_elems = std::max<int64_t>(T * 3 * rp, (3 * d + nq + nk + nv) * rp);
     P.part = w.take((size_t)kMaxSplits * part_elems * 4);
-    for (int i = 0; i < 3; ++i) P.g[i] = take_rank(w, P.D, rp);
+    take_rank_stack(w, P.D, rp, {&P.g[0], &P.g[1], &P.g[2]});
     const int64_t nout[3] = {nq, nk, nv};
     for (int i = 0; i < 3; ++i) P.sc[i] = w.take((size_t)nout[i] * d / 64 * 4);
     P.tail = w.take(kTailBytes);
@@ -791,22 +800,59 @@ void add_rowproj_out(Builder& b, const uint16_t* dO, int64_t T, int64_t C, const
     P.split_stride = T * P.bn;
 }
 
-// column reduction over tokens: part[ks][c][j] = sum_t Z[t][c] * PT[j][t]
+// column reduction over tokens: part[ks][c][j] = sum_t Z[t][c] * PT[j][t], j < nb * rp (PT holds
+// nb stacked blocks of rp rows)
 void add_colreduce(Builder& b, const uint16_t* Z, int64_t T, int64_t C, const uint16_t* PT, const Dims& D,
-                   float* part) {
+                   float* part, int nb = 1) {
     Prob& P = b.prob();
     P.M = (int32_t)C;
-    P.N = D.rp;
-    P.bn = D.rp;
+    P.N = nb * D.rp;
+    P.bn = P.N;
     P.tiles_n = 1;
     Seg& S = seg(P, 0);
     S.a_map = b.map(Z, T, C, C, 64);
-    S.b_map[0] = b.map(PT, D.rp, T, D.ldT, D.rp);
+    S.b_map[0] = b.map(PT, P.N, T, D.ldT, P.N);
     S.kext = (int32_t)T;
     P.out0 = part;
     P.ld_out = P.bn;
     P.split_stride = C * P.bn;
 }
+
+// The dA / dB column reductions of one backward call: one launch of split-K problems, one
+// finalisation launch.  Each problem streams its activation Z once; gradients that reduce the
+// same Z (the dA of every projection fed by X) are one problem whose B stacks their rank blocks.
+struct ColReduce {
+    static constexpr int kMaxJobs = 6;
+    Builder b{G_PART_MNK};
+    const Dims& D;
+    float* next;
+    FinColJob js[kMaxJobs];
+    int prob_of[kMaxJobs];
+    int njobs = 0;
+    ColReduce(const Dims& D_, float* part) : D(D_), next(part) {}
+    // outs[i] = the reduction against rank block i of PT, in dA layout (r x C) if `transposed`,
+    // else in dB layout (C x r)
+    void add(const uint16_t* Z, int64_t C, const uint16_t* PT, std::initializer_list<float*> outs, int transposed) {
+        const int nb = (int)outs.size();
+        const int64_t w = (int64_t)nb * D.rp;
+        float* q = next;
+        next += (size_t)kMaxSplits * C * w;
+        add_colreduce(b, Z, D.T, C, PT, D, q, nb);
+        int i = 0;
+        for (float* o : outs) {
+            js[njobs] = FinColJob{q + (size_t)(i++) * D.rp, C * w, C, 0, D.rp, D.r, transposed, o, (int32_t)w};
+            prob_of[njobs++] = b.p.nprob - 1;
+        }
+    }
+    lm_status run(const char* tag, const char* fin_tag, int sms, int32_t* err, cudaStream_t st) {
+        LM_TRY(b.launch(tag, sms, err, st));
+        for (int i = 0; i < njobs; ++i) js[i].splits = b.p.prob[prob_of[i]].splits;
+        ProfScope prof(fin_tag, st);
+        const cudaError_t e = launch_fin_colreduce(js, njobs, st);
+        if (e != cudaSuccess) return cuda_fail(e, "gradient finalisation launch");
+        return LM_OK;
+    }
+};
 
 lm_status fin_rows(const char* tag, const Builder& b, std::initializer_list<FinRowJob> jobs, int64_t T,
                    cudaStream_t st) {
@@ -820,14 +866,6 @@ lm_status fin_rows(const char* tag, const Builder& b, std::initializer_list<FinR
     ProfScope prof(tag, st);
     const cudaError_t e = launch_fin_rowproj(js, n, T, st);
     if (e != cudaSuccess) return cuda_fail(e, "rank-r finalisation launch");
-    return LM_OK;
-}
-
-lm_status fin_cols(const char* tag, const Builder& b, FinColJob* js, int n, cudaStream_t st) {
-    for (int i = 0; i < n; ++i) js[i].splits = b.p.prob[i].splits;
-    ProfScope prof(tag, st);
-    const cudaError_t e = launch_fin_colreduce(js, n, st);
-    if (e != cudaSuccess) return cuda_fail(e, "gradient finalisation launch");
     return LM_OK;
 }
 
@@ -1206,26 +1244,18 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
                         T, st));
     }
     {  // the six LoRA gradients as column reductions over the tokens
-        Builder b(G_PART_MNK);
-        float* p0 = part;
-        float* p1 = p0 + (size_t)kMaxSplits * n * rp;   // dA_down  (C = n)
-        float* p2 = p1 + (size_t)kMaxSplits * d * rp;   // dB_down  (C = d)
-        float* p3 = p2 + (size_t)kMaxSplits * d * rp;   // dA_gate  (C = d)
-        float* p4 = p3 + (size_t)kMaxSplits * n * rp;   // dB_gate  (C = n)
-        float* p5 = p4 + (size_t)kMaxSplits * d * rp;   // dA_up    (C = d)
-        add_colreduce(b, h_save, T, n, gdT, D, p0);          // dA_down^T = h^T Gd
-        add_colreduce(b, dY, T, d, haT, D, p1);              // dB_down   = dY^T (s h Ad^T)
-        add_colreduce(b, X, T, d, ggT, D, p2);               // dA_gate^T = X^T Gg
-        add_colreduce(b, de, T, n, xaT, D, p3);              // dB_gate   = de^T (s X Ag^T)
-        add_colreduce(b, X, T, d, guT, D, p4);               // dA_up^T   = X^T Gu
-        add_colreduce(b, du, T, n, xaT + (size_t)rp * D.ldT, D, p5);  // dB_up = du^T (s X Au^T)
-        LM_TRY(b.launch("mlp.dAdB", sms, err, st));
-        FinColJob js[6] = {
-            {p0, n * rp, n, 0, rp, r, 1, dA_down}, {p1, d * rp, d, 0, rp, r, 0, dB_down},
-            {p2, d * rp, d, 0, rp, r, 1, dA_gate}, {p3, n * rp, n, 0, rp, r, 0, dB_gate},
-            {p4, d * rp, d, 0, rp, r, 1, dA_up},   {p5, n * rp, n, 0, rp, r, 0, dB_up},
-        };
-        LM_TRY(fin_cols("mlp.dAdB.fin", b, js, 6, st));
+        ColReduce cr(D, part);
+        cr.add(h_save, n, gdT, {dA_down}, 1);              // dA_down^T = h^T Gd
+        cr.add(dY, d, haT, {dB_down}, 0);                  // dB_down   = dY^T (s h Ad^T)
+        if (2 * rp <= 64) {
+            cr.add(X, d, ggT, {dA_gate, dA_up}, 1);        // [dA_gate; dA_up]^T = X^T [Gg | Gu]
+        } else {
+            cr.add(X, d, ggT, {dA_gate}, 1);
+            cr.add(X, d, guT, {dA_up}, 1);
+        }
+        cr.add(de, n, xaT, {dB_gate}, 0);                  // dB_gate   = de^T (s X Ag^T)
+        cr.add(du, n, xaT + (size_t)rp * D.ldT, {dB_up}, 0);  // dB_up  = du^T (s X Au^T)
+        LM_TRY(cr.run("mlp.dAdB", "mlp.dAdB.fin", sms, err, st));
     }
     {  // dX = de Wg + du Wu + Gg Ag + Gu Au on 512 x 256 tiles for every base
         Builder b(G2N_STORE_MN);
@@ -1534,23 +1564,12 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
         LM_TRY(fin_rows("relu2.gu.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {up->s, 0.f, 0.f}, gu, guT, D.ldT}}, T, st));
     }
     {  // the four LoRA gradients as column reductions over the tokens
-        Builder b(G_PART_MNK);
-        float* p0 = part;
-        float* p1 = p0 + (size_t)kMaxSplits * n * rp;   // dB_down  (C = d)
-        float* p2 = p1 + (size_t)kMaxSplits * d * rp;   // dA_up    (C = d)
-        float* p3 = p2 + (size_t)kMaxSplits * d * rp;   // dB_up    (C = n)
-        add_colreduce(b, h_save, T, n, gdT, D, p0);  // dA_down^T = h^T Gd
-        add_colreduce(b, dY, T, d, haT, D, p1);      // dB_down   = dY^T (s h Ad^T)
-        add_colreduce(b, X, T, d, guT, D, p2);       // dA_up^T   = X^T Gu
-        add_colreduce(b, du, T, n, xaT, D, p3);      // dB_up     = du^T (s X Au^T)
-        LM_TRY(b.launch("relu2.dAdB", sms, err, st));
-        FinColJob js[4] = {
-            {p0, n * rp, n, 0, rp, r, 1, dA_down},
-            {p1, d * rp, d, 0, rp, r, 0, dB_down},
-            {p2, d * rp, d, 0, rp, r, 1, dA_up},
-            {p3, n * rp, n, 0, rp, r, 0, dB_up},
-        };
-        LM_TRY(fin_cols("relu2.dAdB.fin", b, js, 4, st));
+        ColReduce cr(D, part);
+        cr.add(h_save, n, gdT, {dA_down}, 1);  // dA_down^T = h^T Gd
+        cr.add(dY, d, haT, {dB_down}, 0);      // dB_down   = dY^T (s h Ad^T)
+        cr.add(X, d, guT, {dA_up}, 1);         // dA_up^T   = X^T Gu
+        cr.add(du, n, xaT, {dB_up}, 0);        // dB_up     = du^T (s X Au^T)
+        LM_TRY(cr.run("relu2.dAdB", "relu2.dAdB.fin", sms, err, st));
     }
     {  // dX = du Wu + Gu Au
         Builder b(G2N_STORE_MN);  // 512 x 256 tiles for every base
@@ -1781,22 +1800,19 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
                          FinRowJob{parts[2], T * rp, 0, rp, rp, {v->s, 0.f, 0.f}, g[2], gT[2], D.ldT}},
                         T, st));
     }
-    {  // dA_x^T = X^T G_x,  dB_x = dOut_x^T (s X A_x^T)
-        Builder b(G_PART_MNK);
-        FinColJob js[6];
-        float* p = part;
-        float* dAs[3] = {dA_q, dA_k, dA_v};
-        float* dBs[3] = {dB_q, dB_k, dB_v};
-        for (int i = 0; i < 3; ++i) {
-            add_colreduce(b, X, T, d, gT[i], D, p);
-            js[2 * i] = FinColJob{p, d * rp, d, 0, rp, r, 1, dAs[i]};
-            p += (size_t)kMaxSplits * d * rp;
-            add_colreduce(b, dOut[i], T, ns[i], xaT + (size_t)i * rp * D.ldT, D, p);
-            js[2 * i + 1] = FinColJob{p, ns[i] * rp, ns[i], 0, rp, r, 0, dBs[i]};
-            p += (size_t)kMaxSplits * ns[i] * rp;
+    {  // dA_x^T = X^T G_x (one pass over X for q, k, v: G_q, G_k, G_v are stacked), dB_x = dOut_x^T (s X A_x^T)
+        ColReduce cr(D, part);
+        if (3 * rp <= 64) {
+            cr.add(X, d, gT[0], {dA_q, dA_k, dA_v}, 1);
+        } else {
+            cr.add(X, d, gT[0], {dA_q}, 1);
+            cr.add(X, d, gT[1], {dA_k}, 1);
+            cr.add(X, d, gT[2], {dA_v}, 1);
         }
-        LM_TRY(b.launch("qkv.dAdB", sms, err, st));
-        LM_TRY(fin_cols("qkv.dAdB.fin", b, js, 6, st));
+        cr.add(dQ, nq, xaT, {dB_q}, 0);
+        cr.add(dK, nk, xaT + (size_t)rp * D.ldT, {dB_k}, 0);
+        cr.add(dV, nv, xaT + (size_t)2 * rp * D.ldT, {dB_v}, 0);
+        LM_TRY(cr.run("qkv.dAdB", "qkv.dAdB.fin", sms, err, st));
     }
     {  // dX = sum_x dOut_x W_x + G_x A_x
         Builder b(q4 ? G2N_STORE_MN : G2_STORE_MN);
@@ -1971,14 +1987,10 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         LM_TRY(fin_rows("o.g.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, g, gT, D.ldT}}, T, st));
     }
     {  // dA^T = X^T G, dB = dY^T (s X A^T)
-        Builder b(G_PART_MNK);
-        float* p0 = part;
-        float* p1 = p0 + (size_t)kMaxSplits * d_in * rp;
-        add_colreduce(b, X, T, d_in, gT, D, p0);
-        add_colreduce(b, dY, T, d_out, xaT, D, p1);
-        LM_TRY(b.launch("o.dAdB", sms, err, st));
-        FinColJob js[2] = {{p0, d_in * rp, d_in, 0, rp, r, 1, dA}, {p1, d_out * rp, d_out, 0, rp, r, 0, dB}};
-        LM_TRY(fin_cols("o.dAdB.fin", b, js, 2, st));
+        ColReduce cr(D, part);
+        cr.add(X, d_in, gT, {dA}, 1);
+        cr.add(dY, d_out, xaT, {dB}, 0);
+        LM_TRY(cr.run("o.dAdB", "o.dAdB.fin", sms, err, st));
     }
     {  // dX = dY W + G A
         Builder b(q4 ? G2N_STORE_MN : G2_STORE_MN);

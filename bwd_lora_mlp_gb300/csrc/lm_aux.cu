@@ -76,7 +76,7 @@ struct FinColJobs {
 };
 
 // One thread per (column c, 4-wide chunk of j), chunk fastest: the partial reads of a warp are
-// contiguous, and so are the writes of out[c][j]; rp is a multiple of 4.
+// contiguous, and so are the writes of out[c][j]; rp and ldp are multiples of 4.
 __global__ void __launch_bounds__(256) fin_colreduce_kernel(FinColJobs jobs) {
     griddep_launch_dependents();
     griddep_wait();
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(256) fin_colreduce_kernel(FinColJobs jobs) {
         const int ch = (int)(idx - c * nchunk);
         const int j0 = ch * 4;
         if (j0 >= J.r) continue;
-        const float4 a = sum_splits(J.part + c * J.rp + j0, J.split_stride, J.splits);
+        const float4 a = sum_splits(J.part + c * J.ldp + j0, J.split_stride, J.splits);
         const float v[4] = {a.x, a.y, a.z, a.w};
         const int nj = min(4, J.r - j0);
 #pragma unroll

@@ -62,7 +62,7 @@ cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cuda
 //   dB layout (transposed == 0): out[c][j] = sum_ks part[ks][c][j], j < r
 //   dA layout (transposed == 1): out[j][c] = sum_ks part[ks][c][j]
 struct FinColJob {
-    const float* part;
+    const float* part;       // column j of the job is part[ks][c][j] (the slice of a wider partial row)
     int64_t split_stride;
     int64_t C;
     int32_t splits;
@@ -70,6 +70,7 @@ struct FinColJob {
     int32_t r;
     int32_t transposed;
     float* out;
+    int32_t ldp;             // floats per partial row: rp, or nb * rp when nb projections share Z
 };
 cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t st);
 

@@ -34,7 +34,8 @@ def _qkv(T, d, nq, nkv, r, alpha, seed, **kw):
     return fw, bw, rf, rb
 
 
-@pytest.mark.parametrize("T,d,nq,nkv,r", [(300, 256, 256, 64, 16), (512, 512, 512, 128, 8), (130, 128, 128, 32, 64)])
+@pytest.mark.parametrize("T,d,nq,nkv,r", [(300, 256, 256, 64, 16), (512, 512, 512, 128, 8), (130, 128, 128, 32, 64),
+                                            (200, 256, 256, 128, 32)])
 def test_qkv_matches_oracle(T, d, nq, nkv, r):
     fw, bw, rf, rb = _qkv(T, d, nq, nkv, r, 2.0 * r, seed=31)
     for t in ("Q", "K", "V"):
