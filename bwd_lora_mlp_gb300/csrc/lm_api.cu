@@ -594,6 +594,31 @@ struct Builder {
         }
     }
 
+    // 2D bf16 tensor (rows x cols, row stride ld elements) read by the staged GLU backward
+    // epilogue of the packed pair kernel: box 16 columns x 128 rows, 32-byte swizzle
+    int map_epi(const void* base, int64_t rows, int64_t cols, int64_t ld) {
+        if (st != LM_OK) return 0;
+        if (nmaps >= kMaxMaps) {
+            st = fail(LM_ERR_UNSUPPORTED, "too many tensor maps in one launch");
+            return 0;
+        }
+        cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+        cuuint32_t box[2] = {16u, 128u};
+        cuuint32_t es[2] = {1u, 1u};
+        const CUresult r = g_encode(&p.maps[nmaps], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            st = fail(LM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %lld x %lld epilogue input", (int)r,
+                      (long long)rows, (long long)cols);
+            return 0;
+        }
+        p.map_bytes[nmaps] = 16u * 128u * 2u;
+        p.map_w[nmaps] = (int32_t)cols;
+        return nmaps++;
+    }
+
     // 2D bf16 tensor (rows x cols, row stride ld elements), box = 64 columns x box_rows rows
     int map(const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
         if (st != LM_OK) return 0;
@@ -622,6 +647,7 @@ struct Builder {
         Prob& P = p.prob[p.nprob++];
         memset(&P, 0, sizeof P);
         P.splits = 1;
+        P.in_map[0] = P.in_map[1] = -1;
         for (int s = 0; s < kMaxSegs; ++s) {
             for (int i = 0; i < 3; ++i) P.seg[s].b_map[i] = -1;
             P.seg[s].b_scale[0] = P.seg[s].b_scale[1] = -1;
@@ -1230,6 +1256,12 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         P.out0 = de;
         P.out1 = du;
         P.ld_out = n;
+        // packed base: the single-accumulator kernel stages e, u through shared memory when every
+        // tile has the four K blocks its slot borrowing needs
+        if (q4 && (d + kBK - 1) / kBK + (rp + kBK - 1) / kBK >= 4) {
+            P.in_map[0] = b.map_epi(e_save, T, n, n);
+            P.in_map[1] = b.map_epi(u_save, T, n, n);
+        }
         LM_TRY(b.launch("mlp.dh", sms, err, st));
     }
     {  // Gg = s_g de Bg, Gu = s_u du Bu, formed once (feed dA and dX)

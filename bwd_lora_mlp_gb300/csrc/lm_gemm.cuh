@@ -76,6 +76,9 @@ struct Prob {
     // row-major blocks of rows x bn) and a finalisation kernel sums the parts in order.
     int32_t tail_begin, tail_splits;
     float* tail_part;
+    // Packed pair kernel, GLU_BWD epilogue: tensor maps of in0 (e) and in1 (u), box 16 columns x
+    // 128 rows with 32-byte swizzle, to stage them through shared memory; -1: plain global loads.
+    int32_t in_map[2];
 };
 
 struct Params {  // CUtensorMap members carry their own 128-byte alignment

@@ -213,6 +213,93 @@ __device__ __forceinline__ void nvfp4_decode_block(const uint32_t (&words)[8], u
     }
 }
 
+// GLU backward epilogue of a 512-row tile with e, u staged through shared memory.  The tile's
+// single accumulator leaves its epilogue exposed, and with one accumulator row per thread each
+// warp access to e, u in global memory would touch 32 rows of 32 bytes; here TMA brings them in
+// chunks of 16 columns (this CTA's two 128-row halves of e and u: 16 KB) into three buffers of
+// the stage slot that held the tile's last K block.  The producer does not refill that slot
+// until every epilogue warp has arrived on `scrfree` (see the producer's gate).  Lane 0 of the
+// first epilogue warp issues the loads, three chunks ahead; each warp releases a buffer as soon
+// as it has read its row from it.  `qn` counts the chunks staged by this CTA so far (buffer
+// qn % 3, phase qn / 3).  Returns false on a timed-out wait.
+constexpr int kStageChunkBytes = 16384;
+constexpr int kStageBuffers = 3;
+
+__device__ __forceinline__ bool glu_bwd_staged(const Params& p, const Prob& P, const Unit& U, uint32_t tacc,
+                                               int64_t m, uint32_t scr, uint32_t efull0, uint32_t eempty0,
+                                               uint32_t rank, bool issuer, int hh, int r, uint32_t& qn,
+                                               volatile int* s_abort) {
+    const int nch = P.bn >> 4;
+    const int32_t row0 = (int32_t)((int64_t)U.mb * 512 + (int64_t)rank * kBM);
+    const int64_t col0 = (int64_t)U.nb * P.out_col_step;
+    const CUtensorMap* me = &p.maps[P.in_map[0]];
+    const CUtensorMap* mu = &p.maps[P.in_map[1]];
+    const uint32_t q0 = qn;
+    // chunk c of this tile into buffer (q0 + c) % 3, once every warp has released that buffer's
+    // previous chunk
+    auto issue = [&](int c) -> bool {
+        const uint32_t q = q0 + (uint32_t)c, b = q % kStageBuffers;
+        if (q >= kStageBuffers && !mbar_wait(eempty0 + 8 * b, ((q - kStageBuffers) / kStageBuffers) & 1u, s_abort))
+            return false;
+        const uint32_t dst = scr + b * kStageChunkBytes, bar = efull0 + 8 * b;
+        const int32_t x = (int32_t)(col0 + 16 * c);
+        mbar_expect_tx(bar, kStageChunkBytes);
+        tma_load_2d(dst, me, bar, x, row0);
+        tma_load_2d(dst + 4096, me, bar, x, row0 + 256);
+        tma_load_2d(dst + 8192, mu, bar, x, row0);
+        tma_load_2d(dst + 12288, mu, bar, x, row0 + 256);
+        return true;
+    };
+    int fail = 0;
+    if (issuer)
+        for (int c = 0; c < kStageBuffers && c < nch && !fail; ++c) fail = !issue(c);
+    if (__any_sync(0xffffffffu, fail)) return false;
+    // this thread's row in a 128-row box: 32 bytes, 16-byte halves swapped on every other group
+    // of four rows (the 32-byte swizzle)
+    const uint32_t sw = (uint32_t)((r >> 2) & 1) << 4;
+    const uint32_t roff = (uint32_t)hh * 4096 + (uint32_t)r * 32;
+#pragma unroll 1
+    for (int c = 0; c < nch; ++c) {
+        const uint32_t q = q0 + (uint32_t)c, b = q % kStageBuffers;
+        if (!mbar_wait_warp(efull0 + 8 * b, (q / kStageBuffers) & 1u, s_abort)) return false;
+        const uint32_t base = scr + b * kStageChunkBytes + roff;
+        uint32_t ev[8], uv[8];
+        ld_shared_v4(base + sw, ev[0], ev[1], ev[2], ev[3]);
+        ld_shared_v4(base + (sw ^ 16u), ev[4], ev[5], ev[6], ev[7]);
+        ld_shared_v4(base + 8192 + sw, uv[0], uv[1], uv[2], uv[3]);
+        ld_shared_v4(base + 8192 + (sw ^ 16u), uv[4], uv[5], uv[6], uv[7]);
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(eempty0 + 8 * b);
+        uint32_t a[16];
+        tmem_ld_x16(tacc + 16 * c, a);
+        tmem_ld_wait16(a);
+        const int64_t gcol = col0 + 16 * c;
+        if (m < P.M && gcol < P.N) {
+            uint32_t deo[8], duo[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float f0, df0, f1, df1;
+                const float e0 = bf16lo(ev[i]), e1 = bf16hi(ev[i]);
+                const float u0 = bf16lo(uv[i]), u1 = bf16hi(uv[i]);
+                act_fwd_bwd(P.act, e0, f0, df0);
+                act_fwd_bwd(P.act, e1, f1, df1);
+                const float h0 = __uint_as_float(a[2 * i]), h1 = __uint_as_float(a[2 * i + 1]);
+                deo[i] = pack_bf16x2(h0 * u0 * df0, h1 * u1 * df1);
+                duo[i] = pack_bf16x2(h0 * f0, h1 * f1);
+            }
+            const int64_t off = m * P.ld_out + gcol;
+            st_global_v8(static_cast<uint16_t*>(P.out0) + off, deo[0], deo[1], deo[2], deo[3], deo[4], deo[5], deo[6],
+                         deo[7]);
+            st_global_v8(static_cast<uint16_t*>(P.out1) + off, duo[0], duo[1], duo[2], duo[3], duo[4], duo[5], duo[6],
+                         duo[7]);
+        }
+        if (issuer && c + kStageBuffers < nch) fail = !issue(c + kStageBuffers);
+        if (__any_sync(0xffffffffu, fail)) return false;
+    }
+    qn = q0 + (uint32_t)nch;
+    return true;
+}
+
 template <bool B_MN, int EPI>
 __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __grid_constant__ Params p) {
     using C = Gemm2Nf4Cfg;
@@ -224,7 +311,10 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
     uint64_t* tfull = empty + C::STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* efull = drain + 1;       // staged e, u chunks of the GLU backward epilogue
+    uint64_t* eempty = efull + kStageBuffers;
+    uint64_t* scrfree = eempty + kStageBuffers;  // the epilogue has released the slot it borrowed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(scrfree + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // what each stage holds, written by this CTA's producer before the stage's loads: 0 bf16 B
     // (nothing to decode), 1 NF4 codes, 3 | G << 8 int4 codes with groups of G, 4 | map << 8 NVFP4
@@ -252,6 +342,11 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
             mbar_init(smem_u32(&tempty[a]), 2 * kNumEpiWarps);
         }
         mbar_init(smem_u32(drain), 1);
+        for (int b = 0; b < kStageBuffers; ++b) {
+            mbar_init(smem_u32(&efull[b]), 1);
+            mbar_init(smem_u32(&eempty[b]), kNumEpiWarps);
+        }
+        mbar_init(smem_u32(scrfree), kNumEpiWarps);
         *s_abort = 0;
         fence_mbar_init();
         for (int i = 0; i < kMaxMaps; ++i)
@@ -280,6 +375,12 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
+            // A GLU backward epilogue that stages e, u borrows the slot of its tile's last K block
+            // (iteration E - 1, E = K blocks issued up to the end of the tile); iteration E + 3 is
+            // the next load into that slot and waits until the epilogue has released it.  Every
+            // unit of such a launch has at least four K blocks, so the gate falls inside the next
+            // tile and the releases are waited for in order, one phase at a time.
+            uint32_t it = 0, gate[4] = {0u, 0u, 0u, 0u}, gh = 0, gt = 0, nrel = 0;
             for (int u = cid; ok && u < p.total_units; u += ncl) {
                 const Unit U = decode_unit(p, u);
                 const Prob& P = p.prob[U.pi];
@@ -299,10 +400,19 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     const int32_t tag = !nf4 ? 0 : q4g > 0 ? (3 | (q4g << 8)) : q4g < 0 ? (4 | (smap << 8)) : 1;
                     const int brow = U.nb * P.n_step + (int)rank * S.b_rank_off;
                     for (int kb = kb0; kb < kb1; ++kb) {
+                        if (gh != gt && gate[gh & 3] == it) {
+                            if (!mbar_wait(smem_u32(scrfree), nrel & 1u, s_abort)) {
+                                ok = false;
+                                break;
+                            }
+                            ++nrel;
+                            ++gh;
+                        }
                         if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) {
                             ok = false;
                             break;
                         }
+                        ++it;
                         const uint32_t sA = smem_u32(smem + stage * C::STAGE_BYTES);
                         const uint32_t sB = sA + C::A_BYTES;
                         const uint32_t sC = sB + C::B_BYTES;
@@ -339,6 +449,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                         }
                     }
                 }
+                if (EPI == EPI_GLU_BWD && P.in_map[0] >= 0) gate[gt++ & 3] = it + 3;
             }
             // one end-of-work stage for each decode group (the next stage in its round-robin)
             for (int g = 0; ok && g < kPairNf4DecodeGroups; ++g) {
@@ -515,10 +626,15 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
         const int q = warp & 3;
         const int hh = ew >> 2;  // M half
         uint32_t aphase = 0;
+        uint32_t kdone = 0;  // K blocks of this CTA's tiles so far: the stage ring's position
+        uint32_t qn = 0;     // e, u chunks staged so far
         bool ok = true;
         for (int u = cid; u < p.total_units; u += ncl) {
             const Unit U = decode_unit(p, u);
             const Prob& P = p.prob[U.pi];
+            int g0, g1;
+            unit_kslice(P, U, g0, g1);
+            kdone += (uint32_t)(g1 - g0);
             if (!mbar_wait(smem_u32(&tfull[0]), aphase, s_abort)) {
                 ok = false;
                 break;
@@ -526,7 +642,21 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
             tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + hh * 256;
             const int64_t m = (int64_t)U.mb * 512 + hh * 256 + (int64_t)rank * kBM + q * 32 + lane;
-            if constexpr (EPI == EPI_GLU_FWD) {
+            if constexpr (EPI == EPI_GLU_BWD) {
+                if (P.in_map[0] >= 0) {
+                    // the slot of the tile's last K block: free once the MMAs behind tfull are done
+                    const uint32_t scr = smem_u32(smem + ((kdone - 1u) % C::STAGES) * C::STAGE_BYTES);
+                    if (!glu_bwd_staged(p, P, U, tacc, m, scr, smem_u32(&efull[0]), smem_u32(&eempty[0]), rank,
+                                        ew == 0 && lane == 0, hh, q * 32 + lane, qn, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(scrfree));
+                } else {
+                    epilogue_cols<EPI>(P, U, tacc, 0, P.bn, 16, m, m < P.M);
+                }
+            } else if constexpr (EPI == EPI_GLU_FWD) {
                 epilogue_cols<EPI>(P, U, tacc, 0, P.bn >> 1, 16, m, m < P.M);
             } else if (EPI == EPI_STORE && U.tail >= 0) {
                 // part U.ks of a split tail tile: the raw fp32 accumulator row to its block
