@@ -33,6 +33,9 @@ NF4_MLP = [
     ("ragged_nf4_geglu", 300, 256, 448, 16, 32.0, "geglu", False),
     ("nf4_r64", 200, 128, 256, 64, 128.0, "swiglu", False),
     ("nf4_zero_base", 260, 256, 320, 16, 32.0, "geglu", True),
+    # four K blocks per dh tile (the fewest with which its epilogue borrows a stage slot) and
+    # 80 tiles, so that some CTA pairs run two
+    ("nf4_four_kblocks", 2048, 192, 5120, 16, 32.0, "swiglu", False),
 ]
 
 
