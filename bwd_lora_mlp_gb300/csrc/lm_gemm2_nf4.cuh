@@ -33,7 +33,9 @@
 // blocks are decoded at once and each thread decodes one 64-element block of each), warps 10-17
 // epilogue.  The producer tags every stage for the decoders (bf16, NF4, int4 with its group size,
 // NVFP4 with its scale map, or end of work), so they follow the stage ring without walking the
-// work-unit sequence themselves.
+// work-unit sequence themselves.  The GLU backward epilogue (dh) may borrow the stage slot of its
+// tile's last K block to stage e, u through shared memory (glu_bwd_staged); the producer then
+// holds back the next load into that slot until the epilogue releases it.
 #pragma once
 
 #include "lm_gemm2.cuh"
