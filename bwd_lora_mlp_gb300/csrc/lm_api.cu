@@ -848,7 +848,7 @@ void add_colreduce(Builder& b, const uint16_t* Z, int64_t T, int64_t C, const ui
 // finalisation launch.  Each problem streams its activation Z once; gradients that reduce the
 // same Z (the dA of every projection fed by X) are one problem whose B stacks their rank blocks.
 struct ColReduce {
-    static constexpr int kMaxJobs = 6;
+    static constexpr int kMaxJobs = kMaxFinColJobs;
     Builder b{G_PART_MNK};
     const Dims& D;
     float* next;
@@ -860,6 +860,10 @@ struct ColReduce {
     // else in dB layout (C x r)
     void add(const uint16_t* Z, int64_t C, const uint16_t* PT, std::initializer_list<float*> outs, int transposed) {
         const int nb = (int)outs.size();
+        if (njobs + nb > kMaxJobs || b.p.nprob >= kMaxProbs) {
+            if (b.st == LM_OK) b.st = fail(LM_ERR_UNSUPPORTED, "too many gradient reductions in one launch");
+            return;
+        }
         const int64_t w = (int64_t)nb * D.rp;
         float* q = next;
         next += (size_t)kMaxSplits * C * w;

@@ -72,7 +72,7 @@ cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cuda
 }
 
 struct FinColJobs {
-    FinColJob j[6];
+    FinColJob j[kMaxFinColJobs];
 };
 
 // One thread per (column c, 4-wide chunk of j), chunk fastest: the partial reads of a warp are
@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(256) fin_colreduce_kernel(FinColJobs jobs) {
 }
 
 cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t st) {
+    if (njobs < 1 || njobs > kMaxFinColJobs) return cudaErrorInvalidValue;
     FinColJobs js{};
     int64_t most = 0;
     for (int i = 0; i < njobs; ++i) {

@@ -72,6 +72,7 @@ struct FinColJob {
     float* out;
     int32_t ldp;             // floats per partial row: rp, or nb * rp when nb projections share Z
 };
+constexpr int kMaxFinColJobs = 6;  // jobs of one finalisation launch
 cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t st);
 
 cudaError_t launch_nf4_pack(const uint16_t* W, int64_t numel, uint8_t* codes, int8_t* absmax_q,
