@@ -36,6 +36,7 @@ METRICS = {"mlp": METRIC,
            "o": "LoRA-O fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300",
            "relu2": "LoRA ReLU^2-MLP fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300"}
 UNIT = "tokens/s"
+NOMINAL_BF16_TFLOPS = 2250.0  # dense bf16 tensor peak of one GB300, nominal (no sparsity)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -512,7 +513,10 @@ def main():
         "tflops": tflops,
         "roofline_step": {"bound": "tensor", "achieved": tflops / world, "peak": peaks["bf16_tflops_sustained"],
                           "unit": "TFLOP/s", "frac": tflops / world / peaks["bf16_tflops_sustained"],
-                          "peak_source": peak_src + " sustained bf16"},
+                          "peak_source": peak_src + " sustained bf16",
+                          # the same step against the burst figure and the nominal dense bf16 peak
+                          "frac_of_burst": tflops / world / peaks["bf16_tflops"],
+                          "frac_of_nominal": tflops / world / NOMINAL_BF16_TFLOPS},
         "roofline": roofline,
         "gpu_launches": launches,
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
