@@ -91,6 +91,16 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def step_roofline(tflops_per_gpu, peaks, peak_src):
+    """The whole step's TFLOP/s per GPU against the sustained bf16 figure (the headline fraction),
+    and against the burst figure and the nominal dense bf16 peak."""
+    return {"bound": "tensor", "achieved": tflops_per_gpu, "peak": peaks["bf16_tflops_sustained"],
+            "unit": "TFLOP/s", "frac": tflops_per_gpu / peaks["bf16_tflops_sustained"],
+            "peak_source": peak_src + " sustained bf16",
+            "frac_of_burst": tflops_per_gpu / peaks["bf16_tflops"],
+            "frac_of_nominal": tflops_per_gpu / NOMINAL_BF16_TFLOPS}
+
+
 def src_digest():
     """Digest of the code of the GEMM kernel templates (the kernels the traffic figures are for):
     line comments, trailing blanks and blank lines are left out, so a comment edit keeps it."""
@@ -511,12 +521,7 @@ def main():
         "data": "synthetic: seeded W~N(0,0.02), A~U(+-1/sqrt(in)), B~N(0,0.02), X~N(0,1), dY~N(0,0.01), bf16",
         "config": cfg,
         "tflops": tflops,
-        "roofline_step": {"bound": "tensor", "achieved": tflops / world, "peak": peaks["bf16_tflops_sustained"],
-                          "unit": "TFLOP/s", "frac": tflops / world / peaks["bf16_tflops_sustained"],
-                          "peak_source": peak_src + " sustained bf16",
-                          # the same step against the burst figure and the nominal dense bf16 peak
-                          "frac_of_burst": tflops / world / peaks["bf16_tflops"],
-                          "frac_of_nominal": tflops / world / NOMINAL_BF16_TFLOPS},
+        "roofline_step": step_roofline(tflops / world, peaks, peak_src),
         "roofline": roofline,
         "gpu_launches": launches,
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},

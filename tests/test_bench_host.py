@@ -36,3 +36,14 @@ def test_base_gemm_kernel_flops_cover_the_six_base_gemms():
     # inside dh, and G_g A_g + G_u A_u inside dX: 2 T r per output column each
     assert total == 12 * T * d * n + 2 * T * r * (2 * n + d + n + 2 * d)
     assert 5.8e12 < bench.workload_flops(w) < 5.83e12       # 710 MFLOP per token at the 8B sizes
+
+
+def test_step_roofline_fractions():
+    peaks, src = bench.load_peaks()
+    r = bench.step_roofline(1600.0, peaks, src)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["peak"] == peaks["bf16_tflops_sustained"]
+    assert abs(r["frac"] * peaks["bf16_tflops_sustained"] - 1600.0) < 1e-9
+    assert abs(r["frac_of_burst"] * peaks["bf16_tflops"] - 1600.0) < 1e-9
+    assert abs(r["frac_of_nominal"] - 1600.0 / 2250.0) < 1e-12
+    assert r["frac_of_nominal"] < r["frac_of_burst"] <= r["frac"]
