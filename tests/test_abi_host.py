@@ -215,3 +215,162 @@ def test_profile_summary_empty_without_launches(so):
     assert L.lm_profile_summary() == {}
     L.lm_profile_enable(False)
     assert L.call_status("lm_profile_summary", None, 0) == L.LM_ERR_NULL
+
+
+# ---------------------------------------------------------------------------- the other entry points
+
+def _reaches_device(call, a):
+    """The untouched argument set passes every host check: without a GPU the call then fails at
+    its first CUDA call.  With a GPU present it is not made at all (the fake pointers would be
+    launched on)."""
+    import torch
+    if torch.cuda.is_available():
+        return True
+    return call(a) in (L.LM_ERR_CUDA, L.LM_ERR_UNSUPPORTED)
+
+
+def _mlp_bwd_args(T=512, d=256, n=704, r=8):
+    a = _mlp_args(T=T, d=d, n=n, r=r)
+    f = Fake()
+    f.next = 1 << 40
+    a.update(dY=f(T * d * 2), dX=f(T * d * 2), dAg=f(r * d * 4), dBg=f(n * r * 4), dAu=f(r * d * 4),
+             dBu=f(n * r * 4), dAd=f(r * n * 4), dBd=f(d * r * 4))
+    return a
+
+
+def _bwd(a):
+    return L.call_status("lora_mlp_bwd", a["T"], a["d"], a["n"], a["act"], a["X"], a["dY"], a["e"], a["u"], a["h"],
+                         a["saved"], a["saved_bytes"], ctypes.byref(a["gate"]), ctypes.byref(a["up"]),
+                         ctypes.byref(a["down"]), a["dX"], a["dAg"], a["dBg"], a["dAu"], a["dBu"], a["dAd"],
+                         a["dBd"], a["ws"], a["ws_bytes"], None)
+
+
+def test_mlp_bwd_argument_errors(so):
+    a = _mlp_bwd_args()
+    assert _reaches_device(_bwd, a)
+    assert _bwd(dict(a, dX=None)) == L.LM_ERR_NULL
+    assert _bwd(dict(a, dAd=None)) == L.LM_ERR_NULL
+    assert _bwd(dict(a, dY=a["dY"] + 2)) == L.LM_ERR_ALIGN
+    assert _bwd(dict(a, dX=a["dY"])) == L.LM_ERR_ALIAS                     # output over an input
+    assert _bwd(dict(a, dBg=a["dAg"])) == L.LM_ERR_ALIAS                   # two outputs overlap
+    assert _bwd(dict(a, ws_bytes=a["ws_bytes"] - 1)) == L.LM_ERR_WORKSPACE
+    assert _bwd(dict(a, saved_bytes=16)) == L.LM_ERR_WORKSPACE
+    assert _bwd(dict(a, act=7)) == L.LM_ERR_DTYPE
+    assert _bwd(dict(a, n=720)) == L.LM_ERR_SHAPE                          # W shapes say 704
+
+
+def _relu2_args(T=384, d=256, n=512, r=16):
+    f = Fake()
+    a = dict(T=T, d=d, n=n, X=f(T * d * 2), up=_lora(f, d, n, r), down=_lora(f, n, d, r), y=f(T * d * 2),
+             u=f(T * n * 2), h=f(T * n * 2), dY=f(T * d * 2), dX=f(T * d * 2), dAu=f(r * d * 4),
+             dBu=f(n * r * 4), dAd=f(r * n * 4), dBd=f(d * r * 4))
+    a["saved_bytes"] = _size("lora_relu2_mlp_saved_size", T, r)[1]
+    a["saved"] = f(a["saved_bytes"])
+    a["ws_bytes"] = _size("lora_relu2_mlp_workspace_size", T, d, n, r)[1]
+    a["ws"] = f(a["ws_bytes"])
+    return a
+
+
+def _relu2_fwd(a):
+    return L.call_status("lora_relu2_mlp_fwd", a["T"], a["d"], a["n"], a["X"], ctypes.byref(a["up"]),
+                         ctypes.byref(a["down"]), a["y"], a["u"], a["h"], a["saved"], a["saved_bytes"], a["ws"],
+                         a["ws_bytes"], None)
+
+
+def _relu2_bwd(a):
+    return L.call_status("lora_relu2_mlp_bwd", a["T"], a["d"], a["n"], a["X"], a["dY"], a["u"], a["h"], a["saved"],
+                         a["saved_bytes"], ctypes.byref(a["up"]), ctypes.byref(a["down"]), a["dX"], a["dAu"],
+                         a["dBu"], a["dAd"], a["dBd"], a["ws"], a["ws_bytes"], None)
+
+
+def test_relu2_argument_errors(so):
+    a = _relu2_args()
+    assert _reaches_device(_relu2_fwd, a)
+    assert _reaches_device(_relu2_bwd, a)
+    assert _relu2_fwd(dict(a, y=None)) == L.LM_ERR_NULL
+    assert _relu2_fwd(dict(a, X=a["X"] + 2)) == L.LM_ERR_ALIGN
+    assert _relu2_fwd(dict(a, h=a["u"])) == L.LM_ERR_ALIAS
+    assert _relu2_fwd(dict(a, ws_bytes=a["ws_bytes"] - 1)) == L.LM_ERR_WORKSPACE
+    assert _relu2_fwd(dict(a, d=250)) == L.LM_ERR_SHAPE
+    assert _relu2_bwd(dict(a, dBu=None)) == L.LM_ERR_NULL
+    assert _relu2_bwd(dict(a, dX=a["X"])) == L.LM_ERR_ALIAS
+    assert _relu2_bwd(dict(a, saved_bytes=16)) == L.LM_ERR_WORKSPACE
+
+
+def _qkv_args(T=300, d=256, nq=256, nk=64, nv=128, r=16):
+    f = Fake()
+    a = dict(T=T, d=d, nq=nq, nk=nk, nv=nv, X=f(T * d * 2), q=_lora(f, d, nq, r), k=_lora(f, d, nk, r),
+             v=_lora(f, d, nv, r), Q=f(T * nq * 2), K=f(T * nk * 2), V=f(T * nv * 2), dQ=f(T * nq * 2),
+             dK=f(T * nk * 2), dV=f(T * nv * 2), dX=f(T * d * 2),
+             dAq=f(r * d * 4), dBq=f(nq * r * 4), dAk=f(r * d * 4), dBk=f(nk * r * 4), dAv=f(r * d * 4),
+             dBv=f(nv * r * 4))
+    a["saved_bytes"] = _size("lora_qkv_saved_size", T, r)[1]
+    a["saved"] = f(a["saved_bytes"])
+    a["ws_bytes"] = _size("lora_qkv_workspace_size", T, d, nq, nk, nv, r)[1]
+    a["ws"] = f(a["ws_bytes"])
+    return a
+
+
+def _qkv_fwd(a):
+    return L.call_status("lora_qkv_fwd", a["T"], a["d"], a["nq"], a["nk"], a["nv"], a["X"], ctypes.byref(a["q"]),
+                         ctypes.byref(a["k"]), ctypes.byref(a["v"]), a["Q"], a["K"], a["V"], a["saved"],
+                         a["saved_bytes"], a["ws"], a["ws_bytes"], None)
+
+
+def _qkv_bwd(a):
+    return L.call_status("lora_qkv_bwd", a["T"], a["d"], a["nq"], a["nk"], a["nv"], a["X"], a["dQ"], a["dK"],
+                         a["dV"], a["saved"], a["saved_bytes"], ctypes.byref(a["q"]), ctypes.byref(a["k"]),
+                         ctypes.byref(a["v"]), a["dX"], a["dAq"], a["dBq"], a["dAk"], a["dBk"], a["dAv"],
+                         a["dBv"], a["ws"], a["ws_bytes"], None)
+
+
+def test_qkv_argument_errors(so):
+    a = _qkv_args()                          # K and V of different widths are accepted
+    assert _reaches_device(_qkv_fwd, a)
+    assert _reaches_device(_qkv_bwd, a)
+    assert _qkv_fwd(dict(a, K=None)) == L.LM_ERR_NULL
+    assert _qkv_fwd(dict(a, X=a["X"] + 2)) == L.LM_ERR_ALIGN
+    assert _qkv_fwd(dict(a, V=a["Q"])) == L.LM_ERR_ALIAS
+    assert _qkv_fwd(dict(a, ws_bytes=a["ws_bytes"] - 1)) == L.LM_ERR_WORKSPACE
+    assert _qkv_fwd(dict(a, nv=96)) == L.LM_ERR_SHAPE                      # v.W has 128 rows
+    b = _qkv_args()
+    b["k"].r = 8
+    assert _qkv_fwd(b) == L.LM_ERR_SHAPE                                   # ranks differ
+    assert _qkv_bwd(dict(a, dBv=None)) == L.LM_ERR_NULL
+    assert _qkv_bwd(dict(a, dX=a["dQ"])) == L.LM_ERR_ALIAS
+    assert _qkv_bwd(dict(a, saved_bytes=16)) == L.LM_ERR_WORKSPACE
+
+
+def _o_args(T=257, din=512, dout=256, r=16):
+    f = Fake()
+    a = dict(T=T, din=din, dout=dout, X=f(T * din * 2), o=_lora(f, din, dout, r), Y=f(T * dout * 2),
+             dY=f(T * dout * 2), dX=f(T * din * 2), dA=f(r * din * 4), dB=f(dout * r * 4))
+    a["saved_bytes"] = _size("lora_o_saved_size", T, r)[1]
+    a["saved"] = f(a["saved_bytes"])
+    a["ws_bytes"] = _size("lora_o_workspace_size", T, din, dout, r)[1]
+    a["ws"] = f(a["ws_bytes"])
+    return a
+
+
+def _o_fwd(a):
+    return L.call_status("lora_o_fwd", a["T"], a["din"], a["dout"], a["X"], ctypes.byref(a["o"]), a["Y"], a["saved"],
+                         a["saved_bytes"], a["ws"], a["ws_bytes"], None)
+
+
+def _o_bwd(a):
+    return L.call_status("lora_o_bwd", a["T"], a["din"], a["dout"], a["X"], a["dY"], a["saved"], a["saved_bytes"],
+                         ctypes.byref(a["o"]), a["dX"], a["dA"], a["dB"], a["ws"], a["ws_bytes"], None)
+
+
+def test_o_argument_errors(so):
+    a = _o_args()
+    assert _reaches_device(_o_fwd, a)
+    assert _reaches_device(_o_bwd, a)
+    assert _o_fwd(dict(a, Y=None)) == L.LM_ERR_NULL
+    assert _o_fwd(dict(a, X=a["X"] + 2)) == L.LM_ERR_ALIGN
+    assert _o_fwd(dict(a, Y=a["X"])) == L.LM_ERR_ALIAS
+    assert _o_fwd(dict(a, ws_bytes=a["ws_bytes"] - 1)) == L.LM_ERR_WORKSPACE
+    assert _o_fwd(dict(a, dout=288)) == L.LM_ERR_SHAPE                     # W has 256 rows
+    assert _o_bwd(dict(a, dA=None)) == L.LM_ERR_NULL
+    assert _o_bwd(dict(a, dB=a["dA"])) == L.LM_ERR_ALIAS
+    assert _o_bwd(dict(a, saved_bytes=16)) == L.LM_ERR_WORKSPACE
