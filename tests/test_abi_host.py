@@ -374,3 +374,10 @@ def test_o_argument_errors(so):
     assert _o_bwd(dict(a, dA=None)) == L.LM_ERR_NULL
     assert _o_bwd(dict(a, dB=a["dA"])) == L.LM_ERR_ALIAS
     assert _o_bwd(dict(a, saved_bytes=16)) == L.LM_ERR_WORKSPACE
+
+
+def test_empty_token_count_forwards_are_no_ops(so):
+    # (the backwards zero their gradients for T = 0, a device call, so they are not made here)
+    assert _relu2_fwd(_relu2_args(T=0)) == L.LM_OK
+    assert _qkv_fwd(_qkv_args(T=0)) == L.LM_OK
+    assert _o_fwd(_o_args(T=0)) == L.LM_OK
