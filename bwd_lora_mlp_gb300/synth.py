@@ -105,9 +105,10 @@ def relu2_workload(name, T, d, n, r, alpha, nf4=False) -> Workload:
                     nf4=nf4)
 
 
-def qkv_workload(name, T, d, q, kv, r, alpha, nf4=False) -> Workload:
+def qkv_workload(name, T, d, q, kv, r, alpha, nf4=False, v=None) -> Workload:
+    """Q (d -> q), K (d -> kv) and V (d -> kv, or d -> v when given)."""
     return Workload(name, "qkv", T, r, alpha,
-                    [ProjSpec("q", d, q), ProjSpec("k", d, kv), ProjSpec("v", d, kv)], nf4=nf4)
+                    [ProjSpec("q", d, q), ProjSpec("k", d, kv), ProjSpec("v", d, kv if v is None else v)], nf4=nf4)
 
 
 def o_workload(name, T, d_in, d_out, r, alpha, nf4=False) -> Workload:

@@ -140,8 +140,8 @@ def test_activation_values_and_derivatives():
         np.testing.assert_allclose(fp(xs), fd, rtol=1e-8, atol=1e-9)
 
 
-def _small_qkv():
-    w = synth.qkv_workload("t", 40, 64, 64, 32, 8, 16.0)
+def _small_qkv(v=None):
+    w = synth.qkv_workload("t", 40, 64, 64, 32, 8, 16.0, v=v)
     inp = synth.make_inputs(w, seed=5)
     p = {}
     for t in ("q", "k", "v"):
@@ -153,8 +153,10 @@ def _small_qkv():
     return O.from_bf16(inp["X"]), dys, p
 
 
-def test_qkv_is_three_lora_w_with_summed_dX():
-    X, (dQ, dK, dV), p = _small_qkv()
+@pytest.mark.parametrize("v", [None, 96])   # V as wide as K, or wider
+def test_qkv_is_three_lora_w_with_summed_dX(v):
+    X, (dQ, dK, dV), p = _small_qkv(v)
+    assert dV.shape[1] == (32 if v is None else v)
     fw = O.qkv_forward(X, p)
     bw = O.qkv_backward(X, dQ, dK, dV, p)
     dX = np.zeros_like(X)
