@@ -47,3 +47,25 @@ def test_step_roofline_fractions():
     assert abs(r["frac_of_burst"] * peaks["bf16_tflops"] - 1600.0) < 1e-9
     assert abs(r["frac_of_nominal"] - 1600.0 / 2250.0) < 1e-12
     assert r["frac_of_nominal"] < r["frac_of_burst"] <= r["frac"]
+
+
+def test_traffic_record_is_used_only_for_the_sources_it_was_taken_on(monkeypatch):
+    rec = bench.committed_traffic("mlp.gateup", "llama3_8b_mlp_bf16")
+    assert rec is None or rec > 10 ** 9          # a full-size launch moves over a GB
+    monkeypatch.setattr(bench, "src_digest", lambda: "0000000000000000")
+    assert bench.committed_traffic("mlp.gateup", "llama3_8b_mlp_bf16") is None
+    assert bench.committed_traffic("mlp.unknown", "llama3_8b_mlp_bf16") is None
+
+
+def test_source_digest_ignores_comments(tmp_path, monkeypatch):
+    src = tmp_path / "bwd_lora_mlp_gb300" / "csrc"
+    src.mkdir(parents=True)
+    names = ("lm_gemm.cuh", "lm_gemm2.cuh", "lm_gemm2_nf4.cuh", "lm_ptx.cuh")
+    for n in names:
+        (src / n).write_text("int a = 1;  // one\n\n// note\nint b = 2;\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d0 = bench.src_digest()
+    (src / names[0]).write_text("int a = 1;  // changed comment\n// another note\nint b = 2;   \n")
+    assert bench.src_digest() == d0
+    (src / names[0]).write_text("int a = 3;\nint b = 2;\n")
+    assert bench.src_digest() != d0
