@@ -36,6 +36,8 @@ METRICS = {"mlp": METRIC,
            "o": "LoRA-O fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300",
            "relu2": "LoRA ReLU^2-MLP fwd+bwd tokens/s and TFLOP/s (frac. of BF16 roofline), 1×GB300"}
 UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "llama3_8b_mlp_bf16"
+NF4_WORKLOAD = "llama3_8b_mlp_nf4"
 NOMINAL_BF16_TFLOPS = 2250.0  # dense bf16 tensor peak of one GB300, nominal (no sparsity)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -295,10 +297,11 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama3_8b_mlp_bf16")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--tokens", type=int, default=None,
                     help="run the workload's shapes with this many tokens (small cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-nf4", action="store_true", help="skip the NF4-base step the default run adds")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -318,7 +321,51 @@ def main():
     import torch
     import __graft_entry__
     __graft_entry__.build()
+
+    rec = measure(w, args, world, local, e2e=True)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and w.kind == "mlp":
+        cpu = cpu_baseline(w, rec.pop("_inputs"))
+    rec.pop("_inputs", None)
+    line = {
+        "metric": METRICS[w.kind], "value": rec["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": rec["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded W~N(0,0.02), A~U(+-1/sqrt(in)), B~N(0,0.02), X~N(0,1), dY~N(0,0.01), bf16",
+        "config": rec["config"],
+        "tflops": rec["tflops"],
+        "roofline_step": rec["roofline_step"],
+        "roofline": rec["roofline"],
+        "gpu_launches": rec["gpu_launches"],
+        "kernels_ms_per_step": rec["kernels_ms_per_step"],
+        "clocks": rec["clocks"],
+        "e2e": rec["e2e"],
+        "cpu_baseline": cpu,
+    }
+    # the default run also times the same MLP on an NF4-packed base (QLoRA), in the same process
+    # after the headline: its own step time, roofline and kernel times, nested under "nf4"
+    if args.workload == DEFAULT_WORKLOAD and not args.tokens and not args.no_nf4:
+        wn = synth.WORKLOADS[NF4_WORKLOAD]
+        rn = measure(wn, args, world, local, e2e=False)
+        rn.pop("_inputs", None)
+        line["nf4"] = {k: rn[k] for k in ("ms_per_step", "value", "tflops", "config", "roofline_step", "roofline",
+                                          "gpu_launches", "kernels_ms_per_step", "clocks")}
+        line["nf4"]["metric"] = METRICS["mlp"].replace("LoRA-MLP", "QLoRA-MLP (NF4 base)")
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def measure(w, args, world, local, e2e=True):
+    """Time args.steps steps of workload w (after args.warmup untimed ones) with CUDA events on the
+    launching stream; then the same steps with the library's launch tracing for per-kernel times;
+    then (e2e) the end-to-end figure through the C ABI from pinned host buffers."""
+    import torch
     from bwd_lora_mlp_gb300 import lib as L
+    from bwd_lora_mlp_gb300 import synth
 
     T, r = w.T, w.r
     inp = synth.make_inputs(w)
@@ -448,62 +495,80 @@ def main():
         roofline = {"bound": "tensor", "kernel": dom_tag, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                     "frac": ach / peak, "traffic": committed_traffic(dom_tag, w.name),
                     "peak_source": peak_src + " sustained bf16", "flops_per_launch": kf,
-                    "ms_per_launch": per_launch_ms}
+                    "ms_per_launch": per_launch_ms, "frac_of_burst": ach / peaks["bf16_tflops"],
+                    "burst_peak": peaks["bf16_tflops"]}
 
-    # ---- end to end through the C ABI from pinned host buffers: every step copies its inputs in
-    # and its results out; the copies of neighbouring steps run on their own streams and overlap
-    # the current step's kernels (inputs and outputs are double-buffered on the device)
-    host_in = [host_pinned(inp[k]) for k in in_names]
-    host_out = [{k: torch.empty_like(v, device="cpu").pin_memory() for k, v in dev_outs.items()} for _ in range(2)]
-    dev_in = [[torch.empty_like(t) for t in ins] for _ in range(2)]
-    dev_out = [{k: torch.empty_like(v) for k, v in dev_outs.items()} for _ in range(2)]
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = lambda: torch.cuda.Event()
-    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-    for e_ in out_done + comp_done:
-        e_.record(stream)
+    e2e_rec = None
+    if e2e:
+        # ---- end to end through the C ABI from pinned host buffers: every step copies its inputs in
+        # and its results out; the copies of neighbouring steps run on their own streams and overlap
+        # the current step's kernels (inputs and outputs are double-buffered on the device)
+        host_in = [host_pinned(inp[k]) for k in in_names]
+        host_out = [{k: torch.empty_like(v, device="cpu").pin_memory() for k, v in dev_outs.items()} for _ in range(2)]
+        dev_in = [[torch.empty_like(t) for t in ins] for _ in range(2)]
+        dev_out = [{k: torch.empty_like(v) for k, v in dev_outs.items()} for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event()
+        in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        for e_ in out_done + comp_done:
+            e_.record(stream)
 
-    def e2e_run(nsteps):
-        for i in range(nsteps):
-            b = i & 1
-            with torch.cuda.stream(s_in):          # inputs of step i (after step i-2 stopped reading them)
-                s_in.wait_event(comp_done[b])
-                for dst, src in zip(dev_in[b], host_in):
-                    dst.copy_(src, non_blocking=True)
-                in_done[b].record(s_in)
-            stream.wait_event(in_done[b])           # step i's kernels
-            stream.wait_event(out_done[b])          # after step i-2's results were copied out
-            run(dev_in[b], dev_out[b])
-            comp_done[b].record(stream)
-            with torch.cuda.stream(s_out):         # results of step i
-                s_out.wait_event(comp_done[b])
-                for k, v in host_out[b].items():
-                    v.copy_(dev_out[b][k], non_blocking=True)
-                out_done[b].record(s_out)
+        def e2e_run(nsteps):
+            for i in range(nsteps):
+                b = i & 1
+                with torch.cuda.stream(s_in):          # inputs of step i (after step i-2 stopped reading them)
+                    s_in.wait_event(comp_done[b])
+                    for dst, src in zip(dev_in[b], host_in):
+                        dst.copy_(src, non_blocking=True)
+                    in_done[b].record(s_in)
+                stream.wait_event(in_done[b])           # step i's kernels
+                stream.wait_event(out_done[b])          # after step i-2's results were copied out
+                run(dev_in[b], dev_out[b])
+                comp_done[b].record(stream)
+                with torch.cuda.stream(s_out):         # results of step i
+                    s_out.wait_event(comp_done[b])
+                    for k, v in host_out[b].items():
+                        v.copy_(dev_out[b][k], non_blocking=True)
+                    out_done[b].record(s_out)
 
-    e2e_steps = max(4, min(args.steps, 20))
-    e2e_run(2)
-    torch.cuda.synchronize()
-    barrier(world)
-    # three windows of e2e_steps steps each; the median window (the host-copy path shows
-    # occasional slow windows)
-    windows = []
-    for _ in range(3):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        s_in.wait_stream(stream)
-        e2e_run(e2e_steps)
-        stream.wait_stream(s_out)
-        e1.record(stream)
+        e2e_steps = max(4, min(args.steps, 20))
+        e2e_run(2)
         torch.cuda.synchronize()
-        windows.append(e0.elapsed_time(e1) / e2e_steps)
-    e2e_ms = max_over_ranks(statistics.median(windows), world)
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and w.kind == "mlp":
-        cpu = cpu_baseline(w, inp)
+        barrier(world)
+        # three windows of e2e_steps steps each; the median window (the host-copy path shows
+        # occasional slow windows)
+        windows = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            s_in.wait_stream(stream)
+            e2e_run(e2e_steps)
+            stream.wait_stream(s_out)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            windows.append(e0.elapsed_time(e1) / e2e_steps)
+        e2e_ms = max_over_ranks(statistics.median(windows), world)
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
+        # the same calls one at a time: a step's copy-in, kernels and copy-out back to back on the
+        # launching stream, the host waiting for each step (what one synchronous call costs)
+        sync = []
+        for _ in range(e2e_steps):
+            t0 = time.perf_counter()
+            for dst, src in zip(dev_in[0], host_in):
+                dst.copy_(src, non_blocking=True)
+            run(dev_in[0], dev_out[0])
+            for k, v in host_out[0].items():
+                v.copy_(dev_out[0][k], non_blocking=True)
+            stream.synchronize()
+            sync.append((time.perf_counter() - t0) * 1e3)
+        sync_ms = max_over_ranks(statistics.median(sync), world)
+        e2e_rec = {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                   "copies": "pipelined: step i's host copies overlap steps i-1 and i+1",
+                   "sync_call": {"ms_per_step": sync_ms, "value": world * T / (sync_ms / 1e3),
+                                 "how": "copy-in, fwd+bwd and copy-out of one step, then a host wait; median "
+                                        "of %d calls" % e2e_steps}}
 
     d_in, d_out = w.projs[0].d_in, w.projs[-1].d_out
     cfg = {"workload": w.name, "T": T, "r": r, "alpha": w.alpha, "base": "nf4" if w.nf4 else ("int4_g%d" % w.int4_group if w.int4_group else ("nvfp4" if w.nvfp4 else "bf16")), "lora_params": "fp32" if w.ab_f32 else "bf16"}
@@ -514,28 +579,13 @@ def main():
     cfg.update(parallelism="replicas" if world > 1 else "single",
                l2="no flush: the working set (weights, activations and saved tensors of the step) exceeds the "
                   "129 MB L2")
-    line = {
-        "metric": METRICS[w.kind], "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic: seeded W~N(0,0.02), A~U(+-1/sqrt(in)), B~N(0,0.02), X~N(0,1), dY~N(0,0.01), bf16",
-        "config": cfg,
-        "tflops": tflops,
-        "roofline_step": step_roofline(tflops / world, peaks, peak_src),
-        "roofline": roofline,
-        "gpu_launches": launches,
-        "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
-        "clocks": clocks,
-        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "cpu_baseline": cpu,
-    }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    return 0
+    if clocks and clocks.get("sm_mhz"):
+        # the step in SM clock cycles at the median clock under load, to read clock dependence
+        clocks["step_mcycles_at_median_clock"] = ms * clocks["sm_mhz"] / 1e3
+    return {"value": value, "ms_per_step": ms, "tflops": tflops, "config": cfg,
+            "roofline_step": step_roofline(tflops / world, peaks, peak_src), "roofline": roofline,
+            "gpu_launches": launches, "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
+            "clocks": clocks, "e2e": e2e_rec, "_inputs": inp}
 
 
 if __name__ == "__main__":

@@ -1,6 +1,11 @@
 """Build liblora_mlp.so in-tree with nvcc for sm_103a.
 
-    python -m bwd_lora_mlp_gb300.build          # build if any source is newer than the library
+    python -m bwd_lora_mlp_gb300.build          # build unless the library matches the sources
+
+The library is reused only when the digest stored beside it (liblora_mlp.so.digest) equals the
+digest of the current sources (every file of csrc/, the public header, this script) and of the
+compiler flags; file times play no part, so a library copied in from elsewhere, or left over from
+other sources, is rebuilt.
 
 The translation units compile in parallel; the library links the CUDA runtime statically and
 reaches the driver only through cudaGetDriverEntryPointByVersion, so it loads on machines
@@ -8,6 +13,7 @@ without a GPU (the host-side argument checks and the NF4 code table work there).
 """
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -20,6 +26,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblora_mlp.so")
+DIGEST = LIB + ".digest"
 
 SOURCES = ["lm_api.cu", "lm_aux.cu", "lm_gemm_fwd.cu", "lm_gemm_bwd.cu", "lm_gemm2.cu", "lm_gemm2_nf4.cu", "lm_static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -37,18 +44,33 @@ def _nvcc() -> str:
 def _deps() -> list:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "lora_mlp.h"),
                                                                   os.path.abspath(__file__)]
-    return [f for f in files if os.path.isfile(f)]
+    return sorted(f for f in files if os.path.isfile(f))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def source_digest(extra_flags=None) -> str:
+    """sha256 over the build inputs: each source file's name and bytes, the target and the flags."""
+    h = hashlib.sha256()
+    for f in _deps():
+        h.update(os.path.relpath(f, ROOT).encode() + b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+        h.update(b"\0")
+    # the flags without the include paths, which name this checkout's location
+    flags = [f for f in ARCH + FLAGS + list(extra_flags or []) if not f.startswith("-I")]
+    h.update(" ".join(flags).encode())
+    return h.hexdigest()
+
+
+def up_to_date(extra_flags=None) -> bool:
+    if not (os.path.exists(LIB) and os.path.exists(DIGEST)):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(f) <= t for f in _deps())
+    with open(DIGEST) as f:
+        return f.read().strip() == source_digest(extra_flags)
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and up_to_date():
+    digest = source_digest(extra_flags)
+    if not force and up_to_date(extra_flags):
         return LIB
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
@@ -72,6 +94,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
     os.replace(tmp, LIB)
+    with open(DIGEST + ".tmp", "w") as f:
+        f.write(digest + "\n")
+    os.replace(DIGEST + ".tmp", DIGEST)
     return LIB
 
 

@@ -1975,9 +1975,13 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     return LM_OK;
 }
 
-extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const uint16_t* X, const uint16_t* dY,
-                                const void* saved, size_t saved_bytes, const lm_lora* o, uint16_t* dX, float* dA,
-                                float* dB, void* ws, size_t ws_bytes, lm_stream stream) {
+// Every argument check of lora_o_bwd; touches no device state.  With lib_ws the scratch is the
+// library's own array (lora_o_bwd_static): ws and ws_bytes are not looked at, the caller has
+// checked the scratch size, and no caller buffer can overlap a __device__ array of the library.
+namespace lm {
+lm_status check_o_bwd_args(int64_t T, int64_t d_in, int64_t d_out, const uint16_t* X, const uint16_t* dY,
+                           const void* saved, size_t saved_bytes, const lm_lora* o, uint16_t* dX, float* dA,
+                           float* dB, void* ws, size_t ws_bytes, bool lib_ws) {
     LM_TRY(check_o_common(T, d_in, d_out, o));
     LM_TRY(need_ptr(X, "X"));
     LM_TRY(need_ptr(dY, "dY"));
@@ -1985,17 +1989,34 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(need_ptr(dX, "dX"));
     LM_TRY(need_ptr(dA, "dA"));
     LM_TRY(need_ptr(dB, "dB"));
-    LM_TRY(need_ptr(ws, "ws"));
+    if (!lib_ws) LM_TRY(need_ptr(ws, "ws"));
     const int32_t r = o->r;
-    const bool q4 = o->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4, int4 or NVFP4)
     const OPlan PL = plan_o(T, d_in, d_out, r);
     if (saved_bytes < PL.saved_total)
         return fail(LM_ERR_WORKSPACE, "saved buffer has %zu bytes, needs %zu", saved_bytes, PL.saved_total);
-    if (ws_bytes < PL.ws_total) return fail(LM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, PL.ws_total);
-    LM_TRY(check_alias({{dX, (size_t)T * d_in * 2, "dX"}, {dA, (size_t)r * d_in * 4, "dA"},
-                        {dB, (size_t)d_out * r * 4, "dB"}, {ws, PL.ws_total, "ws"}},
-                       {{X, (size_t)T * d_in * 2, "X"}, {dY, (size_t)T * d_out * 2, "dY"},
-                        {saved, PL.saved_total, "saved"}, wspan(o, "o.W")}));
+    if (!lib_ws && ws_bytes < PL.ws_total)
+        return fail(LM_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, PL.ws_total);
+    const Span ins[] = {{X, (size_t)T * d_in * 2, "X"}, {dY, (size_t)T * d_out * 2, "dY"},
+                        {saved, PL.saved_total, "saved"}, wspan(o, "o.W")};
+    if (lib_ws)
+        LM_TRY(check_alias({{dX, (size_t)T * d_in * 2, "dX"}, {dA, (size_t)r * d_in * 4, "dA"},
+                            {dB, (size_t)d_out * r * 4, "dB"}},
+                           {ins[0], ins[1], ins[2], ins[3]}));
+    else
+        LM_TRY(check_alias({{dX, (size_t)T * d_in * 2, "dX"}, {dA, (size_t)r * d_in * 4, "dA"},
+                            {dB, (size_t)d_out * r * 4, "dB"}, {ws, PL.ws_total, "ws"}},
+                           {ins[0], ins[1], ins[2], ins[3]}));
+    return LM_OK;
+}
+}  // namespace lm
+
+extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const uint16_t* X, const uint16_t* dY,
+                                const void* saved, size_t saved_bytes, const lm_lora* o, uint16_t* dX, float* dA,
+                                float* dB, void* ws, size_t ws_bytes, lm_stream stream) {
+    LM_TRY(check_o_bwd_args(T, d_in, d_out, X, dY, saved, saved_bytes, o, dX, dA, dB, ws, ws_bytes, false));
+    const int32_t r = o->r;
+    const bool q4 = o->W.kind != LM_WEIGHT_BF16;  // packed 4-bit base (NF4, int4 or NVFP4)
+    const OPlan PL = plan_o(T, d_in, d_out, r);
     cudaStream_t st = (cudaStream_t)stream;
     if (T == 0) {
         LM_CUDA(cudaMemsetAsync(dA, 0, (size_t)r * d_in * 4, st), "cudaMemsetAsync");

@@ -31,7 +31,9 @@
  *    weight-gradient GEMMs use beta = 0).
  *  - Every pointer argument is a DEVICE pointer unless stated otherwise.  The caller owns every
  *    buffer, including the workspace; the library allocates no device memory and keeps no state
- *    other than a per-thread last-error string and cached function pointers.
+ *    other than a per-thread last-error string, cached function pointers and per-device launch
+ *    attributes.  The one exception is lora_o_bwd_static below, whose scratch is a fixed
+ *    64 MiB __device__ array of the library on every GPU that loads it.
  *  - Every compute call is asynchronous on the given stream (a cudaStream_t; NULL is the legacy
  *    default stream) and never synchronises.  Calls that share a workspace or a saved buffer
  *    must be ordered (same stream or explicit events).
@@ -252,16 +254,20 @@ LM_API lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const uint16
  * have no counterpart: this is a deployment variant, not a step of the method.  The arguments and
  * results are those of lora_o_bwd without ws / ws_bytes: the scratch is a 64 MiB __device__ array
  * inside the library, held by every GPU that loads it until the process exits.  Shapes whose
- * lora_o_workspace_size exceeds 64 MiB are rejected with LM_ERR_WORKSPACE before any device work.
- * The call allocates nothing.  All calls share the one array and it keeps the last call's contents;
- * each call clears the error word on its stream, so calls whose kernels overlap on the GPU race and
- * must be ordered by the caller.  The first call on a device (that device current) looks up the
- * array's address; make it before capturing any stream.  A bounded-wait timeout inside the kernels
- * cannot be read back through lm_workspace_check here; it shows as wrong results only. */
+ * lora_o_workspace_size exceeds 64 MiB are rejected with LM_ERR_WORKSPACE, and every other argument
+ * error is reported as lora_o_bwd reports it, all before any CUDA call.  The call allocates
+ * nothing.  All calls share the one array and it keeps the last call's contents; each call clears
+ * the array's error word on its stream, so calls whose kernels overlap on the GPU race and must be
+ * ordered by the caller.  Each call looks up the array's address on the current device; the first
+ * call on a device may load the library's device code there, so make it before capturing any
+ * stream.  lm_static_scratch_check(stream) synchronises `stream`, reads and clears the array's
+ * error word and returns LM_ERR_TIMEOUT if a kernel of a static call gave up on a bounded wait
+ * since the last check (LM_OK otherwise), as lm_workspace_check does for a workspace. */
 LM_API lm_status lora_o_bwd_static(int64_t T, int64_t d_in, int64_t d_out, const uint16_t* X,
                                    const uint16_t* dY, const void* saved, size_t saved_bytes,
                                    const lm_lora* o, uint16_t* dX, float* dA, float* dB,
                                    lm_stream stream);
+LM_API lm_status lm_static_scratch_check(lm_stream stream);
 
 /* ---- NF4 ([LL] QLoRA section) -----------------------------------------------------------
  * nf4_pack: quantise numel bf16 values W (flattened row-major) to NF4.  numel must be a

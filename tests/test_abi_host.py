@@ -19,10 +19,20 @@ def so():
 
 def test_exports_every_header_symbol(so):
     names = L.header_symbols()
-    assert len(names) == 30
+    assert len(names) == 31
     for n in names:
         assert hasattr(so, n), n
     assert set(names) == set(L._SIGS)
+
+
+def test_build_is_keyed_on_source_content(so, tmp_path):
+    """The built library is reused only while the digest stored beside it matches the sources and
+    flags; any other digest (other sources, other flags, or none at all) means a rebuild."""
+    assert B.up_to_date()
+    with open(B.DIGEST) as f:
+        assert f.read().strip() == B.source_digest()
+    assert B.source_digest(["-DLM_SOMETHING_ELSE"]) != B.source_digest()
+    assert not B.up_to_date(["-DLM_SOMETHING_ELSE"])
 
 
 def test_codebook_matches_oracle_bitwise(so):
@@ -381,3 +391,24 @@ def test_empty_token_count_forwards_are_no_ops(so):
     assert _relu2_fwd(_relu2_args(T=0)) == L.LM_OK
     assert _qkv_fwd(_qkv_args(T=0)) == L.LM_OK
     assert _o_fwd(_o_args(T=0)) == L.LM_OK
+
+
+def _o_bwd_static(a):
+    return L.call_status("lora_o_bwd_static", a["T"], a["din"], a["dout"], a["X"], a["dY"], a["saved"],
+                         a["saved_bytes"], ctypes.byref(a["o"]), a["dX"], a["dA"], a["dB"], None)
+
+
+def test_o_bwd_static_argument_errors_before_any_device_call(so):
+    """The static-scratch backward reports every argument error of lora_o_bwd, and a shape too large
+    for its scratch, on the host, before it clears the scratch's error word or launches anything."""
+    a = _o_args()
+    assert _reaches_device(_o_bwd_static, a)
+    assert _o_bwd_static(dict(a, dA=None)) == L.LM_ERR_NULL
+    assert _o_bwd_static(dict(a, X=a["X"] + 16)) == L.LM_ERR_ALIGN
+    assert _o_bwd_static(dict(a, dB=a["dA"])) == L.LM_ERR_ALIAS
+    assert _o_bwd_static(dict(a, dX=a["X"])) == L.LM_ERR_ALIAS
+    assert _o_bwd_static(dict(a, saved_bytes=16)) == L.LM_ERR_WORKSPACE
+    assert _o_bwd_static(dict(a, dout=288)) == L.LM_ERR_SHAPE
+    big = _o_args(T=1 << 20, din=4096, dout=4096, r=64)
+    assert _o_bwd_static(big) == L.LM_ERR_WORKSPACE
+    assert "static scratch" in L.last_error()

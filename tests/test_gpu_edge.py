@@ -3,7 +3,7 @@
 * a different LoRA scale s for every projection (a swapped or shared scale shows at once),
 * a single token for every entry point and base,
 * the Llama-3-8B feature sizes with a ragged token count (partial 512-row tiles, split tail
-  tiles and a long K in one launch), checked on sampled rows and columns,
+  tiles and a long K in one launch), every output against the oracle in full,
 * a token count of 50 row tiles with small features, every output against the oracle in full."""
 import numpy as np
 import pytest
@@ -133,35 +133,21 @@ def test_single_token_o_and_relu2(base):
         check(k, host64(bw[k]), ref[rk])
 
 
-def _rows(T, k=20, seed=0):
-    rng = np.random.default_rng(seed)
-    return np.unique(np.concatenate([[0, T - 1, T - 2], rng.integers(0, T, k)]))
-
-
 @pytest.mark.parametrize("base", ["bf16", "nf4"])
 def test_8b_features_ragged_tokens(base):
+    """The Llama-3-8B feature sizes with T = 2500 (a partial last 512-row tile and split tail tiles):
+    every output and gradient against the full oracle."""
     T, d, n = 2500, 4096, 14336
     w = synth.mlp_workload("ragged8b", T, d, n, 16, 32.0)
     inp = synth.make_inputs(w, seed=79)
     scales = {"gate": w.s, "up": w.s, "down": w.s}
     fw, bw, p = _mlp(inp, scales, base, "swiglu")
-    R = _rows(T)
-    Rt = torch.from_numpy(R).cuda()
-    Xo, dYo = O.from_bf16(inp["X"]), O.from_bf16(inp["dY"])
-    ref = O.mlp_backward(Xo[R], dYo[R], p, "swiglu")      # row-local outputs at rows R
+    ref = O.mlp_backward(O.from_bf16(inp["X"]), O.from_bf16(inp["dY"]), p, "swiglu")
     for k in ("e", "u", "h", "y"):
-        check(k, host64(fw[k].index_select(0, Rt)), ref[k])
-    check("dX", host64(bw["dX"].index_select(0, Rt)), ref["dX"])
-    C = _rows(n, k=10, seed=1)
-    col = O.mlp_backward_columns(Xo, dYo, p, C, "swiglu")
-    Ct = torch.from_numpy(C).cuda()
-    check("dB_gate", host64(bw["dB_gate"].index_select(0, Ct)), col["dBg"])
-    check("dB_up", host64(bw["dB_up"].index_select(0, Ct)), col["dBu"])
-    check("dA_down", host64(bw["dA_down"].index_select(1, Ct)), col["dAd"])
-    for t, k in (("gate", "g"), ("up", "u"), ("down", "d")):
-        a = float(np.sum(p["A" + k] * host64(bw["dA_" + t])))
-        b = float(np.sum(p["B" + k] * host64(bw["dB_" + t])))
-        assert abs(a - b) <= 1e-2 * max(abs(a), abs(b)), (t, a, b)
+        check(k, host64(fw[k]), ref[k])
+    check("dX", host64(bw["dX"]), ref["dX"])
+    for k, rk in MLP_GRADS:
+        check(k, host64(bw[k]), ref[rk])
 
 
 @pytest.mark.parametrize("base", ["bf16", "nf4"])

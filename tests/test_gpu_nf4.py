@@ -52,24 +52,17 @@ def test_pack_zero_blocks_zero_groups_and_block_maxima():
     _check_pack(synth.f32_to_bf16_bits(x).reshape(bits.shape))
 
 
-def test_pack_sampled_groups_of_a_full_size_weight():
-    """A 14336 x 4096 weight (the Llama-3-8B gate projection): every byte of 48 sampled groups."""
+def test_pack_every_group_of_a_full_size_weight():
+    """A 14336 x 4096 weight (the Llama-3-8B gate projection): every code byte, block scale, group
+    scale and dequantised value of all 3584 groups, bit for bit."""
     rows, cols = 14336, 4096
     bits = _weight_bits(rows, cols, 3)
     pk = L.nf4_pack(dev_bf16(bits))
     deq = L.nf4_dequant(pk, torch.float32)
     torch.cuda.synchronize()
     x = synth.bf16_bits_to_f32(bits).reshape(-1)
-    ngroups = rows * cols // 16384
-    rng = np.random.default_rng(0)
-    codes_all = pk.codes.cpu().numpy()
-    q_all = pk.absmax_q.cpu().numpy()
-    c_all = pk.group_scale.cpu().numpy()
-    deq_all = deq.cpu().numpy()
-    for g in sorted(set(rng.integers(0, ngroups, 47).tolist()) | {ngroups - 1}):
-        sl = slice(g * 16384, (g + 1) * 16384)
-        codes, q, c = onf4.quantize(x[sl])
-        assert np.array_equal(codes_all[g * 8192:(g + 1) * 8192], codes), g
-        assert np.array_equal(q_all[g * 256:(g + 1) * 256], q), g
-        assert c_all[g].view(np.uint32) == c.view(np.uint32)[0], g
-        assert np.array_equal(deq_all[sl].view(np.uint32), onf4.dequantize(codes, q, c).view(np.uint32)), g
+    codes, q, c = onf4.quantize(x)
+    assert np.array_equal(pk.codes.cpu().numpy(), codes)
+    assert np.array_equal(pk.absmax_q.cpu().numpy(), q)
+    assert np.array_equal(pk.group_scale.cpu().numpy().view(np.uint32), c.view(np.uint32))
+    assert np.array_equal(deq.cpu().numpy().view(np.uint32), onf4.dequantize(codes, q, c).view(np.uint32))

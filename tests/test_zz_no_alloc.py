@@ -1,18 +1,21 @@
 """lora_o_bwd_static, the entry point for callers that must not allocate device memory (for
 example a plugin whose host framework owns the device memory pool, or a process under a hard
 device-memory cap): its scratch is a fixed device array inside the library instead of a
-caller-provided workspace.  Checked through the C ABI against lora_o_bwd on the same inputs, on
-two calls in a row (the array keeps the previous call's contents).  This file is collected last
-so that a run stopping at its first failure has already run every other test."""
+caller-provided workspace.  Checked through the C ABI on two calls in a row (the array keeps the
+previous call's contents): bit for bit against lora_o_bwd on the same inputs (the same kernels run
+in the same order), element by element against the fp64 oracle, its error word read back clean
+with lm_static_scratch_check, and the device's free memory and torch's allocated bytes unchanged
+across a call made after the first one.  This file is collected last so that a run stopping at its
+first failure has already run every other test."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 from bwd_lora_mlp_gb300 import build as B
 from bwd_lora_mlp_gb300 import lib as L
 from bwd_lora_mlp_gb300 import synth
+from oracle import lora as O
 
 from gpu_util import check, dev_bf16, host64
 
@@ -35,6 +38,11 @@ def _static_call(X, dY, saved, o, dX, dA, dB):
     assert st == L.LM_OK, L.last_error()
 
 
+def _scratch_check():
+    st = L.call_status("lm_static_scratch_check", torch.cuda.current_stream().cuda_stream)
+    assert st == L.LM_OK, L.last_error()
+
+
 @pytest.mark.parametrize("T,din,dout,r", [(300, 256, 192, 16), (1000, 512, 384, 64)])
 def test_static_scratch_matches_workspace_entry_point(T, din, dout, r):
     w = synth.o_workload("o", T, din, dout, r, 2.0 * r)
@@ -44,16 +52,26 @@ def test_static_scratch_matches_workspace_entry_point(T, din, dout, r):
     fw = L.lora_o_fwd(X, o)
     ref = L.lora_o_bwd(X, dY, fw, o)
     L.lm_workspace_check(fw["ws"])
-    want = {k: host64(v) for k, v in ref.items()}
-    for _ in range(2):
-        dX = torch.full_like(ref["dX"], float("nan"))
-        dA = torch.full_like(ref["dA"], float("nan"))
-        dB = torch.full_like(ref["dB"], float("nan"))
-        _static_call(X, dY, fw["saved"], o, dX, dA, dB)
+    Xo, dYo = O.from_bf16(inp["X"]), O.from_bf16(inp["dY"])
+    W, A, Bm = (O.from_bf16(inp[k]) for k in ("W_o", "A_o", "B_o"))
+    g = O.lora_w_backward(Xo, dYo, W, A, Bm, w.s)
+    outs = [{k: torch.full_like(ref[k], float("nan")) for k in ("dX", "dA", "dB")} for _ in range(2)]
+    torch.cuda.synchronize()
+    usage = []
+    for i in range(2):
+        usage.append((torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()))
+        out = outs[i]
+        _static_call(X, dY, fw["saved"], o, out["dX"], out["dA"], out["dB"])
         torch.cuda.synchronize()
-        check("dX", host64(dX), want["dX"])
-        check("dA", host64(dA), want["dA"])
-        check("dB", host64(dB), want["dB"])
+        _scratch_check()
+        for k in ("dX", "dA", "dB"):
+            assert torch.equal(out[k], ref[k]), k
+        check("dX", host64(out["dX"]), g["dX"])
+        check("dA", host64(out["dA"]), g["dA"])
+        check("dB", host64(out["dB"]), g["dB"])
+    # the second call allocated nothing: device free memory and torch's allocated bytes are what
+    # they were before it
+    assert (torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()) == usage[1]
 
 
 def test_static_scratch_rejects_shapes_beyond_its_size():
