@@ -21,6 +21,9 @@ using namespace lm;
 namespace {
 
 thread_local char g_err[768] = "";
+// test hook (lm_debug_inject): kernel families whose producers issue no loads, and the wait limit
+thread_local int32_t g_inject_mask = 0;
+thread_local uint64_t g_wait_ns = 0;
 
 lm_status fail(lm_status s, const char* fmt, ...) {
     va_list ap;
@@ -658,6 +661,9 @@ struct Builder {
     // tiles, split-K and work-unit numbering; returns the grid size
     int finish(int sms, int32_t* err) {
         p.err = err;
+        p.kernel_id = gemm_is_pair(kind) ? 2 : gemm_is_pair_nf4(kind) ? 3 : 1;
+        p.wait_ns = g_wait_ns ? g_wait_ns : kDefaultWaitNs;
+        p.inject = (g_inject_mask >> (p.kernel_id - 1)) & 1;
         if (kind == G_PART_KK) {  // the narrower stage layout keeps twice the bytes in flight
             bool narrow = true;
             for (int i = 0; i < p.nprob; ++i) narrow = narrow && p.prob[i].bn <= 64;
@@ -936,6 +942,13 @@ extern "C" lm_status lm_workspace_reset(void* ws, lm_stream stream) {
     return LM_OK;
 }
 
+extern "C" lm_status lm_debug_inject(int32_t family_mask, uint64_t wait_ns) {
+    if (family_mask < 0 || family_mask > 7) return fail(LM_ERR_SHAPE, "family_mask = %d is not in [0, 7]", family_mask);
+    g_inject_mask = family_mask;
+    g_wait_ns = wait_ns;
+    return LM_OK;
+}
+
 extern "C" lm_status lm_workspace_check(void* ws, lm_stream stream) {
     LM_TRY(need_ptr(ws, "ws"));
     int32_t h[4] = {0, 0, 0, 0};
@@ -944,7 +957,8 @@ extern "C" lm_status lm_workspace_check(void* ws, lm_stream stream) {
     if (h[0] != 0) {
         LM_CUDA(cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream), "cudaMemsetAsync");
         LM_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "cudaStreamSynchronize");
-        return fail((lm_status)h[0], "a kernel gave up on a bounded wait (role %d, block %d)", h[1], h[2]);
+        return fail((lm_status)h[0], "a kernel gave up on a bounded wait (kernel family %d, role %d, block %d)", h[3],
+                    h[1], h[2]);
     }
     return LM_OK;
 }

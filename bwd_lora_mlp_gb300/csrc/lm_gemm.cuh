@@ -94,6 +94,10 @@ struct Params {  // CUtensorMap members carry their own 128-byte alignment
     int32_t nprob;
     int32_t total_units;
     int32_t* err;
+    uint64_t wait_ns;               // time limit of every pipeline wait (nanoseconds)
+    int32_t inject;                 // test-only: nonzero = the producers issue no loads at all,
+                                    // so every consumer wait runs out (see lm_debug_inject)
+    int32_t kernel_id;              // recorded with an error: 1 split-K, 2 bf16 pair, 3 packed pair
 };
 
 template <int BN_MAX, bool A_MN, bool B_MN>
@@ -163,11 +167,14 @@ __device__ __forceinline__ void unit_kslice(const Prob& P, const Unit& U, int& g
     }
 }
 
+// error word: [0] status, [1] role that gave up (1 producer, 2 MMA issuer, 3 epilogue, 4 decoder,
+// 5 drain of in-flight loads), [2] block, [3] kernel family (Params::kernel_id)
 __device__ __forceinline__ void record_error(const Params& p, int code, int where) {
     if (p.err) {
         atomicExch(p.err, code);
         p.err[1] = where;
         p.err[2] = blockIdx.x;
+        p.err[3] = p.kernel_id;
     }
 }
 
@@ -408,8 +415,9 @@ __global__ void __launch_bounds__(kNumThreads, BN_MAX <= 64 ? 2 : 1) gemm_kernel
         if (lane == 0) {  // ---------------- TMA producer
             int stage = 0;
             uint32_t phase = 0;
+            uint32_t nfill = 0;  // stage fills issued
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+            for (int u = blockIdx.x; ok && !p.inject && u < p.total_units; u += gridDim.x) {
                 const Unit U = decode_unit(p, u);
                 const Prob& P = p.prob[U.pi];
                 for (int si = 0; ok && si < P.nseg; ++si) {
@@ -421,7 +429,7 @@ __global__ void __launch_bounds__(kNumThreads, BN_MAX <= 64 ? 2 : 1) gemm_kernel
                         kb1 = min(nkb, kb0 + P.kb_per_split);
                     }
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) {
+                        if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -465,6 +473,7 @@ __global__ void __launch_bounds__(kNumThreads, BN_MAX <= 64 ? 2 : 1) gemm_kernel
                                     tma_load_2d(sB + i * S.b_rows * 128, &p.maps[S.b_map[i]], fb, kx + S.b_xoff[i],
                                                 U.nb * P.n_step);
                         }
+                        ++nfill;
                         if (++stage == C::STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -476,6 +485,9 @@ __global__ void __launch_bounds__(kNumThreads, BN_MAX <= 64 ? 2 : 1) gemm_kernel
                 record_error(p, kErrTimeout, 1);
                 *s_abort = 1;
             }
+            // no load of this CTA may land after it exits (another role may have given up
+            // before consuming the last fills)
+            if (!drain_fills(smem_u32(&full[0]), C::STAGES, nfill, p.wait_ns)) record_error(p, kErrTimeout, 5);
         }
     } else if (warp == 1) {
         {  // ---------------- MMA issuer: the whole warp, lane 0 issues
@@ -488,7 +500,7 @@ __global__ void __launch_bounds__(kNumThreads, BN_MAX <= 64 ? 2 : 1) gemm_kernel
             for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
                 const Unit U = decode_unit(p, u);
                 const Prob& P = p.prob[U.pi];
-                if (!mbar_wait_warp(smem_u32(&tempty[acc]), aphase ^ 1u, s_abort)) {
+                if (!mbar_wait_warp(smem_u32(&tempty[acc]), aphase ^ 1u, s_abort, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -507,7 +519,7 @@ __global__ void __launch_bounds__(kNumThreads, BN_MAX <= 64 ? 2 : 1) gemm_kernel
                     }
                     const bool dual = !B_MN && S.dual_split > 0;
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!mbar_wait_warp(smem_u32(&full[stage]), phase, s_abort)) {
+                        if (!mbar_wait_warp(smem_u32(&full[stage]), phase, s_abort, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -555,7 +567,7 @@ __global__ void __launch_bounds__(kNumThreads, BN_MAX <= 64 ? 2 : 1) gemm_kernel
             // wait until every MMA the leader issued has finished before TMEM is released
             umma_commit_if(smem_u32(drain), leader);
             volatile int never = 0;
-            mbar_wait(smem_u32(drain), 0, &never);
+            mbar_wait(smem_u32(drain), 0, &never, p.wait_ns);
             __syncwarp();
         }
     } else {  // ---------------- epilogue warps
@@ -568,7 +580,7 @@ __global__ void __launch_bounds__(kNumThreads, BN_MAX <= 64 ? 2 : 1) gemm_kernel
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
             const Unit U = decode_unit(p, u);
             const Prob& P = p.prob[U.pi];
-            if (!mbar_wait(smem_u32(&tfull[acc]), aphase, s_abort)) {
+            if (!mbar_wait(smem_u32(&tfull[acc]), aphase, s_abort, p.wait_ns)) {
                 ok = false;
                 break;
             }

@@ -38,6 +38,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // stage fills issued by each CTA's producer (both written into CTA 0's copy), read by CTA 0
+    // when it waits out the pair's loads still in flight before either CTA leaves
+    volatile uint32_t* s_fill = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -78,8 +81,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
         if (lane == 0) {  // ---------------- TMA producer (both CTAs)
             int stage = 0;
             uint32_t phase = 0;
+            uint32_t nfill = 0;  // stage fills issued by this CTA
             bool ok = true;
-            for (int u = cid; ok && u < p.total_units; u += ncl) {
+            for (int u = cid; ok && !p.inject && u < p.total_units; u += ncl) {
                 const Unit U = decode_unit(p, u);
                 const Prob& P = p.prob[U.pi];
                 for (int si = 0; ok && si < P.nseg; ++si) {
@@ -88,7 +92,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
                     const int bmap = (rank == 1 && S.b_map[1] >= 0) ? S.b_map[1] : S.b_map[0];
                     const int brow = U.nb * P.n_step + (int)rank * S.b_rank_off;
                     for (int kb = 0; kb < nkb; ++kb) {
-                        if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) {
+                        if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -104,6 +108,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
                         } else {
                             tma_load_2d_pair(sB, &p.maps[bmap], fb, kx + S.b_xoff[0], brow);
                         }
+                        ++nfill;
                         if (++stage == C::STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -115,6 +120,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
                 record_error(p, kErrTimeout, 1);
                 *s_abort = 1;
             }
+            st_cluster_u32(map_to_rank(smem_u32(const_cast<uint32_t*>(&s_fill[rank])), 0), nfill);
         }
     } else if (warp == 1) {
         if (rank == 0) {  // ---------------- MMA issuer (CTA 0 only): the whole warp, lane 0 issues
@@ -127,7 +133,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
             for (int u = cid; ok && u < p.total_units; u += ncl) {
                 const Unit U = decode_unit(p, u);
                 const Prob& P = p.prob[U.pi];
-                if (!mbar_wait_warp(smem_u32(&tempty[acc]), aphase ^ 1u, s_abort)) {
+                if (!mbar_wait_warp(smem_u32(&tempty[acc]), aphase ^ 1u, s_abort, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -139,7 +145,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
                     const Seg& S = P.seg[si];
                     const int nkb = (S.kext + kBK - 1) / kBK;
                     for (int kb = 0; kb < nkb; ++kb) {
-                        if (!mbar_wait_warp(smem_u32(&full[stage]), phase, s_abort)) {
+                        if (!mbar_wait_warp(smem_u32(&full[stage]), phase, s_abort, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
             }
             umma_commit_pair_if(smem_u32(drain), 0x1, leader);
             volatile int never = 0;
-            mbar_wait(smem_u32(drain), 0, &never);
+            mbar_wait(smem_u32(drain), 0, &never, p.wait_ns);
             __syncwarp();
         }
     } else {  // ---------------- epilogue warps (both CTAs)
@@ -192,7 +198,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
         for (int u = cid; u < p.total_units; u += ncl) {
             const Unit U = decode_unit(p, u);
             const Prob& P = p.prob[U.pi];
-            if (!mbar_wait(smem_u32(&tfull[acc]), aphase, s_abort)) {
+            if (!mbar_wait(smem_u32(&tfull[acc]), aphase, s_abort, p.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -215,6 +221,26 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm2_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // neither CTA leaves while its peer may still signal its barriers
+    if (rank == 0 && threadIdx.x == 0) {
+        // Both CTAs' loads complete on CTA 0's stage barriers, so CTA 0 waits out the pair's
+        // fills still in flight (a role that gave up may have left the last ones unconsumed).
+        // The two producers issue the same fill sequence and neither can run a whole ring ahead
+        // of the other, so only the last STAGES fills of the longer sequence can be pending.  A
+        // fill CTA 0 armed for both CTAs but CTA 1 never issued has CTA 1's bytes completed here;
+        // one CTA 1 issued but CTA 0 never armed is armed here with CTA 1's bytes.
+        const uint32_t n0 = s_fill[0], n1 = s_fill[1], hi = n0 > n1 ? n0 : n1;
+        const uint32_t S = (uint32_t)C::STAGES, half = (uint32_t)(C::A_BYTES + C::B_BYTES);
+        volatile int never = 0;
+        bool ok = true;
+        for (uint32_t k = hi > S ? hi - S : 0u; k < hi; ++k) {
+            const uint32_t bar = smem_u32(&full[k % S]);
+            if (k < n0 && k >= n1) mbar_complete_tx(bar, half);
+            else if (k >= n0 && k < n1) mbar_expect_tx(bar, half);
+            ok = mbar_wait(bar, (k / S) & 1u, &never, p.wait_ns) && ok;
+        }
+        if (!ok) record_error(p, kErrTimeout, 5);
+    }
+    cluster_sync();
     if (warp == 0) {
         __syncwarp();
         tc_fence_after();

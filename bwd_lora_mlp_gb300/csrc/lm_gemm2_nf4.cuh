@@ -223,14 +223,16 @@ __device__ __forceinline__ void nvfp4_decode_block(const uint32_t (&words)[8], u
 // until every epilogue warp has arrived on `scrfree` (see the producer's gate).  Lane 0 of the
 // first epilogue warp issues the loads, three chunks ahead; each warp releases a buffer as soon
 // as it has read its row from it.  `qn` counts the chunks staged by this CTA so far (buffer
-// qn % 3, phase qn / 3).  Returns false on a timed-out wait.
+// qn % 3, phase qn / 3); *s_qi counts the chunks issued, which may run three ahead of qn, so that
+// the loads still in flight can be waited out before the CTA leaves.  Returns false on a timed-out
+// wait.
 constexpr int kStageChunkBytes = 16384;
 constexpr int kStageBuffers = 3;
 
 __device__ __forceinline__ bool glu_bwd_staged(const Params& p, const Prob& P, const Unit& U, uint32_t tacc,
                                                int64_t m, uint32_t scr, uint32_t efull0, uint32_t eempty0,
                                                uint32_t rank, bool issuer, int hh, int r, uint32_t& qn,
-                                               volatile int* s_abort) {
+                                               volatile uint32_t* s_qi, volatile int* s_abort) {
     const int nch = P.bn >> 4;
     const int32_t row0 = (int32_t)((int64_t)U.mb * 512 + (int64_t)rank * kBM);
     const int64_t col0 = (int64_t)U.nb * P.out_col_step;
@@ -241,7 +243,8 @@ __device__ __forceinline__ bool glu_bwd_staged(const Params& p, const Prob& P, c
     // previous chunk
     auto issue = [&](int c) -> bool {
         const uint32_t q = q0 + (uint32_t)c, b = q % kStageBuffers;
-        if (q >= kStageBuffers && !mbar_wait(eempty0 + 8 * b, ((q - kStageBuffers) / kStageBuffers) & 1u, s_abort))
+        if (q >= kStageBuffers &&
+            !mbar_wait(eempty0 + 8 * b, ((q - kStageBuffers) / kStageBuffers) & 1u, s_abort, p.wait_ns))
             return false;
         const uint32_t dst = scr + b * kStageChunkBytes, bar = efull0 + 8 * b;
         const int32_t x = (int32_t)(col0 + 16 * c);
@@ -250,6 +253,7 @@ __device__ __forceinline__ bool glu_bwd_staged(const Params& p, const Prob& P, c
         tma_load_2d(dst + 4096, me, bar, x, row0 + 256);
         tma_load_2d(dst + 8192, mu, bar, x, row0);
         tma_load_2d(dst + 12288, mu, bar, x, row0 + 256);
+        *s_qi = q + 1;
         return true;
     };
     int fail = 0;
@@ -263,7 +267,7 @@ __device__ __forceinline__ bool glu_bwd_staged(const Params& p, const Prob& P, c
 #pragma unroll 1
     for (int c = 0; c < nch; ++c) {
         const uint32_t q = q0 + (uint32_t)c, b = q % kStageBuffers;
-        if (!mbar_wait_warp(efull0 + 8 * b, (q / kStageBuffers) & 1u, s_abort)) return false;
+        if (!mbar_wait_warp(efull0 + 8 * b, (q / kStageBuffers) & 1u, s_abort, p.wait_ns)) return false;
         const uint32_t base = scr + b * kStageChunkBytes + roff;
         uint32_t ev[8], uv[8];
         ld_shared_v4(base + sw, ev[0], ev[1], ev[2], ev[3]);
@@ -325,6 +329,8 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
     volatile int32_t* stage_kind = reinterpret_cast<volatile int32_t*>(tmem_slot + 2);
     // fp32 tensor scale of each NVFP4 scale map, read once at launch
     float* s_gscale = const_cast<float*>(reinterpret_cast<volatile float*>(stage_kind + C::STAGES));
+    // e, u chunks the staged GLU backward epilogue has issued (its issuing thread writes it)
+    volatile uint32_t* s_qi = reinterpret_cast<volatile uint32_t*>(s_gscale + kMaxMaps);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -350,6 +356,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
         }
         mbar_init(smem_u32(scrfree), kNumEpiWarps);
         *s_abort = 0;
+        *s_qi = 0;
         fence_mbar_init();
         for (int i = 0; i < kMaxMaps; ++i)
             if (p.map_bytes[i]) tma_prefetch_map(&p.maps[i]);
@@ -383,7 +390,8 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
             // unit of such a launch has at least four K blocks, so the gate falls inside the next
             // tile and the releases are waited for in order, one phase at a time.
             uint32_t it = 0, gate[4] = {0u, 0u, 0u, 0u}, gh = 0, gt = 0, nrel = 0;
-            for (int u = cid; ok && u < p.total_units; u += ncl) {
+            uint32_t nfill = 0;  // stage fills (loads and end-of-work marks) issued
+            for (int u = cid; ok && !p.inject && u < p.total_units; u += ncl) {
                 const Unit U = decode_unit(p, u);
                 const Prob& P = p.prob[U.pi];
                 int g0, g1;
@@ -403,14 +411,14 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     const int brow = U.nb * P.n_step + (int)rank * S.b_rank_off;
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (gh != gt && gate[gh & 3] == it) {
-                            if (!mbar_wait(smem_u32(scrfree), nrel & 1u, s_abort)) {
+                            if (!mbar_wait(smem_u32(scrfree), nrel & 1u, s_abort, p.wait_ns)) {
                                 ok = false;
                                 break;
                             }
                             ++nrel;
                             ++gh;
                         }
-                        if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) {
+                        if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -445,6 +453,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                         } else {
                             tma_load_2d(sB, &p.maps[bmap], fb, kx + S.b_xoff[0], brow);
                         }
+                        ++nfill;
                         if (++stage == C::STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -454,13 +463,14 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                 if (EPI == EPI_GLU_BWD && P.in_map[0] >= 0) gate[gt++ & 3] = it + 3;
             }
             // one end-of-work stage for each decode group (the next stage in its round-robin)
-            for (int g = 0; ok && g < kPairNf4DecodeGroups; ++g) {
-                if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) {
+            for (int g = 0; ok && !p.inject && g < kPairNf4DecodeGroups; ++g) {
+                if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort, p.wait_ns)) {
                     ok = false;
                     break;
                 }
                 stage_kind[stage] = 2;
                 mbar_arrive(smem_u32(&full[stage]));
+                ++nfill;
                 if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -470,6 +480,8 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                 record_error(p, kErrTimeout, 1);
                 *s_abort = 1;
             }
+            // this CTA's loads complete on its own stage barriers: wait out the ones in flight
+            if (!drain_fills(smem_u32(&full[0]), C::STAGES, nfill, p.wait_ns)) record_error(p, kErrTimeout, 5);
         }
     } else if (warp == 1) {
         if (rank == 0) {  // ---------------- MMA issuer (CTA 0 only): the whole warp, lane 0 issues
@@ -481,7 +493,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
             for (int u = cid; ok && u < p.total_units; u += ncl) {
                 const Unit U = decode_unit(p, u);
                 const Prob& P = p.prob[U.pi];
-                if (!mbar_wait_warp(smem_u32(&tempty[0]), aphase ^ 1u, s_abort)) {
+                if (!mbar_wait_warp(smem_u32(&tempty[0]), aphase ^ 1u, s_abort, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -496,7 +508,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     const int kb0 = max(0, g0 - g), kb1 = min(nkb, g1 - g);
                     g += nkb;
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!mbar_wait_warp(smem_u32(&bready[stage]), phase, s_abort)) {
+                        if (!mbar_wait_warp(smem_u32(&bready[stage]), phase, s_abort, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -534,7 +546,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
             }
             umma_commit_pair_if(smem_u32(drain), 0x1, leader);
             volatile int never = 0;
-            mbar_wait(smem_u32(drain), 0, &never);
+            mbar_wait(smem_u32(drain), 0, &never, p.wait_ns);
             __syncwarp();
         }
     } else if (warp < 2 + kPairNf4DecodeWarps) {  // ---------------- decoders (both CTAs)
@@ -546,7 +558,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
         for (uint32_t iter = (uint32_t)group;; iter += kPairNf4DecodeGroups) {
             const int stage = (int)(iter % C::STAGES);
             const uint32_t phase = (iter / C::STAGES) & 1u;
-            if (!mbar_wait(smem_u32(&full[stage]), phase, s_abort)) {
+            if (!mbar_wait(smem_u32(&full[stage]), phase, s_abort, p.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -637,7 +649,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
             int g0, g1;
             unit_kslice(P, U, g0, g1);
             kdone += (uint32_t)(g1 - g0);
-            if (!mbar_wait(smem_u32(&tfull[0]), aphase, s_abort)) {
+            if (!mbar_wait(smem_u32(&tfull[0]), aphase, s_abort, p.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -649,7 +661,7 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
                     // the slot of the tile's last K block: free once the MMAs behind tfull are done
                     const uint32_t scr = smem_u32(smem + ((kdone - 1u) % C::STAGES) * C::STAGE_BYTES);
                     if (!glu_bwd_staged(p, P, U, tacc, m, scr, smem_u32(&efull[0]), smem_u32(&eempty[0]), rank,
-                                        ew == 0 && lane == 0, hh, q * 32 + lane, qn, s_abort)) {
+                                        ew == 0 && lane == 0, hh, q * 32 + lane, qn, s_qi, s_abort)) {
                         ok = false;
                         break;
                     }
@@ -687,6 +699,12 @@ __global__ void __launch_bounds__(kPairNf4Threads, 1) gemm2_nf4_kernel(const __g
             record_error(p, kErrTimeout, 3);
             *s_abort = 1;
         }
+    }
+    if constexpr (EPI == EPI_GLU_BWD) {
+        // the thread that staged e, u chunks waits out its loads still in flight
+        if (threadIdx.x == 32 * (2 + kPairNf4DecodeWarps) &&
+            !drain_fills(smem_u32(&efull[0]), kStageBuffers, *s_qi, p.wait_ns))
+            record_error(p, kErrTimeout, 5);
     }
 
     tc_fence_before();

@@ -9,11 +9,10 @@
 
 namespace lm {
 
-// A pipeline wait gives up after this many nanoseconds; the kernel then records
-// LM_ERR_TIMEOUT in the workspace error word and returns instead of hanging.
-#ifndef LM_WAIT_NS
-#define LM_WAIT_NS 2000000000ull
-#endif
+// A pipeline wait gives up after a time limit (nanoseconds, per launch: Params::wait_ns, this by
+// default); the kernel then records LM_ERR_TIMEOUT in the workspace error word and returns
+// instead of hanging.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -53,9 +52,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait for phase `parity` of barrier `bar`.  Returns false on timeout or when another
-// role of the CTA has already given up (*abort != 0).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// Bounded wait for phase `parity` of barrier `bar`: gives up after limit_ns nanoseconds, or
+// as soon as another role of the CTA has given up (*abort != 0).  Returns false then.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
@@ -63,13 +62,36 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > LM_WAIT_NS) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
 // The same wait made by every lane of a warp; the result is warp-uniform.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit_ns));
+}
+
+// Lowers the pending transaction count of the current phase of `bar` by `bytes`, as the landing
+// of that many bytes would.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Before a CTA leaves: waits, bounded by limit_ns each but regardless of any abort flag, until
+// the last min(nfill, stages) fills of a stage ring have completed on their barriers
+// (bar0 + 8 s for slot s; fill k went to slot k % stages as that slot's phase k / stages).  Only
+// the most recent fill of a slot can still be in flight -- the one before it was waited for
+// before the slot was refilled -- so no copy issued by this thread lands in shared memory after
+// these waits.  On the normal path every fill has been consumed and each wait returns at once.
+// Returns false if a fill never completes.
+__device__ __forceinline__ bool drain_fills(uint32_t bar0, int stages, uint32_t nfill, uint64_t limit_ns) {
+    volatile int never = 0;
+    bool ok = true;
+    const uint32_t k0 = nfill > (uint32_t)stages ? nfill - (uint32_t)stages : 0u;
+    for (uint32_t k = k0; k < nfill; ++k)
+        ok = mbar_wait(bar0 + 8u * (k % (uint32_t)stages), (k / (uint32_t)stages) & 1u, &never, limit_ns) && ok;
+    return ok;
 }
 
 // ---------------------------------------------------------------- TMA
@@ -230,6 +252,10 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
 // shared-memory stores, this one does not.
 __device__ __forceinline__ void mbar_arrive_peer(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// 32-bit store to shared memory of either CTA of the cluster (shared::cluster address)
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");

@@ -86,6 +86,7 @@ _SIGS = {
     "lora_o_bwd": ([_I64, _I64, _I64, _P, _P, _P, _SZ, _LP, _P, _P, _P, _P, _SZ, _P], _I32),
     "lora_o_bwd_static": ([_I64, _I64, _I64, _P, _P, _P, _SZ, _LP, _P, _P, _P, _P], _I32),
     "lm_static_scratch_check": ([_P], _I32),
+    "lm_debug_inject": ([_I32, ctypes.c_uint64], _I32),
     "nf4_pack": ([_P, _I64, _P, _P, _P, _P], _I32),
     "nf4_dequant": ([_P, _P, _P, _I64, _I32, _P, _P], _I32),
     "int4_pack": ([_P, _I64, _I64, _I32, _P, _P, _P], _I32),

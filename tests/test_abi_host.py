@@ -19,7 +19,7 @@ def so():
 
 def test_exports_every_header_symbol(so):
     names = L.header_symbols()
-    assert len(names) == 31
+    assert len(names) == 32
     for n in names:
         assert hasattr(so, n), n
     assert set(names) == set(L._SIGS)
