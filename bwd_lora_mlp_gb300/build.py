@@ -28,7 +28,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblora_mlp.so")
 DIGEST = LIB + ".digest"
 
-SOURCES = ["lm_api.cu", "lm_aux.cu", "lm_gemm_fwd.cu", "lm_gemm_bwd.cu", "lm_gemm2.cu", "lm_gemm2_nf4.cu", "lm_static_ws.cu"]
+SOURCES = ["lm_api.cu", "lm_aux.cu", "lm_gemm_fwd.cu", "lm_gemm_bwd.cu", "lm_gemm2.cu", "lm_gemm2_nf4.cu", "lm_static_ws.cu",
+           "lm_dual.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]

@@ -21,7 +21,9 @@ using namespace lm;
 namespace {
 
 thread_local char g_err[768] = "";
-// test hook (lm_debug_inject): kernel families whose producers issue no loads, and the wait limit
+// test hook (lm_debug_inject): kernel families whose producers issue no loads (bits 0-3), the dual
+// rank-r reductions wherever feasible (bit 4), and the wait limit
+constexpr int32_t kForceDual = 16;
 thread_local int32_t g_inject_mask = 0;
 thread_local uint64_t g_wait_ns = 0;
 
@@ -272,6 +274,10 @@ struct Bump {
 };
 
 constexpr int kMaxSplits = 16;
+// Row or column ranges of a dual rank-r reduction (lm_dual.cuh).  Its G partials (ranges x T x rp
+// per job, at most three jobs) then fit the split-K partial region, which is free until the
+// gradient reductions; its dB partials have their own regions.
+constexpr int kDualMaxSplits = 16;
 // Split tail tiles of a plain-store NF4 pair GEMM: at most this many fp32 partial tiles
 // (512 x 256 each) per launch, in a workspace slot of kTailParts * 512 KiB.
 constexpr int kTailParts = 80;
@@ -324,6 +330,7 @@ struct MlpPlan {
     size_t sc[3];           // NF4 base: fp32 block-scale tables of W_gate, W_up, W_down
     size_t tail;            // NF4 base: split tail tiles of the down and dX GEMMs
     size_t abc;             // bf16 copies of fp32 LoRA A and B
+    size_t dpart[3];        // dual reductions: dB partials of dBd ([ranges][d][rp]), dBg, dBu ([ranges][n][rp])
     size_t ws_total;
 };
 
@@ -347,6 +354,10 @@ MlpPlan plan_mlp(int64_t T, int64_t d, int64_t n, int32_t r) {
     for (int i = 0; i < 3; ++i) P.sc[i] = w.take((size_t)n * d / 64 * 4);
     P.tail = w.take(kTailBytes);
     P.abc = w.take((size_t)(2 * ab_elems(r, d, n) + ab_elems(r, n, d)) * 2);
+    const int64_t cols[3] = {d, n, n};
+    for (int i = 0; i < 3; ++i) {
+        P.dpart[i] = w.take((size_t)kDualMaxSplits * cols[i] * rp * 4);
+    }
     P.ws_total = w.off;
     return P;
 }
@@ -360,6 +371,7 @@ struct QkvPlan {
     size_t sc[3];           // NF4 base: fp32 block-scale tables of W_q, W_k, W_v
     size_t tail;            // NF4 base: split tail tiles of the dX GEMM
     size_t abc;             // bf16 copies of fp32 LoRA A and B
+    size_t dpart[3];        // dual reduction: dB partials ([ranges][out][rp] fp32)
     size_t ws_total;
 };
 
@@ -379,6 +391,9 @@ QkvPlan plan_qkv(int64_t T, int64_t d, int64_t nq, int64_t nk, int64_t nv, int32
     for (int i = 0; i < 3; ++i) P.sc[i] = w.take((size_t)nout[i] * d / 64 * 4);
     P.tail = w.take(kTailBytes);
     P.abc = w.take((size_t)(ab_elems(r, d, nq) + ab_elems(r, d, nk) + ab_elems(r, d, nv)) * 2);
+    for (int i = 0; i < 3; ++i) {
+        P.dpart[i] = w.take((size_t)kDualMaxSplits * nout[i] * rp * 4);
+    }
     P.ws_total = w.off;
     return P;
 }
@@ -392,6 +407,7 @@ struct OPlan {
     size_t sc;              // NF4 base: fp32 block-scale table of W_o
     size_t tail;            // NF4 base: split tail tiles of the O and dX GEMMs
     size_t abc;             // bf16 copies of fp32 LoRA A and B
+    size_t dpart;           // dual reduction: dB partials
     size_t ws_total;
 };
 
@@ -410,6 +426,7 @@ OPlan plan_o(int64_t T, int64_t d_in, int64_t d_out, int32_t r) {
     P.sc = w.take((size_t)d_out * d_in / 64 * 4);
     P.tail = w.take(kTailBytes);
     P.abc = w.take((size_t)ab_elems(r, d_in, d_out) * 2);
+    P.dpart = w.take((size_t)kDualMaxSplits * d_out * rp * 4);
     P.ws_total = w.off;
     return P;
 }
@@ -457,6 +474,37 @@ lm_status ab_to_bf16(const char* tag, std::initializer_list<AbProj> projs, uint1
     ProfScope prof(tag, st);
     const cudaError_t e = launch_f32_to_bf16(jobs, nj, st);
     return e == cudaSuccess ? LM_OK : cuda_fail(e, "fp32 -> bf16 launch");
+}
+
+// 2D bf16 tensor map (rows x cols, row stride ld elements), box 64 columns x box_rows rows,
+// 128-byte swizzle
+lm_status encode_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1u, 1u};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(LM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %lld x %lld tensor, box rows %d", (int)r,
+                    (long long)rows, (long long)cols, box_rows);
+    return LM_OK;
+}
+
+// A LoRA B matrix (C rows x r columns bf16, row-major) as the MN-major B operand of the dual
+// reduction's row reduction: box 16 columns x 128 rows with 32-byte swizzle (columns beyond r read 0)
+lm_status encode_b_sw32(CUtensorMap* m, const void* base, int64_t C, int r) {
+    cuuint64_t dims[2] = {(cuuint64_t)r, (cuuint64_t)C};
+    cuuint64_t strides[1] = {(cuuint64_t)r * 2};
+    cuuint32_t box[2] = {16u, 128u};
+    cuuint32_t es[2] = {1u, 1u};
+    const CUresult res = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS)
+        return fail(LM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %lld x %d LoRA B", (int)res, (long long)C, r);
+    return LM_OK;
 }
 
 // ------------------------------------------------------------------ GEMM launch builder
@@ -629,18 +677,8 @@ struct Builder {
             st = fail(LM_ERR_UNSUPPORTED, "too many tensor maps in one launch");
             return 0;
         }
-        cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-        cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-        cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-        cuuint32_t es[2] = {1u, 1u};
-        const CUresult r = g_encode(&p.maps[nmaps], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) {
-            st = fail(LM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %lld x %lld tensor, box rows %d", (int)r,
-                      (long long)rows, (long long)cols, box_rows);
-            return 0;
-        }
+        st = encode_bf16(&p.maps[nmaps], base, rows, cols, ld, box_rows);
+        if (st != LM_OK) return 0;
         p.map_bytes[nmaps] = 128u * (uint32_t)box_rows;
         p.map_w[nmaps] = (int32_t)cols;
         return nmaps++;
@@ -663,7 +701,7 @@ struct Builder {
         p.err = err;
         p.kernel_id = gemm_is_pair(kind) ? 2 : gemm_is_pair_nf4(kind) ? 3 : 1;
         p.wait_ns = g_wait_ns ? g_wait_ns : kDefaultWaitNs;
-        p.inject = (g_inject_mask >> (p.kernel_id - 1)) & 1;
+        p.inject = (g_inject_mask >> (p.kernel_id - 1)) & 1;  // (ids 1-3: bits 0-2)
         if (kind == G_PART_KK) {  // the narrower stage layout keeps twice the bytes in flight
             bool narrow = true;
             for (int i = 0; i < p.nprob; ++i) narrow = narrow && p.prob[i].bn <= 64;
@@ -880,9 +918,20 @@ struct ColReduce {
             prob_of[njobs++] = b.p.nprob - 1;
         }
     }
+    // one more finalisation job over partials another launch wrote (its split count set)
+    void add_fin(const FinColJob& j) {
+        if (njobs >= kMaxJobs) {
+            if (b.st == LM_OK) b.st = fail(LM_ERR_UNSUPPORTED, "too many gradient reductions in one launch");
+            return;
+        }
+        js[njobs] = j;
+        prob_of[njobs++] = -1;
+    }
     lm_status run(const char* tag, const char* fin_tag, int sms, int32_t* err, cudaStream_t st) {
-        LM_TRY(b.launch(tag, sms, err, st));
-        for (int i = 0; i < njobs; ++i) js[i].splits = b.p.prob[prob_of[i]].splits;
+        if (b.p.nprob > 0) LM_TRY(b.launch(tag, sms, err, st));
+        else LM_TRY(b.st);
+        for (int i = 0; i < njobs; ++i)
+            if (prob_of[i] >= 0) js[i].splits = b.p.prob[prob_of[i]].splits;
         ProfScope prof(fin_tag, st);
         const cudaError_t e = launch_fin_colreduce(js, njobs, st);
         if (e != cudaSuccess) return cuda_fail(e, "gradient finalisation launch");
@@ -904,6 +953,128 @@ lm_status fin_rows(const char* tag, const Builder& b, std::initializer_list<FinR
     if (e != cudaSuccess) return cuda_fail(e, "rank-r finalisation launch");
     return LM_OK;
 }
+
+// Explicit split counts (a dual reduction's column ranges)
+lm_status fin_rows_split(const char* tag, std::initializer_list<FinRowJob> jobs, int64_t T, cudaStream_t st) {
+    FinRowJob js[3];
+    int n = 0;
+    for (const FinRowJob& j : jobs) js[n++] = j;
+    ProfScope prof(tag, st);
+    const cudaError_t e = launch_fin_rowproj(js, n, T, st);
+    if (e != cudaSuccess) return cuda_fail(e, "rank-r finalisation launch");
+    return LM_OK;
+}
+
+// ------------------------------------------------------------------ dual rank-r reduction
+// One pass over an output gradient Z for both G = Z B (row reduction) and dB = Z^T (s X A^T)
+// (column reduction); see lm_dual.cuh.  A unit is RB x CB tiles of 128 x 128; the partials of G
+// have one slice per column range, those of dB one per row range.
+
+struct DualShape {
+    int RB = 0, CB = 0, nrr = 0;  // the column ranges of a job follow its width (dual_ranges)
+    bool use = false;
+};
+
+// The unit shape with the shortest estimated time: the busiest CTA's tiles at what one SM draws
+// (about 50 GB/s) or all bytes -- Z once, the partials written and read back -- at HBM speed,
+// whichever is longer; at most kDualMaxSplits row and column ranges, and two sets of CB dB
+// accumulators beside the two G accumulators in TMEM (512 columns).  `use` when that beats the
+// separate row- and column-reduction passes, which stream Z twice at HBM speed (or always where
+// feasible under the test hook's flag).
+constexpr double kSmBytesPerS = 50e9, kHbmBytesPerS = 6.5e12;
+// One shape for every job of a launch (jobs of widths Cs, all T rows); ncr of the job of width C
+// is dual_ranges(C, CB).
+inline int dual_ranges(int64_t C, int CB) { return (int)(((C + 127) / 128 + CB - 1) / CB); }
+DualShape plan_dual(int64_t T, std::initializer_list<int64_t> Cs, int rp, int grid) {
+    DualShape best;
+    const int64_t nrb = (T + 127) / 128;
+    const int cbmax = std::min(8, (512 - 2 * rp) / (2 * rp));
+    double best_t = 1e300;
+    for (int CB = 1; CB <= cbmax; ++CB) {
+        bool fits = true;
+        for (int64_t C : Cs) fits = fits && dual_ranges(C, CB) <= kDualMaxSplits;
+        if (!fits) continue;
+        for (int RB = 1; RB <= 16; ++RB) {
+            const int64_t nrr = (nrb + RB - 1) / RB;
+            if (nrr > kDualMaxSplits) continue;
+            int64_t units = 0;
+            double total = 0.0;
+            for (int64_t C : Cs) {
+                const int64_t ncr = dual_ranges(C, CB);
+                units += nrr * ncr;
+                total += (double)T * C * 2.0 + 2.0 * (double)(ncr * T + nrr * C) * rp * 4.0;
+            }
+            const int64_t waves = (units + grid - 1) / grid;
+            const double busiest = (double)waves * RB * CB * 32768.0;
+            const double t = std::max(busiest / kSmBytesPerS, total / kHbmBytesPerS);
+            if (t < best_t * 0.999) {
+                best_t = t;
+                best.RB = RB;
+                best.CB = CB;
+                best.nrr = (int)nrr;
+            }
+        }
+    }
+    double separate = 0.0;
+    for (int64_t C : Cs) separate += 2.0 * (double)T * C * 2.0 / kHbmBytesPerS;
+    best.use = best.RB > 0 && (best_t < separate || (g_inject_mask & kForceDual));
+    return best;
+}
+
+struct DualLaunch {
+    DualParams p;
+    int nmaps = 0;
+    lm_status st = LM_OK;
+    DualLaunch() { memset(&p, 0, sizeof p); }
+    // Z (T x C), B (C x r), rows [p_row0, p_row0 + rp) of P (p_rows x T, row stride ldT)
+    void add(const uint16_t* Z, int64_t T, int64_t C, const void* B, int r, const uint16_t* P, int64_t p_rows, int p_row0,
+             int64_t ldT, int rp, const DualShape& sh, float* gpart, float* dpart) {
+        if (st != LM_OK) return;
+        if (p.njobs >= kDualMaxJobs) {
+            st = fail(LM_ERR_UNSUPPORTED, "too many jobs in one dual reduction");
+            return;
+        }
+        DualJob& J = p.job[p.njobs++];
+        J.z_map = nmaps;
+        if ((st = encode_bf16(&p.maps[nmaps++], Z, T, C, C, 128)) != LM_OK) return;
+        J.b_map = nmaps;
+        if ((st = encode_b_sw32(&p.maps[nmaps++], B, C, r)) != LM_OK) return;
+        J.p_map = nmaps;
+        if ((st = encode_bf16(&p.maps[nmaps++], P, p_rows, T, ldT, rp)) != LM_OK) return;
+        J.p_row0 = p_row0;
+        J.T = (int32_t)T;
+        J.C = (int32_t)C;
+        J.nrb = (int32_t)((T + 127) / 128);
+        J.ncb = (int32_t)((C + 127) / 128);
+        J.RB = sh.RB;
+        J.CB = sh.CB;
+        J.nrr = sh.nrr;
+        J.ncr = dual_ranges(C, sh.CB);
+        J.gpart = gpart;
+        J.dpart = dpart;
+    }
+    lm_status launch(const char* tag, int sms, int rp, int32_t* err, cudaStream_t st_) {
+        if (st != LM_OK) return st;
+        int64_t units = 0;
+        for (int j = 0; j < p.njobs; ++j) {
+            p.job[j].unit_begin = (int32_t)units;
+            units += (int64_t)p.job[j].nrr * p.job[j].ncr;
+        }
+        p.total_units = (int32_t)units;
+        p.rp = rp;
+        p.stage_bytes = 32768 + 512 * rp;
+        p.stages = std::min(kDualMaxStages, (kDualSmemBytes - 2048) / p.stage_bytes);
+        p.err = err;
+        p.kernel_id = 4;
+        p.wait_ns = g_wait_ns ? g_wait_ns : kDefaultWaitNs;
+        p.inject = (g_inject_mask >> 3) & 1;
+        const int grid = (int)std::min<int64_t>(units, sms);
+        if (grid == 0) return LM_OK;
+        ProfScope prof(tag, st_);
+        const cudaError_t e = launch_dual_reduce(p, grid, st_);
+        return e == cudaSuccess ? LM_OK : cuda_fail(e, "dual reduction launch");
+    }
+};
 
 template <typename T_>
 T_* at(void* base, size_t off) {
@@ -943,7 +1114,7 @@ extern "C" lm_status lm_workspace_reset(void* ws, lm_stream stream) {
 }
 
 extern "C" lm_status lm_debug_inject(int32_t family_mask, uint64_t wait_ns) {
-    if (family_mask < 0 || family_mask > 7) return fail(LM_ERR_SHAPE, "family_mask = %d is not in [0, 7]", family_mask);
+    if (family_mask < 0 || family_mask > 31) return fail(LM_ERR_SHAPE, "family_mask = %d is not in [0, 31]", family_mask);
     g_inject_mask = family_mask;
     g_wait_ns = wait_ns;
     return LM_OK;
@@ -1242,7 +1413,21 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     uint16_t* de = at<uint16_t>(ws, PL.de);
     uint16_t* du = at<uint16_t>(ws, PL.du);
 
-    {  // Gd = s_d dY Bd, formed once (feeds dh and dA_down)
+    // The dual rank-r reductions (lm_dual.cuh) read each output gradient once for both its G and
+    // its dB, where the planner finds that cheaper than the two separate passes.
+    const DualShape dsA = plan_dual(T, {d}, rp, sms), dsB = plan_dual(T, {n, n}, rp, sms);
+    // G partials in the split-K partial region ([ranges][T][rp] each, at most kDualMaxSplits
+    // ranges): Gd's are finalised before the de, du pass writes Gg's and Gu's
+    float* gp[3] = {part, part, part + (size_t)kDualMaxSplits * T * rp};
+    float* dp[3] = {at<float>(ws, PL.dpart[0]), at<float>(ws, PL.dpart[1]), at<float>(ws, PL.dpart[2])};
+    if (dsA.use) {  // Gd = s_d dY Bd, formed once (feeds dh and dA_down), and dB_down's partials
+        DualLaunch L;
+        L.add(dY, T, d, down->B, r, haT, rp, 0, D.ldT, rp, dsA, gp[0], dp[0]);
+        LM_TRY(L.launch("mlp.gd", sms, rp, err, st));
+        LM_TRY(fin_rows_split("mlp.gd.fin",
+                              {FinRowJob{gp[0], T * rp, dual_ranges(d, dsA.CB), rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}},
+                              T, st));
+    } else {  // Gd = s_d dY Bd, formed once (feeds dh and dA_down)
         Builder b(G_PART_KMN);
         add_rowproj_out(b, dY, T, d, down->B, D, part);
         LM_TRY(b.launch("mlp.gd", sms, err, st));
@@ -1282,7 +1467,16 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         }
         LM_TRY(b.launch("mlp.dh", sms, err, st));
     }
-    {  // Gg = s_g de Bg, Gu = s_u du Bu, formed once (feed dA and dX)
+    if (dsB.use) {  // Gg = s_g de Bg, Gu = s_u du Bu, formed once (feed dA and dX), and dB_gate's, dB_up's partials
+        DualLaunch L;
+        L.add(de, T, n, gate->B, r, xaT, 2 * rp, 0, D.ldT, rp, dsB, gp[1], dp[1]);
+        L.add(du, T, n, up->B, r, xaT, 2 * rp, rp, D.ldT, rp, dsB, gp[2], dp[2]);
+        LM_TRY(L.launch("mlp.gg_gu", sms, rp, err, st));
+        LM_TRY(fin_rows_split("mlp.gg_gu.fin",
+                              {FinRowJob{gp[1], T * rp, dual_ranges(n, dsB.CB), rp, rp, {gate->s, 0.f, 0.f}, gg, ggT, D.ldT},
+                               FinRowJob{gp[2], T * rp, dual_ranges(n, dsB.CB), rp, rp, {up->s, 0.f, 0.f}, gu, guT, D.ldT}},
+                              T, st));
+    } else {  // Gg = s_g de Bg, Gu = s_u du Bu, formed once (feed dA and dX)
         Builder b(G_PART_KMN);
         float* part_u = part + (size_t)kMaxSplits * T * rp;
         add_rowproj_out(b, de, T, n, gate->B, D, part);
@@ -1293,18 +1487,26 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
                          FinRowJob{part_u, T * rp, 0, rp, rp, {up->s, 0.f, 0.f}, gu, guT, D.ldT}},
                         T, st));
     }
-    {  // the six LoRA gradients as column reductions over the tokens
+    {  // the six LoRA gradients as column reductions over the tokens (those of B from the dual
+       // reductions' partials where they ran), one finalisation launch for all six
         ColReduce cr(D, part);
         cr.add(h_save, n, gdT, {dA_down}, 1);              // dA_down^T = h^T Gd
-        cr.add(dY, d, haT, {dB_down}, 0);                  // dB_down   = dY^T (s h Ad^T)
+        if (!dsA.use) cr.add(dY, d, haT, {dB_down}, 0);    // dB_down   = dY^T (s h Ad^T)
         if (2 * rp <= 64) {
             cr.add(X, d, ggT, {dA_gate, dA_up}, 1);        // [dA_gate; dA_up]^T = X^T [Gg | Gu]
         } else {
             cr.add(X, d, ggT, {dA_gate}, 1);
             cr.add(X, d, guT, {dA_up}, 1);
         }
-        cr.add(de, n, xaT, {dB_gate}, 0);                  // dB_gate   = de^T (s X Ag^T)
-        cr.add(du, n, xaT + (size_t)rp * D.ldT, {dB_up}, 0);  // dB_up  = du^T (s X Au^T)
+        if (!dsB.use) {
+            cr.add(de, n, xaT, {dB_gate}, 0);                  // dB_gate   = de^T (s X Ag^T)
+            cr.add(du, n, xaT + (size_t)rp * D.ldT, {dB_up}, 0);  // dB_up  = du^T (s X Au^T)
+        }
+        if (dsA.use) cr.add_fin(FinColJob{dp[0], d * rp, d, dsA.nrr, rp, r, 0, dB_down, rp});
+        if (dsB.use) {
+            cr.add_fin(FinColJob{dp[1], n * rp, n, dsB.nrr, rp, r, 0, dB_gate, rp});
+            cr.add_fin(FinColJob{dp[2], n * rp, n, dsB.nrr, rp, r, 0, dB_up, rp});
+        }
         LM_TRY(cr.run("mlp.dAdB", "mlp.dAdB.fin", sms, err, st));
     }
     {  // dX = de Wg + du Wu + Gg Ag + Gu Au on 512 x 256 tiles for every base
@@ -1836,7 +2038,23 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
         g[i] = at<uint16_t>(ws, PL.g[i].rows_off);
         gT[i] = at<uint16_t>(ws, PL.g[i].t_off);
     }
-    {  // G_x = s_x dOut_x B_x, formed once per projection
+    // the dual rank-r reduction reads each dOut_x once for both G_x and dB_x, where that pays
+    const DualShape ds = plan_dual(T, {nq, nk, nv}, rp, sms);
+    float* dps[3] = {at<float>(ws, PL.dpart[0]), at<float>(ws, PL.dpart[1]), at<float>(ws, PL.dpart[2])};
+    if (ds.use) {  // G_x = s_x dOut_x B_x once per projection, and dB_x's partials
+        float* gps[3];
+        for (int i = 0; i < 3; ++i) gps[i] = part + (size_t)i * kDualMaxSplits * T * rp;  // in the split-K partial region
+        DualLaunch L;
+        for (int i = 0; i < 3; ++i)
+            L.add(dOut[i], T, ns[i], Ls[i]->B, r, xaT, 3 * rp, i * rp, D.ldT, rp, ds, gps[i], dps[i]);
+        LM_TRY(L.launch("qkv.g", sms, rp, err, st));
+        LM_TRY(fin_rows_split(
+            "qkv.g.fin",
+            {FinRowJob{gps[0], T * rp, dual_ranges(nq, ds.CB), rp, rp, {q->s, 0.f, 0.f}, g[0], gT[0], D.ldT},
+             FinRowJob{gps[1], T * rp, dual_ranges(nk, ds.CB), rp, rp, {k->s, 0.f, 0.f}, g[1], gT[1], D.ldT},
+             FinRowJob{gps[2], T * rp, dual_ranges(nv, ds.CB), rp, rp, {v->s, 0.f, 0.f}, g[2], gT[2], D.ldT}},
+            T, st));
+    } else {  // G_x = s_x dOut_x B_x, formed once per projection
         Builder b(G_PART_KMN);
         float* parts[3];
         for (int i = 0; i < 3; ++i) {
@@ -1859,9 +2077,14 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             cr.add(X, d, gT[1], {dA_k}, 1);
             cr.add(X, d, gT[2], {dA_v}, 1);
         }
-        cr.add(dQ, nq, xaT, {dB_q}, 0);
-        cr.add(dK, nk, xaT + (size_t)rp * D.ldT, {dB_k}, 0);
-        cr.add(dV, nv, xaT + (size_t)2 * rp * D.ldT, {dB_v}, 0);
+        if (ds.use) {
+            float* dBs[3] = {dB_q, dB_k, dB_v};
+            for (int i = 0; i < 3; ++i) cr.add_fin(FinColJob{dps[i], ns[i] * rp, ns[i], ds.nrr, rp, r, 0, dBs[i], rp});
+        } else {
+            cr.add(dQ, nq, xaT, {dB_q}, 0);
+            cr.add(dK, nk, xaT + (size_t)rp * D.ldT, {dB_k}, 0);
+            cr.add(dV, nv, xaT + (size_t)2 * rp * D.ldT, {dB_v}, 0);
+        }
         LM_TRY(cr.run("qkv.dAdB", "qkv.dAdB.fin", sms, err, st));
     }
     {  // dX = sum_x dOut_x W_x + G_x A_x
@@ -2051,7 +2274,17 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     uint16_t* g = at<uint16_t>(ws, PL.g.rows_off);
     uint16_t* gT = at<uint16_t>(ws, PL.g.t_off);
-    {  // G = s dY B, formed once (feeds dA and dX)
+    // the dual rank-r reduction reads dY once for both G and dB, where that pays
+    const DualShape ds = plan_dual(T, {d_out}, rp, sms);
+    float* dpo = at<float>(ws, PL.dpart);
+    if (ds.use) {  // G = s dY B, formed once (feeds dA and dX), and dB's partials
+        float* gpo = part;  // in the split-K partial region
+        DualLaunch L;
+        L.add(dY, T, d_out, o->B, r, xaT, rp, 0, D.ldT, rp, ds, gpo, dpo);
+        LM_TRY(L.launch("o.g", sms, rp, err, st));
+        LM_TRY(fin_rows_split(
+            "o.g.fin", {FinRowJob{gpo, T * rp, dual_ranges(d_out, ds.CB), rp, rp, {o->s, 0.f, 0.f}, g, gT, D.ldT}}, T, st));
+    } else {  // G = s dY B, formed once (feeds dA and dX)
         Builder b(G_PART_KMN);
         add_rowproj_out(b, dY, T, d_out, o->B, D, part);
         LM_TRY(b.launch("o.g", sms, err, st));
@@ -2060,7 +2293,8 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     {  // dA^T = X^T G, dB = dY^T (s X A^T)
         ColReduce cr(D, part);
         cr.add(X, d_in, gT, {dA}, 1);
-        cr.add(dY, d_out, xaT, {dB}, 0);
+        if (ds.use) cr.add_fin(FinColJob{dpo, d_out * rp, d_out, ds.nrr, rp, r, 0, dB, rp});
+        else cr.add(dY, d_out, xaT, {dB}, 0);
         LM_TRY(cr.run("o.dAdB", "o.dAdB.fin", sms, err, st));
     }
     {  // dX = dY W + G A

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "lm_dual.cuh"
 #include "lm_gemm.cuh"
 
 namespace lm {
@@ -41,6 +42,9 @@ cudaError_t launch_gemm_pair_nf4(GemmKind k, const Params& p, int max_units, cud
 cudaError_t launch_blockdiag(const uint16_t* Bg, const uint16_t* Bu, int64_t n, int r, int rp, uint16_t* out,
                              cudaStream_t st);
 cudaError_t launch_gemm(GemmKind k, const Params& p, int grid, cudaStream_t st);
+// The dual rank-r reduction (lm_dual.cuh): `grid` CTAs, one per SM.
+cudaError_t launch_dual_reduce(const DualParams& p, int grid, cudaStream_t st);
+
 
 // Finalisation of split-K partials of rank-r projections:
 //   out[t][c] = bf16(s[c / group] * sum_ks part[ks][t][c]), also written transposed to

@@ -189,6 +189,18 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lb
     return d;
 }
 
+// The same for a 32-byte-swizzled operand (layout 6): an MN-major tile whose rows (one per K
+// index) hold 16 elements of M/N in 32 bytes, 8-row groups SBO apart, 16-wide M/N chunks LBO apart.
+__device__ __forceinline__ uint64_t make_sdesc_sw32(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)6 << 61;
+    return d;
+}
+
 // TMEM -> registers: 32 lanes x 32 bit, `N` consecutive columns per thread.  The wait carries
 // the registers as operands so no use of them can be scheduled before it.
 __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {

@@ -10,7 +10,7 @@
 //
 // The scratch is kStaticWsBytes (64 MiB) of __device__ memory per GPU that loads the library,
 // held until the process exits.  It covers the O-projection shapes whose lora_o_workspace_size
-// is at most that (for example T = 8192 tokens, 4096 -> 4096, r = 16 needs about 49.5 MiB);
+// is at most that (for example T = 8192 tokens, 4096 -> 4096, r = 16 needs about 54 MiB);
 // larger shapes are rejected with LM_ERR_WORKSPACE before anything is enqueued.  So is every
 // other argument error: all of lora_o_bwd's checks run on the host before the first device call.
 //

@@ -152,15 +152,18 @@ LM_API lm_status lm_workspace_reset(void* ws, lm_stream stream);
  * a kernel recorded a timeout since the last reset (LM_OK otherwise).  This call synchronises. */
 LM_API lm_status lm_workspace_check(void* ws, lm_stream stream);
 
-/* Test hook for the timeout path ([LO] names no failure handling beyond argument validation; the
- * bounded waits are this library's).  Applies to the kernels launched afterwards by the calling
- * thread.  family_mask selects GEMM kernel families whose TMA producers issue no loads at all --
- * bit 0 the split-K rank-r kernel, bit 1 the bf16 CTA-pair kernel, bit 2 the packed-base (and
- * plain-store) CTA-pair kernel -- so their consumers' waits run out, no copy is in flight when
- * they do, and the call's error word reads LM_ERR_TIMEOUT (lm_workspace_check); the outputs of
- * such a call are undefined.  wait_ns sets the time limit of every pipeline wait, in nanoseconds
- * (0: the default, 2 s).  lm_debug_inject(0, 0) restores normal operation.  Host only; never
- * fails for a mask in [0, 7] (else LM_ERR_SHAPE). */
+/* Test hook for the timeout path and the planner ([LO] names no failure handling beyond argument
+ * validation; the bounded waits are this library's).  Applies to the kernels launched afterwards
+ * by the calling thread.  Bits 0-3 of family_mask select kernel families whose TMA producers issue
+ * no loads at all -- bit 0 the split-K rank-r kernel, bit 1 the bf16 CTA-pair kernel, bit 2 the
+ * packed-base (and plain-store) CTA-pair kernel, bit 3 the dual rank-r reduction -- so their
+ * consumers' waits run out, no copy is in flight when they do, and the call's error word reads
+ * LM_ERR_TIMEOUT (lm_workspace_check); the outputs of such a call are undefined.  Bit 4 makes the
+ * MLP backward take the dual rank-r reductions wherever they are feasible, not only where they
+ * are estimated faster (the results are the same up to the order of fp32 additions).  wait_ns
+ * sets the time limit of every pipeline wait, in nanoseconds (0: the default, 2 s).
+ * lm_debug_inject(0, 0) restores normal operation.  Host only; never fails for a mask in [0, 31]
+ * (else LM_ERR_SHAPE). */
 LM_API lm_status lm_debug_inject(int32_t family_mask, uint64_t wait_ns);
 
 /* ---- tracing ---------------------------------------------------------------------------

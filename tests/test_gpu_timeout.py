@@ -7,7 +7,8 @@ free their tensor memory and return, and lm_workspace_check reports the status. 
 made again with the switch off must then match the fp64 oracle: the context stays usable.
 Families: 1 the split-K rank-r kernel, 2 the bf16 CTA-pair kernel (gate/up, dh of a bf16 base),
 3 the packed-base CTA-pair kernel (down and dX of every base; gate/up and dh of an NF4 base, whose
-decode warps and staged dh epilogue then time out too)."""
+decode warps and staged dh epilogue then time out too), 4 the dual rank-r reduction (forced onto
+this small case by the hook's flag 16)."""
 import ctypes
 
 import pytest
@@ -46,7 +47,8 @@ def _step(inp, Ls, act):
     return fw, bw
 
 
-@pytest.mark.parametrize("base,mask,family", [("bf16", 1, 1), ("bf16", 2, 2), ("bf16", 4, 3), ("nf4", 4, 3)])
+@pytest.mark.parametrize("base,mask,family", [("bf16", 1, 1), ("bf16", 2, 2), ("bf16", 4, 3), ("nf4", 4, 3),
+                                              ("bf16", 8 | 16, 4)])
 def test_starved_family_reports_timeout_then_recovers(base, mask, family):
     w, inp, Ls = _mlp(base)
     _inject(mask, WAIT_NS)
