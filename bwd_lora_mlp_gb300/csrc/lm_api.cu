@@ -1555,6 +1555,7 @@ struct Relu2Plan {
     size_t sc[2];           // NF4 base: fp32 block-scale tables of W_up, W_down
     size_t tail;            // NF4 base: split tail tiles of the down and dX GEMMs
     size_t abc;             // bf16 copies of fp32 LoRA A and B
+    size_t dpart[2];        // dual reductions: dB partials of dBd ([ranges][d][rp]), dBu ([ranges][n][rp])
     size_t ws_total;
 };
 
@@ -1577,6 +1578,8 @@ Relu2Plan plan_relu2(int64_t T, int64_t d, int64_t n, int32_t r) {
     P.sc[1] = w.take((size_t)d * n / 64 * 4);
     P.tail = w.take(kTailBytes);
     P.abc = w.take((size_t)(ab_elems(r, d, n) + ab_elems(r, n, d)) * 2);
+    P.dpart[0] = w.take((size_t)kDualMaxSplits * d * rp * 4);
+    P.dpart[1] = w.take((size_t)kDualMaxSplits * n * rp * 4);
     P.ws_total = w.off;
     return P;
 }
@@ -1777,7 +1780,18 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
     uint16_t* guT = at<uint16_t>(ws, PL.gu.t_off);
     uint16_t* du = at<uint16_t>(ws, PL.du);
 
-    {  // Gd = s_d dY Bd, formed once (feeds dh and dA_down)
+    // the dual rank-r reductions (lm_dual.cuh) read dY and du once each for both G and dB, where
+    // the planner finds that cheaper than the separate passes
+    const DualShape dsA = plan_dual(T, {d}, rp, sms), dsB = plan_dual(T, {n}, rp, sms);
+    float* dp[2] = {at<float>(ws, PL.dpart[0]), at<float>(ws, PL.dpart[1])};
+    if (dsA.use) {  // Gd = s_d dY Bd (feeds dh and dA_down) and dB_down's partials
+        DualLaunch L;
+        L.add(dY, T, d, down->B, r, haT, rp, 0, D.ldT, rp, dsA, part, dp[0]);
+        LM_TRY(L.launch("relu2.gd", sms, rp, err, st));
+        LM_TRY(fin_rows_split("relu2.gd.fin",
+                              {FinRowJob{part, T * rp, dual_ranges(d, dsA.CB), rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}},
+                              T, st));
+    } else {  // Gd = s_d dY Bd, formed once (feeds dh and dA_down)
         Builder b(G_PART_KMN);
         add_rowproj_out(b, dY, T, d, down->B, D, part);
         LM_TRY(b.launch("relu2.gd", sms, err, st));
@@ -1809,18 +1823,28 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
         P.ld_out = n;
         LM_TRY(b.launch("relu2.dh", sms, err, st));
     }
-    {  // Gu = s_u du Bu, formed once (feeds dA_up and dX)
+    if (dsB.use) {  // Gu = s_u du Bu (feeds dA_up and dX) and dB_up's partials
+        DualLaunch L;
+        L.add(du, T, n, up->B, r, xaT, rp, 0, D.ldT, rp, dsB, part, dp[1]);
+        LM_TRY(L.launch("relu2.gu", sms, rp, err, st));
+        LM_TRY(fin_rows_split("relu2.gu.fin",
+                              {FinRowJob{part, T * rp, dual_ranges(n, dsB.CB), rp, rp, {up->s, 0.f, 0.f}, gu, guT, D.ldT}},
+                              T, st));
+    } else {  // Gu = s_u du Bu, formed once (feeds dA_up and dX)
         Builder b(G_PART_KMN);
         add_rowproj_out(b, du, T, n, up->B, D, part);
         LM_TRY(b.launch("relu2.gu", sms, err, st));
         LM_TRY(fin_rows("relu2.gu.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {up->s, 0.f, 0.f}, gu, guT, D.ldT}}, T, st));
     }
-    {  // the four LoRA gradients as column reductions over the tokens
+    {  // the four LoRA gradients as column reductions over the tokens (those of B from the dual
+       // reductions' partials where they ran), one finalisation launch
         ColReduce cr(D, part);
-        cr.add(h_save, n, gdT, {dA_down}, 1);  // dA_down^T = h^T Gd
-        cr.add(dY, d, haT, {dB_down}, 0);      // dB_down   = dY^T (s h Ad^T)
-        cr.add(X, d, guT, {dA_up}, 1);         // dA_up^T   = X^T Gu
-        cr.add(du, n, xaT, {dB_up}, 0);        // dB_up     = du^T (s X Au^T)
+        cr.add(h_save, n, gdT, {dA_down}, 1);                  // dA_down^T = h^T Gd
+        if (!dsA.use) cr.add(dY, d, haT, {dB_down}, 0);        // dB_down   = dY^T (s h Ad^T)
+        cr.add(X, d, guT, {dA_up}, 1);                         // dA_up^T   = X^T Gu
+        if (!dsB.use) cr.add(du, n, xaT, {dB_up}, 0);          // dB_up     = du^T (s X Au^T)
+        if (dsA.use) cr.add_fin(FinColJob{dp[0], d * rp, d, dsA.nrr, rp, r, 0, dB_down, rp});
+        if (dsB.use) cr.add_fin(FinColJob{dp[1], n * rp, n, dsB.nrr, rp, r, 0, dB_up, rp});
         LM_TRY(cr.run("relu2.dAdB", "relu2.dAdB.fin", sms, err, st));
     }
     {  // dX = du Wu + Gu Au
