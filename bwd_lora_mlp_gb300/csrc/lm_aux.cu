@@ -34,40 +34,50 @@ __device__ __forceinline__ float4 sum_splits(const float* p0, int64_t stride, in
     return acc;
 }
 
-// One thread per (4-column chunk, row), rows fastest: the transposed writes are coalesced across
-// a warp, the row write is 8 contiguous bytes.  ncols and group are multiples of 4.
+// One CTA per 32 rows of one job: the rows' partials are one contiguous span of 32 ncols floats
+// per split, read with coalesced 16-byte loads; the row-major result is written the same way and
+// the transposed one through a shared-memory tile, 32 contiguous values per output row.  ncols
+// (at most kFinRowMaxCols) and group are multiples of 4.
+constexpr int kFinRowMaxCols = 192;
+constexpr int kFinRowTile = 32;
 __global__ void __launch_bounds__(256) fin_rowproj_kernel(FinRowJobs jobs, int64_t T) {
+    __shared__ uint16_t tileT[kFinRowMaxCols * (kFinRowTile + 2)];  // [column][row], padded pitch
     griddep_launch_dependents();
     griddep_wait();
     const FinRowJob& J = jobs.j[blockIdx.y];
-    const int nchunk = J.ncols / 4;
-    const int64_t total = (int64_t)nchunk * T;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int ch = (int)(idx / T);
-        const int64_t t = idx - (int64_t)ch * T;
-        const int c0 = ch * 4;
-        const float4 a = sum_splits(J.part + t * J.ncols + c0, J.split_stride, J.splits);
+    const int nc = J.ncols;
+    const int pitch = kFinRowTile + 2;
+    const int64_t t0 = (int64_t)blockIdx.x * kFinRowTile;
+    if (t0 >= T) return;
+    const int rows = T - t0 < kFinRowTile ? (int)(T - t0) : kFinRowTile;
+    const int n4 = rows * nc / 4;
+    const float* base = J.part + t0 * nc;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const int e = 4 * i, row = e / nc, c0 = e - row * nc;
+        const float4 a = sum_splits(base + e, J.split_stride, J.splits);
         const float sc = J.s[c0 / J.group];
         const uint32_t w0 = pack_bf16x2(a.x * sc, a.y * sc), w1 = pack_bf16x2(a.z * sc, a.w * sc);
-        *reinterpret_cast<uint2*>(J.out + t * J.ncols + c0) = make_uint2(w0, w1);
-        J.outT[(int64_t)(c0 + 0) * J.ldT + t] = (uint16_t)(w0 & 0xFFFFu);
-        J.outT[(int64_t)(c0 + 1) * J.ldT + t] = (uint16_t)(w0 >> 16);
-        J.outT[(int64_t)(c0 + 2) * J.ldT + t] = (uint16_t)(w1 & 0xFFFFu);
-        J.outT[(int64_t)(c0 + 3) * J.ldT + t] = (uint16_t)(w1 >> 16);
+        *reinterpret_cast<uint2*>(J.out + (t0 + row) * nc + c0) = make_uint2(w0, w1);
+        tileT[(c0 + 0) * pitch + row] = (uint16_t)(w0 & 0xFFFFu);
+        tileT[(c0 + 1) * pitch + row] = (uint16_t)(w0 >> 16);
+        tileT[(c0 + 2) * pitch + row] = (uint16_t)(w1 & 0xFFFFu);
+        tileT[(c0 + 3) * pitch + row] = (uint16_t)(w1 >> 16);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nc * kFinRowTile; i += blockDim.x) {
+        const int c = i / kFinRowTile, row = i - c * kFinRowTile;
+        if (row < rows) J.outT[(int64_t)c * J.ldT + t0 + row] = tileT[c * pitch + row];
     }
 }
 
 cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cudaStream_t st) {
     FinRowJobs js{};
-    int64_t most = 0;
     for (int i = 0; i < njobs; ++i) {
+        if (jobs[i].ncols > kFinRowMaxCols || jobs[i].ncols % 4 || jobs[i].group % 4) return cudaErrorInvalidValue;
         js.j[i] = jobs[i];
-        most = std::max<int64_t>(most, (int64_t)(jobs[i].ncols / 4) * T);
     }
-    const int threads = 256;
-    const int64_t blocks = std::min<int64_t>((most + threads - 1) / threads, 4096);
-    return launch_pdl(fin_rowproj_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1), njobs), dim3(threads), 0, st, nullptr, 0,
+    const int64_t blocks = (T + kFinRowTile - 1) / kFinRowTile;
+    return launch_pdl(fin_rowproj_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1), njobs), dim3(256), 0, st, nullptr, 0,
                       js, T);
 }
 
