@@ -6,17 +6,18 @@
 //     Gpart[cr][t][0..rp)  = sum over the columns c of unit (rr, cr) of  Z[t][c] B[c][.]
 //     Dpart[rr][c][0..rp)  = sum over the rows    t of unit (rr, cr) of  Z[t][c] P[.][t]
 // with B the projection's LoRA B (C x r, row-major; columns r..rp read as zeros) and P the rank
-// block of s (X A^T)^T (rp rows of a K-major rows x T array).  Summing Gpart over cr gives the row reduction Z B, summing Dpart over
-// rr the column reduction Z^T (s X A^T): the two finalisation kernels do that in fixed order.
+// block of s (X A^T)^T (rp rows of a K-major rows x T array).  Summing Gpart over cr gives the row
+// reduction Z B, summing Dpart over rr the column reduction Z^T (s X A^T): the two finalisation
+// kernels do that in fixed order.
 //
 // A work unit is a rectangle of RB x CB tiles of 128 x 128 elements.  Each tile reaches shared
 // memory once (two 64-column TMA boxes, 128-byte swizzle) and feeds two sets of tcgen05 MMAs
 // (M = 128, N = rp, K = 16): read K-major it is the A operand of Z B (M = rows, K = columns), read
 // MN-major the A operand of Z^T P (M = columns, K = rows).  B comes as it is stored: its rows are
 // the K index and its r columns the N index, an MN-major operand of 16-column boxes with 32-byte
-// swizzle.  The G accumulator of a row block
-// (rp TMEM columns, two alternating) is drained after the unit's last column block; the CB dB
-// accumulators (CB x rp columns, two alternating sets) after the unit's last row block.
+// swizzle.  The G accumulator of a row block (rp TMEM columns, two alternating) is drained after
+// the unit's last column block; the CB dB accumulators (CB x rp columns, two alternating sets)
+// after the unit's last row block.
 //
 // Roles (192 threads): warp 0 lane 0 TMA producer, warp 1 MMA issuer (the whole warp runs the
 // issue loop, lane 0 issues), warps 2-5 drain TMEM to the fp32 partials.  Every wait is bounded.

@@ -42,11 +42,12 @@ def test_step_roofline_fractions():
     peaks, src = bench.load_peaks()
     r = bench.step_roofline(1600.0, peaks, src)
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
-    assert r["peak"] == peaks["bf16_tflops_sustained"]
-    assert abs(r["frac"] * peaks["bf16_tflops_sustained"] - 1600.0) < 1e-9
-    assert abs(r["frac_of_burst"] * peaks["bf16_tflops"] - 1600.0) < 1e-9
+    assert r["peak"] == peaks["bf16_tflops"]                      # the headline: burst
+    assert abs(r["frac"] * peaks["bf16_tflops"] - 1600.0) < 1e-9
+    assert r["frac_of_burst"] == r["frac"]
+    assert abs(r["frac_of_sustained"] * peaks["bf16_tflops_sustained"] - 1600.0) < 1e-9
     assert abs(r["frac_of_nominal"] - 1600.0 / 2250.0) < 1e-12
-    assert r["frac_of_nominal"] < r["frac_of_burst"] <= r["frac"]
+    assert r["frac_of_nominal"] < r["frac"] <= r["frac_of_sustained"]
 
 
 def test_traffic_record_is_used_only_for_the_sources_it_was_taken_on(monkeypatch):
