@@ -138,7 +138,8 @@ class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
     FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
-              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap",
+              "enforced.power.limit"]
 
     def __init__(self, gpu_id):
         self.gpu_id = gpu_id
@@ -183,8 +184,20 @@ class ClockSampler:
             for nm, v in zip(names, r[5:9]):
                 if v.lower() == "active":
                     reasons.add(nm)
+        def num(i):
+            out = []
+            for r in rows:
+                try:
+                    out.append(float(r[i]))
+                except ValueError:
+                    pass
+            return out
+        pw, plim = num(3), num(9)
+        # power draw and the enforced limit: tensor-bound kernels run at the power cap, so the limit
+        # of the GPU at hand sets their clock (it differs between otherwise identical GPUs)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w": statistics.median(pw) if pw else None, "power_limit_w": max(plim) if plim else None}
 
 
 def dist_setup():
@@ -421,15 +434,15 @@ def measure(w, args, world, local, e2e=True):
             L.lora_relu2_mlp_bwd(xs[0], xs[1], fw, up, down, dX=outs["dX"],
                                  grads={k: outs[k] for k in outs if k not in ("y", "dX")})
     elif w.kind == "qkv":
-        q, k_, v = projs["q"], projs["k"], projs["v"]
-        fw = L.lora_qkv_fwd(ins[0], q, k_, v)
-        bw = L.lora_qkv_bwd(ins[0], ins[1], ins[2], ins[3], fw, q, k_, v)
+        q, k_, v_ = projs["q"], projs["k"], projs["v"]
+        fw = L.lora_qkv_fwd(ins[0], q, k_, v_)
+        bw = L.lora_qkv_bwd(ins[0], ins[1], ins[2], ins[3], fw, q, k_, v_)
         out_keys = ["Q", "K", "V"]
 
         def run(xs, outs):
-            L.lora_qkv_fwd(xs[0], q, k_, v, out={t: outs[t] for t in ("Q", "K", "V")}, saved=fw["saved"],
+            L.lora_qkv_fwd(xs[0], q, k_, v_, out={t: outs[t] for t in ("Q", "K", "V")}, saved=fw["saved"],
                            ws=fw["ws"])
-            L.lora_qkv_bwd(xs[0], xs[1], xs[2], xs[3], fw, q, k_, v, dX=outs["dX"],
+            L.lora_qkv_bwd(xs[0], xs[1], xs[2], xs[3], fw, q, k_, v_, dX=outs["dX"],
                            grads={t: outs[t] for t in ("dA_q", "dB_q", "dA_k", "dB_k", "dA_v", "dB_v")})
     else:
         o = projs["o"]
@@ -561,8 +574,8 @@ def measure(w, args, world, local, e2e=True):
             for dst, src in zip(dev_in[0], host_in):
                 dst.copy_(src, non_blocking=True)
             run(dev_in[0], dev_out[0])
-            for k, v in host_out[0].items():
-                v.copy_(dev_out[0][k], non_blocking=True)
+            for name, buf in host_out[0].items():  # (names that run()'s closure does not use)
+                buf.copy_(dev_out[0][name], non_blocking=True)
             stream.synchronize()
             sync.append((time.perf_counter() - t0) * 1e3)
         sync_ms = max_over_ranks(statistics.median(sync), world)
