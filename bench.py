@@ -192,12 +192,12 @@ class ClockSampler:
                 except ValueError:
                     pass
             return out
-        pw, plim = num(3), num(9)
-        # power draw and the enforced limit: tensor-bound kernels run at the power cap, so the limit
-        # of the GPU at hand sets their clock (it differs between otherwise identical GPUs)
+        plim = num(9)
+        # the enforced power limit: tensor-bound kernels run at the power cap, so the limit of the
+        # GPU at hand sets their clock (the sampled draw is a trailing average, too slow to follow a
+        # sub-second timed region, and is not reported)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(rows),
-                "power_w": statistics.median(pw) if pw else None, "power_limit_w": max(plim) if plim else None}
+                "reasons": sorted(reasons), "samples": len(rows), "power_limit_w": max(plim) if plim else None}
 
 
 def dist_setup():

@@ -85,29 +85,42 @@ struct FinColJobs {
     FinColJob j[kMaxFinColJobs];
 };
 
-// One thread per (column c, 4-wide chunk of j), chunk fastest: the partial reads of a warp are
-// contiguous, and so are the writes of out[c][j]; rp and ldp are multiples of 4.
+// One CTA per 32 columns of one job.  The columns' partial rows are read with coalesced 16-byte
+// loads (4-wide chunk of j fastest; rp and ldp are multiples of 4) and summed over the splits in
+// split order.  The dB layout out[c][j] of 32 columns is one contiguous span, written directly;
+// the dA layout out[j][c] goes through a shared-memory tile so that each output row gets 32
+// contiguous values.
+constexpr int kFinColTile = 32;
+constexpr int kFinColMaxRp = 64;
 __global__ void __launch_bounds__(256) fin_colreduce_kernel(FinColJobs jobs) {
+    __shared__ float tile[kFinColMaxRp * (kFinColTile + 1)];  // [j][column], padded pitch
     griddep_launch_dependents();
     griddep_wait();
     const FinColJob& J = jobs.j[blockIdx.y];
+    const int64_t c0 = (int64_t)blockIdx.x * kFinColTile;
+    if (c0 >= J.C) return;
+    const int cols = J.C - c0 < kFinColTile ? (int)(J.C - c0) : kFinColTile;
     const int nchunk = J.rp / 4;
-    const int64_t total = J.C * nchunk;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t c = idx / nchunk;
-        const int ch = (int)(idx - c * nchunk);
-        const int j0 = ch * 4;
+    const int pitch = kFinColTile + 1;
+    for (int i = threadIdx.x; i < cols * nchunk; i += blockDim.x) {
+        const int cl = i / nchunk, j0 = 4 * (i - cl * nchunk);
         if (j0 >= J.r) continue;
+        const int64_t c = c0 + cl;
         const float4 a = sum_splits(J.part + c * J.ldp + j0, J.split_stride, J.splits);
         const float v[4] = {a.x, a.y, a.z, a.w};
         const int nj = min(4, J.r - j0);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (i < nj) {
-                if (J.transposed) J.out[(int64_t)(j0 + i) * J.C + c] = v[i];  // out[j][c]
-                else J.out[c * J.r + j0 + i] = v[i];                          // out[c][j]
+        for (int k = 0; k < 4; ++k)
+            if (k < nj) {
+                if (J.transposed) tile[(j0 + k) * pitch + cl] = v[k];
+                else J.out[c * J.r + j0 + k] = v[k];  // out[c][j]
             }
+    }
+    if (!J.transposed) return;  // (uniform across the CTA: one job per blockIdx.y)
+    __syncthreads();
+    for (int i = threadIdx.x; i < J.r * kFinColTile; i += blockDim.x) {
+        const int j = i / kFinColTile, cl = i - j * kFinColTile;
+        if (cl < cols) J.out[(int64_t)j * J.C + c0 + cl] = tile[j * pitch + cl];  // out[j][c]
     }
 }
 
@@ -116,12 +129,13 @@ cudaError_t launch_fin_colreduce(const FinColJob* jobs, int njobs, cudaStream_t 
     FinColJobs js{};
     int64_t most = 0;
     for (int i = 0; i < njobs; ++i) {
+        if (jobs[i].rp > kFinColMaxRp || jobs[i].rp % 4 || jobs[i].ldp % 4 || jobs[i].r > jobs[i].rp)
+            return cudaErrorInvalidValue;
         js.j[i] = jobs[i];
-        most = std::max<int64_t>(most, jobs[i].C * (jobs[i].rp / 4));
+        most = std::max<int64_t>(most, jobs[i].C);
     }
-    const int threads = 256;
-    const int64_t blocks = std::min<int64_t>((most + threads - 1) / threads, 4096);
-    return launch_pdl(fin_colreduce_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1), njobs), dim3(threads), 0, st, nullptr,
+    const int64_t blocks = (most + kFinColTile - 1) / kFinColTile;
+    return launch_pdl(fin_colreduce_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1), njobs), dim3(256), 0, st, nullptr,
                       0, js);
 }
 
