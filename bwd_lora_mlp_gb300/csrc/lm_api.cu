@@ -729,19 +729,28 @@ struct Builder {
         }
         int S = 1;
         if (partial) {
-            // split count with the fewest K blocks on the busiest CTA: waves x blocks per unit
-            int64_t best = INT64_MAX;
+            // split count with the least modelled time, counted in A-tile loads (128 x 64 bf16) of
+            // one CTA: waves x (K blocks per unit + the unit's fp32 partial write, bn / 32 of them)
+            // + the finalisation's read of every partial spread over as many CTAs.  (Without the
+            // partial terms six column reductions over 4096 tokens at r = 64 took eight splits,
+            // one wave fewer, and 226 MB of partials to write and read back.)
+            double best = 1e300;
             for (int cand = 1; cand <= kMaxSplits; ++cand) {
                 int64_t units_c = 0, kbps_max = 0;
+                double ep_max = 0.0, part = 0.0;
                 for (int i = 0; i < p.nprob; ++i) {
                     const Prob& P = p.prob[i];
                     const int64_t nkb = (P.seg[0].kext + kBK - 1) / kBK;
                     const int64_t kbps = (nkb + cand - 1) / cand;
-                    units_c += (int64_t)P.tiles_m * P.tiles_n * ((nkb + kbps - 1) / kbps);
+                    const int64_t u = (int64_t)P.tiles_m * P.tiles_n * ((nkb + kbps - 1) / kbps);
+                    units_c += u;
                     kbps_max = std::max(kbps_max, kbps);
+                    ep_max = std::max(ep_max, P.bn / 32.0);
+                    part += (double)u * kBM * P.bn * 4.0;
                 }
-                const int64_t cost = (units_c + slots - 1) / slots * kbps_max;
-                if (cost < best) {
+                const double cost = (double)((units_c + slots - 1) / slots) * ((double)kbps_max + ep_max) +
+                                     part / ((double)kBM * kBK * 2.0 * slots);
+                if (cost < best * (1.0 - 1e-9)) {
                     best = cost;
                     S = cand;
                 }
