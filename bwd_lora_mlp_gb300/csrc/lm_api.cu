@@ -431,22 +431,17 @@ OPlan plan_o(int64_t T, int64_t d_in, int64_t d_out, int32_t r) {
     return P;
 }
 
-// fp32 block-scale tables of the NF4 weights among `ws` for the NF4 GEMMs, one launch (traced
-// under `tag`); int4 and NVFP4 weights need none: their scales are read where they are
+// fp32 block-scale tables of the NF4 weights among `ws` for the NF4 GEMMs, built as side work of
+// a finalisation launch (FinSide) that runs before the first GEMM reading them; int4 and NVFP4
+// weights need none: their scales are read where they are
 struct ScaleTable {
     const lm_weight* W;
     float* table;
 };
-lm_status scale_tables(const char* tag, std::initializer_list<ScaleTable> ws, cudaStream_t st) {
-    Nf4ScaleJobs jobs{};
-    int nj = 0;
+void side_scale_tables(FinSide& side, std::initializer_list<ScaleTable> ws) {
     for (const ScaleTable& t : ws)
         if (t.W->kind == LM_WEIGHT_NF4)
-            jobs.j[nj++] = Nf4ScaleJob{t.W->absmax_q, t.W->group_scale, t.W->rows, t.W->cols / 64, t.table};
-    if (nj == 0) return LM_OK;
-    ProfScope prof(tag, st);
-    const cudaError_t e = launch_nf4_scale_tables(jobs, nj, st);
-    return e == cudaSuccess ? LM_OK : cuda_fail(e, "NF4 scale table launch");
+            side.nf4.j[side.nf4_jobs++] = Nf4ScaleJob{t.W->absmax_q, t.W->group_scale, t.W->rows, t.W->cols / 64, t.table};
 }
 
 // fp32 LoRA parameters ([LO] "FP32 LoRA gradients"): A (r x in) and B (out x r) of every fp32
@@ -554,7 +549,7 @@ struct Builder {
     // codes map of an NF4 weight read MN-major (input gradient: box 64 bytes = 128 elements x 64 rows)
     int codes_mn(const lm_weight& W) { return map_u8(W.codes, W.rows, W.cols / 2, W.cols / 2, 64, 64); }
 
-    // fp32 block-scale table of an NF4 weight ([cols / 64][rows], see launch_nf4_scale_tables):
+    // fp32 block-scale table of an NF4 weight ([cols / 64][rows], see nf4_scale_tile):
     // box 128 rows x 1 K block (weight read K-major) or 64 rows x 2 column blocks (MN-major);
     // rows outside the weight read 0
     // An NVFP4 weight maps its E4M3 block scales the same way (four per 32-bit word); an int4
@@ -949,7 +944,7 @@ struct ColReduce {
 };
 
 lm_status fin_rows(const char* tag, const Builder& b, std::initializer_list<FinRowJob> jobs, int64_t T,
-                   cudaStream_t st) {
+                   cudaStream_t st, const FinSide* side = nullptr) {
     FinRowJob js[3];
     int n = 0;
     for (const FinRowJob& j : jobs) {
@@ -958,18 +953,19 @@ lm_status fin_rows(const char* tag, const Builder& b, std::initializer_list<FinR
         ++n;
     }
     ProfScope prof(tag, st);
-    const cudaError_t e = launch_fin_rowproj(js, n, T, st);
+    const cudaError_t e = launch_fin_rowproj(js, n, T, st, side);
     if (e != cudaSuccess) return cuda_fail(e, "rank-r finalisation launch");
     return LM_OK;
 }
 
 // Explicit split counts (a dual reduction's column ranges)
-lm_status fin_rows_split(const char* tag, std::initializer_list<FinRowJob> jobs, int64_t T, cudaStream_t st) {
+lm_status fin_rows_split(const char* tag, std::initializer_list<FinRowJob> jobs, int64_t T, cudaStream_t st,
+                         const FinSide* side = nullptr) {
     FinRowJob js[3];
     int n = 0;
     for (const FinRowJob& j : jobs) js[n++] = j;
     ProfScope prof(tag, st);
-    const cudaError_t e = launch_fin_rowproj(js, n, T, st);
+    const cudaError_t e = launch_fin_rowproj(js, n, T, st, side);
     if (e != cudaSuccess) return cuda_fail(e, "rank-r finalisation launch");
     return LM_OK;
 }
@@ -1266,9 +1262,18 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     up = &up_c;
     down = &down_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
-    if (q4) {  // the NF4 GEMMs read per-K-block fp32 block scales of W_gate, W_up, W_down
-        LM_TRY(scale_tables("mlp.nf4s", {{&gate->W, sc[0]}, {&up->W, sc[1]}, {&down->W, sc[2]}}, st));
-    }
+    // Side work of the X A^T finalisation launch, which nothing before the gate/up GEMM needs: the
+    // per-K-block fp32 block scales of the NF4 weights (read by the NF4 GEMMs) and the
+    // block-diagonal rank-r operand [Bg | 0 ; 0 | Bu] of the gate/up GEMM
+    uint16_t* bdiag = at<uint16_t>(ws, PL.bdiag);
+    FinSide side;
+    side_scale_tables(side, {{&gate->W, sc[0]}, {&up->W, sc[1]}, {&down->W, sc[2]}});
+    side.bd_Bg = bf(gate->B);
+    side.bd_Bu = bf(up->B);
+    side.bd_n = n;
+    side.bd_r = r;
+    side.bd_rp = rp;
+    side.bd_out = bdiag;
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
     uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     uint16_t* ha = at<uint16_t>(saved, PL.ha.rows_off);
@@ -1278,17 +1283,12 @@ extern "C" lm_status lora_mlp_fwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         Builder b(G_PART_KK);
         add_rowproj_in(b, X, T, d, {gate->A, up->A}, D, part);
         LM_TRY(b.launch("mlp.xa", sms, err, st));
-        LM_TRY(fin_rows("mlp.xa.fin", b, {FinRowJob{part, T * 2 * rp, 0, 2 * rp, rp, {gate->s, up->s, 0.f}, xa, xaT, D.ldT}}, T, st));
+        LM_TRY(fin_rows("mlp.xa.fin", b, {FinRowJob{part, T * 2 * rp, 0, 2 * rp, rp, {gate->s, up->s, 0.f}, xa, xaT, D.ldT}}, T,
+                        st, &side));
     }
     {  // e, u and h = act(e) * u; the rank-r terms enter the same accumulator
         // CTA pair: CTA 0 holds (or decodes) the 128 W_g rows of a tile, CTA 1 the matching W_u rows;
         // the rank-r segment multiplies [s XAg | s XAu] by the block-diagonal [Bg | 0 ; 0 | Bu]
-        uint16_t* bdiag = at<uint16_t>(ws, PL.bdiag);
-        {
-            ProfScope prof("mlp.bdiag", st);
-            const cudaError_t be = launch_blockdiag(bf(gate->B), bf(up->B), n, r, rp, bdiag, st);
-            if (be != cudaSuccess) return cuda_fail(be, "rank-r operand launch");
-        }
         Builder b(q4 ? G2N_GLU_FWD : G2_GLU_FWD);
         Prob& P = b.prob();
         P.M = (int32_t)T;
@@ -1408,9 +1408,10 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
     up = &up_c;
     down = &down_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
-    if (q4) {
-        LM_TRY(scale_tables("mlp.nf4s", {{&gate->W, sc[0]}, {&up->W, sc[1]}, {&down->W, sc[2]}}, st));
-    }
+    // the NF4 weights' fp32 block-scale tables, first read by the dh GEMM: side work of the G_d
+    // finalisation launch
+    FinSide side;
+    side_scale_tables(side, {{&gate->W, sc[0]}, {&up->W, sc[1]}, {&down->W, sc[2]}});
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     const uint16_t* haT = at<uint16_t>(saved, PL.ha.t_off);
     uint16_t* gd = at<uint16_t>(ws, PL.gd.rows_off);
@@ -1435,12 +1436,13 @@ extern "C" lm_status lora_mlp_bwd(int64_t T, int64_t d, int64_t n, int32_t act, 
         LM_TRY(L.launch("mlp.gd", sms, rp, err, st));
         LM_TRY(fin_rows_split("mlp.gd.fin",
                               {FinRowJob{gp[0], T * rp, dual_ranges(d, dsA.CB), rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}},
-                              T, st));
+                              T, st, &side));
     } else {  // Gd = s_d dY Bd, formed once (feeds dh and dA_down)
         Builder b(G_PART_KMN);
         add_rowproj_out(b, dY, T, d, down->B, D, part);
         LM_TRY(b.launch("mlp.gd", sms, err, st));
-        LM_TRY(fin_rows("mlp.gd.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st));
+        LM_TRY(fin_rows("mlp.gd.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st,
+                        &side));
     }
     {  // dh = dY Wd + Gd Ad with the activation backward in the epilogue: de, du
         Builder b(q4 ? G2N_GLU_BWD : G2_GLU_BWD);
@@ -1659,9 +1661,8 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
     up = &up_c;
     down = &down_c;
     float* sc[2] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1])};
-    if (q4) {
-        LM_TRY(scale_tables("relu2.nf4s", {{&up->W, sc[0]}, {&down->W, sc[1]}}, st));
-    }
+    FinSide side;  // the NF4 tables: side work of the X A^T finalisation, before the up GEMM
+    side_scale_tables(side, {{&up->W, sc[0]}, {&down->W, sc[1]}});
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
     uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     uint16_t* ha = at<uint16_t>(saved, PL.ha.rows_off);
@@ -1670,7 +1671,8 @@ extern "C" lm_status lora_relu2_mlp_fwd(int64_t T, int64_t d, int64_t n, const u
         Builder b(G_PART_KK);
         add_rowproj_in(b, X, T, d, {up->A}, D, part);
         LM_TRY(b.launch("relu2.xa", sms, err, st));
-        LM_TRY(fin_rows("relu2.xa.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {up->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st));
+        LM_TRY(fin_rows("relu2.xa.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {up->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st,
+                        &side));
     }
     {  // u = X Wu^T + (s_u X Au^T) Bu^T; the epilogue writes u and h = relu(u)^2
         Builder b(q4 ? G2N_ACT_FWD : G2_ACT_FWD);
@@ -1778,9 +1780,8 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
     up = &up_c;
     down = &down_c;
     float* sc[2] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1])};
-    if (q4) {
-        LM_TRY(scale_tables("relu2.nf4s", {{&up->W, sc[0]}, {&down->W, sc[1]}}, st));
-    }
+    FinSide side;  // the NF4 tables: side work of the G_d finalisation, before the dh GEMM
+    side_scale_tables(side, {{&up->W, sc[0]}, {&down->W, sc[1]}});
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     const uint16_t* haT = at<uint16_t>(saved, PL.ha.t_off);
     uint16_t* gd = at<uint16_t>(ws, PL.gd.rows_off);
@@ -1799,12 +1800,13 @@ extern "C" lm_status lora_relu2_mlp_bwd(int64_t T, int64_t d, int64_t n, const u
         LM_TRY(L.launch("relu2.gd", sms, rp, err, st));
         LM_TRY(fin_rows_split("relu2.gd.fin",
                               {FinRowJob{part, T * rp, dual_ranges(d, dsA.CB), rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}},
-                              T, st));
+                              T, st, &side));
     } else {  // Gd = s_d dY Bd, formed once (feeds dh and dA_down)
         Builder b(G_PART_KMN);
         add_rowproj_out(b, dY, T, d, down->B, D, part);
         LM_TRY(b.launch("relu2.gd", sms, err, st));
-        LM_TRY(fin_rows("relu2.gd.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st));
+        LM_TRY(fin_rows("relu2.gd.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {down->s, 0.f, 0.f}, gd, gdT, D.ldT}}, T, st,
+                        &side));
     }
     {  // dh = dY Wd + Gd Ad with the ReLU^2 derivative in the epilogue: du = dh * 2 relu(u)
         Builder b(q4 ? G2N_ACT_BWD : G2_ACT_BWD);
@@ -1955,16 +1957,16 @@ extern "C" lm_status lora_qkv_fwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     k = &k_c;
     v = &v_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
-    if (q4) {  // the NF4 GEMMs read per-K-block fp32 block scales of W_q, W_k, W_v
-        LM_TRY(scale_tables("qkv.nf4s", {{&q->W, sc[0]}, {&k->W, sc[1]}, {&v->W, sc[2]}}, st));
-    }
+    FinSide side;  // the NF4 tables of W_q, W_k, W_v: side work of the X A^T finalisation
+    side_scale_tables(side, {{&q->W, sc[0]}, {&k->W, sc[1]}, {&v->W, sc[2]}});
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
     uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     {
         Builder b(G_PART_KK);
         add_rowproj_in(b, X, T, d, {q->A, k->A, v->A}, D, part);
         LM_TRY(b.launch("qkv.xa", sms, err, st));
-        LM_TRY(fin_rows("qkv.xa.fin", b, {FinRowJob{part, T * 3 * rp, 0, 3 * rp, rp, {q->s, k->s, v->s}, xa, xaT, D.ldT}}, T, st));
+        LM_TRY(fin_rows("qkv.xa.fin", b, {FinRowJob{part, T * 3 * rp, 0, 3 * rp, rp, {q->s, k->s, v->s}, xa, xaT, D.ldT}}, T,
+                        st, &side));
     }
     // A bf16 base keeps the 256 x 256 kernel here: with outputs this narrow (4096 / 1024 columns)
     // the 512-row tiles leave too few units for the machine (measured at the 8B sizes: QKV 0.614
@@ -2058,9 +2060,8 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
     k = &k_c;
     v = &v_c;
     float* sc[3] = {at<float>(ws, PL.sc[0]), at<float>(ws, PL.sc[1]), at<float>(ws, PL.sc[2])};
-    if (q4) {
-        LM_TRY(scale_tables("qkv.nf4s", {{&q->W, sc[0]}, {&k->W, sc[1]}, {&v->W, sc[2]}}, st));
-    }
+    FinSide side;  // the NF4 tables: side work of the G finalisation, before the dX GEMM
+    side_scale_tables(side, {{&q->W, sc[0]}, {&k->W, sc[1]}, {&v->W, sc[2]}});
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     const lm_lora* Ls[3] = {q, k, v};
     const uint16_t* dOut[3] = {dQ, dK, dV};
@@ -2086,7 +2087,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
             {FinRowJob{gps[0], T * rp, dual_ranges(nq, ds.CB), rp, rp, {q->s, 0.f, 0.f}, g[0], gT[0], D.ldT},
              FinRowJob{gps[1], T * rp, dual_ranges(nk, ds.CB), rp, rp, {k->s, 0.f, 0.f}, g[1], gT[1], D.ldT},
              FinRowJob{gps[2], T * rp, dual_ranges(nv, ds.CB), rp, rp, {v->s, 0.f, 0.f}, g[2], gT[2], D.ldT}},
-            T, st));
+            T, st, &side));
     } else {  // G_x = s_x dOut_x B_x, formed once per projection
         Builder b(G_PART_KMN);
         float* parts[3];
@@ -2099,7 +2100,7 @@ extern "C" lm_status lora_qkv_bwd(int64_t T, int64_t d, int64_t nq, int64_t nk, 
                         {FinRowJob{parts[0], T * rp, 0, rp, rp, {q->s, 0.f, 0.f}, g[0], gT[0], D.ldT},
                          FinRowJob{parts[1], T * rp, 0, rp, rp, {k->s, 0.f, 0.f}, g[1], gT[1], D.ldT},
                          FinRowJob{parts[2], T * rp, 0, rp, rp, {v->s, 0.f, 0.f}, g[2], gT[2], D.ldT}},
-                        T, st));
+                        T, st, &side));
     }
     {  // dA_x^T = X^T G_x (one pass over X for q, k, v: G_q, G_k, G_v are stacked), dB_x = dOut_x^T (s X A_x^T)
         ColReduce cr(D, part);
@@ -2208,14 +2209,15 @@ extern "C" lm_status lora_o_fwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(ab_to_bf16("o.ab", {{&o_c, d_in, d_out}}, at<uint16_t>(ws, PL.abc), st));
     o = &o_c;
     float* sc = at<float>(ws, PL.sc);
-    if (q4) LM_TRY(scale_tables("o.nf4s", {{&o->W, sc}}, st));  // per-K-block fp32 block scales of W_o
+    FinSide side;  // the NF4 table of W_o: side work of the X A^T finalisation
+    side_scale_tables(side, {{&o->W, sc}});
     uint16_t* xa = at<uint16_t>(saved, PL.xa.rows_off);
     uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     {
         Builder b(G_PART_KK);
         add_rowproj_in(b, X, T, d_in, {o->A}, D, part);
         LM_TRY(b.launch("o.xa", sms, err, st));
-        LM_TRY(fin_rows("o.xa.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st));
+        LM_TRY(fin_rows("o.xa.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, xa, xaT, D.ldT}}, T, st, &side));
     }
     // (a bf16 base keeps the 256 x 256 kernel: see the QKV forward)
     {
@@ -2303,7 +2305,8 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
     LM_TRY(ab_to_bf16("o.ab", {{&o_c, d_in, d_out}}, at<uint16_t>(ws, PL.abc), st));
     o = &o_c;
     float* sc = at<float>(ws, PL.sc);
-    if (q4) LM_TRY(scale_tables("o.nf4s", {{&o->W, sc}}, st));
+    FinSide side;  // the NF4 table of W_o: side work of the G finalisation, before the dX GEMM
+    side_scale_tables(side, {{&o->W, sc}});
     const uint16_t* xaT = at<uint16_t>(saved, PL.xa.t_off);
     uint16_t* g = at<uint16_t>(ws, PL.g.rows_off);
     uint16_t* gT = at<uint16_t>(ws, PL.g.t_off);
@@ -2316,12 +2319,13 @@ extern "C" lm_status lora_o_bwd(int64_t T, int64_t d_in, int64_t d_out, const ui
         L.add(dY, T, d_out, o->B, r, xaT, rp, 0, D.ldT, rp, ds, gpo, dpo);
         LM_TRY(L.launch("o.g", sms, rp, err, st));
         LM_TRY(fin_rows_split(
-            "o.g.fin", {FinRowJob{gpo, T * rp, dual_ranges(d_out, ds.CB), rp, rp, {o->s, 0.f, 0.f}, g, gT, D.ldT}}, T, st));
+            "o.g.fin", {FinRowJob{gpo, T * rp, dual_ranges(d_out, ds.CB), rp, rp, {o->s, 0.f, 0.f}, g, gT, D.ldT}}, T, st,
+            &side));
     } else {  // G = s dY B, formed once (feeds dA and dX)
         Builder b(G_PART_KMN);
         add_rowproj_out(b, dY, T, d_out, o->B, D, part);
         LM_TRY(b.launch("o.g", sms, err, st));
-        LM_TRY(fin_rows("o.g.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, g, gT, D.ldT}}, T, st));
+        LM_TRY(fin_rows("o.g.fin", b, {FinRowJob{part, T * rp, 0, rp, rp, {o->s, 0.f, 0.f}, g, gT, D.ldT}}, T, st, &side));
     }
     {  // dA^T = X^T G, dB = dY^T (s X A^T)
         ColReduce cr(D, part);

@@ -37,13 +37,38 @@ __device__ __forceinline__ float4 sum_splits(const float* p0, int64_t stride, in
 // One CTA per 32 rows of one job: the rows' partials are one contiguous span of 32 ncols floats
 // per split, read with coalesced 16-byte loads; the row-major result is written the same way and
 // the transposed one through a shared-memory tile, 32 contiguous values per output row.  ncols
-// (at most kFinRowMaxCols) and group are multiples of 4.
+// (at most kFinRowMaxCols) and group are multiples of 4.  The blocks with blockIdx.y == njobs do
+// the launch's side work (FinSide), which depends on nothing the row jobs produce.
 constexpr int kFinRowMaxCols = 192;
 constexpr int kFinRowTile = 32;
-__global__ void __launch_bounds__(256) fin_rowproj_kernel(FinRowJobs jobs, int64_t T) {
-    __shared__ uint16_t tileT[kFinRowMaxCols * (kFinRowTile + 2)];  // [column][row], padded pitch
+
+__device__ void blockdiag_rows(const uint16_t* __restrict__ Bg, const uint16_t* __restrict__ Bu, int64_t n, int r,
+                               int rp, uint16_t* __restrict__ out, int64_t first, int64_t stride);
+__device__ void nf4_scale_tile(const Nf4ScaleJobs& jobs, int njobs, int t, float (*tile)[65]);
+__host__ __device__ inline int64_t nf4_scale_tiles(const Nf4ScaleJobs& jobs, int njobs) {
+    int64_t tiles = 0;
+    for (int j = 0; j < njobs; ++j) tiles += ((jobs.j[j].rows + 63) / 64) * ((jobs.j[j].kblocks + 63) / 64);
+    return tiles;
+}
+
+__global__ void __launch_bounds__(256) fin_rowproj_kernel(FinRowJobs jobs, int njobs, int64_t T, FinSide side) {
+    __shared__ union {
+        uint16_t tileT[kFinRowMaxCols * (kFinRowTile + 2)];  // row jobs: [column][row], padded pitch
+        float nf4[64][65];                                   // NF4 table tiles
+    } sm;
     griddep_launch_dependents();
     griddep_wait();
+    if ((int)blockIdx.y == njobs) {  // side work: the block-diagonal operand, then NF4 tables
+        if (side.bd_out)
+            blockdiag_rows(side.bd_Bg, side.bd_Bu, side.bd_n, side.bd_r, side.bd_rp, side.bd_out,
+                           (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
+        const int64_t tiles = nf4_scale_tiles(side.nf4, side.nf4_jobs);
+        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {  // (uniform across the CTA)
+            nf4_scale_tile(side.nf4, side.nf4_jobs, (int)t, sm.nf4);
+            __syncthreads();
+        }
+        return;
+    }
     const FinRowJob& J = jobs.j[blockIdx.y];
     const int nc = J.ncols;
     const int pitch = kFinRowTile + 2;
@@ -52,6 +77,7 @@ __global__ void __launch_bounds__(256) fin_rowproj_kernel(FinRowJobs jobs, int64
     const int rows = T - t0 < kFinRowTile ? (int)(T - t0) : kFinRowTile;
     const int n4 = rows * nc / 4;
     const float* base = J.part + t0 * nc;
+    uint16_t* tileT = sm.tileT;
     for (int i = threadIdx.x; i < n4; i += blockDim.x) {
         const int e = 4 * i, row = e / nc, c0 = e - row * nc;
         const float4 a = sum_splits(base + e, J.split_stride, J.splits);
@@ -70,15 +96,22 @@ __global__ void __launch_bounds__(256) fin_rowproj_kernel(FinRowJobs jobs, int64
     }
 }
 
-cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cudaStream_t st) {
+cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cudaStream_t st, const FinSide* side) {
     FinRowJobs js{};
+    if (njobs < 0 || njobs > 3) return cudaErrorInvalidValue;
     for (int i = 0; i < njobs; ++i) {
         if (jobs[i].ncols > kFinRowMaxCols || jobs[i].ncols % 4 || jobs[i].group % 4) return cudaErrorInvalidValue;
         js.j[i] = jobs[i];
     }
-    const int64_t blocks = (T + kFinRowTile - 1) / kFinRowTile;
-    return launch_pdl(fin_rowproj_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1), njobs), dim3(256), 0, st, nullptr, 0,
-                      js, T);
+    FinSide sd{};
+    if (side) sd = *side;
+    const bool extra = sd.bd_out != nullptr || sd.nf4_jobs > 0;
+    int64_t blocks = (T + kFinRowTile - 1) / kFinRowTile;
+    if (sd.bd_out) blocks = std::max<int64_t>(blocks, std::min<int64_t>((2 * sd.bd_n * (2 * sd.bd_rp / 8) + 255) / 256, 512));
+    if (sd.nf4_jobs > 0) blocks = std::max<int64_t>(blocks, std::min<int64_t>(nf4_scale_tiles(sd.nf4, sd.nf4_jobs), 2048));
+    if (njobs + (extra ? 1 : 0) == 0) return cudaSuccess;
+    return launch_pdl(fin_rowproj_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1), njobs + (extra ? 1 : 0)), dim3(256),
+                      0, st, nullptr, 0, js, njobs, T, sd);
 }
 
 struct FinColJobs {
@@ -202,15 +235,12 @@ cudaError_t launch_tail_fin(const TailFin& f, cudaStream_t st) {
 // ------------------------------------------------------------------ block-diagonal rank-r operand
 // [Bg | 0 ; 0 | Bu] (2n x 2rp bf16): one thread per 8 consecutive columns of a row (one 16-byte
 // store); 2rp is a multiple of 32.
-__global__ void __launch_bounds__(256) blockdiag_kernel(const uint16_t* __restrict__ Bg,
-                                                        const uint16_t* __restrict__ Bu, int64_t n, int r,
-                                                        int rp, uint16_t* __restrict__ out) {
-    griddep_launch_dependents();
-    griddep_wait();
+// Rows [first, ...) step `stride` of the flattened (row, 8-column group) index of [B_g 0; 0 B_u]
+__device__ void blockdiag_rows(const uint16_t* __restrict__ Bg, const uint16_t* __restrict__ Bu, int64_t n, int r,
+                               int rp, uint16_t* __restrict__ out, int64_t first, int64_t stride) {
     const int groups = (2 * rp) / 8;
     const int64_t total = 2 * n * groups;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
+    for (int64_t idx = first; idx < total; idx += stride) {
         const int64_t row = idx / groups;
         const int c0 = (int)(idx - row * groups) * 8;
         const bool upper = row < n;
@@ -226,14 +256,6 @@ __global__ void __launch_bounds__(256) blockdiag_kernel(const uint16_t* __restri
             make_uint4(v[0] | ((uint32_t)v[1] << 16), v[2] | ((uint32_t)v[3] << 16), v[4] | ((uint32_t)v[5] << 16),
                        v[6] | ((uint32_t)v[7] << 16));
     }
-}
-
-cudaError_t launch_blockdiag(const uint16_t* Bg, const uint16_t* Bu, int64_t n, int r, int rp, uint16_t* out,
-                             cudaStream_t st) {
-    const int64_t total = 2 * n * (2 * rp / 8);
-    const int64_t blocks = std::min<int64_t>((total + 255) / 256, 2048);
-    return launch_pdl(blockdiag_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1)), dim3(256), 0, st, nullptr, 0, Bg, Bu, n,
-                      r, rp, out);
 }
 
 // ------------------------------------------------------------------ NF4
@@ -390,11 +412,8 @@ cudaError_t launch_nf4_dequant(const uint8_t* codes, const int8_t* absmax_q, con
 // One CTA per 64-row x 64-K-block tile of one job: the int8 block scales are read along K (64
 // consecutive bytes of a row) and the table is written along rows (64 consecutive floats of a K
 // block), transposed through shared memory, so both sides are coalesced.
-__global__ void __launch_bounds__(256) nf4_scale_table_kernel(Nf4ScaleJobs jobs, int njobs) {
-    griddep_launch_dependents();
-    griddep_wait();
-    __shared__ float tile[64][65];
-    int t = blockIdx.x, j = 0;
+__device__ void nf4_scale_tile(const Nf4ScaleJobs& jobs, int njobs, int t, float (*tile)[65]) {
+    int j = 0;
     for (; j < njobs; ++j) {
         const int tiles = (int)(((jobs.j[j].rows + 63) / 64) * ((jobs.j[j].kblocks + 63) / 64));
         if (t < tiles) break;
@@ -437,12 +456,6 @@ __global__ void __launch_bounds__(256) nf4_scale_table_kernel(Nf4ScaleJobs jobs,
     }
 }
 
-cudaError_t launch_nf4_scale_tables(const Nf4ScaleJobs& jobs, int njobs, cudaStream_t st) {
-    int64_t tiles = 0;
-    for (int j = 0; j < njobs; ++j) tiles += ((jobs.j[j].rows + 63) / 64) * ((jobs.j[j].kblocks + 63) / 64);
-    if (tiles == 0) return cudaSuccess;
-    return launch_pdl(nf4_scale_table_kernel, dim3((unsigned)tiles), dim3(256), 0, st, nullptr, 0, jobs, njobs);
-}
 
 // ------------------------------------------------------------------ int4 groupwise base
 // "loralei" README, QLoRA section (int4 base, groups of 32 to 256 elements of a row): asymmetric

@@ -38,9 +38,6 @@ inline bool gemm_is_pair_nf4(GemmKind k) { return k >= G2N_GLU_FWD && k <= G2N_A
 cudaError_t launch_gemm_pair(GemmKind k, const Params& p, int max_units, cudaStream_t st);
 cudaError_t launch_gemm_pair_nf4(GemmKind k, const Params& p, int max_units, cudaStream_t st);
 
-// [Bg | 0 ; 0 | Bu]: (2n x 2rp) bf16, the rank-r operand of the CTA-pair gate/up GEMM.
-cudaError_t launch_blockdiag(const uint16_t* Bg, const uint16_t* Bu, int64_t n, int r, int rp, uint16_t* out,
-                             cudaStream_t st);
 cudaError_t launch_gemm(GemmKind k, const Params& p, int grid, cudaStream_t st);
 // The dual rank-r reduction (lm_dual.cuh): `grid` CTAs, one per SM.
 cudaError_t launch_dual_reduce(const DualParams& p, int grid, cudaStream_t st);
@@ -60,7 +57,6 @@ struct FinRowJob {
     uint16_t* outT;
     int64_t ldT;
 };
-cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cudaStream_t st);
 
 // Finalisation of split-K partials of the dA / dB column reductions:
 //   dB layout (transposed == 0): out[c][j] = sum_ks part[ks][c][j], j < r
@@ -116,7 +112,20 @@ struct Nf4ScaleJob {
 struct Nf4ScaleJobs {
     Nf4ScaleJob j[3];
 };
-cudaError_t launch_nf4_scale_tables(const Nf4ScaleJobs& jobs, int njobs, cudaStream_t st);
+// Independent work a row finalisation launch can carry in blocks of its own (blockIdx.y past the
+// row jobs), in place of launches of their own: the block-diagonal rank-r operand [B_g 0; 0 B_u]
+// (2n x 2rp, when bd_out is set) and NF4 block-scale tables (nf4_jobs of them).
+struct FinSide {
+    const uint16_t* bd_Bg = nullptr;
+    const uint16_t* bd_Bu = nullptr;
+    int64_t bd_n = 0;
+    int32_t bd_r = 0, bd_rp = 0;
+    uint16_t* bd_out = nullptr;
+    Nf4ScaleJobs nf4{};
+    int32_t nf4_jobs = 0;
+};
+cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cudaStream_t st,
+                               const FinSide* side = nullptr);
 void nf4_codebook_host(float* out16);
 // int4 groupwise base: codes (rows * cols / 2 bytes) and (scale, zero) words sz[g * rows + row]
 cudaError_t launch_int4_pack(const uint16_t* W, int64_t rows, int64_t cols, int group, uint8_t* codes,
