@@ -439,8 +439,9 @@ struct ScaleTable {
     float* table;
 };
 void side_scale_tables(FinSide& side, std::initializer_list<ScaleTable> ws) {
+    constexpr int kMax = (int)(sizeof(side.nf4.j) / sizeof(side.nf4.j[0]));  // every block has at most 3 weights
     for (const ScaleTable& t : ws)
-        if (t.W->kind == LM_WEIGHT_NF4)
+        if (t.W->kind == LM_WEIGHT_NF4 && side.nf4_jobs < kMax)
             side.nf4.j[side.nf4_jobs++] = Nf4ScaleJob{t.W->absmax_q, t.W->group_scale, t.W->rows, t.W->cols / 64, t.table};
 }
 
