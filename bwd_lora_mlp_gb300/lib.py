@@ -141,6 +141,18 @@ def call_status(name: str, *args) -> int:
 # tensor marshalling
 
 
+_EMPTY = {}
+
+
+def _empty_ptr(device) -> int:
+    """A valid device address for a zero-element tensor: torch gives those a null data pointer,
+    the C ABI wants every buffer argument non-null, and a zero-byte buffer is never accessed."""
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    if key not in _EMPTY:
+        _EMPTY[key] = torch.empty(256, dtype=torch.uint8, device=device)
+    return _EMPTY[key].data_ptr()
+
+
 def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor") -> int:
     if t is None:
         return 0
@@ -152,6 +164,8 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor") -> int:
         raise ValueError("%s must be contiguous" % name)
     if dtype is not None and t.dtype != dtype:
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.numel() == 0:  # (T == 0: the token-sized buffers of a call with no tokens)
+        return _empty_ptr(t.device)
     return t.data_ptr()
 
 
