@@ -63,6 +63,34 @@ def test_B_zero_gives_exact_zero_dA():
     _compare(w, inp, fw, bw, "swiglu")
 
 
+def test_A_zero_gives_exact_zero_dB():
+    """A = 0: every rank-r product X Aᵀ (and h A_dᵀ) vanishes, so dB = dOutᵀ (s X Aᵀ) is exactly zero
+    while dA = s Gᵀ X is not."""
+    w = synth.mlp_workload("a0", 256, 128, 192, 16, 32.0)
+    inp = synth.make_inputs(w, seed=4, zero_A=True)
+    fw, bw = run_mlp(inp, w.s, "geglu")
+    for k in ("dB_gate", "dB_up", "dB_down"):
+        assert torch.count_nonzero(bw[k]).item() == 0, k
+    for k in ("dA_gate", "dA_up", "dA_down"):
+        assert torch.count_nonzero(bw[k]).item() > 0, k
+    _compare(w, inp, fw, bw, "geglu")
+
+
+def test_zero_scale_is_the_base_mlp():
+    """s = 0 (alpha = 0): the outputs are the base MLP's and every LoRA gradient is exactly zero."""
+    w = synth.mlp_workload("s0", 300, 256, 320, 16, 0.0)
+    assert w.s == 0.0
+    inp = synth.make_inputs(w, seed=6)
+    fw, bw = run_mlp(inp, w.s, "swiglu")
+    for k in ("dA_gate", "dB_gate", "dA_up", "dB_up", "dA_down", "dB_down"):
+        assert torch.count_nonzero(bw[k]).item() == 0, k
+    _compare(w, inp, fw, bw, "swiglu")
+    base = synth.make_inputs(w, seed=6, zero_B=True)  # the same W, X, dY with the LoRA term removed
+    fw0, _ = run_mlp(base, 1.0, "swiglu")
+    for k in ("y", "e", "u", "h"):
+        assert torch.equal(fw[k], fw0[k]), k
+
+
 def test_bitwise_deterministic():
     w = synth.mlp_workload("det", 640, 256, 448, 16, 32.0)
     inp = synth.make_inputs(w, seed=11)
