@@ -37,8 +37,9 @@ __device__ __forceinline__ float4 sum_splits(const float* p0, int64_t stride, in
 // One CTA per 32 rows of one job: the rows' partials are one contiguous span of 32 ncols floats
 // per split, read with coalesced 16-byte loads; the row-major result is written the same way and
 // the transposed one through a shared-memory tile, 32 contiguous values per output row.  ncols
-// (at most kFinRowMaxCols) and group are multiples of 4.  The blocks with blockIdx.y == njobs do
-// the launch's side work (FinSide), which depends on nothing the row jobs produce.
+// (at most kFinRowMaxCols) and group are multiples of 4.  The grid is flat: njobs x row_blocks
+// blocks for the row jobs, then side_blocks blocks that loop over the launch's side work
+// (FinSide), which depends on nothing the row jobs produce.
 constexpr int kFinRowMaxCols = 192;
 constexpr int kFinRowTile = 32;
 
@@ -51,28 +52,31 @@ __host__ __device__ inline int64_t nf4_scale_tiles(const Nf4ScaleJobs& jobs, int
     return tiles;
 }
 
-__global__ void __launch_bounds__(256) fin_rowproj_kernel(FinRowJobs jobs, int njobs, int64_t T, FinSide side) {
+__global__ void __launch_bounds__(256) fin_rowproj_kernel(FinRowJobs jobs, int njobs, int64_t T, int64_t row_blocks,
+                                                             int64_t side_blocks, FinSide side) {
     __shared__ union {
         uint16_t tileT[kFinRowMaxCols * (kFinRowTile + 2)];  // row jobs: [column][row], padded pitch
         float nf4[64][65];                                   // NF4 table tiles
     } sm;
     griddep_launch_dependents();
     griddep_wait();
-    if ((int)blockIdx.y == njobs) {  // side work: the block-diagonal operand, then NF4 tables
+    const int64_t bid = blockIdx.x;
+    if (bid >= njobs * row_blocks) {  // side work: the block-diagonal operand, then NF4 tables
+        const int64_t sb = bid - njobs * row_blocks;
         if (side.bd_out)
             blockdiag_rows(side.bd_Bg, side.bd_Bu, side.bd_n, side.bd_r, side.bd_rp, side.bd_out,
-                           (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
+                           sb * blockDim.x + threadIdx.x, side_blocks * blockDim.x);
         const int64_t tiles = nf4_scale_tiles(side.nf4, side.nf4_jobs);
-        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {  // (uniform across the CTA)
+        for (int64_t t = sb; t < tiles; t += side_blocks) {  // (uniform across the CTA)
             nf4_scale_tile(side.nf4, side.nf4_jobs, (int)t, sm.nf4);
             __syncthreads();
         }
         return;
     }
-    const FinRowJob& J = jobs.j[blockIdx.y];
+    const FinRowJob& J = jobs.j[bid / row_blocks];
     const int nc = J.ncols;
     const int pitch = kFinRowTile + 2;
-    const int64_t t0 = (int64_t)blockIdx.x * kFinRowTile;
+    const int64_t t0 = (bid % row_blocks) * kFinRowTile;
     if (t0 >= T) return;
     const int rows = T - t0 < kFinRowTile ? (int)(T - t0) : kFinRowTile;
     const int n4 = rows * nc / 4;
@@ -105,13 +109,21 @@ cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cuda
     }
     FinSide sd{};
     if (side) sd = *side;
-    const bool extra = sd.bd_out != nullptr || sd.nf4_jobs > 0;
-    int64_t blocks = (T + kFinRowTile - 1) / kFinRowTile;
-    if (sd.bd_out) blocks = std::max<int64_t>(blocks, std::min<int64_t>((2 * sd.bd_n * (2 * sd.bd_rp / 8) + 255) / 256, 512));
-    if (sd.nf4_jobs > 0) blocks = std::max<int64_t>(blocks, std::min<int64_t>(nf4_scale_tiles(sd.nf4, sd.nf4_jobs), 2048));
-    if (njobs + (extra ? 1 : 0) == 0) return cudaSuccess;
-    return launch_pdl(fin_rowproj_kernel, dim3((unsigned)std::max<int64_t>(blocks, 1), njobs + (extra ? 1 : 0)), dim3(256),
-                      0, st, nullptr, 0, js, njobs, T, sd);
+    const int64_t row_blocks = (T + kFinRowTile - 1) / kFinRowTile;
+    // side blocks: about one resident wave (three CTAs per SM at this kernel's register count), each
+    // looping over its share
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 148;
+    int64_t side_blocks = 0;
+    if (sd.bd_out) side_blocks = (2 * sd.bd_n * (2 * sd.bd_rp / 8) + 255) / 256;
+    if (sd.nf4_jobs > 0) side_blocks = std::max<int64_t>(side_blocks, nf4_scale_tiles(sd.nf4, sd.nf4_jobs));
+    side_blocks = std::min<int64_t>(side_blocks, 3 * (int64_t)sms);
+    const int64_t blocks = njobs * row_blocks + side_blocks;
+    if (blocks == 0) return cudaSuccess;
+    // (the kernel divides by row_blocks only for blocks below njobs * row_blocks, so 0 is safe)
+    return launch_pdl(fin_rowproj_kernel, dim3((unsigned)blocks), dim3(256), 0, st, nullptr, 0, js, njobs, T, row_blocks,
+                      side_blocks, sd);
 }
 
 struct FinColJobs {
@@ -423,27 +435,37 @@ __device__ void nf4_scale_tile(const Nf4ScaleJobs& jobs, int njobs, int t, float
     const Nf4ScaleJob& J = jobs.j[j];
     const int64_t tk = (J.kblocks + 63) / 64;
     const int64_t r0 = (t / tk) * 64, k0 = (t % tk) * 64;
-    // read: rows of 64 consecutive K blocks, four per thread (one 32-bit load when the four are
-    // inside the row and 4-byte aligned, else byte by byte)
+    // read: rows of 64 consecutive K blocks, four per thread: one 32-bit load of the four codes when
+    // they are inside the row and 4-byte aligned (then one group scale serves all four: 256 is a
+    // multiple of 4), else byte by byte.  The loads of all four iterations are issued first.
+    uint32_t q4[4];
+    float g4[4];
+    bool whole[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int i = threadIdx.x + 256 * it;
+        const int rr = i >> 4, kk = (i & 15) * 4;
+        const int64_t row = r0 + rr, kb = k0 + kk;
+        const int64_t b = row * J.kblocks + kb;
+        whole[it] = row < J.rows && kb + 4 <= J.kblocks && (b & 3) == 0;
+        q4[it] = whole[it] ? __ldg(reinterpret_cast<const uint32_t*>(J.absmax_q + b)) : 0u;
+        g4[it] = whole[it] ? __ldg(J.scale + (b >> 8)) : 0.0f;
+    }
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int i = threadIdx.x + 256 * it;
         const int rr = i >> 4, kk = (i & 15) * 4;
         const int64_t row = r0 + rr, kb = k0 + kk;
         float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (row < J.rows) {
+        if (whole[it]) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[c] = __fmul_rn((float)(int8_t)(q4[it] >> (8 * c)), g4[it]);
+        } else if (row < J.rows) {
             const int64_t b = row * J.kblocks + kb;
-            if (kb + 4 <= J.kblocks && (b & 3) == 0) {
-                const uint32_t q4 = __ldg(reinterpret_cast<const uint32_t*>(J.absmax_q + b));
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    v[c] = __fmul_rn((float)(int8_t)(q4 >> (8 * c)), __ldg(J.scale + ((b + c) >> 8)));
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    if (kb + c < J.kblocks)
-                        v[c] = __fmul_rn((float)__ldg(J.absmax_q + b + c), __ldg(J.scale + ((b + c) >> 8)));
-            }
+            for (int c = 0; c < 4; ++c)
+                if (kb + c < J.kblocks)
+                    v[c] = __fmul_rn((float)__ldg(J.absmax_q + b + c), __ldg(J.scale + ((b + c) >> 8)));
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) tile[kk + c][rr] = v[c];
