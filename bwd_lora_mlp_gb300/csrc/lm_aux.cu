@@ -114,7 +114,7 @@ cudaError_t launch_fin_rowproj(const FinRowJob* jobs, int njobs, int64_t T, cuda
     // looping over its share
     int sms = 0, dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 148;
+        sms = 152;  // (a GB300's count; only the side blocks' number depends on it)
     int64_t side_blocks = 0;
     if (sd.bd_out) side_blocks = (2 * sd.bd_n * (2 * sd.bd_rp / 8) + 255) / 256;
     if (sd.nf4_jobs > 0) side_blocks = std::max<int64_t>(side_blocks, nf4_scale_tiles(sd.nf4, sd.nf4_jobs));
