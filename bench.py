@@ -547,14 +547,16 @@ def measure(w, args, world, local, e2e=True):
                         v.copy_(dev_out[b][k], non_blocking=True)
                     out_done[b].record(s_out)
 
-        e2e_steps = max(4, min(args.steps, 20))
+        # windows of up to 50 steps: the first step's copy-in and the last one's copy-out, which
+        # nothing overlaps, are then a small part of a window
+        e2e_steps = max(4, min(args.steps, 50))
         e2e_run(2)
         torch.cuda.synchronize()
         barrier(world)
-        # three windows of e2e_steps steps each; the median window (the host-copy path shows
+        # five windows of e2e_steps steps each; the median window (the host-copy path shows
         # occasional slow windows)
         windows = []
-        for _ in range(3):
+        for _ in range(5):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             s_in.wait_stream(stream)
