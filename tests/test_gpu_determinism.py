@@ -69,3 +69,34 @@ def test_bitwise_twice_and_on_a_side_stream(kind, base):
     for k in a:
         assert torch.equal(a[k], b[k]), (k, "second call")
         assert torch.equal(a[k], c[k]), (k, "side stream")
+
+
+def test_two_streams_at_once_match_sequential_calls():
+    """Two MLP fwd+bwd calls with their own workspaces issued on two streams without waiting for each
+    other: each gives the bits it gives when run alone (the library keeps no shared device state)."""
+    def setup(seed):
+        w = synth.mlp_workload("conc", 600, 256, 512, 16, 32.0)
+        inp = synth.make_inputs(w, seed=seed)
+        ps = {t: _dev(inp, t, w.s, "bf16") for t in ("gate", "up", "down")}
+        return w, dev_bf16(inp["X"]), dev_bf16(inp["dY"]), ps
+
+    def call(X, dY, ps, stream=None):
+        fw = L.lora_mlp_fwd(X, ps["gate"], ps["up"], ps["down"], stream=stream)
+        bw = L.lora_mlp_bwd(X, dY, fw, ps["gate"], ps["up"], ps["down"], stream=stream)
+        return {"y": fw["y"], **bw}
+
+    jobs = [setup(61), setup(62)]
+    alone = [call(X, dY, ps) for _, X, dY, ps in jobs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    together = []
+    for (_, X, dY, ps), s in zip(jobs, streams):
+        with torch.cuda.stream(s):
+            together.append(call(X, dY, ps, stream=s))
+    for s in streams:
+        s.synchronize()
+    for a, b in zip(alone, together):
+        for k in a:
+            assert torch.equal(a[k], b[k]), k
