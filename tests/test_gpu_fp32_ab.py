@@ -118,3 +118,52 @@ def test_qkv_fp32_parameters():
         _same(k, f1[k], f2[k])
     for k in b1:
         _same(k, b1[k], b2[k])
+
+
+@pytest.mark.parametrize("base", ["int4", "nvfp4"])
+def test_mlp_fp32_parameters_over_int4_and_nvfp4_bases(base):
+    """The conversion does not depend on the base: with an int4 (G = 64) or NVFP4 base the
+    fp32-parameter run equals the bf16 run on the rounded parameters bit for bit."""
+    w = synth.mlp_workload("ab32q", 300, 256, 512, 16, 32.0)
+    inp = synth.make_inputs(w, seed=37)
+    ab = synth.fp32_ab(w)
+    rb = {k: O.to_bf16_bits(v) for k, v in ab.items()}
+    pack = (lambda W: L.int4_pack(W, 64)) if base == "int4" else L.nvfp4_pack
+    W = {t: pack(dev_bf16(inp["W_" + t])) for t in ("gate", "up", "down")}
+    f32 = [L.Lora(W[t], _f32(ab["A_" + t]), _f32(ab["B_" + t]), w.s) for t in ("gate", "up", "down")]
+    b16 = [L.Lora(W[t], dev_bf16(rb["A_" + t]), dev_bf16(rb["B_" + t]), w.s) for t in ("gate", "up", "down")]
+    X, dY = dev_bf16(inp["X"]), dev_bf16(inp["dY"])
+    out = []
+    for ps in (f32, b16):
+        fw = L.lora_mlp_fwd(X, *ps)
+        bw = L.lora_mlp_bwd(X, dY, fw, *ps)
+        L.lm_workspace_check(fw["ws"])
+        out.append((fw, bw))
+    torch.cuda.synchronize()
+    (f1, b1), (f2, b2) = out
+    for k in ("y", "e", "u", "h"):
+        _same(k, f1[k], f2[k])
+    for k in b1:
+        _same(k, b1[k], b2[k])
+
+
+def test_relu2_fp32_parameters():
+    w = synth.relu2_workload("ab32r", 300, 256, 512, 16, 32.0)
+    inp = synth.make_inputs(w, seed=39)
+    ab = synth.fp32_ab(w)
+    rb = {k: O.to_bf16_bits(v) for k, v in ab.items()}
+    W = {t: dev_bf16(inp["W_" + t]) for t in ("up", "down")}
+    X, dY = dev_bf16(inp["X"]), dev_bf16(inp["dY"])
+    out = []
+    for mk in (lambda t: (_f32(ab["A_" + t]), _f32(ab["B_" + t])), lambda t: (dev_bf16(rb["A_" + t]), dev_bf16(rb["B_" + t]))):
+        up, down = (L.Lora(W[t], *mk(t), w.s) for t in ("up", "down"))
+        fw = L.lora_relu2_mlp_fwd(X, up, down)
+        bw = L.lora_relu2_mlp_bwd(X, dY, fw, up, down)
+        L.lm_workspace_check(fw["ws"])
+        out.append((fw, bw))
+    torch.cuda.synchronize()
+    (f1, b1), (f2, b2) = out
+    for k in ("y", "u", "h"):
+        _same(k, f1[k], f2[k])
+    for k in b1:
+        _same(k, b1[k], b2[k])
